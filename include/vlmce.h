@@ -1,0 +1,130 @@
+/*
+ * vlmce.h -- C ABI of the GB300 (sm_103a) fused large-vocabulary language-model
+ * cross-entropy library (libvlmce.so).
+ *
+ * Plain pointers and sizes only.  Every buffer argument is DEVICE memory that
+ * the caller allocates and owns; the library never allocates, frees or
+ * synchronises.  All work is enqueued on the caller's stream, in stream order,
+ * and a call returns as soon as it is enqueued.  Arguments are checked on the
+ * host before anything is enqueued; a non-zero status means nothing was
+ * enqueued (except VLMCE_ERR_CUDA, which reports a failed launch).
+ *
+ * Notation (per row r of an [N, V] logits tensor; x_j the input logit):
+ *   t_j = tanh(x_j / T), z_j = T t_j  when the softcap T > 0, else z_j = x_j
+ *   q_j = (1 - eps) [j = y] + eps / V          (label smoothing eps, label y)
+ *   lse = log sum_j exp(z_j),  p_j = exp(z_j - lse)
+ *   loss_r = lse - (1 - eps) z_y - (eps / V) sum_j z_j
+ *   grad_j = scale (p_j - q_j) (T > 0 ? 1 - t_j^2 : 1)
+ * with scale = grad_scale / n_valid for the mean reduction and grad_scale for
+ * the sum, n_valid = the number of rows whose label is in [0, V).
+ *
+ * Sources (web pages on Liger-Kernel / Megatron-LM cross-entropy):
+ *  - "Add Megatron-LM cross-entropy integration", Summary: ignore_index and
+ *    label_smoothing arguments; online softmax; gradient written in place of
+ *    the logits; no full-softmax materialisation.
+ *  - "Add opt-in Liger vocab-parallel cross entropy through ops/loss", What
+ *    does this PR do: fp32 per-token losses, gradient kept in the incoming
+ *    dtype, optional global argmax with smallest-index ties; Contribution
+ *    process: strided inputs and arbitrary upstream gradients.
+ *  - "Add Liger Kernel support for Muse Glimmer", Summary and Details: token
+ *    accuracy, the final-logit softcap T tanh(x/T) with the multiplier folded
+ *    into the hidden states, and a fused linear cross-entropy that never
+ *    builds the [B, S, V] logits and keeps grad_weight in fp32; the native
+ *    Blackwell fused path accepts only 16-bit inputs and mean/sum.
+ */
+#ifndef VLMCE_H_
+#define VLMCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *vlmce_stream_t;
+
+typedef enum {
+    VLMCE_OK = 0,
+    VLMCE_ERR_INVALID_ARG = 1,        /* NULL pointer, bad size, bad option value   */
+    VLMCE_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype not accepted by this entry point      */
+    VLMCE_ERR_MISALIGNED = 3,         /* a pointer is not aligned as documented      */
+    VLMCE_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    VLMCE_ERR_WORKSPACE_TOO_SMALL = 5,/* workspace NULL or smaller than the query    */
+    VLMCE_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed        */
+    VLMCE_ERR_TOO_LARGE = 7           /* a size beyond what the kernels support      */
+} vlmce_status;
+
+typedef enum { VLMCE_F32 = 0, VLMCE_BF16 = 1 } vlmce_dtype;
+typedef enum { VLMCE_MEAN = 1, VLMCE_SUM = 2 } vlmce_reduction;
+
+/* Bits of out_counts[3]: errors the kernels detected on the device. */
+#define VLMCE_DEVERR_TIMEOUT 1 /* an on-chip wait gave up; results are invalid */
+
+/* Largest vocabulary ce_fwd_bwd accepts, in elements, for the given dtype
+ * (rows are kept on chip across a cluster of up to 8 CTAs). */
+int64_t vlmce_ce_max_vocab(int32_t dtype);
+
+/* Bytes of device workspace ce_fwd_bwd needs for N rows (16-byte aligned). */
+size_t vlmce_ce_workspace_bytes(int64_t N, int64_t V, int32_t dtype);
+
+/*
+ * ce_fwd_bwd -- fused cross-entropy forward + backward over N rows, in place.
+ *
+ * logits       in:  [N, row_stride] elements of `dtype` (VLMCE_F32 or
+ *                   VLMCE_BF16), rows of V valid elements; the element pointer
+ *                   must be aligned to the element size.
+ *              out: columns [0, V) of every row hold grad_j in the same dtype
+ *                   (fp32 -> bf16 rounding is round-to-nearest-even).  Columns
+ *                   [V, row_stride) are neither read nor written.  The input
+ *                   logits are destroyed.
+ * labels       [N] int64, device, 8-byte aligned.  A row whose label equals
+ *              ignore_index gets loss 0 and a zero gradient.  A label outside
+ *              [0, V) that is not ignore_index is a caller error: that row's
+ *              loss is NaN, its gradient zero, and it is counted in
+ *              out_counts[2] (the reduced loss is then NaN).
+ * N >= 0, 1 <= V <= vlmce_ce_max_vocab(dtype), row_stride >= V (elements).
+ * label_smoothing in [0, 1]; softcap T >= 0 and finite (0 = off);
+ * reduction VLMCE_MEAN (over rows with labels in [0, V); 0 when there are none)
+ * or VLMCE_SUM; grad_scale finite: the upstream gradient of the reduced loss.
+ * out_loss     [N] fp32 per-token loss (0 for ignored rows), or NULL.
+ * out_argmax   [N] int64, or NULL: per row the smallest j with x_j = max_k x_k
+ *              (raw input values), written for ignored rows too.
+ * out_reduced  [2] fp32, or NULL: reduced loss, token accuracy
+ *              (n_correct / n_valid, 0 when n_valid = 0).
+ * out_counts   [4] int64, or NULL: n_valid, n_correct (argmax = label among
+ *              valid rows), n_bad_labels, device error bits (VLMCE_DEVERR_*).
+ * workspace    device, >= vlmce_ce_workspace_bytes(N, V, dtype) bytes,
+ *              16-byte aligned; contents need no initialisation and are
+ *              scratch between calls.  Calls that share a workspace or
+ *              output buffers must be ordered on one stream.
+ * stream       the stream every kernel is launched on.
+ *
+ * Deterministic: the same inputs give bit-identical outputs (fixed-order
+ * reductions, no floating-point atomics).
+ */
+vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int64_t N, int64_t V,
+                        int64_t row_stride, int64_t ignore_index, float label_smoothing,
+                        float softcap, int32_t reduction, float grad_scale, float *out_loss,
+                        int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
+                        void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
+
+/*
+ * Profiling hook: the next ce_fwd_bwd call made by this host thread records
+ * `ev_begin` immediately before and `ev_end` immediately after its row kernel
+ * (the dominant kernel) on the call's stream, then forgets both.  The two
+ * arguments are cudaEvent_t handles created by the caller (NULL clears the
+ * hook).  Recording the events costs the overlap of that one launch with its
+ * neighbours, so time whole calls without the hook.
+ */
+void vlmce_profile_events(void *ev_begin, void *ev_end);
+
+/* Static, human-readable name of a status code. */
+const char *vlmce_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLMCE_H_ */

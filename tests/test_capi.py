@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every symbol include/vlmce.h declares, and
+rejects bad arguments on the host before touching the GPU.  CPU only: no
+compute call is made."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+import torch
+
+from vocabulary_lm_cross_gb300 import build, capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return capi.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", text):
+            name = m.group(1)
+            if name in ("if", "sizeof", "defined"):
+                continue
+            names.add(name)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"ce_fwd_bwd", "vlmce_ce_workspace_bytes", "vlmce_status_string",
+            "vlmce_ce_max_vocab"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in capi.SIGNATURES, n
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = capi.status_string(code)
+        assert s.startswith("VLMCE_")
+    assert "unknown" in capi.status_string(99)
+
+
+def test_sizes(lib):
+    assert lib.vlmce_ce_max_vocab(capi.BF16) >= 262144
+    assert lib.vlmce_ce_max_vocab(capi.F32) >= 131072
+    assert lib.vlmce_ce_max_vocab(7) == 0
+    assert lib.vlmce_ce_workspace_bytes(2048, 131072, capi.BF16) >= 2048 * 12
+    assert lib.vlmce_ce_workspace_bytes(0, 10, capi.BF16) > 0
+
+
+# Fake, suitably aligned device addresses: the checks below fail before any use.
+P = 1 << 20
+
+
+def call(lib, **kw):
+    a = dict(logits=P, dtype=capi.BF16, labels=P, N=4, V=100, row_stride=100, ignore_index=-100,
+             eps=0.0, softcap=0.0, reduction=capi.MEAN, grad_scale=1.0, out_loss=P,
+             out_argmax=P, out_reduced=P, out_counts=P, ws=P, ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return lib.ce_fwd_bwd(a["logits"], a["dtype"], a["labels"], a["N"], a["V"], a["row_stride"],
+                          a["ignore_index"], a["eps"], a["softcap"], a["reduction"],
+                          a["grad_scale"], a["out_loss"], a["out_argmax"], a["out_reduced"],
+                          a["out_counts"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=5), capi.ERR_UNSUPPORTED_DTYPE),
+    (dict(N=-1), capi.ERR_INVALID_ARG),
+    (dict(V=0), capi.ERR_INVALID_ARG),
+    (dict(row_stride=99), capi.ERR_INVALID_ARG),
+    (dict(logits=None), capi.ERR_INVALID_ARG),
+    (dict(labels=None), capi.ERR_INVALID_ARG),
+    (dict(eps=-0.1), capi.ERR_INVALID_ARG),
+    (dict(eps=1.5), capi.ERR_INVALID_ARG),
+    (dict(eps=math.nan), capi.ERR_INVALID_ARG),
+    (dict(softcap=-1.0), capi.ERR_INVALID_ARG),
+    (dict(softcap=math.inf), capi.ERR_INVALID_ARG),
+    (dict(softcap=math.nan), capi.ERR_INVALID_ARG),
+    (dict(grad_scale=math.nan), capi.ERR_INVALID_ARG),
+    (dict(grad_scale=math.inf), capi.ERR_INVALID_ARG),
+    (dict(reduction=0), capi.ERR_INVALID_ARG),
+    (dict(reduction=3), capi.ERR_INVALID_ARG),
+    (dict(V=10_000_000, row_stride=10_000_000), capi.ERR_TOO_LARGE),
+    (dict(ws=None), capi.ERR_WORKSPACE_TOO_SMALL),
+    (dict(ws_bytes=16), capi.ERR_WORKSPACE_TOO_SMALL),
+    (dict(ws=P + 8), capi.ERR_MISALIGNED),
+    (dict(logits=P + 1), capi.ERR_MISALIGNED),
+    (dict(logits=P + 2, dtype=capi.F32), capi.ERR_MISALIGNED),
+    (dict(labels=P + 4), capi.ERR_MISALIGNED),
+    (dict(out_argmax=P + 4), capi.ERR_MISALIGNED),
+    (dict(out_counts=P + 4), capi.ERR_MISALIGNED),
+    (dict(out_loss=P + 2), capi.ERR_MISALIGNED),
+])
+def test_argument_errors_are_reported_before_any_launch(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_call_without_a_gpu_fails_cleanly(lib):
+    st = call(lib)
+    assert st in (capi.ERR_CUDA, capi.ERR_UNSUPPORTED_DEVICE)
+
+
+def test_binding_raises_loudly_on_bad_input():
+    import vocabulary_lm_cross_gb300 as v
+    with pytest.raises((ValueError, TypeError)):
+        v.ce_fwd_bwd(torch.zeros(3, 4), torch.zeros(3, dtype=torch.int64))

@@ -1,0 +1,210 @@
+"""GPU parity of ce_fwd_bwd (through the C ABI) against the fp64 oracle.
+
+Small grids are compared element by element; the four full-size workloads
+are run in the launch configuration the benchmark times and compared on
+every row for loss / argmax / counts / reduced loss, and element by element
+on sampled rows for the gradient.  Tolerances: see tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import vocabulary_lm_cross_gb300 as v
+from oracle import ce as oc
+from tests.parity import bf16_bits_np, check_grad, check_loss, check_reduced
+from vocabulary_lm_cross_gb300.workloads import (CE_WORKLOADS, IGNORE_INDEX, CEWorkload,
+                                                 make_ce_inputs)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from vocabulary_lm_cross_gb300 import build
+    build.build()
+
+
+def host_rows(x: torch.Tensor, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return bf16_bits_np(x)
+    return x.detach().cpu().contiguous().numpy()
+
+
+def got_rows(x: torch.Tensor, dtype: str) -> np.ndarray:
+    return host_rows(x, dtype)
+
+
+def run_and_check(w: CEWorkload, *, full_grad: bool = True, sample_rows=None, plan=None,
+                  monkeypatch=None):
+    x, lab = make_ce_inputs(w, device=DEV)
+    V = w.V
+    xin = host_rows(x, w.dtype)
+    labh = lab.cpu().numpy()
+    if plan is not None:
+        monkeypatch.setenv("VLMCE_CE_PLAN", plan)
+    res = v.ce_fwd_bwd(x[:, :V], lab, ignore_index=IGNORE_INDEX, label_smoothing=w.label_smoothing,
+                       softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale)
+    torch.cuda.synchronize()
+    out = got_rows(x, w.dtype)
+    # loss / argmax / reductions over every row (oracle without the gradient)
+    ref = oc.ce_fwd_bwd(xin, w.dtype, V, labh, label_smoothing=w.label_smoothing,
+                        softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
+                        want_grad=False)
+    check_loss(res.loss.cpu().numpy(), ref["loss"])
+    assert np.array_equal(res.argmax.cpu().numpy(), ref["argmax"])
+    counts = res.counts.cpu().numpy()
+    assert counts[0] == ref["n_valid"] and counts[1] == ref["n_correct"]
+    assert counts[2] == ref["n_bad"] and counts[3] == 0
+    red = res.reduced.cpu().numpy()
+    check_reduced(float(red[0]), ref["reduced_loss"], w.reduction)
+    assert red[1] == np.float32(ref["accuracy"])
+    # gradient, element by element
+    rows = np.arange(w.N) if full_grad else np.asarray(sample_rows)
+    if rows.size:
+        _, _, g = oc.rows(xin[rows], w.dtype, V, labh[rows], ignore_index=IGNORE_INDEX,
+                          label_smoothing=w.label_smoothing, softcap=w.softcap,
+                          row_scale=ref["row_scale"])
+        stats = check_grad(out[rows][:, :V], g, labh[rows], V, w.label_smoothing,
+                           ref["row_scale"], w.dtype)
+    else:
+        stats = {}
+    # padding columns untouched
+    if w.stride > V:
+        before = xin[:, V:]
+        after = out[:, V:]
+        assert np.array_equal(before.view(np.uint8), after.view(np.uint8)), "padding modified"
+    return res, ref, stats
+
+
+def small(N, V, dtype="bf16", stride=0, eps=0.0, T=0.0, reduction="mean", gs=1.0, seed=7,
+          sigma=3.0, ignore=0.1, boost=0.0, dup=0.0):
+    return CEWorkload(f"t{N}x{V}", N=N, V=V, dtype=dtype, sigma=sigma, ignore_frac=ignore,
+                      label_smoothing=eps, softcap=T, reduction=reduction, grad_scale=gs,
+                      seed=seed, row_stride=stride, label_boost=boost, dup_max_frac=dup)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 127, 4096, 4097, 65537])
+def test_small_grid_contiguous(dtype, V):
+    run_and_check(small(37, V, dtype, eps=0.1, boost=2.0, dup=0.1))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V,stride", [(5, 6), (129, 131), (1000, 1003), (4097, 4100),
+                                      (30011, 30016)])
+@pytest.mark.parametrize("T,eps,red", [(0.0, 0.0, "mean"), (30.0, 0.1, "sum"), (5.0, 0.3, "mean")])
+def test_small_grid_strided_unaligned_rows(dtype, V, stride, T, eps, red):
+    run_and_check(small(29, V, dtype, stride=stride, eps=eps, T=T, reduction=red, gs=0.37,
+                        sigma=8.0 if T else 3.0))
+
+
+@pytest.mark.parametrize("plan", ["1,2", "2,3", "3,2", "4,4", "8,2"])
+def test_every_cluster_shape_agrees(plan, monkeypatch):
+    w = small(23, 20000, "bf16", stride=20003, eps=0.1, T=30.0, boost=4.0, dup=0.2)
+    run_and_check(w, plan=plan, monkeypatch=monkeypatch)
+
+
+def test_largest_vocabulary():
+    Vmax = v.max_vocab(torch.bfloat16)
+    run_and_check(small(3, Vmax, "bf16", eps=0.1, T=30.0, ignore=0.0))
+    Vmax32 = v.max_vocab(torch.float32)
+    run_and_check(small(2, Vmax32, "f32", eps=0.0, ignore=0.0))
+
+
+def test_no_rows():
+    lab = torch.zeros(0, dtype=torch.int64, device=DEV)
+    x = torch.zeros(0, 10, dtype=torch.bfloat16, device=DEV)
+    res = v.ce_fwd_bwd(x, lab)
+    torch.cuda.synchronize()
+    assert res.reduced.cpu().tolist() == [0.0, 0.0]
+    assert res.counts.cpu().tolist() == [0, 0, 0, 0]
+
+
+def test_all_rows_ignored_and_bad_labels():
+    w = small(16, 3000, "bf16", ignore=1.0)
+    res, ref, _ = run_and_check(w)
+    assert res.reduced.cpu().tolist() == [0.0, 0.0]
+    x, lab = make_ce_inputs(small(8, 300, "bf16", ignore=0.0), device=DEV)
+    lab[1] = 300
+    lab[5] = -7
+    xin = bf16_bits_np(x)
+    res = v.ce_fwd_bwd(x, lab)
+    torch.cuda.synchronize()
+    ref = oc.ce_fwd_bwd(xin, "bf16", 300, lab.cpu().numpy())
+    check_loss(res.loss.cpu().numpy(), ref["loss"])
+    counts = res.counts.cpu().tolist()
+    assert counts[0] == 6 and counts[2] == 2
+    assert np.isnan(res.reduced.cpu().numpy()[0])
+    g = bf16_bits_np(x)
+    assert np.all(g[1] == 0) and np.all(g[5] == 0)
+
+
+def test_deterministic_bit_identical():
+    w = CE_WORKLOADS["ce-bf16-2048x131072-ls0.1-argmax"].resized(N=300)
+    outs = []
+    for _ in range(2):
+        x, lab = make_ce_inputs(w, device=DEV)
+        res = v.ce_fwd_bwd(x, lab, label_smoothing=0.1)
+        torch.cuda.synchronize()
+        outs.append((bf16_bits_np(x), res.loss.cpu().numpy(), res.reduced.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+    assert np.array_equal(outs[0][2].view(np.uint32), outs[1][2].view(np.uint32))
+
+
+def test_guard_bytes_around_the_buffer_are_untouched():
+    N, V = 17, 5001
+    w = small(N, V, "bf16", eps=0.1)
+    x, lab = make_ce_inputs(w, device=DEV)
+    big = torch.full((N * V + 64,), 7.0, dtype=torch.bfloat16, device=DEV)
+    view = big[32:32 + N * V].view(N, V)
+    view.copy_(x)
+    v.ce_fwd_bwd(view, lab, label_smoothing=0.1)
+    torch.cuda.synchronize()
+    b = big.float().cpu()
+    assert torch.all(b[:32] == 7.0) and torch.all(b[32 + N * V:] == 7.0)
+
+
+def test_non_default_stream():
+    w = small(64, 9000, "bf16", eps=0.1)
+    x, lab = make_ce_inputs(w, device=DEV)
+    xin = bf16_bits_np(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        res = v.ce_fwd_bwd(x, lab, label_smoothing=0.1)
+    s.synchronize()
+    ref = oc.ce_fwd_bwd(xin, "bf16", 9000, lab.cpu().numpy(), label_smoothing=0.1)
+    check_loss(res.loss.cpu().numpy(), ref["loss"])
+    check_grad(bf16_bits_np(x), ref["grad"], lab.cpu().numpy(), 9000, 0.1, ref["row_scale"], "bf16")
+
+
+def _sample(N, labels, extra=()):
+    rng = np.random.default_rng(0)
+    base = {0, 1, N - 1, N - 2}
+    ign = np.flatnonzero(labels == IGNORE_INDEX)[:3]
+    base |= set(int(i) for i in ign)
+    base |= set(int(i) for i in extra)
+    base |= set(int(i) for i in rng.choice(N, size=min(N, 40), replace=False))
+    return sorted(base)
+
+
+@pytest.mark.parametrize("name", list(CE_WORKLOADS))
+def test_full_size_workloads(name):
+    w = CE_WORKLOADS[name]
+    if w.N * w.V <= 4_000_000:
+        run_and_check(w, full_grad=True)
+        return
+    # sampled rows: ends, ignored rows, rows with duplicate maxima, random rows
+    x, lab = make_ce_inputs(w, device=DEV)
+    labh = lab.cpu().numpy()
+    xf = x[:, :w.V]
+    mx = xf.max(dim=1, keepdim=True).values
+    dup_rows = torch.nonzero(((xf == mx).sum(dim=1) >= 2)).flatten().cpu().numpy()
+    del x, lab, xf, mx
+    torch.cuda.empty_cache()
+    rows = _sample(w.N, labh, extra=dup_rows[:40])
+    _, ref, stats = run_and_check(w, full_grad=False, sample_rows=rows)
+    print(name, stats)

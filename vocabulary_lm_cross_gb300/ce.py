@@ -1,0 +1,83 @@
+"""PyTorch-facing binding of ce_fwd_bwd (argument marshalling only).
+
+Every step of the computation runs in libvlmce.so's CUDA kernels; this module
+only checks tensors, takes their device pointers and the current CUDA stream,
+and calls the C ABI.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import capi
+
+_DTYPES = {torch.float32: capi.F32, torch.bfloat16: capi.BF16}
+_REDUCTIONS = {"mean": capi.MEAN, "sum": capi.SUM}
+
+
+@dataclass
+class CEResult:
+    """Outputs of one ce_fwd_bwd call (device tensors; the gradient is the logits buffer)."""
+    loss: torch.Tensor      # fp32 [N] per-token loss
+    argmax: torch.Tensor    # int64 [N]
+    reduced: torch.Tensor   # fp32 [2]: reduced loss, token accuracy
+    counts: torch.Tensor    # int64 [4]: n_valid, n_correct, n_bad_labels, device error bits
+
+
+def workspace_bytes(N: int, V: int, dtype: torch.dtype) -> int:
+    return int(capi.lib().vlmce_ce_workspace_bytes(N, V, _DTYPES[dtype]))
+
+
+def max_vocab(dtype: torch.dtype) -> int:
+    return int(capi.lib().vlmce_ce_max_vocab(_DTYPES[dtype]))
+
+
+def ce_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, *, ignore_index: int = -100,
+               label_smoothing: float = 0.0, softcap: float = 0.0, reduction: str = "mean",
+               grad_scale: float = 1.0, out: CEResult | None = None,
+               workspace: torch.Tensor | None = None) -> CEResult:
+    """Fused cross-entropy forward + backward; the gradient overwrites ``logits``.
+
+    logits: CUDA tensor [N, V] (fp32 or bf16) whose rows may be strided
+        (``logits.stride(1) == 1``; ``stride(0)`` is the row stride, so a view
+        ``buf[:, :V]`` of a padded buffer works).  After the call it holds the
+        gradient of ``grad_scale * reduced_loss`` and the input is gone; its
+        autograd version counter is bumped so stale uses are caught.
+    labels: int64 CUDA tensor [N].
+    """
+    if logits.dim() != 2 or labels.dim() != 1 or labels.shape[0] != logits.shape[0]:
+        raise ValueError("logits must be [N, V] and labels [N]")
+    if logits.dtype not in _DTYPES:
+        raise TypeError(f"unsupported logits dtype {logits.dtype}")
+    if labels.dtype != torch.int64:
+        raise TypeError("labels must be int64")
+    if not logits.is_cuda or not labels.is_cuda or logits.device != labels.device:
+        raise ValueError("logits and labels must be CUDA tensors on one device")
+    N, V = logits.shape
+    if V > 1 and logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous (stride(1) == 1)")
+    row_stride = logits.stride(0) if N > 1 else V
+    labels = labels.contiguous()
+    dev = logits.device
+    if out is None:
+        out = CEResult(loss=torch.empty(N, dtype=torch.float32, device=dev),
+                       argmax=torch.empty(N, dtype=torch.int64, device=dev),
+                       reduced=torch.empty(2, dtype=torch.float32, device=dev),
+                       counts=torch.empty(4, dtype=torch.int64, device=dev))
+    need = workspace_bytes(N, V, logits.dtype)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    st = capi.lib().ce_fwd_bwd(
+        logits.data_ptr(), _DTYPES[logits.dtype], labels.data_ptr(), N, V, row_stride,
+        ignore_index, float(label_smoothing), float(softcap), _REDUCTIONS[reduction],
+        float(grad_scale), out.loss.data_ptr(), out.argmax.data_ptr(), out.reduced.data_ptr(),
+        out.counts.data_ptr(), workspace.data_ptr(), workspace.numel(), stream)
+    capi.check(st, "ce_fwd_bwd")
+    try:
+        torch.autograd.graph.increment_version(logits)
+    except Exception:  # older/newer torch without the helper: nothing to bump
+        pass
+    return out
