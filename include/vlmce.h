@@ -120,6 +120,11 @@ vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int6
  */
 void vlmce_profile_events(void *ev_begin, void *ev_end);
 
+/* The last failed CUDA call made by this library on this host thread, as
+ * "where: cudaErrorName (description)"; "" if none.  Valid until the next
+ * failing call on the same thread. */
+const char *vlmce_last_error(void);
+
 /* Static, human-readable name of a status code. */
 const char *vlmce_status_string(int32_t status);
 

@@ -7,15 +7,20 @@ Tolerances (stated once, used by every parity test):
 * argmax, n_valid, n_correct, n_bad: exact;
 * reduced loss: 1e-4 absolute for the mean, 1e-6 relative for the sum;
 * gradient: the stored value g (bf16 or fp32, widened exactly) satisfies
-      |g - g_o| <= ulp(g_o) + KAPPA (|g_o| + |scale| q_j)
+      |g - g_o| <= ulp(g_o) + kappa(T) (|g_o| + |scale| q_j)
   where ulp is the spacing of the storage dtype at g_o, q_j the smoothed
-  target (eps/V, plus 1 - eps at the label) and KAPPA = 4e-6 bounds the
-  relative error of the kernel's fp32 evaluation of p_j = exp(z_j - lse)
-  (two fp32 roundings of an exponent of magnitude < 60, times ln 2, plus the
-  MUFU exp2 error).  Away from cancellation (p_j far from q_j) this is the
-  1-ulp rule; where p_j ~ q_j no fp32 evaluation can do better.  In addition
-  at least 99.99 % of bf16 elements must be within 1 ulp of RN(g_o) by
-  ordered-integer distance.
+  target (eps/V, plus 1 - eps at the label) and kappa bounds the relative
+  error of the kernel's fp32 evaluation of p_j = exp(z_j - lse):
+      kappa(T) = 4e-6 + 3e-7 T
+  (4e-6: two fp32 roundings of an exponent of magnitude < 60, times ln 2,
+  plus the MUFU exp2 error of about 2^-22; 3e-7 T: with the softcap,
+  z = T tanh(x/T) is formed from 1 - exp(-2|x|/T), whose exp2 error of
+  2^-22 turns into an absolute error of at most T 2^-22 in z).
+  An element is "well conditioned" when that error term is at most half an
+  ulp: kappa (|g_o| + |scale| q_j) <= ulp(g_o) / 2.  Every well-conditioned
+  bf16 element must be within 1 ulp of RN(g_o) by ordered-integer distance
+  (the benchmark spec's 1-ulp rule).  The others sit where p_j ~ q_j, where no fp32
+  evaluation can resolve the difference, and get the absolute bound above.
 """
 from __future__ import annotations
 
@@ -24,7 +29,14 @@ import torch
 
 from oracle import ce as oc
 
-KAPPA = 4e-6
+KAPPA0 = 4e-6
+KAPPA_PER_T = 3e-7
+
+
+def kappa(softcap: float) -> float:
+    return KAPPA0 + KAPPA_PER_T * softcap
+
+
 LOSS_ATOL = 1e-4
 
 
@@ -51,7 +63,8 @@ def ordered(bits: np.ndarray) -> np.ndarray:
 
 
 def check_grad(got: np.ndarray, ref: np.ndarray, labels: np.ndarray, V: int, eps: float,
-               scale: float, dtype: str, ignore_index: int = -100, what: str = "grad") -> dict:
+               scale: float, dtype: str, softcap: float = 0.0, ignore_index: int = -100,
+               what: str = "grad") -> dict:
     """got: [n, V] stored gradient (uint16 bf16 bits or float32); ref: fp64 [n, V]."""
     n = ref.shape[0]
     q = np.full((n, V), eps / V)
@@ -63,21 +76,28 @@ def check_grad(got: np.ndarray, ref: np.ndarray, labels: np.ndarray, V: int, eps
         g = bits_to_f64(got)
     else:
         g = got.astype(np.float64)
-    tol = ulp(ref, dtype) + KAPPA * (np.abs(ref) + abs(scale) * q)
+    u = ulp(ref, dtype)
+    cond = kappa(softcap) * (np.abs(ref) + abs(scale) * q)
+    tol = u + cond
     err = np.abs(g - ref)
     bad = ~(err <= tol)
     stats = {"n": int(ref.size), "max_err_over_tol": float(np.max(err / tol)) if ref.size else 0.0}
-    if dtype == "bf16":
-        d = np.abs(ordered(got) - ordered(oc.round_bf16(ref)))
-        stats["within_1ulp_frac"] = float(np.mean(d <= 1)) if ref.size else 1.0
-        stats["max_ulp"] = int(d.max()) if ref.size else 0
     if bad.any():
         i, j = np.argwhere(bad)[0]
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {ref.size} elements out of tolerance; first at row {i} "
             f"col {j}: got {g[i, j]!r} oracle {ref[i, j]!r} tol {tol[i, j]!r} label {labels[i]}")
     if dtype == "bf16" and ref.size:
-        assert stats["within_1ulp_frac"] >= 0.9999, stats
+        d = np.abs(ordered(got) - ordered(oc.round_bf16(ref)))
+        well = cond <= 0.5 * u
+        stats["well_conditioned_frac"] = float(np.mean(well))
+        stats["max_ulp_well_conditioned"] = int(d[well].max()) if well.any() else 0
+        stats["within_1ulp_frac"] = float(np.mean(d <= 1))
+        if well.any() and d[well].max() > 1:
+            i, j = np.argwhere(well & (d > 1))[0]
+            raise AssertionError(
+                f"{what}: {int((well & (d > 1)).sum())} well-conditioned elements more than 1 ulp "
+                f"from RN(oracle); first at row {i} col {j}: got {g[i, j]!r} oracle {ref[i, j]!r}")
     return stats
 
 

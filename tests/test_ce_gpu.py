@@ -67,7 +67,7 @@ def run_and_check(w: CEWorkload, *, full_grad: bool = True, sample_rows=None, pl
                           label_smoothing=w.label_smoothing, softcap=w.softcap,
                           row_scale=ref["row_scale"])
         stats = check_grad(out[rows][:, :V], g, labh[rows], V, w.label_smoothing,
-                           ref["row_scale"], w.dtype)
+                           ref["row_scale"], w.dtype, softcap=w.softcap)
     else:
         stats = {}
     # padding columns untouched
@@ -178,7 +178,8 @@ def test_non_default_stream():
     s.synchronize()
     ref = oc.ce_fwd_bwd(xin, "bf16", 9000, lab.cpu().numpy(), label_smoothing=0.1)
     check_loss(res.loss.cpu().numpy(), ref["loss"])
-    check_grad(bf16_bits_np(x), ref["grad"], lab.cpu().numpy(), 9000, 0.1, ref["row_scale"], "bf16")
+    check_grad(bf16_bits_np(x), ref["grad"], lab.cpu().numpy(), 9000, 0.1, ref["row_scale"],
+               "bf16")
 
 
 def _sample(N, labels, extra=()):

@@ -39,6 +39,7 @@ _sz = ctypes.c_size_t
 # name -> (restype, argtypes); every function include/vlmce.h declares.
 SIGNATURES = {
     "vlmce_status_string": (ctypes.c_char_p, [_i32]),
+    "vlmce_last_error": (ctypes.c_char_p, []),
     "vlmce_ce_max_vocab": (_i64, [_i32]),
     "vlmce_profile_events": (None, [_vp, _vp]),
     "vlmce_ce_workspace_bytes": (_sz, [_i64, _i64, _i32]),
@@ -50,7 +51,10 @@ SIGNATURES = {
 class VlmceError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)}")
+        detail = ""
+        if status == ERR_CUDA:
+            detail = " [" + lib().vlmce_last_error().decode() + "]"
+        super().__init__(f"{where}: {status_string(status)}{detail}")
 
 
 def lib():

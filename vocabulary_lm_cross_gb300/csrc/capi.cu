@@ -1,4 +1,5 @@
 // capi.cu -- status strings and the per-device properties cache.
+#include <cstdio>
 #include <mutex>
 
 #include "host_util.h"
@@ -6,18 +7,27 @@
 namespace vlmce {
 
 namespace {
+thread_local char t_last_error[256] = "";
 constexpr int kMaxDevices = 64;
 DeviceInfo g_info[kMaxDevices];
 bool g_have[kMaxDevices] = {};
 std::mutex g_mu;
 }  // namespace
 
+cudaError_t record_cuda(cudaError_t e, const char *where) {
+    if (e != cudaSuccess) {
+        snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+                 cudaGetErrorString(e));
+        cudaGetLastError();
+    }
+    return e;
+}
+
 vlmce_status current_device(DeviceInfo *out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
+    if (record_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess || dev < 0 ||
+        dev >= kMaxDevices)
         return VLMCE_ERR_CUDA;
-    }
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_have[dev]) {
@@ -31,7 +41,7 @@ vlmce_status current_device(DeviceInfo *out) {
                     cudaSuccess ||
                 cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                        dev) != cudaSuccess) {
-                cudaGetLastError();
+                record_cuda(cudaGetLastError(), "cudaDeviceGetAttribute");
                 return VLMCE_ERR_CUDA;
             }
             g_info[dev] = d;
@@ -45,6 +55,8 @@ vlmce_status current_device(DeviceInfo *out) {
 }
 
 }  // namespace vlmce
+
+extern "C" const char *vlmce_last_error(void) { return vlmce::t_last_error; }
 
 extern "C" const char *vlmce_status_string(int32_t status) {
     switch (status) {

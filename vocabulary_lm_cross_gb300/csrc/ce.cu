@@ -759,11 +759,12 @@ vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t V, P
     Plan pl;
     if (!shape_plan(d.smem_optin, bf16, V, fk, fs, &pl)) return VLMCE_ERR_TOO_LARGE;
     RowKernel kern = pick_kernel(bf16, softcap);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) !=
-        cudaSuccess) {
-        cudaGetLastError();
+    // The attribute belongs to the kernel, not to the plan: set it to the device
+    // maximum so every plan of this kernel can launch.
+    if (record_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         d.smem_optin),
+                    "cudaFuncSetAttribute(ce_rows_kernel)") != cudaSuccess)
         return VLMCE_ERR_CUDA;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.k * d.sm_count, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -776,10 +777,10 @@ vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t V, P
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) != cudaSuccess || ncl < 1) {
-        cudaGetLastError();
+    if (record_cuda(cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg),
+                    "cudaOccupancyMaxActiveClusters(ce_rows_kernel)") != cudaSuccess)
         return VLMCE_ERR_CUDA;
-    }
+    if (ncl < 1) return VLMCE_ERR_TOO_LARGE;
     pl.max_clusters = ncl;
     g_plans[key] = pl;
     *out = pl;
@@ -856,7 +857,7 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
     int64_t *amax = out_argmax ? out_argmax : w.argmax;
 
     ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
-    st = launch_status(cudaSuccess);
+    st = launch_status(cudaSuccess, "ce_count_kernel");
     if (st != VLMCE_OK) return st;
 
     cudaLaunchAttribute attr[2];
@@ -897,10 +898,12 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
         cfg.numAttrs = 2;
         cudaEvent_t eb = t_prof_begin, ee = t_prof_end;
         t_prof_begin = t_prof_end = nullptr;
-        if (eb && cudaEventRecord(eb, cs) != cudaSuccess) return launch_status(cudaErrorUnknown);
-        st = launch_status(cudaLaunchKernelEx(&cfg, pick_kernel(bf16, capped), p));
+        if (eb && (st = launch_status(cudaEventRecord(eb, cs), "cudaEventRecord")) != VLMCE_OK)
+            return st;
+        st = launch_status(cudaLaunchKernelEx(&cfg, pick_kernel(bf16, capped), p), "ce_rows_kernel");
         if (st != VLMCE_OK) return st;
-        if (ee && cudaEventRecord(ee, cs) != cudaSuccess) return launch_status(cudaErrorUnknown);
+        if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
+            return st;
     }
 
     {
@@ -917,7 +920,8 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
                                               ignore_index, static_cast<int>(reduction),
                                               static_cast<const int64_t *>(w.counts),
                                               static_cast<const int *>(w.err), out_reduced,
-                                              out_counts));
+                                              out_counts),
+                           "ce_finalize_kernel");
     }
     return st;
 }

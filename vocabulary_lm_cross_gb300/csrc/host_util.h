@@ -28,9 +28,16 @@ inline bool aligned(const void *p, uintptr_t a) {
 
 inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-inline vlmce_status launch_status(cudaError_t e) {
+// Remember a failed CUDA call (per host thread) for vlmce_last_error(), and
+// clear the runtime's error state.  Returns `e`.
+cudaError_t record_cuda(cudaError_t e, const char *where);
+
+// Status of a launch: `e` from the launch API, else the runtime's last error.
+inline vlmce_status launch_status(cudaError_t e, const char *where) {
     if (e == cudaSuccess) e = cudaGetLastError();
-    return e == cudaSuccess ? VLMCE_OK : VLMCE_ERR_CUDA;
+    if (e == cudaSuccess) return VLMCE_OK;
+    record_cuda(e, where);
+    return VLMCE_ERR_CUDA;
 }
 
 }  // namespace vlmce
