@@ -372,7 +372,8 @@ def run_ours(args, w):
                          f"ring of {n_buf} buffers of {buf_bytes / 1e6:.0f} MB (> L2)",
                    "vs_baseline_is": "value per GPU / 1510 GB/s = TE CE 0.711 ms on H100 "
                                      "(the pages' number, another machine: context)",
-                   "device_status_ok": ok_status},
+                   "device_status_ok": ok_status,
+                   "plan": v.describe_plan(V, x0.dtype, w.softcap)},
         "roofline": {"bound": "hbm", "kernel": "ce_rows_kernel", "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} (copy GB/s)", "unit": "GB/s",
                      "frac": achieved / peak, "kernel_ms": kern_ms,

@@ -100,10 +100,19 @@ def test_small_grid_strided_unaligned_rows(dtype, V, stride, T, eps, red):
                         sigma=8.0 if T else 3.0))
 
 
-@pytest.mark.parametrize("plan", ["1,2", "2,3", "3,2", "4,4", "8,2"])
+@pytest.mark.parametrize("plan", ["1,16", "1,8", "2,8", "3,12", "4,4", "8,4"])
 def test_every_cluster_shape_agrees(plan, monkeypatch):
     w = small(23, 20000, "bf16", stride=20003, eps=0.1, T=30.0, boost=4.0, dup=0.2)
     run_and_check(w, plan=plan, monkeypatch=monkeypatch)
+
+
+def test_plans_of_the_benchmarked_workloads():
+    for name, w in CE_WORKLOADS.items():
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        pl = v.describe_plan(w.V, dt, w.softcap)
+        assert pl["cluster"] * pl["granules_per_cta"] * (8 if w.dtype == "bf16" else 4) >= w.V
+        assert pl["clusters"] >= 1, (name, pl)
+        print(name, pl)
 
 
 def test_largest_vocabulary():

@@ -4,4 +4,4 @@ The compute lives in ``lib/libvlmce.so`` (hand-written CUDA kernels behind the
 C ABI in ``include/vlmce.h``); this package holds the build script, a thin
 ctypes/PyTorch binding and the seeded synthetic workloads.
 """
-from .ce import CEResult, ce_fwd_bwd, max_vocab, workspace_bytes  # noqa: F401
+from .ce import CEResult, ce_fwd_bwd, describe_plan, max_vocab, workspace_bytes  # noqa: F401

@@ -29,6 +29,19 @@ def workspace_bytes(N: int, V: int, dtype: torch.dtype) -> int:
     return int(capi.lib().vlmce_ce_workspace_bytes(N, V, _DTYPES[dtype]))
 
 
+def describe_plan(V: int, dtype: torch.dtype, softcap: float = 0.0,
+                  aligned_rows: bool = True) -> dict:
+    """The launch plan of the row kernel for rows of V elements on the current device."""
+    import ctypes
+    out = (ctypes.c_int32 * 6)()
+    st = capi.lib().vlmce_ce_describe_plan(V, _DTYPES[dtype], float(softcap), int(aligned_rows),
+                                           ctypes.cast(out, ctypes.c_void_p))
+    capi.check(st, "vlmce_ce_describe_plan")
+    keys = ("cluster", "granules_per_thread", "granules_per_cta", "clusters", "threads",
+            "smem_bytes")
+    return dict(zip(keys, list(out)))
+
+
 def max_vocab(dtype: torch.dtype) -> int:
     return int(capi.lib().vlmce_ce_max_vocab(_DTYPES[dtype]))
 
