@@ -8,12 +8,14 @@
 // move each slot into registers (2 granules per thread per slot) and release
 // it at once, so the ring keeps refilling while the row is still being
 // worked on.  With the whole slice in registers:
-//   pass A: max and first argmax of the raw logits, online sum of
-//           exp(z - m) and sum of z (packed f32x2 arithmetic);
-//   merge:  warp shuffles, then the 15 warp partials, then the k CTA
-//           partials through distributed shared memory (one release/acquire
-//           mbarrier exchange per row; every warp merges the k partials in the
-//           same fixed order, so every CTA holds the same lse);
+//   pass A: per-thread max and first argmax of the raw logits, then the sums
+//           of exp(z - m) and of z (packed f32x2 arithmetic, independent
+//           accumulators);
+//   merge:  warp shuffles; then every consumer warp writes its partial into
+//           every CTA of the cluster through distributed shared memory and
+//           release-arrives on each CTA's row barrier; after the acquire-wait
+//           every warp merges the k x 15 partials in the same fixed order, so
+//           every CTA holds the same lse;
 //   pass B: gradient scale (p - q) (1 - t^2), rounded to the storage dtype,
 //           16-byte streaming stores over the logits.
 // Each byte of the row crosses HBM once in and once out.
@@ -37,7 +39,7 @@ constexpr int kThreads = kConsumers + 32;         // + 1 producer warp: 16 warps
 constexpr int kChunkGranules = 2 * kConsumers;    // 960 granules = 15 KB per slot
 constexpr int kChunkBytes = 16 * kChunkGranules;
 constexpr int kSlots = 13;                        // 195 KB ring
-constexpr int kCtlBytes = 2048;
+constexpr int kCtlBytes = 8192;
 constexpr int kSmemBytes = kCtlBytes + kSlots * kChunkBytes;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxGpt = 16;                       // granules per consumer thread
@@ -58,9 +60,10 @@ struct __align__(16) RowPart {
 struct Ctl {
     unsigned long long full[kSlots];   // slot landed (transaction bytes)
     unsigned long long empty[kSlots];  // slot released by the 15 consumer warps
-    unsigned long long stat[2];        // all k partials of a row written (k arrivals)
-    RowPart slot[2];                   // this CTA's partial, read by the whole cluster
-    RowPart warp[2][kConsumerWarps];   // per-warp partials
+    unsigned long long stat[2];        // all partials of a row arrived (k x 15 arrivals)
+    // Row partials of every consumer warp of every CTA of the cluster, written
+    // by their owners through distributed shared memory; indexed by row parity.
+    RowPart xslot[2][kMaxCluster * kConsumerWarps];
     int abort;                         // an on-chip wait gave up
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
@@ -290,76 +293,52 @@ __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Per-thread pass-A accumulators.
-struct Acc {
-    float mv;      // max raw logit seen
-    int midx;      // its first column
-    float mz;      // z of mv: reference of s
-    uint64_t mzL;  // (-mz log2e, -mz log2e)
-    uint64_t s;    // sums of exp(z - mz), two lanes
-    uint64_t sz;   // sums of z, two lanes
-};
+// Max of one granule over its valid columns (all of them for a full granule).
+template <bool BF16>
+__device__ __forceinline__ float granule_max_masked(const uint4 w, int jg, int V) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    if (jg >= 0 && jg + EPG <= V) return granule_max<BF16>(w);
+    float x[EPG];
+    unpack<BF16>(w, x);
+    float gm = -INFINITY;
+#pragma unroll
+    for (int l = 0; l < EPG; ++l)
+        if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
+    return gm;
+}
 
-// Fold one granule (already in registers) into the pass-A accumulators.
+// Add exp(z - mz) and z of one granule's valid columns to the two-lane sums.
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void pass_a_granule(Acc &a, const uint4 w, int jg, int V, float T,
-                                               float k2) {
+__device__ __forceinline__ void granule_sums(const uint4 w, int jg, int V, float T, float k2,
+                                             uint64_t negmzL2, uint64_t &s, uint64_t &sz) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
-    const bool full = jg >= 0 && jg + EPG <= V;
-    float gm;
-    if (full) {
-        gm = granule_max<BF16>(w);
-    } else {
-        gm = -INFINITY;
-#pragma unroll
-        for (int l = 0; l < EPG; ++l)
-            if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
-    }
-    if (gm > a.mv) {  // new maximum: locate it, rescale the running sums
-        int li = EPG - 1;
-#pragma unroll
-        for (int l = EPG - 1; l >= 0; --l)
-            if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
-        const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
-        const float f = ptx::ex2((a.mz - nz) * kLog2e);
-        float s0, s1;
-        upk(a.s, s0, s1);
-        s0 = (s0 == 0.f) ? 0.f : s0 * f;
-        s1 = (s1 == 0.f) ? 0.f : s1 * f;
-        a.s = pk(s0, s1);
-        a.mv = gm;
-        a.midx = jg + li;
-        a.mz = nz;
-        a.mzL = pk(-nz * kLog2e, -nz * kLog2e);
-    }
     const uint64_t L2 = pk(kLog2e, kLog2e);
-    if (full) {
+    if (jg >= 0 && jg + EPG <= V) {
 #pragma unroll
         for (int l = 0; l < EPG; l += 2) {
             const float za = softcap_z<SOFTCAP>(x[l], T, k2).z;
             const float zb = softcap_z<SOFTCAP>(x[l + 1], T, k2).z;
             const uint64_t z2 = pk(za, zb);
-            a.s = add2(a.s, ex2x2(fma2(z2, L2, a.mzL)));
-            a.sz = add2(a.sz, z2);
+            s = add2(s, ex2x2(fma2(z2, L2, negmzL2)));
+            sz = add2(sz, z2);
         }
     } else {
-        float s0, s1, z0, z1;
-        upk(a.s, s0, s1);
-        upk(a.sz, z0, z1);
-        float mzL, dummy;
-        upk(a.mzL, mzL, dummy);
+        float s0, s1, z0, z1, nm, dummy;
+        upk(s, s0, s1);
+        upk(sz, z0, z1);
+        upk(negmzL2, nm, dummy);
 #pragma unroll
         for (int l = 0; l < EPG; ++l) {
             if (jg + l >= 0 && jg + l < V) {
                 const float z = softcap_z<SOFTCAP>(x[l], T, k2).z;
-                s0 += ptx::ex2(fmaf(z, kLog2e, mzL));
+                s0 += ptx::ex2(fmaf(z, kLog2e, nm));
                 z0 += z;
             }
         }
-        a.s = pk(s0, s1);
-        a.sz = pk(z0, z1);
+        s = pk(s0, s1);
+        sz = pk(z0, z1);
     }
 }
 
@@ -459,10 +438,6 @@ __device__ __forceinline__ void produce(const Params &p, Ctl &ctl, uint32_t ring
     }
 }
 
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
-
 template <bool BF16, bool SOFTCAP, int GPT>
 __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
     static_assert(GPT % 2 == 0 && GPT <= kMaxGpt, "granules per thread");
@@ -486,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
             ptx::mbar_init(full0 + 8u * s, 1);
             ptx::mbar_init(empty0 + 8u * s, kConsumerWarps);
         }
-        ptx::mbar_init(ptx::smem_addr(&ctl.stat[0]), k);
-        ptx::mbar_init(ptx::smem_addr(&ctl.stat[1]), k);
+        ptx::mbar_init(ptx::smem_addr(&ctl.stat[0]), k * kConsumerWarps);
+        ptx::mbar_init(ptx::smem_addr(&ctl.stat[1]), k * kConsumerWarps);
         ctl.abort = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -524,15 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
             const RowGeo g = row_geo<BF16>(p, r, crank);
             const int nch = (g.n_my + kChunkGranules - 1) / kChunkGranules;
 
-            // ---- stream the slice into registers; pass A as it arrives
+            // ---- stream the slice into registers (slot i of the ring holds
+            // granules [960 c, 960 c + 960) of the slice: two per thread)
             uint4 reg[GPT];
-            Acc a;
-            a.mv = -INFINITY;
-            a.midx = INT_MAX;
-            a.mz = -INFINITY;
-            a.mzL = pk(INFINITY, INFINITY);
-            a.s = pk(0.f, 0.f);
-            a.sz = pk(0.f, 0.f);
             float zy = 0.f;
 #pragma unroll
             for (int c = 0; c < GPT / 2; ++c) {
@@ -546,71 +515,121 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
                     if (g0 < g.n_my) reg[2 * c] = *reinterpret_cast<const uint4 *>(sb + 16 * tid);
                     if (g1 < g.n_my)
                         reg[2 * c + 1] = *reinterpret_cast<const uint4 *>(sb + 16 * (tid + kConsumers));
-                    if (valid) {  // the label's logit, from whichever thread holds it
-                        const int gy = static_cast<int>((y + g.lead) / EPG) - g.g_beg;
-                        const int ly = static_cast<int>((y + g.lead) % EPG);
-                        if (gy >= 0 && gy < g.n_my && (gy == g0 || gy == g1)) {
-                            const uint4 w = (gy == g0) ? reg[2 * c] : reg[2 * c + 1];
-                            float xv[EPG];
-                            unpack<BF16>(w, xv);
-                            float xy = xv[0];
-#pragma unroll
-                            for (int l = 1; l < EPG; ++l)
-                                if (l == ly) xy = xv[l];
-                            zy = softcap_z<SOFTCAP>(xy, T, k2).z;
-                        }
-                    }
                     __syncwarp();
-                    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8u * slot) : "memory");
+                    if (lane == 0)
+                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8u * slot)
+                                     : "memory");
                     ++q;
-                    if (g0 < g.n_my)
-                        pass_a_granule<BF16, SOFTCAP>(a, reg[2 * c], (g.g_beg + g0) * EPG - g.lead,
-                                                      p.V, T, k2);
-                    if (g1 < g.n_my)
-                        pass_a_granule<BF16, SOFTCAP>(a, reg[2 * c + 1],
-                                                      (g.g_beg + g1) * EPG - g.lead, p.V, T, k2);
+                }
+            }
+
+            // ---- pass A.1: max of the raw logits over this thread's granules, and
+            // the first column holding it (granules are visited in column order)
+            float gmax[GPT];
+            float mv = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < GPT; ++i) {
+                const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
+                gmax[i] = (gl < g.n_my) ? granule_max_masked<BF16>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V)
+                                        : -INFINITY;
+                mv = fmaxf(mv, gmax[i]);
+            }
+            int midx = INT_MAX;
+            if (mv > -INFINITY) {
+                int fi = 0;
+#pragma unroll
+                for (int i = GPT - 1; i >= 0; --i)
+                    if (gmax[i] == mv) fi = i;
+                uint4 w = reg[0];
+#pragma unroll
+                for (int i = 1; i < GPT; ++i)
+                    if (i == fi) w = reg[i];
+                const int gl = (fi >> 1) * kChunkGranules + (fi & 1) * kConsumers + tid;
+                const int jg = (g.g_beg + gl) * EPG - g.lead;
+                float xv[EPG];
+                unpack<BF16>(w, xv);
+#pragma unroll
+                for (int l = EPG - 1; l >= 0; --l)
+                    if (xv[l] == mv && jg + l >= 0 && jg + l < p.V) midx = jg + l;
+            }
+
+            // ---- pass A.2: sum of exp(z - mz) (mz = z of this thread's max) and of z,
+            // four independent two-lane accumulators
+            const float mz = (mv > -INFINITY) ? softcap_z<SOFTCAP>(mv, T, k2).z : -INFINITY;
+            const uint64_t negmzL2 = pk(-mz * kLog2e, -mz * kLog2e);
+            uint64_t sa = pk(0.f, 0.f), sb2 = pk(0.f, 0.f), za = pk(0.f, 0.f), zb = pk(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < GPT; ++i) {
+                const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
+                if (gl < g.n_my) {
+                    if (i & 1)
+                        granule_sums<BF16, SOFTCAP>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V, T, k2,
+                                                    negmzL2, sb2, zb);
+                    else
+                        granule_sums<BF16, SOFTCAP>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V, T, k2,
+                                                    negmzL2, sa, za);
+                }
+            }
+            // the label's z, from the thread that holds it
+            if (valid) {
+                const int gy = static_cast<int>((y + g.lead) / EPG) - g.g_beg;
+                const int ly = static_cast<int>((y + g.lead) % EPG);
+#pragma unroll
+                for (int i = 0; i < GPT; ++i) {
+                    const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
+                    if (gl == gy && gy < g.n_my) {
+                        float xv[EPG];
+                        unpack<BF16>(reg[i], xv);
+                        float xy = xv[0];
+#pragma unroll
+                        for (int l = 1; l < EPG; ++l)
+                            if (l == ly) xy = xv[l];
+                        zy = softcap_z<SOFTCAP>(xy, T, k2).z;
+                    }
                 }
             }
             RowPart part = part_identity();
-            part.mx = a.mv;
-            part.idx = a.midx;
-            part.mz = a.mz;
+            part.mx = mv;
+            part.idx = midx;
+            part.mz = mz;
             {
+                const uint64_t s2 = add2(sa, sb2), z2 = add2(za, zb);
                 float s0, s1, z0, z1;
-                upk(a.s, s0, s1);
-                upk(a.sz, z0, z1);
+                upk(s2, s0, s1);
+                upk(z2, z0, z1);
                 part.s = s0 + s1;
                 part.sz = z0 + z1;
             }
             part.zy = zy;
             warp_allreduce(part);
-            if (lane == 0) ctl.warp[pp][warp] = part;
-            consumers_sync();
 
-            // ---- CTA partial -> cluster exchange
-            if (warp == 0) {
-                RowPart w = lane < kConsumerWarps ? ctl.warp[pp][lane] : part_identity();
-                warp_allreduce(w);
-                if (lane == 0) {
-                    ctl.slot[pp] = w;
-                    const uint32_t bar = ptx::smem_addr(&ctl.stat[pp]);
-                    for (uint32_t c = 0; c < k; ++c)
-                        ptx::mbar_remote_arrive_release(ptx::mapa(bar, c));
+            // ---- publish this warp's partial to every CTA of the cluster, then
+            // merge all k x 15 partials of the row (same order everywhere)
+            if (lane == 0) {
+                const uint32_t dst = ptx::smem_addr(&ctl.xslot[pp][crank * kConsumerWarps + warp]);
+                const uint32_t bar = ptx::smem_addr(&ctl.stat[pp]);
+                const uint4 v0 = make_uint4(__float_as_uint(part.mx), static_cast<uint32_t>(part.idx),
+                                            __float_as_uint(part.mz), __float_as_uint(part.s));
+                const uint4 v1 = make_uint4(__float_as_uint(part.sz), __float_as_uint(part.zy), 0u, 0u);
+                for (uint32_t c = 0; c < k; ++c) {
+                    const uint32_t ra = ptx::mapa(dst, c);
+                    ptx::st_dsmem_v4(ra, v0);
+                    ptx::st_dsmem_v4(ra + 16, v1);
                 }
+                for (uint32_t c = 0; c < k; ++c) ptx::mbar_remote_arrive_release(ptx::mapa(bar, c));
             }
             bounded_wait<true, false>(ptx::smem_addr(&ctl.stat[pp]),
                                       static_cast<uint32_t>((it >> 1) & 1), abort, p.err);
             RowPart rp = part_identity();
-            if (lane < static_cast<int>(k)) {
-                const uint32_t ad = ptx::mapa(ptx::smem_addr(&ctl.slot[pp]), lane);
-                const uint4 v0 = ptx::ld_dsmem_v4(ad);
-                const uint4 v1 = ptx::ld_dsmem_v4(ad + 16);
-                rp.mx = __uint_as_float(v0.x);
-                rp.idx = static_cast<int>(v0.y);
-                rp.mz = __uint_as_float(v0.z);
-                rp.s = __uint_as_float(v0.w);
-                rp.sz = __uint_as_float(v1.x);
-                rp.zy = __uint_as_float(v1.y);
+            {
+                const int n_parts = static_cast<int>(k) * kConsumerWarps;
+#pragma unroll
+                for (int e = lane; e < kMaxCluster * kConsumerWarps; e += 32) {
+                    if (e < n_parts) {
+                        const RowPart &o = ctl.xslot[pp][e];
+                        part_merge(rp, o.mx, o.idx, o.mz, o.s, o.sz, o.zy);
+                    }
+                }
             }
             warp_allreduce(rp);
             const float lse = rp.mz + logf(rp.s);

@@ -97,6 +97,12 @@ __device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // --------------------------------------------------------------- bulk copy
 // Global -> this CTA's shared memory, completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
