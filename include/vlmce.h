@@ -63,12 +63,12 @@ typedef enum { VLMCE_MEAN = 1, VLMCE_SUM = 2 } vlmce_reduction;
 #define VLMCE_DEVERR_TIMEOUT 1 /* an on-chip wait gave up; results are invalid */
 
 /* Largest vocabulary ce_fwd_bwd accepts, in elements, for the given dtype
- * (a row is kept on chip, in registers, across a cluster of up to 8 CTAs). */
+ * (a row is kept on chip, in shared memory, across a cluster of up to 8 CTAs). */
 int64_t vlmce_ce_max_vocab(int32_t dtype);
 
 /* The launch plan ce_fwd_bwd uses for rows of V elements on the current device:
- * out[6] = {CTAs per cluster (row split), granules (16 B) per consumer thread,
- * granules per CTA, co-resident clusters, threads per CTA, shared-memory bytes
+ * out[6] = {CTAs per cluster (row split), ring slots per row slice, granules
+ * (16 B) per CTA, co-resident clusters, threads per CTA, shared-memory bytes
  * per CTA}.  aligned_rows: every row starts on a 16-byte boundary.  Returns a
  * vlmce_status. */
 int32_t vlmce_ce_describe_plan(int64_t V, int32_t dtype, float softcap, int32_t aligned_rows,

@@ -100,7 +100,7 @@ def test_small_grid_strided_unaligned_rows(dtype, V, stride, T, eps, red):
                         sigma=8.0 if T else 3.0))
 
 
-@pytest.mark.parametrize("plan", ["1,16", "1,8", "2,8", "3,12", "4,4", "8,4"])
+@pytest.mark.parametrize("plan", ["1", "2", "3", "5", "8"])
 def test_every_cluster_shape_agrees(plan, monkeypatch):
     w = small(23, 20000, "bf16", stride=20003, eps=0.1, T=30.0, boost=4.0, dup=0.2)
     run_and_check(w, plan=plan, monkeypatch=monkeypatch)

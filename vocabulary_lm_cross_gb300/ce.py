@@ -37,7 +37,7 @@ def describe_plan(V: int, dtype: torch.dtype, softcap: float = 0.0,
     st = capi.lib().vlmce_ce_describe_plan(V, _DTYPES[dtype], float(softcap), int(aligned_rows),
                                            ctypes.cast(out, ctypes.c_void_p))
     capi.check(st, "vlmce_ce_describe_plan")
-    keys = ("cluster", "granules_per_thread", "granules_per_cta", "clusters", "threads",
+    keys = ("cluster", "slots_per_slice", "granules_per_cta", "clusters", "threads",
             "smem_bytes")
     return dict(zip(keys, list(out)))
 

@@ -11,7 +11,8 @@
 // Three launches on the caller's stream:
 //   1. count_kernel    -- label census (n_valid for the mean, bad labels).
 //   2. rows_kernel     -- the row kernel (ce_rows.cuh): clusters of k CTAs,
-//      producer warp + shared-memory ring, row slice held in registers.
+//      two CTAs per SM, producer warp streaming row slices into a
+//      shared-memory ring.
 //   3. finalize_kernel -- fixed-order fp64 reduction of the per-row losses
 //      and correct-prediction count.
 // Kernels 2 and 3 use programmatic dependent launch so that their prologues
@@ -162,22 +163,10 @@ Workspace carve(void *ws, int64_t N) {
 
 struct Plan {
     int k = 0;             // CTAs per cluster (row split)
-    int gpt = 0;           // granules per consumer thread (register capacity)
     int gran_per_cta = 0;  // granules of a row per CTA
     int max_clusters = 0;  // co-resident clusters (persistent grid)
     RowKernel kernel = nullptr;
 };
-
-constexpr int kGptChoices[] = {4, 8, 12, 16};
-
-RowKernel kernel_for(int gpt, bool bf16, bool softcap) {
-    switch (gpt) {
-        case 4: return rows_kernel_gpt4(bf16, softcap);
-        case 8: return rows_kernel_gpt8(bf16, softcap);
-        case 12: return rows_kernel_gpt12(bf16, softcap);
-        default: return rows_kernel_gpt16(bf16, softcap);
-    }
-}
 
 // Granules of a row: exact when every row starts on a 16-byte boundary, else
 // the worst case over the possible offsets of its first element.
@@ -186,33 +175,24 @@ int64_t row_granules(bool bf16, int64_t V, bool aligned_rows) {
     return aligned_rows ? (V + epg - 1) / epg : (epg - 1 + V + epg - 1) / epg;
 }
 
-// Smallest cluster whose per-CTA slice fits the register capacity, then the
-// smallest capacity that holds the slice.  Tuning override (environment
-// VLMCE_CE_PLAN = "k" or "k,gpt").
+// Smallest cluster whose per-CTA slice fits kPreferredChunks ring slots (two
+// rows in flight per CTA); past 8 CTAs, slices of up to the whole ring.
+// Tuning override: environment VLMCE_CE_PLAN = "k".
 bool shape_plan(int64_t G, Plan *pl) {
-    int fk = 0, fg = 0;
+    int fk = 0;
     const char *e = getenv("VLMCE_CE_PLAN");
     if (e && *e) {
-        int a = 0, b = 0;
-        const int n = sscanf(e, "%d,%d", &a, &b);
-        if (n >= 1 && a >= 1 && a <= kMaxCluster) fk = a;
-        if (n == 2) fg = b;
+        int a = 0;
+        if (sscanf(e, "%d", &a) == 1 && a >= 1 && a <= kMaxCluster) fk = a;
     }
-    const int64_t cap = static_cast<int64_t>(kMaxGpt) * kConsumers;
-    int k = fk ? fk : static_cast<int>((G + cap - 1) / cap);
+    const int64_t pref = static_cast<int64_t>(kPreferredChunks) * kChunkGranules;
+    const int64_t cap = static_cast<int64_t>(kSlots) * kChunkGranules;
+    int k = fk ? fk : static_cast<int>((G + pref - 1) / pref);
     if (k < 1) k = 1;
-    if (k > kMaxCluster) return false;
+    if (k > kMaxCluster) k = kMaxCluster;
     const int64_t gc = (G + k - 1) / k;
     if (gc > cap) return false;
-    int gpt = 0;
-    for (int c : kGptChoices)
-        if (static_cast<int64_t>(c) * kConsumers >= gc && (!fg || c >= fg)) {
-            gpt = c;
-            break;
-        }
-    if (!gpt) return false;
     pl->k = k;
-    pl->gpt = gpt;
     pl->gran_per_cta = static_cast<int>(gc);
     return true;
 }
@@ -233,7 +213,7 @@ vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t G, P
     Plan pl;
     if (!shape_plan(G, &pl)) return VLMCE_ERR_TOO_LARGE;
     if (d.smem_optin < kSmemBytes) return VLMCE_ERR_UNSUPPORTED_DEVICE;
-    pl.kernel = kernel_for(pl.gpt, bf16, softcap);
+    pl.kernel = bf16 ? rows_kernel_bf16(softcap) : rows_kernel_f32(softcap);
     if (!g_attr_set.count({d.device, pl.kernel})) {
         if (record_cuda(cudaFuncSetAttribute(pl.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes),
@@ -284,9 +264,9 @@ extern "C" void vlmce_profile_events(void *ev_begin, void *ev_end) {
 
 extern "C" int64_t vlmce_ce_max_vocab(int32_t dtype) {
     if (dtype != VLMCE_F32 && dtype != VLMCE_BF16) return 0;
-    // kMaxCluster CTAs x kMaxGpt granules x kConsumers threads, worst-case row offset.
+    // kMaxCluster CTAs x a whole ring of slots each, worst-case row offset.
     const int64_t epg = dtype == VLMCE_BF16 ? 8 : 4;
-    const int64_t G = static_cast<int64_t>(kMaxCluster) * kMaxGpt * kConsumers;
+    const int64_t G = static_cast<int64_t>(kMaxCluster) * kSlots * kChunkGranules;
     return G * epg - (epg - 1);
 }
 
@@ -301,7 +281,7 @@ extern "C" int32_t vlmce_ce_describe_plan(int64_t V, int32_t dtype, float softca
                   row_granules(dtype == VLMCE_BF16, V, aligned_rows != 0), &pl);
     if (st != VLMCE_OK) return st;
     out[0] = pl.k;
-    out[1] = pl.gpt;
+    out[1] = (pl.gran_per_cta + kChunkGranules - 1) / kChunkGranules;
     out[2] = pl.gran_per_cta;
     out[3] = pl.max_clusters;
     out[4] = kThreads;

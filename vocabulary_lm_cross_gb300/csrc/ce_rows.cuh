@@ -2,15 +2,17 @@
 //
 // One thread-block cluster of k CTAs owns one row at a time; CTA c of the
 // cluster owns the c-th 1/k of the row's 16-byte granules (its "slice").
+// Two CTAs share each SM (16 warps each), so one CTA's per-row exchange
+// bubble is filled by the other's arithmetic.
+//
 // Warp 15 of each CTA is a producer: one lane streams the slices of the
-// cluster's rows, in order, through a ring of 15 KB shared-memory slots with
-// bulk (TMA) copies, as far ahead as the ring allows.  The 15 consumer warps
-// move each slot into registers (2 granules per thread per slot) and release
-// it at once, so the ring keeps refilling while the row is still being
-// worked on.  With the whole slice in registers:
-//   pass A: per-thread max and first argmax of the raw logits, then the sums
-//           of exp(z - m) and of z (packed f32x2 arithmetic, independent
-//           accumulators);
+// cluster's rows, in order, through a ring of 7.5 KB shared-memory slots
+// (480 granules: one per consumer thread) with bulk (TMA) copies, as far
+// ahead as free slots allow.  A row's slots stay resident until its gradient
+// has been written, then the 15 consumer warps release them.  Per row:
+//   pass A: one pass over the slice in shared memory: max and first argmax of
+//           the raw logits, online sum of exp(z - m) and sum of z (packed
+//           f32x2 arithmetic);
 //   merge:  warp shuffles; then every consumer warp writes its partial into
 //           every CTA of the cluster through distributed shared memory and
 //           release-arrives on each CTA's row barrier; after the acquire-wait
@@ -35,14 +37,15 @@ namespace ce {
 
 constexpr int kConsumerWarps = 15;
 constexpr int kConsumers = 32 * kConsumerWarps;   // 480 consumer threads
-constexpr int kThreads = kConsumers + 32;         // + 1 producer warp: 16 warps, 128 regs each
-constexpr int kChunkGranules = 2 * kConsumers;    // 960 granules = 15 KB per slot
-constexpr int kChunkBytes = 16 * kChunkGranules;
-constexpr int kSlots = 13;                        // 195 KB ring
+constexpr int kThreads = kConsumers + 32;         // + 1 producer warp
+constexpr int kCtasPerSm = 2;
+constexpr int kChunkGranules = kConsumers;        // one granule per consumer thread
+constexpr int kChunkBytes = 16 * kChunkGranules;  // 7.5 KB per slot
+constexpr int kSlots = 13;
 constexpr int kCtlBytes = 8192;
-constexpr int kSmemBytes = kCtlBytes + kSlots * kChunkBytes;
+constexpr int kSmemBytes = kCtlBytes + kSlots * kChunkBytes;  // 108,032 B: two CTAs per SM
 constexpr int kMaxCluster = 8;
-constexpr int kMaxGpt = 16;                       // granules per consumer thread
+constexpr int kPreferredChunks = 6;  // slices of <= 6 slots keep two rows in the ring
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per on-chip wait
 
@@ -53,7 +56,7 @@ struct __align__(16) RowPart {
     float mz;   // reference maximum (z space) of s
     float s;    // sum exp(z - mz)
     float sz;   // sum z
-    float zy;   // z at the label column (only its owner CTA adds it)
+    float zy;   // z at the label column (only its owner adds it)
     float pad0, pad1;
 };
 
@@ -83,7 +86,7 @@ struct Params {
     int64_t *argmax;
     const int64_t *counts;  // [0] n_valid (written by the count kernel)
     int *err;
-    int gran_per_cta;       // granules of a row owned by one CTA (<= GPT * kConsumers)
+    int gran_per_cta;       // granules of a row owned by one CTA (<= kSlots * kChunkGranules)
 };
 
 using RowKernel = void (*)(Params);
@@ -113,20 +116,10 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 __device__ __forceinline__ uint64_t ex2x2(uint64_t a) {
     float x, y;
     upk(a, x, y);
     return pk(ptx::ex2(x), ptx::ex2(y));
-}
-
-// The two fp32 values of a bf16x2 word (low element first).
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t u) {
-    return pk(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
 __device__ __forceinline__ RowPart part_identity() {
@@ -224,8 +217,7 @@ __device__ __forceinline__ float granule_max(const uint4 w) {
     }
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack_pair(float a, float b) {
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     uint32_t u;
     memcpy(&u, &v, 4);
@@ -266,18 +258,17 @@ __device__ __forceinline__ RowGeo row_geo(const Params &p, int64_t r, uint32_t c
     return g;
 }
 
-// Bounded mbarrier wait.  CLUSTER: acquire at cluster scope (pairs with the
-// peers' release-arrives).  Gives up after kWaitLimitNs (1 ms once another
-// wait has already given up), setting the abort flag and the device error
-// bit; SKIP_IF_ABORT returns at once when aborted (waits whose arrival may
-// never come once the pipeline stopped).
+// Bounded mbarrier wait (slow path).  CLUSTER: acquire at cluster scope (pairs
+// with the peers' release-arrives).  Gives up after kWaitLimitNs (1 ms once
+// another wait has already given up), setting the abort flag and the device
+// error bit; SKIP_IF_ABORT returns at once when aborted (waits whose arrival
+// may never come once the pipeline stopped).
 template <bool CLUSTER, bool SKIP_IF_ABORT>
-__device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *err) {
+__device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               int *err) {
     auto poll = [&]() {
         return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
     };
-    if (poll()) return true;
     if (SKIP_IF_ABORT && *abort) return false;
     const unsigned long long t0 = ptx::globaltimer_ns();
     const unsigned long long limit = *abort ? 1000000ull : kWaitLimitNs;
@@ -293,42 +284,74 @@ __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Max of one granule over its valid columns (all of them for a full granule).
-template <bool BF16>
-__device__ __forceinline__ float granule_max_masked(const uint4 w, int jg, int V) {
-    constexpr int EPG = Elem<BF16>::kPerGranule;
-    if (jg >= 0 && jg + EPG <= V) return granule_max<BF16>(w);
-    float x[EPG];
-    unpack<BF16>(w, x);
-    float gm = -INFINITY;
-#pragma unroll
-    for (int l = 0; l < EPG; ++l)
-        if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
-    return gm;
+template <bool CLUSTER, bool SKIP_IF_ABORT>
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             int *err) {
+    const bool ok =
+        CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    if (ok) return true;
+    return bounded_wait_slow<CLUSTER, SKIP_IF_ABORT>(bar, parity, abort, err);
 }
 
-// Add exp(z - mz) and z of one granule's valid columns to the two-lane sums.
+// Per-thread pass-A accumulators.
+struct Acc {
+    float mv;      // max raw logit seen
+    int midx;      // its first column
+    float mz;      // z of mv: reference of s
+    uint64_t nmL;  // (-mz log2e, -mz log2e)
+    uint64_t s;    // sums of exp(z - mz), two lanes
+    uint64_t sz;   // sums of z, two lanes
+};
+
+// Fold one granule into the pass-A accumulators (granules arrive in column order).
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void granule_sums(const uint4 w, int jg, int V, float T, float k2,
-                                             uint64_t negmzL2, uint64_t &s, uint64_t &sz) {
+__device__ __forceinline__ void pass_a_granule(Acc &a, const uint4 w, int jg, int V, float T,
+                                               float k2) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
+    const bool full = jg >= 0 && jg + EPG <= V;
+    float gm;
+    if (full) {
+        gm = granule_max<BF16>(w);
+    } else {
+        gm = -INFINITY;
+#pragma unroll
+        for (int l = 0; l < EPG; ++l)
+            if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
+    }
+    if (gm > a.mv) {  // new maximum (rare after the first granules): locate it, rescale
+        int li = EPG - 1;
+#pragma unroll
+        for (int l = EPG - 1; l >= 0; --l)
+            if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
+        const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
+        const float f = ptx::ex2((a.mz - nz) * kLog2e);
+        float s0, s1;
+        upk(a.s, s0, s1);
+        s0 = (s0 == 0.f) ? 0.f : s0 * f;
+        s1 = (s1 == 0.f) ? 0.f : s1 * f;
+        a.s = pk(s0, s1);
+        a.mv = gm;
+        a.midx = jg + li;
+        a.mz = nz;
+        a.nmL = pk(-nz * kLog2e, -nz * kLog2e);
+    }
     const uint64_t L2 = pk(kLog2e, kLog2e);
-    if (jg >= 0 && jg + EPG <= V) {
+    if (full) {
 #pragma unroll
         for (int l = 0; l < EPG; l += 2) {
             const float za = softcap_z<SOFTCAP>(x[l], T, k2).z;
             const float zb = softcap_z<SOFTCAP>(x[l + 1], T, k2).z;
             const uint64_t z2 = pk(za, zb);
-            s = add2(s, ex2x2(fma2(z2, L2, negmzL2)));
-            sz = add2(sz, z2);
+            a.s = add2(a.s, ex2x2(fma2(z2, L2, a.nmL)));
+            a.sz = add2(a.sz, z2);
         }
     } else {
         float s0, s1, z0, z1, nm, dummy;
-        upk(s, s0, s1);
-        upk(sz, z0, z1);
-        upk(negmzL2, nm, dummy);
+        upk(a.s, s0, s1);
+        upk(a.sz, z0, z1);
+        upk(a.nmL, nm, dummy);
 #pragma unroll
         for (int l = 0; l < EPG; ++l) {
             if (jg + l >= 0 && jg + l < V) {
@@ -337,15 +360,15 @@ __device__ __forceinline__ void granule_sums(const uint4 w, int jg, int V, float
                 z0 += z;
             }
         }
-        s = pk(s0, s1);
-        sz = pk(z0, z1);
+        a.s = pk(s0, s1);
+        a.sz = pk(z0, z1);
     }
 }
 
 // Gradient of one granule, stored over the logits.
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, unsigned char *dst,
-                                               float T, float k2, uint64_t lseL2, uint64_t scale2,
+                                               float T, float k2, uint64_t nlseL2, uint64_t scale2,
                                                uint64_t negc2, int label_lane, float scale,
                                                float c_label) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
@@ -359,8 +382,8 @@ __device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, uns
         const Capped cb = softcap_z<SOFTCAP>(x[l + 1], T, k2);
         dz[l] = ca.dz;
         dz[l + 1] = cb.dz;
-        const uint64_t p2 = ex2x2(fma2(pk(ca.z, cb.z), L2, lseL2));  // p_j
-        const uint64_t g2 = fma2(p2, scale2, negc2);                 // scale (p_j - eps/V)
+        const uint64_t p2 = ex2x2(fma2(pk(ca.z, cb.z), L2, nlseL2));  // p_j
+        const uint64_t g2 = fma2(p2, scale2, negc2);                  // scale (p_j - eps/V)
         upk(g2, g[l], g[l + 1]);
         if (label_lane >= 0) {  // the label column: q_y = 1 - eps + eps/V
             float pa, pb;
@@ -376,8 +399,8 @@ __device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, uns
     if (jg >= 0 && jg + EPG <= V) {
         uint4 o;
         if constexpr (BF16) {
-            o = make_uint4(pack_pair<true>(g[0], g[1]), pack_pair<true>(g[2], g[3]),
-                           pack_pair<true>(g[4], g[5]), pack_pair<true>(g[6], g[7]));
+            o = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                           pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
         } else {
             o = make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]),
                            __float_as_uint(g[3]));
@@ -438,14 +461,12 @@ __device__ __forceinline__ void produce(const Params &p, Ctl &ctl, uint32_t ring
     }
 }
 
-template <bool BF16, bool SOFTCAP, int GPT>
-__global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
-    static_assert(GPT % 2 == 0 && GPT <= kMaxGpt, "granules per thread");
+template <bool BF16, bool SOFTCAP>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) rows_kernel(const Params p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
-    constexpr int ELT = Elem<BF16>::kBytes;
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctl &ctl = *reinterpret_cast<Ctl *>(smem);
-    const uint32_t ring0 = ptx::smem_addr(smem + kCtlBytes);
+    unsigned char *ring = smem + kCtlBytes;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -473,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
     volatile int *abort = &ctl.abort;
 
     if (warp == kConsumerWarps) {
-        if (lane == 0) produce<BF16>(p, ctl, ring0, cid, ncl, crank, n_iter);
+        if (lane == 0) produce<BF16>(p, ctl, ptx::smem_addr(ring), cid, ncl, crank, n_iter);
         __syncwarp();
     } else {
         // The label census of this call must be complete before it is read.
@@ -489,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
         const float T = p.softcap;
         const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
 
-        int64_t q = 0;  // ring position, in step with the producer
+        int64_t q = 0;  // ring position of the row's first chunk, in step with the producer
         for (int64_t it = 0; it < n_iter; ++it) {
             const int pp = static_cast<int>(it & 1);
             const int64_t r = static_cast<int64_t>(cid) + it * ncl;
@@ -498,88 +519,31 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
             const bool valid = !ignored && y >= 0 && y < p.V;
             const RowGeo g = row_geo<BF16>(p, r, crank);
             const int nch = (g.n_my + kChunkGranules - 1) / kChunkGranules;
+            const int gy = valid ? static_cast<int>((y + g.lead) / EPG) - g.g_beg : -1;
+            const int ly = valid ? static_cast<int>((y + g.lead) % EPG) : 0;
 
-            // ---- stream the slice into registers (slot i of the ring holds
-            // granules [960 c, 960 c + 960) of the slice: two per thread)
-            uint4 reg[GPT];
+            // ---- pass A over the slice as its slots land
+            Acc a;
+            a.mv = -INFINITY;
+            a.midx = INT_MAX;
+            a.mz = -INFINITY;
+            a.nmL = pk(INFINITY, INFINITY);
+            a.s = pk(0.f, 0.f);
+            a.sz = pk(0.f, 0.f);
             float zy = 0.f;
-#pragma unroll
-            for (int c = 0; c < GPT / 2; ++c) {
-                if (c < nch) {
-                    const int slot = static_cast<int>(q % kSlots);
-                    bounded_wait<false, true>(full0 + 8u * slot,
-                                              static_cast<uint32_t>((q / kSlots) & 1), abort, p.err);
-                    const unsigned char *sb = smem + kCtlBytes + static_cast<size_t>(slot) * kChunkBytes;
-                    const int g0 = c * kChunkGranules + tid;
-                    const int g1 = g0 + kConsumers;
-                    if (g0 < g.n_my) reg[2 * c] = *reinterpret_cast<const uint4 *>(sb + 16 * tid);
-                    if (g1 < g.n_my)
-                        reg[2 * c + 1] = *reinterpret_cast<const uint4 *>(sb + 16 * (tid + kConsumers));
-                    __syncwarp();
-                    if (lane == 0)
-                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8u * slot)
-                                     : "memory");
-                    ++q;
-                }
-            }
-
-            // ---- pass A.1: max of the raw logits over this thread's granules, and
-            // the first column holding it (granules are visited in column order)
-            float gmax[GPT];
-            float mv = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < GPT; ++i) {
-                const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
-                gmax[i] = (gl < g.n_my) ? granule_max_masked<BF16>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V)
-                                        : -INFINITY;
-                mv = fmaxf(mv, gmax[i]);
-            }
-            int midx = INT_MAX;
-            if (mv > -INFINITY) {
-                int fi = 0;
-#pragma unroll
-                for (int i = GPT - 1; i >= 0; --i)
-                    if (gmax[i] == mv) fi = i;
-                uint4 w = reg[0];
-#pragma unroll
-                for (int i = 1; i < GPT; ++i)
-                    if (i == fi) w = reg[i];
-                const int gl = (fi >> 1) * kChunkGranules + (fi & 1) * kConsumers + tid;
-                const int jg = (g.g_beg + gl) * EPG - g.lead;
-                float xv[EPG];
-                unpack<BF16>(w, xv);
-#pragma unroll
-                for (int l = EPG - 1; l >= 0; --l)
-                    if (xv[l] == mv && jg + l >= 0 && jg + l < p.V) midx = jg + l;
-            }
-
-            // ---- pass A.2: sum of exp(z - mz) (mz = z of this thread's max) and of z,
-            // four independent two-lane accumulators
-            const float mz = (mv > -INFINITY) ? softcap_z<SOFTCAP>(mv, T, k2).z : -INFINITY;
-            const uint64_t negmzL2 = pk(-mz * kLog2e, -mz * kLog2e);
-            uint64_t sa = pk(0.f, 0.f), sb2 = pk(0.f, 0.f), za = pk(0.f, 0.f), zb = pk(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < GPT; ++i) {
-                const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
+            for (int c = 0; c < nch; ++c) {
+                const int64_t qc = q + c;
+                const int slot = static_cast<int>(qc % kSlots);
+                bounded_wait<false, true>(full0 + 8u * slot,
+                                          static_cast<uint32_t>((qc / kSlots) & 1), abort, p.err);
+                const int gl = c * kChunkGranules + tid;
                 if (gl < g.n_my) {
-                    if (i & 1)
-                        granule_sums<BF16, SOFTCAP>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V, T, k2,
-                                                    negmzL2, sb2, zb);
-                    else
-                        granule_sums<BF16, SOFTCAP>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V, T, k2,
-                                                    negmzL2, sa, za);
-                }
-            }
-            // the label's z, from the thread that holds it
-            if (valid) {
-                const int gy = static_cast<int>((y + g.lead) / EPG) - g.g_beg;
-                const int ly = static_cast<int>((y + g.lead) % EPG);
-#pragma unroll
-                for (int i = 0; i < GPT; ++i) {
-                    const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
-                    if (gl == gy && gy < g.n_my) {
+                    const uint4 w =
+                        *reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes + 16 * tid);
+                    pass_a_granule<BF16, SOFTCAP>(a, w, (g.g_beg + gl) * EPG - g.lead, p.V, T, k2);
+                    if (gl == gy) {  // the label's logit
                         float xv[EPG];
-                        unpack<BF16>(reg[i], xv);
+                        unpack<BF16>(w, xv);
                         float xy = xv[0];
 #pragma unroll
                         for (int l = 1; l < EPG; ++l)
@@ -589,14 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
                 }
             }
             RowPart part = part_identity();
-            part.mx = mv;
-            part.idx = midx;
-            part.mz = mz;
+            part.mx = a.mv;
+            part.idx = a.midx;
+            part.mz = a.mz;
             {
-                const uint64_t s2 = add2(sa, sb2), z2 = add2(za, zb);
                 float s0, s1, z0, z1;
-                upk(s2, s0, s1);
-                upk(z2, z0, z1);
+                upk(a.s, s0, s1);
+                upk(a.sz, z0, z1);
                 part.s = s0 + s1;
                 part.sz = z0 + z1;
             }
@@ -644,52 +607,45 @@ __global__ void __launch_bounds__(kThreads, 1) rows_kernel(const Params p) {
                 p.argmax[r] = rp.idx;
             }
 
-            // ---- pass B: gradient from registers, in place
+            // ---- pass B: gradient from shared memory, stored over the logits
             unsigned char *grow = reinterpret_cast<unsigned char *>(g.gbase) + 16 * g.g_beg;
-            if (valid) {
-                const uint64_t lseL2 = pk(-lse * kLog2e, -lse * kLog2e);
-                const int gy = static_cast<int>((y + g.lead) / EPG) - g.g_beg;
-                const int ly = static_cast<int>((y + g.lead) % EPG);
-#pragma unroll
-                for (int i = 0; i < GPT; ++i) {
-                    const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
-                    if ((i >> 1) < nch && gl < g.n_my)
-                        pass_b_granule<BF16, SOFTCAP>(reg[i], (g.g_beg + gl) * EPG - g.lead, p.V,
-                                                      grow + 16 * gl, T, k2, lseL2, scale2, negc2,
-                                                      gl == gy ? ly : -1, scale, c_label);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < GPT; ++i) {
-                    const int gl = (i >> 1) * kChunkGranules + (i & 1) * kConsumers + tid;
-                    if ((i >> 1) < nch && gl < g.n_my)
-                        store_zero_granule<BF16>((g.g_beg + gl) * EPG - g.lead, p.V, grow + 16 * gl);
+            const uint64_t nlseL2 = pk(-lse * kLog2e, -lse * kLog2e);
+            for (int c = 0; c < nch; ++c) {
+                const int slot = static_cast<int>((q + c) % kSlots);
+                const int gl = c * kChunkGranules + tid;
+                if (gl < g.n_my) {
+                    const int jg = (g.g_beg + gl) * EPG - g.lead;
+                    if (valid) {
+                        const uint4 w =
+                            *reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes + 16 * tid);
+                        pass_b_granule<BF16, SOFTCAP>(w, jg, p.V, grow + 16 * gl, T, k2, nlseL2,
+                                                      scale2, negc2, gl == gy ? ly : -1, scale,
+                                                      c_label);
+                    } else {
+                        store_zero_granule<BF16>(jg, p.V, grow + 16 * gl);
+                    }
                 }
             }
+            // ---- the row's slots are free again
+            __syncwarp();
+            if (lane == 0) {
+                for (int c = 0; c < nch; ++c)
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                                     empty0 + 8u * static_cast<uint32_t>((q + c) % kSlots))
+                                 : "memory");
+            }
+            q += nch;
         }
-        (void)ELT;
     }
     ptx::griddep_launch_dependents();
     __syncthreads();
     ptx::cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
-// Kernel for the given element type, softcap and granules per thread
-// (defined in the per-GPT translation units).
-RowKernel rows_kernel_gpt4(bool bf16, bool softcap);
-RowKernel rows_kernel_gpt8(bool bf16, bool softcap);
-RowKernel rows_kernel_gpt12(bool bf16, bool softcap);
-RowKernel rows_kernel_gpt16(bool bf16, bool softcap);
+// The row kernel for the given softcap, per element type (ce_rows_bf16.cu,
+// ce_rows_f32.cu).
+RowKernel rows_kernel_bf16(bool softcap);
+RowKernel rows_kernel_f32(bool softcap);
 
 }  // namespace ce
 }  // namespace vlmce
-
-#define VLMCE_DEFINE_ROWS_KERNEL_GETTER(G)                                            \
-    namespace vlmce {                                                                 \
-    namespace ce {                                                                    \
-    RowKernel rows_kernel_gpt##G(bool bf16, bool softcap) {                           \
-        if (bf16) return softcap ? rows_kernel<true, true, G> : rows_kernel<true, false, G>; \
-        return softcap ? rows_kernel<false, true, G> : rows_kernel<false, false, G>;  \
-    }                                                                                 \
-    }                                                                                 \
-    }
