@@ -56,11 +56,20 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_sources_sha() -> str:
+    """sha256 over every CUDA source of the library (any change invalidates a capture)."""
+    import glob
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "vocabulary_lm_cross_gb300", "csrc", "*"))):
+        h.update(os.path.basename(path).encode())
+        h.update(open(path, "rb").read())
+    return h.hexdigest()
+
+
 def recorded_traffic(kernel: str, workload: str):
     """dram bytes per launch from the committed ncu summary, if the kernel
     source has not changed since the capture (else None)."""
-    src = os.path.join(ROOT, "vocabulary_lm_cross_gb300", "csrc", "ce.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = kernel_sources_sha()
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -353,6 +362,8 @@ def run_ours(args, w):
         return
 
     bytes_step = w.algorithmic_bytes
+    plan = v.describe_plan(w.N, V, x0.dtype, w.softcap)
+    kernel_name = "rows_kernel" if plan["kernel"] == "rows" else "split_kernel"
     value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kern_ms * 1e-3) / 1e9
@@ -373,12 +384,12 @@ def run_ours(args, w):
                    "vs_baseline_is": "value per GPU / 1510 GB/s = TE CE 0.711 ms on H100 "
                                      "(the pages' number, another machine: context)",
                    "device_status_ok": ok_status,
-                   "plan": v.describe_plan(V, x0.dtype, w.softcap)},
-        "roofline": {"bound": "hbm", "kernel": "ce_rows_kernel", "achieved": achieved,
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} (copy GB/s)", "unit": "GB/s",
                      "frac": achieved / peak, "kernel_ms": kern_ms,
                      "bytes_per_launch": bytes_step,
-                     "traffic": recorded_traffic("ce_rows", w.name)},
+                     "traffic": recorded_traffic(kernel_name, w.name)},
         "cpu_baseline": cpu,
         "e2e": {"value": bytes_step / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

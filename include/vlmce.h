@@ -62,17 +62,17 @@ typedef enum { VLMCE_MEAN = 1, VLMCE_SUM = 2 } vlmce_reduction;
 /* Bits of out_counts[3]: errors the kernels detected on the device. */
 #define VLMCE_DEVERR_TIMEOUT 1 /* an on-chip wait gave up; results are invalid */
 
-/* Largest vocabulary ce_fwd_bwd accepts, in elements, for the given dtype
- * (a row is kept on chip, in shared memory, across a cluster of up to 8 CTAs). */
+/* Largest vocabulary ce_fwd_bwd accepts, in elements, for the given dtype. */
 int64_t vlmce_ce_max_vocab(int32_t dtype);
 
-/* The launch plan ce_fwd_bwd uses for rows of V elements on the current device:
- * out[6] = {CTAs per cluster (row split), ring slots per row slice, granules
- * (16 B) per CTA, co-resident clusters, threads per CTA, shared-memory bytes
- * per CTA}.  aligned_rows: every row starts on a 16-byte boundary.  Returns a
+/* The launch plan ce_fwd_bwd uses for N rows of V elements on the current
+ * device: out[6] = {kernel (0: one CTA per row, 1: a cluster per row),
+ * CTAs per row, 16-byte granules per CTA, co-resident CTAs (kernel 0) or
+ * clusters (kernel 1), threads per CTA, dynamic shared-memory bytes per CTA}.
+ * aligned_rows: every row starts on a 16-byte boundary.  Returns a
  * vlmce_status. */
-int32_t vlmce_ce_describe_plan(int64_t V, int32_t dtype, float softcap, int32_t aligned_rows,
-                               int32_t *out);
+int32_t vlmce_ce_describe_plan(int64_t N, int64_t V, int32_t dtype, float softcap,
+                               int32_t aligned_rows, int32_t *out);
 
 /* Bytes of device workspace ce_fwd_bwd needs for N rows (16-byte aligned). */
 size_t vlmce_ce_workspace_bytes(int64_t N, int64_t V, int32_t dtype);

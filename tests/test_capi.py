@@ -91,7 +91,8 @@ def call(lib, **kw):
     (dict(grad_scale=math.inf), capi.ERR_INVALID_ARG),
     (dict(reduction=0), capi.ERR_INVALID_ARG),
     (dict(reduction=3), capi.ERR_INVALID_ARG),
-    (dict(V=10_000_000, row_stride=10_000_000), capi.ERR_TOO_LARGE),
+    (dict(V=(1 << 28) + 1, row_stride=(1 << 28) + 1), capi.ERR_TOO_LARGE),
+    (dict(N=(1 << 31), row_stride=100), capi.ERR_TOO_LARGE),
     (dict(ws=None), capi.ERR_WORKSPACE_TOO_SMALL),
     (dict(ws_bytes=16), capi.ERR_WORKSPACE_TOO_SMALL),
     (dict(ws=P + 8), capi.ERR_MISALIGNED),

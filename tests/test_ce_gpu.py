@@ -36,14 +36,14 @@ def got_rows(x: torch.Tensor, dtype: str) -> np.ndarray:
     return host_rows(x, dtype)
 
 
-def run_and_check(w: CEWorkload, *, full_grad: bool = True, sample_rows=None, plan=None,
+def run_and_check(w: CEWorkload, *, full_grad: bool = True, sample_rows=None, env=None,
                   monkeypatch=None):
     x, lab = make_ce_inputs(w, device=DEV)
     V = w.V
     xin = host_rows(x, w.dtype)
     labh = lab.cpu().numpy()
-    if plan is not None:
-        monkeypatch.setenv("VLMCE_CE_PLAN", plan)
+    for key, val in (env or {}).items():
+        monkeypatch.setenv(key, val)
     res = v.ce_fwd_bwd(x[:, :V], lab, ignore_index=IGNORE_INDEX, label_smoothing=w.label_smoothing,
                        softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale)
     torch.cuda.synchronize()
@@ -95,31 +95,44 @@ def test_small_grid_contiguous(dtype, V):
 @pytest.mark.parametrize("V,stride", [(5, 6), (129, 131), (1000, 1003), (4097, 4100),
                                       (30011, 30016)])
 @pytest.mark.parametrize("T,eps,red", [(0.0, 0.0, "mean"), (30.0, 0.1, "sum"), (5.0, 0.3, "mean")])
-def test_small_grid_strided_unaligned_rows(dtype, V, stride, T, eps, red):
+@pytest.mark.parametrize("path", ["rows", "split"])
+def test_small_grid_strided_unaligned_rows(dtype, V, stride, T, eps, red, path, monkeypatch):
     run_and_check(small(29, V, dtype, stride=stride, eps=eps, T=T, reduction=red, gs=0.37,
-                        sigma=8.0 if T else 3.0))
+                        sigma=8.0 if T else 3.0), env={"VLMCE_CE_PATH": path},
+                  monkeypatch=monkeypatch)
 
 
-@pytest.mark.parametrize("plan", ["1", "2", "3", "5", "8"])
-def test_every_cluster_shape_agrees(plan, monkeypatch):
+@pytest.mark.parametrize("k", ["1", "2", "3", "5", "8"])
+def test_every_cluster_shape_agrees(k, monkeypatch):
     w = small(23, 20000, "bf16", stride=20003, eps=0.1, T=30.0, boost=4.0, dup=0.2)
-    run_and_check(w, plan=plan, monkeypatch=monkeypatch)
+    run_and_check(w, env={"VLMCE_CE_PATH": "split", "VLMCE_CE_SPLIT": k}, monkeypatch=monkeypatch)
+
+
+@pytest.mark.parametrize("path", ["rows", "split"])
+def test_both_kernels_on_the_same_rows(path, monkeypatch):
+    w = small(150, 131072, "bf16", eps=0.1, boost=4.0, dup=0.05)
+    run_and_check(w, full_grad=False, sample_rows=[0, 1, 75, 148, 149],
+                  env={"VLMCE_CE_PATH": path}, monkeypatch=monkeypatch)
 
 
 def test_plans_of_the_benchmarked_workloads():
     for name, w in CE_WORKLOADS.items():
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-        pl = v.describe_plan(w.V, dt, w.softcap)
-        assert pl["cluster"] * pl["granules_per_cta"] * (8 if w.dtype == "bf16" else 4) >= w.V
-        assert pl["clusters"] >= 1, (name, pl)
+        pl = v.describe_plan(w.N, w.V, dt, w.softcap)
+        assert pl["ctas_per_row"] * pl["granules_per_cta"] * (8 if w.dtype == "bf16" else 4) >= w.V
+        assert pl["kernel"] == "rows" and pl["resident"] >= 1, (name, pl)
         print(name, pl)
 
 
-def test_largest_vocabulary():
-    Vmax = v.max_vocab(torch.bfloat16)
-    run_and_check(small(3, Vmax, "bf16", eps=0.1, T=30.0, ignore=0.0))
-    Vmax32 = v.max_vocab(torch.float32)
-    run_and_check(small(2, Vmax32, "f32", eps=0.0, ignore=0.0))
+def test_widest_rows_of_each_kernel(monkeypatch):
+    # the V-split kernel: 8 CTAs x 13 ring slots x 480 granules, rows not 16-byte aligned
+    Vs = 8 * 13 * 480 * 8 - 7
+    run_and_check(small(3, Vs, "bf16", eps=0.1, T=30.0, ignore=0.0),
+                  env={"VLMCE_CE_PATH": "split"}, monkeypatch=monkeypatch)
+    # the row kernel: a 2M-wide row (no width limit below vlmce_ce_max_vocab)
+    monkeypatch.setenv("VLMCE_CE_PATH", "rows")
+    run_and_check(small(2, (1 << 21) + 3, "bf16", eps=0.1, ignore=0.0))
+    run_and_check(small(2, (1 << 20) + 1, "f32", eps=0.0, ignore=0.0))
 
 
 def test_no_rows():

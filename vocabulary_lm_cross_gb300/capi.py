@@ -43,7 +43,7 @@ SIGNATURES = {
     "vlmce_ce_max_vocab": (_i64, [_i32]),
     "vlmce_profile_events": (None, [_vp, _vp]),
     "vlmce_ce_workspace_bytes": (_sz, [_i64, _i64, _i32]),
-    "vlmce_ce_describe_plan": (_i32, [_i64, _i32, _f32, _i32, _vp]),
+    "vlmce_ce_describe_plan": (_i32, [_i64, _i64, _i32, _f32, _i32, _vp]),
     "ce_fwd_bwd": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32, _vp, _vp,
                           _vp, _vp, _vp, _sz, _vp]),
 }

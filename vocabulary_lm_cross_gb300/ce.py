@@ -29,17 +29,18 @@ def workspace_bytes(N: int, V: int, dtype: torch.dtype) -> int:
     return int(capi.lib().vlmce_ce_workspace_bytes(N, V, _DTYPES[dtype]))
 
 
-def describe_plan(V: int, dtype: torch.dtype, softcap: float = 0.0,
+def describe_plan(N: int, V: int, dtype: torch.dtype, softcap: float = 0.0,
                   aligned_rows: bool = True) -> dict:
-    """The launch plan of the row kernel for rows of V elements on the current device."""
+    """The launch plan ce_fwd_bwd uses for N rows of V elements on the current device."""
     import ctypes
     out = (ctypes.c_int32 * 6)()
-    st = capi.lib().vlmce_ce_describe_plan(V, _DTYPES[dtype], float(softcap), int(aligned_rows),
-                                           ctypes.cast(out, ctypes.c_void_p))
+    st = capi.lib().vlmce_ce_describe_plan(N, V, _DTYPES[dtype], float(softcap),
+                                           int(aligned_rows), ctypes.cast(out, ctypes.c_void_p))
     capi.check(st, "vlmce_ce_describe_plan")
-    keys = ("cluster", "slots_per_slice", "granules_per_cta", "clusters", "threads",
-            "smem_bytes")
-    return dict(zip(keys, list(out)))
+    keys = ("kernel", "ctas_per_row", "granules_per_cta", "resident", "threads", "smem_bytes")
+    d = dict(zip(keys, list(out)))
+    d["kernel"] = ("rows", "split")[d["kernel"]]
+    return d
 
 
 def max_vocab(dtype: torch.dtype) -> int:

@@ -10,21 +10,25 @@
 //
 // Three launches on the caller's stream:
 //   1. count_kernel    -- label census (n_valid for the mean, bad labels).
-//   2. rows_kernel     -- the row kernel (ce_rows.cuh): clusters of k CTAs,
-//      two CTAs per SM, producer warp streaming row slices into a
-//      shared-memory ring.
+//   2. the row work, by one of two kernels:
+//      rows::kernel  (ce_rows.cuh)  -- one CTA per row, two passes, the second
+//                    served by L2; the default: every SM busy once N >= 304;
+//      split::split_kernel (ce_split.cuh) -- a thread-block cluster per row,
+//                    the row split over its CTAs in shared memory and merged
+//                    through distributed shared memory; for few, wide rows,
+//                    where one CTA per row would leave most SMs idle.
 //   3. finalize_kernel -- fixed-order fp64 reduction of the per-row losses
 //      and correct-prediction count.
-// Kernels 2 and 3 use programmatic dependent launch so that their prologues
-// overlap the previous kernel's tail (the row kernel's producer starts its
-// bulk copies before the census has finished).  No floating-point atomics:
-// results are bit-reproducible.
+// Kernels 2 and 3 use programmatic dependent launch, so that their prologues
+// overlap the previous kernel's tail.  No floating-point atomics: results are
+// bit-reproducible.
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <set>
@@ -32,6 +36,7 @@
 #include <tuple>
 
 #include "ce_rows.cuh"
+#include "ce_split.cuh"
 #include "host_util.h"
 #include "ptx.cuh"
 #include "vlmce.h"
@@ -146,6 +151,7 @@ struct Workspace {
 };
 
 constexpr int64_t kWsHeader = 256;
+constexpr int64_t kMaxVocab = int64_t(1) << 28;
 
 size_t workspace_bytes(int64_t N) {
     return static_cast<size_t>(kWsHeader + round_up(4 * N, 256) + round_up(8 * N, 256));
@@ -161,35 +167,41 @@ Workspace carve(void *ws, int64_t N) {
     return w;
 }
 
-struct Plan {
-    int k = 0;             // CTAs per cluster (row split)
-    int gran_per_cta = 0;  // granules of a row per CTA
-    int max_clusters = 0;  // co-resident clusters (persistent grid)
-    RowKernel kernel = nullptr;
-};
-
-// Granules of a row: exact when every row starts on a 16-byte boundary, else
-// the worst case over the possible offsets of its first element.
+// Granules (16 B) of a row: exact when every row starts on a 16-byte boundary,
+// else the worst case over the possible offsets of its first element.
 int64_t row_granules(bool bf16, int64_t V, bool aligned_rows) {
     const int64_t epg = bf16 ? 8 : 4;
     return aligned_rows ? (V + epg - 1) / epg : (epg - 1 + V + epg - 1) / epg;
 }
 
+bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
+    return aligned(logits, 16) && ((row_stride * elt) % 16) == 0;
+}
+
+// ---- V-split plans (cluster per row)
+
+struct SplitPlan {
+    int k = 0;             // CTAs per cluster (row split)
+    int gran_per_cta = 0;  // granules of a row per CTA
+    int max_clusters = 0;  // co-resident clusters (persistent grid)
+    split::SplitKernel kernel = nullptr;
+};
+
 // Smallest cluster whose per-CTA slice fits kPreferredChunks ring slots (two
 // rows in flight per CTA); past 8 CTAs, slices of up to the whole ring.
-// Tuning override: environment VLMCE_CE_PLAN = "k".
-bool shape_plan(int64_t G, Plan *pl) {
+// Tuning override: environment VLMCE_CE_SPLIT = "k".
+bool shape_split(int64_t G, SplitPlan *pl) {
     int fk = 0;
-    const char *e = getenv("VLMCE_CE_PLAN");
+    const char *e = getenv("VLMCE_CE_SPLIT");
     if (e && *e) {
         int a = 0;
-        if (sscanf(e, "%d", &a) == 1 && a >= 1 && a <= kMaxCluster) fk = a;
+        if (sscanf(e, "%d", &a) == 1 && a >= 1 && a <= split::kMaxCluster) fk = a;
     }
-    const int64_t pref = static_cast<int64_t>(kPreferredChunks) * kChunkGranules;
-    const int64_t cap = static_cast<int64_t>(kSlots) * kChunkGranules;
+    const int64_t pref = static_cast<int64_t>(split::kPreferredChunks) * split::kChunkGranules;
+    const int64_t cap = static_cast<int64_t>(split::kSlots) * split::kChunkGranules;
     int k = fk ? fk : static_cast<int>((G + pref - 1) / pref);
     if (k < 1) k = 1;
-    if (k > kMaxCluster) k = kMaxCluster;
+    if (k > split::kMaxCluster) k = split::kMaxCluster;
     const int64_t gc = (G + k - 1) / k;
     if (gc > cap) return false;
     pl->k = k;
@@ -198,11 +210,12 @@ bool shape_plan(int64_t G, Plan *pl) {
 }
 
 std::mutex g_mu;
-std::map<std::tuple<int, bool, bool, int64_t, std::string>, Plan> g_plans;
-std::set<std::pair<int, RowKernel>> g_attr_set;
+std::map<std::tuple<int, bool, bool, int64_t, std::string>, SplitPlan> g_plans;
+std::set<std::pair<int, split::SplitKernel>> g_attr_set;
 
-vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t G, Plan *out) {
-    const char *e = getenv("VLMCE_CE_PLAN");
+vlmce_status get_split_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t G,
+                            SplitPlan *out) {
+    const char *e = getenv("VLMCE_CE_SPLIT");
     const auto key = std::make_tuple(d.device, bf16, softcap, G, std::string(e ? e : ""));
     std::lock_guard<std::mutex> lk(g_mu);
     auto itp = g_plans.find(key);
@@ -210,21 +223,21 @@ vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t G, P
         *out = itp->second;
         return VLMCE_OK;
     }
-    Plan pl;
-    if (!shape_plan(G, &pl)) return VLMCE_ERR_TOO_LARGE;
-    if (d.smem_optin < kSmemBytes) return VLMCE_ERR_UNSUPPORTED_DEVICE;
-    pl.kernel = bf16 ? rows_kernel_bf16(softcap) : rows_kernel_f32(softcap);
+    SplitPlan pl;
+    if (!shape_split(G, &pl)) return VLMCE_ERR_TOO_LARGE;
+    if (d.smem_optin < split::kSmemBytes) return VLMCE_ERR_UNSUPPORTED_DEVICE;
+    pl.kernel = bf16 ? split::split_kernel_bf16(softcap) : split::split_kernel_f32(softcap);
     if (!g_attr_set.count({d.device, pl.kernel})) {
         if (record_cuda(cudaFuncSetAttribute(pl.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes),
-                        "cudaFuncSetAttribute(rows_kernel)") != cudaSuccess)
+                                             split::kSmemBytes),
+                        "cudaFuncSetAttribute(split_kernel)") != cudaSuccess)
             return VLMCE_ERR_CUDA;
         g_attr_set.insert({d.device, pl.kernel});
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.k * d.sm_count, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(split::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = split::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = pl.k;
@@ -234,7 +247,7 @@ vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t G, P
     cfg.numAttrs = 1;
     int ncl = 0;
     if (record_cuda(cudaOccupancyMaxActiveClusters(&ncl, pl.kernel, &cfg),
-                    "cudaOccupancyMaxActiveClusters(rows_kernel)") != cudaSuccess)
+                    "cudaOccupancyMaxActiveClusters(split_kernel)") != cudaSuccess)
         return VLMCE_ERR_CUDA;
     if (ncl < 1) return VLMCE_ERR_TOO_LARGE;
     pl.max_clusters = ncl;
@@ -243,12 +256,22 @@ vlmce_status get_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_t G, P
     return VLMCE_OK;
 }
 
+// Which kernel does the row work.  The row kernel keeps every SM busy once
+// N >= 2 x SMs; with fewer rows the V-split kernel spreads each row over a
+// cluster instead, when the row is wide enough to be worth splitting and fits
+// the clusters' shared memory.  Override: environment VLMCE_CE_PATH = "rows"
+// or "split".
+bool use_split(int64_t N, int64_t G, const DeviceInfo &d) {
+    const char *e = getenv("VLMCE_CE_PATH");
+    const int64_t cap = static_cast<int64_t>(split::kMaxCluster) * split::kSlots *
+                        split::kChunkGranules;
+    if (e && strcmp(e, "split") == 0) return G <= cap;
+    if (e && strcmp(e, "rows") == 0) return false;
+    return N < d.sm_count && G >= 4 * split::kChunkGranules && G <= cap;
+}
+
 thread_local cudaEvent_t t_prof_begin = nullptr;
 thread_local cudaEvent_t t_prof_end = nullptr;
-
-bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
-    return aligned(logits, 16) && ((row_stride * elt) % 16) == 0;
-}
 
 }  // namespace
 }  // namespace ce
@@ -264,28 +287,36 @@ extern "C" void vlmce_profile_events(void *ev_begin, void *ev_end) {
 
 extern "C" int64_t vlmce_ce_max_vocab(int32_t dtype) {
     if (dtype != VLMCE_F32 && dtype != VLMCE_BF16) return 0;
-    // kMaxCluster CTAs x a whole ring of slots each, worst-case row offset.
-    const int64_t epg = dtype == VLMCE_BF16 ? 8 : 4;
-    const int64_t G = static_cast<int64_t>(kMaxCluster) * kSlots * kChunkGranules;
-    return G * epg - (epg - 1);
+    return kMaxVocab;
 }
 
-extern "C" int32_t vlmce_ce_describe_plan(int64_t V, int32_t dtype, float softcap,
+extern "C" int32_t vlmce_ce_describe_plan(int64_t N, int64_t V, int32_t dtype, float softcap,
                                           int32_t aligned_rows, int32_t *out) {
-    if (!out || V < 1 || (dtype != VLMCE_F32 && dtype != VLMCE_BF16)) return VLMCE_ERR_INVALID_ARG;
+    if (!out || N < 0 || V < 1 || V > kMaxVocab || (dtype != VLMCE_F32 && dtype != VLMCE_BF16))
+        return VLMCE_ERR_INVALID_ARG;
     DeviceInfo dev;
     vlmce_status st = current_device(&dev);
     if (st != VLMCE_OK) return st;
-    Plan pl;
-    st = get_plan(dev, dtype == VLMCE_BF16, softcap > 0.f,
-                  row_granules(dtype == VLMCE_BF16, V, aligned_rows != 0), &pl);
-    if (st != VLMCE_OK) return st;
-    out[0] = pl.k;
-    out[1] = (pl.gran_per_cta + kChunkGranules - 1) / kChunkGranules;
-    out[2] = pl.gran_per_cta;
-    out[3] = pl.max_clusters;
-    out[4] = kThreads;
-    out[5] = kSmemBytes;
+    const bool bf16 = dtype == VLMCE_BF16;
+    const int64_t G = row_granules(bf16, V, aligned_rows != 0);
+    if (use_split(N, G, dev)) {
+        SplitPlan pl;
+        st = get_split_plan(dev, bf16, softcap > 0.f, G, &pl);
+        if (st != VLMCE_OK) return st;
+        out[0] = 1;
+        out[1] = pl.k;
+        out[2] = pl.gran_per_cta;
+        out[3] = pl.max_clusters;
+        out[4] = split::kThreads;
+        out[5] = split::kSmemBytes;
+    } else {
+        out[0] = 0;
+        out[1] = 1;
+        out[2] = static_cast<int32_t>(G);
+        out[3] = 2 * dev.sm_count;
+        out[4] = rows::kThreads;
+        out[5] = 0;
+    }
     return VLMCE_OK;
 }
 
@@ -310,7 +341,7 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
     if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
     if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
     if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
-    if (V > vlmce_ce_max_vocab(dtype)) return VLMCE_ERR_TOO_LARGE;
+    if (V > kMaxVocab || N > INT_MAX) return VLMCE_ERR_TOO_LARGE;
     const int64_t elt = dtype == VLMCE_BF16 ? 2 : 4;
     if (N > 0 && row_stride > (INT64_MAX / elt) / N) return VLMCE_ERR_TOO_LARGE;
     if (!workspace || workspace_bytes_given < workspace_bytes(N)) return VLMCE_ERR_WORKSPACE_TOO_SMALL;
@@ -328,10 +359,11 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
 
     const bool bf16 = dtype == VLMCE_BF16;
     const bool capped = softcap > 0.f;
-    Plan pl;
-    if (N > 0) {
-        st = get_plan(dev, bf16, capped, row_granules(bf16, V, rows_aligned(logits, row_stride, elt)),
-                      &pl);
+    const int64_t G = row_granules(bf16, V, rows_aligned(logits, row_stride, elt));
+    const bool split_path = N > 0 && use_split(N, G, dev);
+    SplitPlan pl;
+    if (split_path) {
+        st = get_split_plan(dev, bf16, capped, G, &pl);
         if (st != VLMCE_OK) return st;
     }
 
@@ -349,40 +381,66 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
     attr[0].val.programmaticStreamSerializationAllowed = 1;
 
     if (N > 0) {
-        Params p;
-        p.logits = static_cast<unsigned char *>(logits);
-        p.labels = labels;
-        p.N = N;
-        p.V = static_cast<int>(V);
-        p.stride_bytes = row_stride * elt;
-        p.ignore_index = ignore_index;
-        p.eps = label_smoothing;
-        p.softcap = softcap;
-        p.grad_scale = grad_scale;
-        p.reduction = reduction;
-        p.loss = loss;
-        p.argmax = amax;
-        p.counts = w.counts;
-        p.err = w.err;
-        p.gran_per_cta = pl.gran_per_cta;
-
-        const int64_t ncl = N < pl.max_clusters ? N : pl.max_clusters;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(ncl * pl.k), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cfg.stream = cs;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = pl.k;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 2;
         cudaEvent_t eb = t_prof_begin, ee = t_prof_end;
         t_prof_begin = t_prof_end = nullptr;
         if (eb && (st = launch_status(cudaEventRecord(eb, cs), "cudaEventRecord")) != VLMCE_OK)
             return st;
-        st = launch_status(cudaLaunchKernelEx(&cfg, pl.kernel, p), "rows_kernel");
+        if (split_path) {
+            split::SplitParams p;
+            p.logits = static_cast<unsigned char *>(logits);
+            p.labels = labels;
+            p.N = N;
+            p.V = static_cast<int>(V);
+            p.stride_bytes = row_stride * elt;
+            p.ignore_index = ignore_index;
+            p.eps = label_smoothing;
+            p.softcap = softcap;
+            p.grad_scale = grad_scale;
+            p.reduction = reduction;
+            p.loss = loss;
+            p.argmax = amax;
+            p.counts = w.counts;
+            p.err = w.err;
+            p.gran_per_cta = pl.gran_per_cta;
+            const int64_t ncl = N < pl.max_clusters ? N : pl.max_clusters;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(ncl * pl.k), 1, 1);
+            cfg.blockDim = dim3(split::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = split::kSmemBytes;
+            cfg.stream = cs;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = pl.k;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            st = launch_status(cudaLaunchKernelEx(&cfg, pl.kernel, p), "split_kernel");
+        } else {
+            rows::Params p;
+            p.logits = static_cast<unsigned char *>(logits);
+            p.labels = labels;
+            p.V = static_cast<int>(V);
+            p.stride_bytes = row_stride * elt;
+            p.ignore_index = ignore_index;
+            p.eps = label_smoothing;
+            p.softcap = softcap;
+            p.grad_scale = grad_scale;
+            p.reduction = reduction;
+            p.loss = loss;
+            p.argmax = amax;
+            p.counts = w.counts;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(N), 1, 1);
+            cfg.blockDim = dim3(rows::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = cs;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            st = launch_status(cudaLaunchKernelEx(&cfg, bf16 ? rows::kernel_bf16(capped)
+                                                             : rows::kernel_f32(capped),
+                                                  p),
+                               "rows_kernel");
+        }
         if (st != VLMCE_OK) return st;
         if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
             return st;

@@ -1,0 +1,177 @@
+// ce_common.cuh -- device helpers shared by the cross-entropy kernels: row
+// statistics and their merge, the softcap, packed fp32x2 arithmetic, bf16/fp32
+// granule (16-byte) unpacking, packing and stores.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "vlmce.h"
+
+namespace vlmce {
+namespace ce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One CTA's (or warp's, or thread's) statistics of one row.
+struct __align__(16) RowPart {
+    float mx;   // max of the raw logits x
+    int idx;    // smallest column holding mx
+    float mz;   // reference maximum (z space) of s
+    float s;    // sum exp(z - mz)
+    float sz;   // sum z
+    float zy;   // z at the label column (only its owner adds it)
+    float pad0, pad1;
+};
+
+template <bool BF16>
+struct Elem {
+    static constexpr int kBytes = BF16 ? 2 : 4;
+    static constexpr int kPerGranule = 16 / kBytes;
+};
+
+// ----------------------------------------------------------- packed fp32x2
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t ex2x2(uint64_t a) {
+    float x, y;
+    upk(a, x, y);
+    return pk(ptx::ex2(x), ptx::ex2(y));
+}
+
+__device__ __forceinline__ RowPart part_identity() {
+    RowPart p;
+    p.mx = -INFINITY;
+    p.idx = INT_MAX;
+    p.mz = -INFINITY;
+    p.s = 0.f;
+    p.sz = 0.f;
+    p.zy = 0.f;
+    p.pad0 = p.pad1 = 0.f;
+    return p;
+}
+
+// a <- merge(a, b).  Commutative, so a butterfly leaves every lane identical.
+__device__ __forceinline__ void part_merge(RowPart &a, float mx, int idx, float mz, float s,
+                                           float sz, float zy) {
+    if (mx > a.mx || (mx == a.mx && idx < a.idx)) {
+        a.mx = mx;
+        a.idx = idx;
+    }
+    const float M = fmaxf(a.mz, mz);
+    const float u = (a.s == 0.f) ? 0.f : a.s * ptx::ex2((a.mz - M) * kLog2e);
+    const float v = (s == 0.f) ? 0.f : s * ptx::ex2((mz - M) * kLog2e);
+    a.mz = M;
+    a.s = u + v;
+    a.sz = a.sz + sz;
+    a.zy = a.zy + zy;
+}
+
+__device__ __forceinline__ void warp_allreduce(RowPart &p) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float mx = __shfl_xor_sync(0xffffffffu, p.mx, off);
+        const int idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
+        const float mz = __shfl_xor_sync(0xffffffffu, p.mz, off);
+        const float s = __shfl_xor_sync(0xffffffffu, p.s, off);
+        const float sz = __shfl_xor_sync(0xffffffffu, p.sz, off);
+        const float zy = __shfl_xor_sync(0xffffffffu, p.zy, off);
+        part_merge(p, mx, idx, mz, s, sz, zy);
+    }
+}
+
+// z = T tanh(x/T) and dz/dx = 1 - tanh^2, from tanh(u) = sign(u) (1 - a) / (1 + a),
+// a = exp(-2|u|), so that 1 - tanh^2 = 4 a / (1 + a)^2 needs no extra MUFU op.
+struct Capped {
+    float z, dz;
+};
+template <bool SOFTCAP>
+__device__ __forceinline__ Capped softcap_z(float x, float T, float neg2_log2e_over_T) {
+    if constexpr (!SOFTCAP) {
+        return {x, 1.f};
+    } else {
+        const float a = ptx::ex2(fabsf(x) * neg2_log2e_over_T);
+        const float r = ptx::rcp(1.f + a);
+        const float t = copysignf((1.f - a) * r, x);
+        return {T * t, 4.f * a * r * r};
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void unpack(const uint4 w, float (&x)[Elem<BF16>::kPerGranule]) {
+    if constexpr (BF16) {
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x[2 * q] = __uint_as_float(u[q] << 16);
+            x[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(w.x);
+        x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z);
+        x[3] = __uint_as_float(w.w);
+    }
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
+    __nv_bfloat162 r;
+    memcpy(&r, &u, 4);
+    return r;
+}
+
+// Max of a full granule (packed bf16x2 max for bf16).
+template <bool BF16>
+__device__ __forceinline__ float granule_max(const uint4 w) {
+    if constexpr (BF16) {
+        const __nv_bfloat162 a = __hmax2(as_bf162(w.x), as_bf162(w.y));
+        const __nv_bfloat162 b = __hmax2(as_bf162(w.z), as_bf162(w.w));
+        const __nv_bfloat162 c = __hmax2(a, b);
+        return fmaxf(__low2float(c), __high2float(c));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                     fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    return u;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_elem(unsigned char *p, float g) {
+    if constexpr (BF16) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(g);
+        uint16_t u;
+        memcpy(&u, &b, 2);
+        *reinterpret_cast<uint16_t *>(p) = u;
+    } else {
+        *reinterpret_cast<float *>(p) = g;
+    }
+}
+
+}  // namespace ce
+}  // namespace vlmce

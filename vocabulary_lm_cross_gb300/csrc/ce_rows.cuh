@@ -1,80 +1,32 @@
-// ce_rows.cuh -- the cross-entropy row kernel (forward + backward, in place).
+// ce_rows.cuh -- the cross-entropy row kernel (default path): one CTA of 1024
+// threads per row, two CTAs per SM (64 warps: every SM is fully occupied).
 //
-// One thread-block cluster of k CTAs owns one row at a time; CTA c of the
-// cluster owns the c-th 1/k of the row's 16-byte granules (its "slice").
-// Two CTAs share each SM (16 warps each), so one CTA's per-row exchange
-// bubble is filled by the other's arithmetic.
-//
-// Warp 15 of each CTA is a producer: one lane streams the slices of the
-// cluster's rows, in order, through a ring of 7.5 KB shared-memory slots
-// (480 granules: one per consumer thread) with bulk (TMA) copies, as far
-// ahead as free slots allow.  A row's slots stay resident until its gradient
-// has been written, then the 15 consumer warps release them.  Per row:
-//   pass A: one pass over the slice in shared memory: max and first argmax of
-//           the raw logits, online sum of exp(z - m) and sum of z (packed
-//           f32x2 arithmetic);
-//   merge:  warp shuffles; then every consumer warp writes its partial into
-//           every CTA of the cluster through distributed shared memory and
-//           release-arrives on each CTA's row barrier; after the acquire-wait
-//           every warp merges the k x 15 partials in the same fixed order, so
-//           every CTA holds the same lse;
-//   pass B: gradient scale (p - q) (1 - t^2), rounded to the storage dtype,
-//           16-byte streaming stores over the logits.
-// Each byte of the row crosses HBM once in and once out.
+//   pass 1: one thread asks the bulk-copy engine to prefetch the whole row
+//           into L2; all threads stream it in 16-byte granules: max and first
+//           argmax of the raw logits, online sum of exp(z - m) and sum of z;
+//   merge:  warp shuffles, then the 32 warp partials (fixed order);
+//   pass 2: read the row again -- it is still in the 129 MB L2, since at most
+//           2 x 152 rows (78 MB for 256 KB rows) are in flight -- and store the
+//           gradient scale (p - q) (1 - t^2), rounded to the storage dtype,
+//           with 16-byte evict-first stores over the logits.
+// HBM sees one read and one write of every byte; the second read is served by
+// L2.  The label census of the call is only needed by pass 2, so the kernel
+// waits for it (programmatic dependent launch) after pass 1.
 #pragma once
 
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-
-#include <climits>
-#include <cstdint>
-
-#include "ptx.cuh"
-#include "vlmce.h"
+#include "ce_common.cuh"
 
 namespace vlmce {
 namespace ce {
+namespace rows {
 
-constexpr int kConsumerWarps = 15;
-constexpr int kConsumers = 32 * kConsumerWarps;   // 480 consumer threads
-constexpr int kThreads = kConsumers + 32;         // + 1 producer warp
-constexpr int kCtasPerSm = 2;
-constexpr int kChunkGranules = kConsumers;        // one granule per consumer thread
-constexpr int kChunkBytes = 16 * kChunkGranules;  // 7.5 KB per slot
-constexpr int kSlots = 13;
-constexpr int kCtlBytes = 8192;
-constexpr int kSmemBytes = kCtlBytes + kSlots * kChunkBytes;  // 108,032 B: two CTAs per SM
-constexpr int kMaxCluster = 8;
-constexpr int kPreferredChunks = 6;  // slices of <= 6 slots keep two rows in the ring
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per on-chip wait
-
-// One CTA's (or warp's, or thread's) statistics of one row.
-struct __align__(16) RowPart {
-    float mx;   // max of the raw logits x
-    int idx;    // smallest column holding mx
-    float mz;   // reference maximum (z space) of s
-    float s;    // sum exp(z - mz)
-    float sz;   // sum z
-    float zy;   // z at the label column (only its owner adds it)
-    float pad0, pad1;
-};
-
-struct Ctl {
-    unsigned long long full[kSlots];   // slot landed (transaction bytes)
-    unsigned long long empty[kSlots];  // slot released by the 15 consumer warps
-    unsigned long long stat[2];        // all partials of a row arrived (k x 15 arrivals)
-    // Row partials of every consumer warp of every CTA of the cluster, written
-    // by their owners through distributed shared memory; indexed by row parity.
-    RowPart xslot[2][kMaxCluster * kConsumerWarps];
-    int abort;                         // an on-chip wait gave up
-};
-static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kPrefetchBytes = 65536;  // bytes per L2 bulk-prefetch instruction
 
 struct Params {
     unsigned char *logits;
     const int64_t *labels;
-    int64_t N;
     int V;
     int64_t stride_bytes;
     int64_t ignore_index;
@@ -85,228 +37,30 @@ struct Params {
     float *loss;
     int64_t *argmax;
     const int64_t *counts;  // [0] n_valid (written by the count kernel)
-    int *err;
-    int gran_per_cta;       // granules of a row owned by one CTA (<= kSlots * kChunkGranules)
 };
 
-using RowKernel = void (*)(Params);
+using Kernel = void (*)(Params);
 
-template <bool BF16>
-struct Elem {
-    static constexpr int kBytes = BF16 ? 2 : 4;
-    static constexpr int kPerGranule = 16 / kBytes;
-};
-
-// ----------------------------------------------------------- packed fp32x2
-__device__ __forceinline__ uint64_t pk(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void upk(uint64_t r, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t ex2x2(uint64_t a) {
-    float x, y;
-    upk(a, x, y);
-    return pk(ptx::ex2(x), ptx::ex2(y));
+__device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
-__device__ __forceinline__ RowPart part_identity() {
-    RowPart p;
-    p.mx = -INFINITY;
-    p.idx = INT_MAX;
-    p.mz = -INFINITY;
-    p.s = 0.f;
-    p.sz = 0.f;
-    p.zy = 0.f;
-    p.pad0 = p.pad1 = 0.f;
-    return p;
-}
-
-// a <- merge(a, b).  Commutative, so a butterfly leaves every lane identical.
-__device__ __forceinline__ void part_merge(RowPart &a, float mx, int idx, float mz, float s,
-                                           float sz, float zy) {
-    if (mx > a.mx || (mx == a.mx && idx < a.idx)) {
-        a.mx = mx;
-        a.idx = idx;
-    }
-    const float M = fmaxf(a.mz, mz);
-    const float u = (a.s == 0.f) ? 0.f : a.s * ptx::ex2((a.mz - M) * kLog2e);
-    const float v = (s == 0.f) ? 0.f : s * ptx::ex2((mz - M) * kLog2e);
-    a.mz = M;
-    a.s = u + v;
-    a.sz = a.sz + sz;
-    a.zy = a.zy + zy;
-}
-
-__device__ __forceinline__ void warp_allreduce(RowPart &p) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float mx = __shfl_xor_sync(0xffffffffu, p.mx, off);
-        const int idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
-        const float mz = __shfl_xor_sync(0xffffffffu, p.mz, off);
-        const float s = __shfl_xor_sync(0xffffffffu, p.s, off);
-        const float sz = __shfl_xor_sync(0xffffffffu, p.sz, off);
-        const float zy = __shfl_xor_sync(0xffffffffu, p.zy, off);
-        part_merge(p, mx, idx, mz, s, sz, zy);
-    }
-}
-
-// z = T tanh(x/T) and dz/dx = 1 - tanh^2, from tanh(u) = sign(u) (1 - a) / (1 + a),
-// a = exp(-2|u|), so that 1 - tanh^2 = 4 a / (1 + a)^2 needs no extra MUFU op.
-struct Capped {
-    float z, dz;
-};
-template <bool SOFTCAP>
-__device__ __forceinline__ Capped softcap_z(float x, float T, float neg2_log2e_over_T) {
-    if constexpr (!SOFTCAP) {
-        return {x, 1.f};
-    } else {
-        const float a = ptx::ex2(fabsf(x) * neg2_log2e_over_T);
-        const float r = ptx::rcp(1.f + a);
-        const float t = copysignf((1.f - a) * r, x);
-        return {T * t, 4.f * a * r * r};
-    }
-}
-
-template <bool BF16>
-__device__ __forceinline__ void unpack(const uint4 w, float (&x)[Elem<BF16>::kPerGranule]) {
-    if constexpr (BF16) {
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            x[2 * q] = __uint_as_float(u[q] << 16);
-            x[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
-        }
-    } else {
-        x[0] = __uint_as_float(w.x);
-        x[1] = __uint_as_float(w.y);
-        x[2] = __uint_as_float(w.z);
-        x[3] = __uint_as_float(w.w);
-    }
-}
-
-__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
-    __nv_bfloat162 r;
-    memcpy(&r, &u, 4);
-    return r;
-}
-
-// Max of a full granule (packed bf16x2 max for bf16).
-template <bool BF16>
-__device__ __forceinline__ float granule_max(const uint4 w) {
-    if constexpr (BF16) {
-        const __nv_bfloat162 a = __hmax2(as_bf162(w.x), as_bf162(w.y));
-        const __nv_bfloat162 b = __hmax2(as_bf162(w.z), as_bf162(w.w));
-        const __nv_bfloat162 c = __hmax2(a, b);
-        return fmaxf(__low2float(c), __high2float(c));
-    } else {
-        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                     fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
-    }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    uint32_t u;
-    memcpy(&u, &v, 4);
-    return u;
-}
-
-template <bool BF16>
-__device__ __forceinline__ void store_elem(unsigned char *p, float g) {
-    if constexpr (BF16) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(g);
-        uint16_t u;
-        memcpy(&u, &b, 2);
-        *reinterpret_cast<uint16_t *>(p) = u;
-    } else {
-        *reinterpret_cast<float *>(p) = g;
-    }
-}
-
-// Where row r's granules start and which of them this CTA owns.
-struct RowGeo {
-    uintptr_t gbase;  // 16-byte aligned address of the row's first granule
-    int lead;         // elements of the first granule that precede column 0
-    int g_beg;        // first granule owned by this CTA
-    int n_my;         // granules owned by this CTA (may be 0)
-};
-
-template <bool BF16>
-__device__ __forceinline__ RowGeo row_geo(const Params &p, int64_t r, uint32_t crank) {
-    constexpr int EPG = Elem<BF16>::kPerGranule;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p.logits) + r * p.stride_bytes;
-    RowGeo g;
-    g.gbase = a0 & ~static_cast<uintptr_t>(15);
-    g.lead = static_cast<int>((a0 & 15) / Elem<BF16>::kBytes);
-    const int G = (g.lead + p.V + EPG - 1) / EPG;
-    g.g_beg = static_cast<int>(crank) * p.gran_per_cta;
-    g.n_my = min(G - g.g_beg, p.gran_per_cta);
-    if (g.n_my < 0) g.n_my = 0;
-    return g;
-}
-
-// Bounded mbarrier wait (slow path).  CLUSTER: acquire at cluster scope (pairs
-// with the peers' release-arrives).  Gives up after kWaitLimitNs (1 ms once
-// another wait has already given up), setting the abort flag and the device
-// error bit; SKIP_IF_ABORT returns at once when aborted (waits whose arrival
-// may never come once the pipeline stopped).
-template <bool CLUSTER, bool SKIP_IF_ABORT>
-__device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
-                                               int *err) {
-    auto poll = [&]() {
-        return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
-    };
-    if (SKIP_IF_ABORT && *abort) return false;
-    const unsigned long long t0 = ptx::globaltimer_ns();
-    const unsigned long long limit = *abort ? 1000000ull : kWaitLimitNs;
-    for (;;) {
-        for (int i = 0; i < 16; ++i)
-            if (poll()) return true;
-        if (SKIP_IF_ABORT && *abort) return false;
-        if (ptx::globaltimer_ns() - t0 > limit) {
-            *abort = 1;
-            atomicOr(err, VLMCE_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-template <bool CLUSTER, bool SKIP_IF_ABORT>
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                             int *err) {
-    const bool ok =
-        CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
-    if (ok) return true;
-    return bounded_wait_slow<CLUSTER, SKIP_IF_ABORT>(bar, parity, abort, err);
-}
-
-// Per-thread pass-A accumulators.
+// Pass-1 state of one thread.
 struct Acc {
-    float mv;      // max raw logit seen
-    int midx;      // its first column
-    float mz;      // z of mv: reference of s
-    uint64_t nmL;  // (-mz log2e, -mz log2e)
-    uint64_t s;    // sums of exp(z - mz), two lanes
-    uint64_t sz;   // sums of z, two lanes
+    float mv;   // max raw logit seen
+    int midx;   // its first column
+    float mz;   // z of mv: reference of s
+    float nmL;  // -mz log2e
+    float s0, s1, z0, z1;
 };
 
-// Fold one granule into the pass-A accumulators (granules arrive in column order).
+// Fold one granule (first column jg; granules come in column order).
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void pass_a_granule(Acc &a, const uint4 w, int jg, int V, float T,
-                                               float k2) {
+__device__ __forceinline__ void fold(Acc &a, const uint4 w, int jg, int V, float T, float k2) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
@@ -327,74 +81,50 @@ __device__ __forceinline__ void pass_a_granule(Acc &a, const uint4 w, int jg, in
             if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
         const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
         const float f = ptx::ex2((a.mz - nz) * kLog2e);
-        float s0, s1;
-        upk(a.s, s0, s1);
-        s0 = (s0 == 0.f) ? 0.f : s0 * f;
-        s1 = (s1 == 0.f) ? 0.f : s1 * f;
-        a.s = pk(s0, s1);
+        a.s0 = (a.s0 == 0.f) ? 0.f : a.s0 * f;
+        a.s1 = (a.s1 == 0.f) ? 0.f : a.s1 * f;
         a.mv = gm;
         a.midx = jg + li;
         a.mz = nz;
-        a.nmL = pk(-nz * kLog2e, -nz * kLog2e);
+        a.nmL = -nz * kLog2e;
     }
-    const uint64_t L2 = pk(kLog2e, kLog2e);
     if (full) {
 #pragma unroll
         for (int l = 0; l < EPG; l += 2) {
             const float za = softcap_z<SOFTCAP>(x[l], T, k2).z;
             const float zb = softcap_z<SOFTCAP>(x[l + 1], T, k2).z;
-            const uint64_t z2 = pk(za, zb);
-            a.s = add2(a.s, ex2x2(fma2(z2, L2, a.nmL)));
-            a.sz = add2(a.sz, z2);
+            a.s0 += ptx::ex2(fmaf(za, kLog2e, a.nmL));
+            a.s1 += ptx::ex2(fmaf(zb, kLog2e, a.nmL));
+            a.z0 += za;
+            a.z1 += zb;
         }
     } else {
-        float s0, s1, z0, z1, nm, dummy;
-        upk(a.s, s0, s1);
-        upk(a.sz, z0, z1);
-        upk(a.nmL, nm, dummy);
 #pragma unroll
         for (int l = 0; l < EPG; ++l) {
             if (jg + l >= 0 && jg + l < V) {
                 const float z = softcap_z<SOFTCAP>(x[l], T, k2).z;
-                s0 += ptx::ex2(fmaf(z, kLog2e, nm));
-                z0 += z;
+                a.s0 += ptx::ex2(fmaf(z, kLog2e, a.nmL));
+                a.z0 += z;
             }
         }
-        a.s = pk(s0, s1);
-        a.sz = pk(z0, z1);
     }
 }
 
 // Gradient of one granule, stored over the logits.
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, unsigned char *dst,
-                                               float T, float k2, uint64_t nlseL2, uint64_t scale2,
-                                               uint64_t negc2, int label_lane, float scale,
-                                               float c_label) {
+__device__ __forceinline__ void grad_granule(const uint4 w, int jg, int V, unsigned char *dst,
+                                             float T, float k2, float nlseL, float scale,
+                                             float c_smooth, float c_label, int label_lane) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
-    float x[EPG], g[EPG], dz[EPG];
+    float x[EPG], g[EPG];
     unpack<BF16>(w, x);
-    const uint64_t L2 = pk(kLog2e, kLog2e);
 #pragma unroll
-    for (int l = 0; l < EPG; l += 2) {
-        const Capped ca = softcap_z<SOFTCAP>(x[l], T, k2);
-        const Capped cb = softcap_z<SOFTCAP>(x[l + 1], T, k2);
-        dz[l] = ca.dz;
-        dz[l + 1] = cb.dz;
-        const uint64_t p2 = ex2x2(fma2(pk(ca.z, cb.z), L2, nlseL2));  // p_j
-        const uint64_t g2 = fma2(p2, scale2, negc2);                  // scale (p_j - eps/V)
-        upk(g2, g[l], g[l + 1]);
-        if (label_lane >= 0) {  // the label column: q_y = 1 - eps + eps/V
-            float pa, pb;
-            upk(p2, pa, pb);
-            if (label_lane == l) g[l] = fmaf(pa, scale, -c_label);
-            if (label_lane == l + 1) g[l + 1] = fmaf(pb, scale, -c_label);
-        }
-    }
-    if constexpr (SOFTCAP) {
-#pragma unroll
-        for (int l = 0; l < EPG; ++l) g[l] *= dz[l];
+    for (int l = 0; l < EPG; ++l) {
+        const Capped c = softcap_z<SOFTCAP>(x[l], T, k2);
+        const float pr = ptx::ex2(fmaf(c.z, kLog2e, nlseL));  // p_j
+        g[l] = fmaf(pr, scale, (l == label_lane) ? -c_label : -c_smooth);
+        if constexpr (SOFTCAP) g[l] *= c.dz;
     }
     if (jg >= 0 && jg + EPG <= V) {
         uint4 o;
@@ -414,7 +144,7 @@ __device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, uns
 }
 
 template <bool BF16>
-__device__ __forceinline__ void store_zero_granule(int jg, int V, unsigned char *dst) {
+__device__ __forceinline__ void zero_granule(int jg, int V, unsigned char *dst) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
     if (jg >= 0 && jg + EPG <= V) {
@@ -426,226 +156,103 @@ __device__ __forceinline__ void store_zero_granule(int jg, int V, unsigned char 
     }
 }
 
-// Producer lane: stream this cluster's rows (this CTA's slices), one chunk per slot.
-template <bool BF16>
-__device__ __forceinline__ void produce(const Params &p, Ctl &ctl, uint32_t ring0, uint32_t cid,
-                                        uint32_t ncl, uint32_t crank, int64_t n_iter) {
-    volatile int *abort = &ctl.abort;
-    const uint32_t full0 = ptx::smem_addr(&ctl.full[0]);
-    const uint32_t empty0 = ptx::smem_addr(&ctl.empty[0]);
-    int64_t q = 0;
-    for (int64_t it = 0; it < n_iter && !*abort; ++it) {
-        const RowGeo g = row_geo<BF16>(p, static_cast<int64_t>(cid) + it * ncl, crank);
-        const unsigned char *src = reinterpret_cast<const unsigned char *>(g.gbase) + 16 * g.g_beg;
-        for (int c = 0; c * kChunkGranules < g.n_my; ++c, ++q) {
-            const int slot = static_cast<int>(q % kSlots);
-            const int64_t use = q / kSlots;
-            if (use > 0 &&
-                !bounded_wait<false, true>(empty0 + 8u * slot,
-                                           static_cast<uint32_t>((use - 1) & 1), abort, p.err))
-                break;
-            const int gran = min(kChunkGranules, g.n_my - c * kChunkGranules);
-            const uint32_t bytes = static_cast<uint32_t>(gran) * 16u;
-            ptx::mbar_arrive_expect_tx(full0 + 8u * slot, bytes);
-            ptx::bulk_g2s(ring0 + static_cast<uint32_t>(slot) * kChunkBytes,
-                          src + static_cast<size_t>(c) * kChunkBytes, bytes, full0 + 8u * slot);
-        }
-    }
-    // Every issued copy has landed before the CTA may exit.
-    for (int slot = 0; slot < kSlots; ++slot) {
-        if (q <= slot) break;
-        const int64_t last = q - 1 - ((q - 1 - slot) % kSlots);
-        volatile int no_abort = 0;
-        bounded_wait<false, false>(full0 + 8u * slot, static_cast<uint32_t>((last / kSlots) & 1),
-                                   &no_abort, p.err);
-    }
-}
-
 template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) rows_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) kernel(const Params p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    Ctl &ctl = *reinterpret_cast<Ctl *>(smem);
-    unsigned char *ring = smem + kCtlBytes;
+    constexpr int ELT = Elem<BF16>::kBytes;
+    __shared__ RowPart wpart[kWarps];
+    __shared__ float bcast;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const uint32_t k = ptx::cluster_nctarank();
-    const uint32_t crank = ptx::cluster_ctarank();
-    const uint32_t cid = ptx::cluster_id_x();
-    const uint32_t ncl = ptx::ncluster_x();
-    const uint32_t full0 = ptx::smem_addr(&ctl.full[0]);
-    const uint32_t empty0 = ptx::smem_addr(&ctl.empty[0]);
+    const int64_t r = blockIdx.x;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p.logits) + r * p.stride_bytes;
+    unsigned char *gbase = reinterpret_cast<unsigned char *>(a0 & ~static_cast<uintptr_t>(15));
+    const uint4 *row = reinterpret_cast<const uint4 *>(gbase);
+    const int lead = static_cast<int>((a0 & 15) / ELT);
+    const int G = (lead + p.V + EPG - 1) / EPG;
+    const float T = p.softcap;
+    const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
 
-    if (tid == 0) {
-        for (int s = 0; s < kSlots; ++s) {
-            ptx::mbar_init(full0 + 8u * s, 1);
-            ptx::mbar_init(empty0 + 8u * s, kConsumerWarps);
+    // ---- pass 1
+    Acc a;
+    a.mv = -INFINITY;
+    a.midx = INT_MAX;
+    a.mz = -INFINITY;
+    a.nmL = INFINITY;
+    a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
+    if (tid == 0) {  // pull the whole row towards L2 with the bulk-copy engine
+        const uint32_t bytes = static_cast<uint32_t>(G) * 16u;
+        for (uint32_t off = 0; off < bytes; off += kPrefetchBytes)
+            ptx::bulk_prefetch_l2(gbase + off, min(kPrefetchBytes, bytes - off));
+    }
+    int gl;
+    for (gl = tid; gl < G; gl += kThreads)
+        fold<BF16, SOFTCAP>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
+
+    RowPart pt = part_identity();
+    pt.mx = a.mv;
+    pt.idx = a.midx;
+    pt.mz = a.mz;
+    pt.s = a.s0 + a.s1;
+    pt.sz = a.z0 + a.z1;
+    warp_allreduce(pt);
+    if (lane == 0) wpart[warp] = pt;
+
+    const int64_t y = p.labels[r];
+    const bool ignored = (y == p.ignore_index);
+    const bool valid = !ignored && y >= 0 && y < p.V;
+    __syncthreads();
+    if (warp == 0) {
+        RowPart q = wpart[lane];  // kWarps == 32
+        warp_allreduce(q);
+        if (lane == 0) {
+            const float lse = q.mz + logf(q.s);
+            float l = 0.f;
+            if (valid) {
+                const unsigned char *py = reinterpret_cast<const unsigned char *>(a0) + ELT * y;
+                float xy;
+                if constexpr (BF16)
+                    xy = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
+                else
+                    xy = *reinterpret_cast<const float *>(py);
+                const float zy = softcap_z<SOFTCAP>(xy, T, k2).z;
+                l = lse - fmaf(1.f - p.eps, zy, (p.eps / static_cast<float>(p.V)) * q.sz);
+            } else if (!ignored) {
+                l = __int_as_float(0x7fc00000);  // bad label: NaN
+            }
+            p.loss[r] = l;
+            p.argmax[r] = q.idx;
+            bcast = lse;
         }
-        ptx::mbar_init(ptx::smem_addr(&ctl.stat[0]), k * kConsumerWarps);
-        ptx::mbar_init(ptx::smem_addr(&ctl.stat[1]), k * kConsumerWarps);
-        ctl.abort = 0;
-        ptx::fence_mbar_init_cluster();
     }
     __syncthreads();
-    ptx::cluster_sync();  // every CTA's barriers exist before anyone signals them
 
-    const int64_t n_iter = (static_cast<int64_t>(cid) < p.N) ? (p.N - 1 - cid) / ncl + 1 : 0;
-    volatile int *abort = &ctl.abort;
-
-    if (warp == kConsumerWarps) {
-        if (lane == 0) produce<BF16>(p, ctl, ptx::smem_addr(ring), cid, ncl, crank, n_iter);
-        __syncwarp();
-    } else {
-        // The label census of this call must be complete before it is read.
-        ptx::griddep_wait();
+    // ---- pass 2
+    if (valid) {
+        ptx::griddep_wait();  // the label census of this call
         const int64_t n_valid = p.counts[0];
         float scale = p.grad_scale;
         if (p.reduction == VLMCE_MEAN)
             scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
         const float c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
         const float c_label = c_smooth + scale * (1.f - p.eps);            // + scale (1 - eps)
-        const uint64_t scale2 = pk(scale, scale);
-        const uint64_t negc2 = pk(-c_smooth, -c_smooth);
-        const float T = p.softcap;
-        const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
-
-        int64_t q = 0;  // ring position of the row's first chunk, in step with the producer
-        for (int64_t it = 0; it < n_iter; ++it) {
-            const int pp = static_cast<int>(it & 1);
-            const int64_t r = static_cast<int64_t>(cid) + it * ncl;
-            const int64_t y = p.labels[r];
-            const bool ignored = (y == p.ignore_index);
-            const bool valid = !ignored && y >= 0 && y < p.V;
-            const RowGeo g = row_geo<BF16>(p, r, crank);
-            const int nch = (g.n_my + kChunkGranules - 1) / kChunkGranules;
-            const int gy = valid ? static_cast<int>((y + g.lead) / EPG) - g.g_beg : -1;
-            const int ly = valid ? static_cast<int>((y + g.lead) % EPG) : 0;
-
-            // ---- pass A over the slice as its slots land
-            Acc a;
-            a.mv = -INFINITY;
-            a.midx = INT_MAX;
-            a.mz = -INFINITY;
-            a.nmL = pk(INFINITY, INFINITY);
-            a.s = pk(0.f, 0.f);
-            a.sz = pk(0.f, 0.f);
-            float zy = 0.f;
-            for (int c = 0; c < nch; ++c) {
-                const int64_t qc = q + c;
-                const int slot = static_cast<int>(qc % kSlots);
-                bounded_wait<false, true>(full0 + 8u * slot,
-                                          static_cast<uint32_t>((qc / kSlots) & 1), abort, p.err);
-                const int gl = c * kChunkGranules + tid;
-                if (gl < g.n_my) {
-                    const uint4 w =
-                        *reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes + 16 * tid);
-                    pass_a_granule<BF16, SOFTCAP>(a, w, (g.g_beg + gl) * EPG - g.lead, p.V, T, k2);
-                    if (gl == gy) {  // the label's logit
-                        float xv[EPG];
-                        unpack<BF16>(w, xv);
-                        float xy = xv[0];
-#pragma unroll
-                        for (int l = 1; l < EPG; ++l)
-                            if (l == ly) xy = xv[l];
-                        zy = softcap_z<SOFTCAP>(xy, T, k2).z;
-                    }
-                }
-            }
-            RowPart part = part_identity();
-            part.mx = a.mv;
-            part.idx = a.midx;
-            part.mz = a.mz;
-            {
-                float s0, s1, z0, z1;
-                upk(a.s, s0, s1);
-                upk(a.sz, z0, z1);
-                part.s = s0 + s1;
-                part.sz = z0 + z1;
-            }
-            part.zy = zy;
-            warp_allreduce(part);
-
-            // ---- publish this warp's partial to every CTA of the cluster, then
-            // merge all k x 15 partials of the row (same order everywhere)
-            if (lane == 0) {
-                const uint32_t dst = ptx::smem_addr(&ctl.xslot[pp][crank * kConsumerWarps + warp]);
-                const uint32_t bar = ptx::smem_addr(&ctl.stat[pp]);
-                const uint4 v0 = make_uint4(__float_as_uint(part.mx), static_cast<uint32_t>(part.idx),
-                                            __float_as_uint(part.mz), __float_as_uint(part.s));
-                const uint4 v1 = make_uint4(__float_as_uint(part.sz), __float_as_uint(part.zy), 0u, 0u);
-                for (uint32_t c = 0; c < k; ++c) {
-                    const uint32_t ra = ptx::mapa(dst, c);
-                    ptx::st_dsmem_v4(ra, v0);
-                    ptx::st_dsmem_v4(ra + 16, v1);
-                }
-                for (uint32_t c = 0; c < k; ++c) ptx::mbar_remote_arrive_release(ptx::mapa(bar, c));
-            }
-            bounded_wait<true, false>(ptx::smem_addr(&ctl.stat[pp]),
-                                      static_cast<uint32_t>((it >> 1) & 1), abort, p.err);
-            RowPart rp = part_identity();
-            {
-                const int n_parts = static_cast<int>(k) * kConsumerWarps;
-#pragma unroll
-                for (int e = lane; e < kMaxCluster * kConsumerWarps; e += 32) {
-                    if (e < n_parts) {
-                        const RowPart &o = ctl.xslot[pp][e];
-                        part_merge(rp, o.mx, o.idx, o.mz, o.s, o.sz, o.zy);
-                    }
-                }
-            }
-            warp_allreduce(rp);
-            const float lse = rp.mz + logf(rp.s);
-
-            if (crank == 0 && tid == 0) {
-                float l = 0.f;
-                if (valid)
-                    l = lse - fmaf(1.f - p.eps, rp.zy, (p.eps / static_cast<float>(p.V)) * rp.sz);
-                else if (!ignored)
-                    l = __int_as_float(0x7fc00000);  // bad label: NaN
-                p.loss[r] = l;
-                p.argmax[r] = rp.idx;
-            }
-
-            // ---- pass B: gradient from shared memory, stored over the logits
-            unsigned char *grow = reinterpret_cast<unsigned char *>(g.gbase) + 16 * g.g_beg;
-            const uint64_t nlseL2 = pk(-lse * kLog2e, -lse * kLog2e);
-            for (int c = 0; c < nch; ++c) {
-                const int slot = static_cast<int>((q + c) % kSlots);
-                const int gl = c * kChunkGranules + tid;
-                if (gl < g.n_my) {
-                    const int jg = (g.g_beg + gl) * EPG - g.lead;
-                    if (valid) {
-                        const uint4 w =
-                            *reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes + 16 * tid);
-                        pass_b_granule<BF16, SOFTCAP>(w, jg, p.V, grow + 16 * gl, T, k2, nlseL2,
-                                                      scale2, negc2, gl == gy ? ly : -1, scale,
-                                                      c_label);
-                    } else {
-                        store_zero_granule<BF16>(jg, p.V, grow + 16 * gl);
-                    }
-                }
-            }
-            // ---- the row's slots are free again
-            __syncwarp();
-            if (lane == 0) {
-                for (int c = 0; c < nch; ++c)
-                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
-                                     empty0 + 8u * static_cast<uint32_t>((q + c) % kSlots))
-                                 : "memory");
-            }
-            q += nch;
-        }
+        const float nlseL = -bcast * kLog2e;
+        const int gy = static_cast<int>((y + lead) / EPG);
+        const int ly = static_cast<int>((y + lead) % EPG);
+        for (gl = tid; gl < G; gl += kThreads)
+            grad_granule<BF16, SOFTCAP>(ld_v4(row + gl), gl * EPG - lead, p.V, gbase + 16 * gl, T, k2,
+                                        nlseL, scale, c_smooth, c_label, gl == gy ? ly : -1);
+    } else {
+        for (gl = tid; gl < G; gl += kThreads) zero_granule<BF16>(gl * EPG - lead, p.V, gbase + 16 * gl);
     }
-    ptx::griddep_launch_dependents();
-    __syncthreads();
-    ptx::cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // The row kernel for the given softcap, per element type (ce_rows_bf16.cu,
 // ce_rows_f32.cu).
-RowKernel rows_kernel_bf16(bool softcap);
-RowKernel rows_kernel_f32(bool softcap);
+Kernel kernel_bf16(bool softcap);
+Kernel kernel_f32(bool softcap);
 
+}  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

@@ -3,8 +3,8 @@
 
 namespace vlmce {
 namespace ce {
-RowKernel rows_kernel_bf16(bool softcap) {
-    return softcap ? rows_kernel<true, true> : rows_kernel<true, false>;
-}
+namespace rows {
+Kernel kernel_bf16(bool softcap) { return softcap ? kernel<true, true> : kernel<true, false>; }
+}  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

@@ -3,8 +3,8 @@
 
 namespace vlmce {
 namespace ce {
-RowKernel rows_kernel_f32(bool softcap) {
-    return softcap ? rows_kernel<false, true> : rows_kernel<false, false>;
-}
+namespace rows {
+Kernel kernel_f32(bool softcap) { return softcap ? kernel<false, true> : kernel<false, false>; }
+}  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

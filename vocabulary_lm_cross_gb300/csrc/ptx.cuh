@@ -115,6 +115,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Ask the bulk-copy engine to bring [src, src + bytes) into L2 (no completion
+// signal).  src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
