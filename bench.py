@@ -363,7 +363,7 @@ def run_ours(args, w):
 
     bytes_step = w.algorithmic_bytes
     plan = v.describe_plan(w.N, V, x0.dtype, w.softcap)
-    kernel_name = "rows_kernel" if plan["kernel"] == "rows" else "split_kernel"
+    kernel_name = "ce_rows_kernel" if plan["kernel"] == "rows" else "ce_split_kernel"
     value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kern_ms * 1e-3) / 1e9

@@ -9,15 +9,15 @@
 // softmax is never materialised.
 //
 // Three launches on the caller's stream:
-//   1. count_kernel    -- label census (n_valid for the mean, bad labels).
+//   1. ce_count_kernel    -- label census (n_valid for the mean, bad labels).
 //   2. the row work, by one of two kernels:
-//      rows::kernel  (ce_rows.cuh)  -- one CTA per row, two passes, the second
+//      ce_rows_kernel  (ce_rows.cuh)  -- one CTA per row, two passes, the second
 //                    served by L2; the default: every SM busy once N >= 304;
-//      split::split_kernel (ce_split.cuh) -- a thread-block cluster per row,
+//      ce_split_kernel (ce_split.cuh) -- a thread-block cluster per row,
 //                    the row split over its CTAs in shared memory and merged
 //                    through distributed shared memory; for few, wide rows,
 //                    where one CTA per row would leave most SMs idle.
-//   3. finalize_kernel -- fixed-order fp64 reduction of the per-row losses
+//   3. ce_finalize_kernel -- fixed-order fp64 reduction of the per-row losses
 //      and correct-prediction count.
 // Kernels 2 and 3 use programmatic dependent launch, so that their prologues
 // overlap the previous kernel's tail.  No floating-point atomics: results are
@@ -45,7 +45,7 @@ namespace vlmce {
 namespace ce {
 namespace {
 
-__global__ void __launch_bounds__(1024) count_kernel(const int64_t *__restrict__ labels, int64_t N,
+__global__ void __launch_bounds__(1024) ce_count_kernel(const int64_t *__restrict__ labels, int64_t N,
                                                      int64_t V, int64_t ignore_index,
                                                      int64_t *counts, int *err) {
     ptx::griddep_launch_dependents();
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(1024) count_kernel(const int64_t *__restrict__
     }
 }
 
-__global__ void __launch_bounds__(1024) finalize_kernel(
+__global__ void __launch_bounds__(1024) ce_finalize_kernel(
     const float *__restrict__ loss, const int64_t *__restrict__ argmax,
     const int64_t *__restrict__ labels, int64_t N, int64_t V, int64_t ignore_index, int reduction,
     const int64_t *counts, const int *err, float *out_reduced, int64_t *out_counts) {
@@ -230,7 +230,7 @@ vlmce_status get_split_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_
     if (!g_attr_set.count({d.device, pl.kernel})) {
         if (record_cuda(cudaFuncSetAttribute(pl.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              split::kSmemBytes),
-                        "cudaFuncSetAttribute(split_kernel)") != cudaSuccess)
+                        "cudaFuncSetAttribute(ce_split_kernel)") != cudaSuccess)
             return VLMCE_ERR_CUDA;
         g_attr_set.insert({d.device, pl.kernel});
     }
@@ -247,7 +247,7 @@ vlmce_status get_split_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_
     cfg.numAttrs = 1;
     int ncl = 0;
     if (record_cuda(cudaOccupancyMaxActiveClusters(&ncl, pl.kernel, &cfg),
-                    "cudaOccupancyMaxActiveClusters(split_kernel)") != cudaSuccess)
+                    "cudaOccupancyMaxActiveClusters(ce_split_kernel)") != cudaSuccess)
         return VLMCE_ERR_CUDA;
     if (ncl < 1) return VLMCE_ERR_TOO_LARGE;
     pl.max_clusters = ncl;
@@ -372,8 +372,8 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
     float *loss = out_loss ? out_loss : w.loss;
     int64_t *amax = out_argmax ? out_argmax : w.argmax;
 
-    count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
-    st = launch_status(cudaSuccess, "count_kernel");
+    ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
+    st = launch_status(cudaSuccess, "ce_count_kernel");
     if (st != VLMCE_OK) return st;
 
     cudaLaunchAttribute attr[2];
@@ -414,7 +414,7 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
             attr[1].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 2;
-            st = launch_status(cudaLaunchKernelEx(&cfg, pl.kernel, p), "split_kernel");
+            st = launch_status(cudaLaunchKernelEx(&cfg, pl.kernel, p), "ce_split_kernel");
         } else {
             rows::Params p;
             p.logits = static_cast<unsigned char *>(logits);
@@ -439,7 +439,7 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
             st = launch_status(cudaLaunchKernelEx(&cfg, bf16 ? rows::kernel_bf16(capped)
                                                              : rows::kernel_f32(capped),
                                                   p),
-                               "rows_kernel");
+                               "ce_rows_kernel");
         }
         if (st != VLMCE_OK) return st;
         if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
@@ -454,9 +454,9 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return launch_status(
-        cudaLaunchKernelEx(&cfg, finalize_kernel, static_cast<const float *>(loss),
+        cudaLaunchKernelEx(&cfg, ce_finalize_kernel, static_cast<const float *>(loss),
                            static_cast<const int64_t *>(amax), labels, N, V, ignore_index,
                            static_cast<int>(reduction), static_cast<const int64_t *>(w.counts),
                            static_cast<const int *>(w.err), out_reduced, out_counts),
-        "finalize_kernel");
+        "ce_finalize_kernel");
 }

@@ -157,7 +157,7 @@ __device__ __forceinline__ void zero_granule(int jg, int V, unsigned char *dst) 
 }
 
 template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(kThreads, 2) kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
     __shared__ RowPart wpart[kWarps];

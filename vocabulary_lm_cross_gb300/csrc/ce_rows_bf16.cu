@@ -4,7 +4,7 @@
 namespace vlmce {
 namespace ce {
 namespace rows {
-Kernel kernel_bf16(bool softcap) { return softcap ? kernel<true, true> : kernel<true, false>; }
+Kernel kernel_bf16(bool softcap) { return softcap ? ce_rows_kernel<true, true> : ce_rows_kernel<true, false>; }
 }  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

@@ -4,7 +4,7 @@
 namespace vlmce {
 namespace ce {
 namespace rows {
-Kernel kernel_f32(bool softcap) { return softcap ? kernel<false, true> : kernel<false, false>; }
+Kernel kernel_f32(bool softcap) { return softcap ? ce_rows_kernel<false, true> : ce_rows_kernel<false, false>; }
 }  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

@@ -308,7 +308,7 @@ __device__ __forceinline__ void produce(const SplitParams &p, Ctl &ctl, uint32_t
 }
 
 template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const SplitParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const SplitParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctl &ctl = *reinterpret_cast<Ctl *>(smem);

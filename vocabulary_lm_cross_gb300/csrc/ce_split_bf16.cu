@@ -5,7 +5,7 @@ namespace vlmce {
 namespace ce {
 namespace split {
 SplitKernel split_kernel_bf16(bool softcap) {
-    return softcap ? split_kernel<true, true> : split_kernel<true, false>;
+    return softcap ? ce_split_kernel<true, true> : ce_split_kernel<true, false>;
 }
 }  // namespace split
 }  // namespace ce

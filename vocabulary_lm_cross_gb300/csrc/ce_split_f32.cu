@@ -5,7 +5,7 @@ namespace vlmce {
 namespace ce {
 namespace split {
 SplitKernel split_kernel_f32(bool softcap) {
-    return softcap ? split_kernel<false, true> : split_kernel<false, false>;
+    return softcap ? ce_split_kernel<false, true> : ce_split_kernel<false, false>;
 }
 }  // namespace split
 }  // namespace ce
