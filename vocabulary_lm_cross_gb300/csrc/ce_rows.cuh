@@ -1,9 +1,8 @@
 // ce_rows.cuh -- the cross-entropy row kernel (default path): one CTA of 1024
 // threads per row, two CTAs per SM (64 warps: every SM is fully occupied).
 //
-//   pass 1: one thread asks the bulk-copy engine to prefetch the whole row
-//           into L2; all threads stream it in 16-byte granules: max and first
-//           argmax of the raw logits, online sum of exp(z - m) and sum of z;
+//   pass 1: stream the row from HBM in 16-byte granules: max and first argmax
+//           of the raw logits, online sum of exp(z - m) and sum of z;
 //   merge:  warp shuffles, then the 32 warp partials (fixed order);
 //   pass 2: read the row again -- it is still in the 129 MB L2, since at most
 //           2 x 152 rows (78 MB for 256 KB rows) are in flight -- and store the
@@ -12,6 +11,13 @@
 // HBM sees one read and one write of every byte; the second read is served by
 // L2.  The label census of the call is only needed by pass 2, so the kernel
 // waits for it (programmatic dependent launch) after pass 1.
+//
+// The kernel is bound by instruction issue, so the inner loops run over whole
+// granules only, with no per-element tests: the at most two partial granules
+// at the ends of a row are handled apart (the first one before a thread's
+// main loop, the last one after it, so every thread still meets its granules
+// in column order), the label column is patched in a rare branch, and
+// two-lane fp32 arithmetic (f32x2) halves the floating-point instructions.
 #pragma once
 
 #include "ce_common.cuh"
@@ -22,7 +28,6 @@ namespace rows {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr uint32_t kPrefetchBytes = 65536;  // bytes per L2 bulk-prefetch instruction
 
 struct Params {
     unsigned char *logits;
@@ -49,120 +54,183 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
     return v;
 }
 
-// Pass-1 state of one thread.
-struct Acc {
-    float mv;   // max raw logit seen
-    int midx;   // its first column
-    float mz;   // z of mv: reference of s
-    float nmL;  // -mz log2e
-    float s0, s1, z0, z1;
+// The four 32-bit words of a granule as two-lane fp32 pairs of elements
+// (2q, 2q + 1); a bf16 granule gives four pairs, an fp32 granule two.
+template <bool BF16>
+struct Pairs {
+    static constexpr int kN = BF16 ? 4 : 2;
 };
-
-// Fold one granule (first column jg; granules come in column order).
-template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void fold(Acc &a, const uint4 w, int jg, int V, float T, float k2) {
-    constexpr int EPG = Elem<BF16>::kPerGranule;
-    float x[EPG];
-    unpack<BF16>(w, x);
-    const bool full = jg >= 0 && jg + EPG <= V;
-    float gm;
-    if (full) {
-        gm = granule_max<BF16>(w);
+template <bool BF16>
+__device__ __forceinline__ void to_pairs(const uint4 w, uint64_t (&x2)[Pairs<BF16>::kN]) {
+    if constexpr (BF16) {
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            x2[q] = pk(__uint_as_float(u[q] << 16), __uint_as_float(u[q] & 0xffff0000u));
     } else {
-        gm = -INFINITY;
-#pragma unroll
-        for (int l = 0; l < EPG; ++l)
-            if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
-    }
-    if (gm > a.mv) {  // new maximum (rare after the first granules): locate it, rescale
-        int li = EPG - 1;
-#pragma unroll
-        for (int l = EPG - 1; l >= 0; --l)
-            if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
-        const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
-        const float f = ptx::ex2((a.mz - nz) * kLog2e);
-        a.s0 = (a.s0 == 0.f) ? 0.f : a.s0 * f;
-        a.s1 = (a.s1 == 0.f) ? 0.f : a.s1 * f;
-        a.mv = gm;
-        a.midx = jg + li;
-        a.mz = nz;
-        a.nmL = -nz * kLog2e;
-    }
-    if (full) {
-#pragma unroll
-        for (int l = 0; l < EPG; l += 2) {
-            const float za = softcap_z<SOFTCAP>(x[l], T, k2).z;
-            const float zb = softcap_z<SOFTCAP>(x[l + 1], T, k2).z;
-            a.s0 += ptx::ex2(fmaf(za, kLog2e, a.nmL));
-            a.s1 += ptx::ex2(fmaf(zb, kLog2e, a.nmL));
-            a.z0 += za;
-            a.z1 += zb;
-        }
-    } else {
-#pragma unroll
-        for (int l = 0; l < EPG; ++l) {
-            if (jg + l >= 0 && jg + l < V) {
-                const float z = softcap_z<SOFTCAP>(x[l], T, k2).z;
-                a.s0 += ptx::ex2(fmaf(z, kLog2e, a.nmL));
-                a.z0 += z;
-            }
-        }
+        x2[0] = pk(__uint_as_float(w.x), __uint_as_float(w.y));
+        x2[1] = pk(__uint_as_float(w.z), __uint_as_float(w.w));
     }
 }
 
-// Gradient of one granule, stored over the logits.
+// Softcap of a pair: z = T tanh(x / T) (and 1 - tanh^2 when asked).
+template <bool SOFTCAP>
+__device__ __forceinline__ uint64_t cap_pair(uint64_t x2, float T, float k2, uint64_t *dz2) {
+    if constexpr (!SOFTCAP) {
+        return x2;
+    } else {
+        float a, b;
+        upk(x2, a, b);
+        const Capped ca = softcap_z<true>(a, T, k2), cb = softcap_z<true>(b, T, k2);
+        if (dz2) *dz2 = pk(ca.dz, cb.dz);
+        return pk(ca.z, cb.z);
+    }
+}
+
+// Pass-1 state of one thread.
+struct Acc {
+    float mv;       // max raw logit seen
+    int midx;       // its first column
+    float mz;       // z of mv: reference of s
+    uint64_t nmL2;  // (-mz log2e) twice
+    uint64_t s2;    // two-lane sums of exp(z - mz)
+    uint64_t z2;    // two-lane sums of z
+};
+
+// New maximum gm in the granule starting at column jg with elements x:
+// locate its first column among the valid ones, rescale the running sums.
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void grad_granule(const uint4 w, int jg, int V, unsigned char *dst,
-                                             float T, float k2, float nlseL, float scale,
-                                             float c_smooth, float c_label, int label_lane) {
+__device__ __forceinline__ void new_max(Acc &a, const uint4 w, float gm, int jg, int V, float T,
+                                        float k2) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
-    constexpr int ELT = Elem<BF16>::kBytes;
-    float x[EPG], g[EPG];
+    float x[EPG];
     unpack<BF16>(w, x);
+    int li = EPG - 1;
+#pragma unroll
+    for (int l = EPG - 1; l >= 0; --l)
+        if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
+    const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
+    const float f = ptx::ex2((a.mz - nz) * kLog2e);
+    float s0, s1;
+    upk(a.s2, s0, s1);
+    a.s2 = pk((s0 == 0.f) ? 0.f : s0 * f, (s1 == 0.f) ? 0.f : s1 * f);
+    a.mv = gm;
+    a.midx = jg + li;
+    a.mz = nz;
+    a.nmL2 = pk(-nz * kLog2e, -nz * kLog2e);
+}
+
+// Fold a whole granule (every column valid).
+template <bool BF16, bool SOFTCAP, bool SUMZ>
+__device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, float T, float k2) {
+    const float gm = granule_max<BF16>(w);
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, w, gm, jg, V, T, k2);
+    uint64_t x2[Pairs<BF16>::kN];
+    to_pairs<BF16>(w, x2);
+    const uint64_t L2 = pk(kLog2e, kLog2e);
+#pragma unroll
+    for (int q = 0; q < Pairs<BF16>::kN; ++q) {
+        const uint64_t z2 = cap_pair<SOFTCAP>(x2[q], T, k2, nullptr);
+        a.s2 = add2(a.s2, ex2x2(fma2(z2, L2, a.nmL2)));
+        if constexpr (SUMZ) a.z2 = add2(a.z2, z2);
+    }
+}
+
+// Fold a granule of which only the columns in [0, V) count.
+template <bool BF16, bool SOFTCAP>
+__device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int V, float T,
+                                             float k2) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    float x[EPG];
+    unpack<BF16>(w, x);
+    float gm = -INFINITY;
+#pragma unroll
+    for (int l = 0; l < EPG; ++l)
+        if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, w, gm, jg, V, T, k2);
+    float s0, s1, z0, z1, nm, dummy;
+    upk(a.s2, s0, s1);
+    upk(a.z2, z0, z1);
+    upk(a.nmL2, nm, dummy);
 #pragma unroll
     for (int l = 0; l < EPG; ++l) {
-        const Capped c = softcap_z<SOFTCAP>(x[l], T, k2);
-        const float pr = ptx::ex2(fmaf(c.z, kLog2e, nlseL));  // p_j
-        g[l] = fmaf(pr, scale, (l == label_lane) ? -c_label : -c_smooth);
-        if constexpr (SOFTCAP) g[l] *= c.dz;
-    }
-    if (jg >= 0 && jg + EPG <= V) {
-        uint4 o;
-        if constexpr (BF16) {
-            o = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
-                           pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
-        } else {
-            o = make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]),
-                           __float_as_uint(g[3]));
+        if (jg + l >= 0 && jg + l < V) {
+            const float z = softcap_z<SOFTCAP>(x[l], T, k2).z;
+            s0 += ptx::ex2(fmaf(z, kLog2e, nm));
+            z0 += z;
         }
-        ptx::st_global_cs_v4(dst, o);
-    } else {
+    }
+    a.s2 = pk(s0, s1);
+    a.z2 = pk(z0, z1);
+}
+
+struct GradCoef {
+    uint64_t nlseL2;   // (-lse log2e) twice
+    uint64_t scale2;   // scale twice
+    uint64_t negc2;    // -scale eps / V twice
+    float scale, c_smooth, c_label;
+    float T, k2;
+};
+
+// Gradients of the EPG elements of a granule, in fp32.
+template <bool BF16, bool SOFTCAP>
+__device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, int label_lane,
+                                            float (&g)[Elem<BF16>::kPerGranule]) {
+    uint64_t x2[Pairs<BF16>::kN];
+    to_pairs<BF16>(w, x2);
+    const uint64_t L2 = pk(kLog2e, kLog2e);
 #pragma unroll
-        for (int l = 0; l < EPG; ++l)
-            if (jg + l >= 0 && jg + l < V) store_elem<BF16>(dst + ELT * l, g[l]);
+    for (int q = 0; q < Pairs<BF16>::kN; ++q) {
+        uint64_t dz2 = 0;
+        const uint64_t z2 = cap_pair<SOFTCAP>(x2[q], c.T, c.k2, &dz2);
+        const uint64_t p2 = ex2x2(fma2(z2, L2, c.nlseL2));  // p_j
+        uint64_t g2 = fma2(p2, c.scale2, c.negc2);          // scale (p_j - eps/V)
+        if constexpr (SOFTCAP) g2 = mul2(g2, dz2);
+        upk(g2, g[2 * q], g[2 * q + 1]);
+        if (label_lane >> 1 == q) {  // the label column: q_y = 1 - eps + eps/V (rare)
+            float pa, pb;
+            upk(p2, pa, pb);
+            const float pr = (label_lane & 1) ? pb : pa;
+            float gy = fmaf(pr, c.scale, -c.c_label);
+            if constexpr (SOFTCAP) {
+                float da, db;
+                upk(dz2, da, db);
+                gy *= (label_lane & 1) ? db : da;
+            }
+            if (label_lane & 1)
+                g[2 * q + 1] = gy;
+            else
+                g[2 * q] = gy;
+        }
     }
 }
 
 template <bool BF16>
-__device__ __forceinline__ void zero_granule(int jg, int V, unsigned char *dst) {
-    constexpr int EPG = Elem<BF16>::kPerGranule;
-    constexpr int ELT = Elem<BF16>::kBytes;
-    if (jg >= 0 && jg + EPG <= V) {
-        ptx::st_global_cs_v4(dst, make_uint4(0u, 0u, 0u, 0u));
+__device__ __forceinline__ uint4 pack_granule(const float (&g)[Elem<BF16>::kPerGranule]) {
+    if constexpr (BF16) {
+        return make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                          pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
     } else {
-#pragma unroll
-        for (int l = 0; l < EPG; ++l)
-            if (jg + l >= 0 && jg + l < V) store_elem<BF16>(dst + ELT * l, 0.f);
+        return make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]),
+                          __float_as_uint(g[3]));
     }
 }
 
-template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
+// Store only the elements of a partial granule that lie in [0, V).
+template <bool BF16>
+__device__ __forceinline__ void store_partial(unsigned char *dst, int jg, int V,
+                                              const float (&g)[Elem<BF16>::kPerGranule]) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
-    __shared__ RowPart wpart[kWarps];
-    __shared__ float bcast;
+#pragma unroll
+    for (int l = 0; l < EPG; ++l)
+        if (jg + l >= 0 && jg + l < V) store_elem<BF16>(dst + ELT * l, g[l]);
+}
 
+template <bool BF16, bool SOFTCAP, bool SUMZ>
+__device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float *bcast) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    constexpr int ELT = Elem<BF16>::kBytes;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int64_t r = blockIdx.x;
@@ -171,6 +239,13 @@ __global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
     const uint4 *row = reinterpret_cast<const uint4 *>(gbase);
     const int lead = static_cast<int>((a0 & 15) / ELT);
     const int G = (lead + p.V + EPG - 1) / EPG;
+    // Whole granules are [gs, ge); granule 0 is partial when lead > 0 and
+    // granule G - 1 when the row does not end on a granule boundary.
+    const int gs = lead > 0 ? 1 : 0;
+    const int ge = ((lead + p.V) % EPG != 0) ? G - 1 : G;
+    const bool head = gs == 1;                  // granule 0 partial (thread 0)
+    const bool tail = ge == G - 1 && G - 1 >= gs;  // granule G-1 partial, distinct from 0
+    const int tail_tid = tail ? (G - 1 - gs) % kThreads : -1;
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
 
@@ -179,23 +254,26 @@ __global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
     a.mv = -INFINITY;
     a.midx = INT_MAX;
     a.mz = -INFINITY;
-    a.nmL = INFINITY;
-    a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
-    if (tid == 0) {  // pull the whole row towards L2 with the bulk-copy engine
-        const uint32_t bytes = static_cast<uint32_t>(G) * 16u;
-        for (uint32_t off = 0; off < bytes; off += kPrefetchBytes)
-            ptx::bulk_prefetch_l2(gbase + off, min(kPrefetchBytes, bytes - off));
-    }
-    int gl;
-    for (gl = tid; gl < G; gl += kThreads)
-        fold<BF16, SOFTCAP>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
+    a.nmL2 = pk(INFINITY, INFINITY);
+    a.s2 = pk(0.f, 0.f);
+    a.z2 = pk(0.f, 0.f);
+    if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, T, k2);
+    for (int gl = gs + tid; gl < ge; gl += kThreads)
+        fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
+    if (tid == tail_tid)
+        fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, T, k2);
 
     RowPart pt = part_identity();
     pt.mx = a.mv;
     pt.idx = a.midx;
     pt.mz = a.mz;
-    pt.s = a.s0 + a.s1;
-    pt.sz = a.z0 + a.z1;
+    {
+        float s0, s1, z0, z1;
+        upk(a.s2, s0, s1);
+        upk(a.z2, z0, z1);
+        pt.s = s0 + s1;
+        pt.sz = z0 + z1;
+    }
     warp_allreduce(pt);
     if (lane == 0) wpart[warp] = pt;
 
@@ -204,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
     const bool valid = !ignored && y >= 0 && y < p.V;
     __syncthreads();
     if (warp == 0) {
-        RowPart q = wpart[lane];  // kWarps == 32
+        RowPart q = lane < kWarps ? wpart[lane] : part_identity();
         warp_allreduce(q);
         if (lane == 0) {
             const float lse = q.mz + logf(q.s);
@@ -223,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
             }
             p.loss[r] = l;
             p.argmax[r] = q.idx;
-            bcast = lse;
+            *bcast = lse;
         }
     }
     __syncthreads();
@@ -235,17 +313,50 @@ __global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
         float scale = p.grad_scale;
         if (p.reduction == VLMCE_MEAN)
             scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
-        const float c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
-        const float c_label = c_smooth + scale * (1.f - p.eps);            // + scale (1 - eps)
-        const float nlseL = -bcast * kLog2e;
+        GradCoef c;
+        c.scale = scale;
+        c.c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
+        c.c_label = c.c_smooth + scale * (1.f - p.eps);          // + scale (1 - eps)
+        c.nlseL2 = pk(-*bcast * kLog2e, -*bcast * kLog2e);
+        c.scale2 = pk(scale, scale);
+        c.negc2 = pk(-c.c_smooth, -c.c_smooth);
+        c.T = T;
+        c.k2 = k2;
         const int gy = static_cast<int>((y + lead) / EPG);
         const int ly = static_cast<int>((y + lead) % EPG);
-        for (gl = tid; gl < G; gl += kThreads)
-            grad_granule<BF16, SOFTCAP>(ld_v4(row + gl), gl * EPG - lead, p.V, gbase + 16 * gl, T, k2,
-                                        nlseL, scale, c_smooth, c_label, gl == gy ? ly : -1);
+        float g[EPG];
+        if (head && tid == 0) {
+            grad_values<BF16, SOFTCAP>(ld_v4(row), c, gy == 0 ? ly : -1, g);
+            store_partial<BF16>(gbase, -lead, p.V, g);
+        }
+        for (int gl = gs + tid; gl < ge; gl += kThreads) {
+            grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, gl == gy ? ly : -1, g);
+            ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+        }
+        if (tid == tail_tid) {
+            grad_values<BF16, SOFTCAP>(ld_v4(row + (G - 1)), c, gy == G - 1 ? ly : -1, g);
+            store_partial<BF16>(gbase + 16 * (G - 1), (G - 1) * EPG - lead, p.V, g);
+        }
     } else {
-        for (gl = tid; gl < G; gl += kThreads) zero_granule<BF16>(gl * EPG - lead, p.V, gbase + 16 * gl);
+        float z[EPG];
+#pragma unroll
+        for (int l = 0; l < EPG; ++l) z[l] = 0.f;
+        if (head && tid == 0) store_partial<BF16>(gbase, -lead, p.V, z);
+        for (int gl = gs + tid; gl < ge; gl += kThreads)
+            ptx::st_global_cs_v4(gbase + 16 * gl, make_uint4(0u, 0u, 0u, 0u));
+        if (tid == tail_tid) store_partial<BF16>(gbase + 16 * (G - 1), (G - 1) * EPG - lead, p.V, z);
     }
+}
+
+template <bool BF16, bool SOFTCAP>
+__global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
+    __shared__ RowPart wpart[kWarps];
+    __shared__ float bcast;
+    // sum z only matters with label smoothing; skip the adds without it
+    if (p.eps > 0.f)
+        row_work<BF16, SOFTCAP, true>(p, wpart, &bcast);
+    else
+        row_work<BF16, SOFTCAP, false>(p, wpart, &bcast);
 }
 
 // The row kernel for the given softcap, per element type (ce_rows_bf16.cu,
