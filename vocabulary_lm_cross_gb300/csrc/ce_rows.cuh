@@ -16,8 +16,8 @@
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
 // main loop, the last one after it, so every thread still meets its granules
-// in column order), the label column is patched in a rare branch, and
-// two-lane fp32 arithmetic (f32x2) halves the floating-point instructions.
+// in column order), the label column is patched in a rare branch, and the
+// sum of z is only formed when label smoothing needs it.
 #pragma once
 
 #include "ce_common.cuh"
@@ -54,85 +54,54 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
     return v;
 }
 
-// The four 32-bit words of a granule as two-lane fp32 pairs of elements
-// (2q, 2q + 1); a bf16 granule gives four pairs, an fp32 granule two.
-template <bool BF16>
-struct Pairs {
-    static constexpr int kN = BF16 ? 4 : 2;
-};
-template <bool BF16>
-__device__ __forceinline__ void to_pairs(const uint4 w, uint64_t (&x2)[Pairs<BF16>::kN]) {
-    if constexpr (BF16) {
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            x2[q] = pk(__uint_as_float(u[q] << 16), __uint_as_float(u[q] & 0xffff0000u));
-    } else {
-        x2[0] = pk(__uint_as_float(w.x), __uint_as_float(w.y));
-        x2[1] = pk(__uint_as_float(w.z), __uint_as_float(w.w));
-    }
-}
-
-// Softcap of a pair: z = T tanh(x / T) (and 1 - tanh^2 when asked).
-template <bool SOFTCAP>
-__device__ __forceinline__ uint64_t cap_pair(uint64_t x2, float T, float k2, uint64_t *dz2) {
-    if constexpr (!SOFTCAP) {
-        return x2;
-    } else {
-        float a, b;
-        upk(x2, a, b);
-        const Capped ca = softcap_z<true>(a, T, k2), cb = softcap_z<true>(b, T, k2);
-        if (dz2) *dz2 = pk(ca.dz, cb.dz);
-        return pk(ca.z, cb.z);
-    }
-}
-
 // Pass-1 state of one thread.
 struct Acc {
-    float mv;       // max raw logit seen
-    int midx;       // its first column
-    float mz;       // z of mv: reference of s
-    uint64_t nmL2;  // (-mz log2e) twice
-    uint64_t s2;    // two-lane sums of exp(z - mz)
-    uint64_t z2;    // two-lane sums of z
+    float mv;      // max raw logit seen
+    int midx;      // its first column
+    float mz;      // z of mv: reference of s
+    float nmL;     // -mz log2e
+    float s0, s1;  // sums of exp(z - mz) (even, odd columns)
+    float z0, z1;  // sums of z
 };
 
-// New maximum gm in the granule starting at column jg with elements x:
-// locate its first column among the valid ones, rescale the running sums.
+// New maximum gm in the granule starting at column jg: locate its first
+// column among the valid ones, rescale the running sums.
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void new_max(Acc &a, const uint4 w, float gm, int jg, int V, float T,
-                                        float k2) {
+__device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPerGranule],
+                                        float gm, int jg, int V, float T, float k2) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
-    float x[EPG];
-    unpack<BF16>(w, x);
     int li = EPG - 1;
 #pragma unroll
     for (int l = EPG - 1; l >= 0; --l)
         if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
     const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
     const float f = ptx::ex2((a.mz - nz) * kLog2e);
-    float s0, s1;
-    upk(a.s2, s0, s1);
-    a.s2 = pk((s0 == 0.f) ? 0.f : s0 * f, (s1 == 0.f) ? 0.f : s1 * f);
+    a.s0 = (a.s0 == 0.f) ? 0.f : a.s0 * f;
+    a.s1 = (a.s1 == 0.f) ? 0.f : a.s1 * f;
     a.mv = gm;
     a.midx = jg + li;
     a.mz = nz;
-    a.nmL2 = pk(-nz * kLog2e, -nz * kLog2e);
+    a.nmL = -nz * kLog2e;
 }
 
 // Fold a whole granule (every column valid).
 template <bool BF16, bool SOFTCAP, bool SUMZ>
 __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, float T, float k2) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    float x[EPG];
+    unpack<BF16>(w, x);
     const float gm = granule_max<BF16>(w);
-    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, w, gm, jg, V, T, k2);
-    uint64_t x2[Pairs<BF16>::kN];
-    to_pairs<BF16>(w, x2);
-    const uint64_t L2 = pk(kLog2e, kLog2e);
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, T, k2);
 #pragma unroll
-    for (int q = 0; q < Pairs<BF16>::kN; ++q) {
-        const uint64_t z2 = cap_pair<SOFTCAP>(x2[q], T, k2, nullptr);
-        a.s2 = add2(a.s2, ex2x2(fma2(z2, L2, a.nmL2)));
-        if constexpr (SUMZ) a.z2 = add2(a.z2, z2);
+    for (int l = 0; l < EPG; l += 2) {
+        const float za = softcap_z<SOFTCAP>(x[l], T, k2).z;
+        const float zb = softcap_z<SOFTCAP>(x[l + 1], T, k2).z;
+        a.s0 += ptx::ex2(fmaf(za, kLog2e, a.nmL));
+        a.s1 += ptx::ex2(fmaf(zb, kLog2e, a.nmL));
+        if constexpr (SUMZ) {
+            a.z0 += za;
+            a.z1 += zb;
+        }
     }
 }
 
@@ -147,60 +116,48 @@ __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int 
 #pragma unroll
     for (int l = 0; l < EPG; ++l)
         if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
-    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, w, gm, jg, V, T, k2);
-    float s0, s1, z0, z1, nm, dummy;
-    upk(a.s2, s0, s1);
-    upk(a.z2, z0, z1);
-    upk(a.nmL2, nm, dummy);
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, T, k2);
 #pragma unroll
     for (int l = 0; l < EPG; ++l) {
         if (jg + l >= 0 && jg + l < V) {
             const float z = softcap_z<SOFTCAP>(x[l], T, k2).z;
-            s0 += ptx::ex2(fmaf(z, kLog2e, nm));
-            z0 += z;
+            a.s0 += ptx::ex2(fmaf(z, kLog2e, a.nmL));
+            a.z0 += z;
         }
     }
-    a.s2 = pk(s0, s1);
-    a.z2 = pk(z0, z1);
 }
 
 struct GradCoef {
-    uint64_t nlseL2;   // (-lse log2e) twice
-    uint64_t scale2;   // scale twice
-    uint64_t negc2;    // -scale eps / V twice
-    float scale, c_smooth, c_label;
-    float T, k2;
+    float nlseL;     // -lse log2e
+    float scale;     // grad_scale / n_valid (mean) or grad_scale (sum)
+    float c_smooth;  // scale eps / V
+    float c_label;   // scale (1 - eps + eps / V)
+    float T, k2;     // softcap and -2 log2e / T
 };
 
 // Gradients of the EPG elements of a granule, in fp32.
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, int label_lane,
                                             float (&g)[Elem<BF16>::kPerGranule]) {
-    uint64_t x2[Pairs<BF16>::kN];
-    to_pairs<BF16>(w, x2);
-    const uint64_t L2 = pk(kLog2e, kLog2e);
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    float x[EPG];
+    unpack<BF16>(w, x);
 #pragma unroll
-    for (int q = 0; q < Pairs<BF16>::kN; ++q) {
-        uint64_t dz2 = 0;
-        const uint64_t z2 = cap_pair<SOFTCAP>(x2[q], c.T, c.k2, &dz2);
-        const uint64_t p2 = ex2x2(fma2(z2, L2, c.nlseL2));  // p_j
-        uint64_t g2 = fma2(p2, c.scale2, c.negc2);          // scale (p_j - eps/V)
-        if constexpr (SOFTCAP) g2 = mul2(g2, dz2);
-        upk(g2, g[2 * q], g[2 * q + 1]);
-        if (label_lane >> 1 == q) {  // the label column: q_y = 1 - eps + eps/V (rare)
-            float pa, pb;
-            upk(p2, pa, pb);
-            const float pr = (label_lane & 1) ? pb : pa;
-            float gy = fmaf(pr, c.scale, -c.c_label);
-            if constexpr (SOFTCAP) {
-                float da, db;
-                upk(dz2, da, db);
-                gy *= (label_lane & 1) ? db : da;
+    for (int l = 0; l < EPG; ++l) {
+        const Capped cz = softcap_z<SOFTCAP>(x[l], c.T, c.k2);
+        const float pr = ptx::ex2(fmaf(cz.z, kLog2e, c.nlseL));  // p_j
+        g[l] = fmaf(pr, c.scale, -c.c_smooth);                   // scale (p_j - eps/V)
+        if constexpr (SOFTCAP) g[l] *= cz.dz;
+    }
+    if (label_lane >= 0) {  // the label column: q_y = 1 - eps + eps/V (rare)
+#pragma unroll
+        for (int l = 0; l < EPG; ++l) {
+            if (l == label_lane) {
+                const Capped cz = softcap_z<SOFTCAP>(x[l], c.T, c.k2);
+                const float pr = ptx::ex2(fmaf(cz.z, kLog2e, c.nlseL));
+                g[l] = fmaf(pr, c.scale, -c.c_label);
+                if constexpr (SOFTCAP) g[l] *= cz.dz;
             }
-            if (label_lane & 1)
-                g[2 * q + 1] = gy;
-            else
-                g[2 * q] = gy;
         }
     }
 }
@@ -243,7 +200,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     // granule G - 1 when the row does not end on a granule boundary.
     const int gs = lead > 0 ? 1 : 0;
     const int ge = ((lead + p.V) % EPG != 0) ? G - 1 : G;
-    const bool head = gs == 1;                  // granule 0 partial (thread 0)
+    const bool head = gs == 1;                     // granule 0 partial (thread 0)
     const bool tail = ge == G - 1 && G - 1 >= gs;  // granule G-1 partial, distinct from 0
     const int tail_tid = tail ? (G - 1 - gs) % kThreads : -1;
     const float T = p.softcap;
@@ -254,9 +211,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     a.mv = -INFINITY;
     a.midx = INT_MAX;
     a.mz = -INFINITY;
-    a.nmL2 = pk(INFINITY, INFINITY);
-    a.s2 = pk(0.f, 0.f);
-    a.z2 = pk(0.f, 0.f);
+    a.nmL = INFINITY;
+    a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
     if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, T, k2);
     for (int gl = gs + tid; gl < ge; gl += kThreads)
         fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
@@ -267,13 +223,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     pt.mx = a.mv;
     pt.idx = a.midx;
     pt.mz = a.mz;
-    {
-        float s0, s1, z0, z1;
-        upk(a.s2, s0, s1);
-        upk(a.z2, z0, z1);
-        pt.s = s0 + s1;
-        pt.sz = z0 + z1;
-    }
+    pt.s = a.s0 + a.s1;
+    pt.sz = a.z0 + a.z1;
     warp_allreduce(pt);
     if (lane == 0) wpart[warp] = pt;
 
@@ -310,16 +261,13 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     if (valid) {
         ptx::griddep_wait();  // the label census of this call
         const int64_t n_valid = p.counts[0];
-        float scale = p.grad_scale;
-        if (p.reduction == VLMCE_MEAN)
-            scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
         GradCoef c;
-        c.scale = scale;
-        c.c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
-        c.c_label = c.c_smooth + scale * (1.f - p.eps);          // + scale (1 - eps)
-        c.nlseL2 = pk(-*bcast * kLog2e, -*bcast * kLog2e);
-        c.scale2 = pk(scale, scale);
-        c.negc2 = pk(-c.c_smooth, -c.c_smooth);
+        c.scale = p.grad_scale;
+        if (p.reduction == VLMCE_MEAN)
+            c.scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
+        c.c_smooth = c.scale * (p.eps / static_cast<float>(p.V));
+        c.c_label = c.c_smooth + c.scale * (1.f - p.eps);
+        c.nlseL = -*bcast * kLog2e;
         c.T = T;
         c.k2 = k2;
         const int gy = static_cast<int>((y + lead) / EPG);
@@ -348,8 +296,10 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     }
 }
 
+// Two CTAs per SM (32 registers per thread); the softcap's extra arithmetic
+// needs more registers than that, so its kernels run one CTA per SM.
 template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(kThreads, 2) ce_rows_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, SOFTCAP ? 1 : 2) ce_rows_kernel(const Params p) {
     __shared__ RowPart wpart[kWarps];
     __shared__ float bcast;
     // sum z only matters with label smoothing; skip the adds without it
