@@ -119,6 +119,35 @@ vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int6
                         void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
 
 /*
+ * ce_fwd_bwd_noalloc -- ce_fwd_bwd without a workspace argument, for callers
+ * that cannot allocate device memory (for instance code inside a framework
+ * whose allocator owns all device memory, or latency-critical code that
+ * cannot afford cudaMalloc's implicit device synchronisation).  The pages have
+ * no counterpart of this entry point; it exists for such callers only.
+ *
+ * Arguments, outputs, errors and results are those of ce_fwd_bwd.  Its
+ * scratch is a fixed array of 786,688 bytes in the library's device image
+ * (256 B + 12 B per row), which every GPU that loads the library holds until
+ * the process exits.  N may not exceed vlmce_ce_noalloc_max_rows() (65536):
+ * larger N returns VLMCE_ERR_TOO_LARGE before anything is enqueued.  No
+ * device memory is allocated or freed.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Every call on a device shares the one array:
+ * calls that overlap on the GPU (different streams without ordering between
+ * them) race on it and must not be issued; calls ordered on one stream are
+ * safe.  The array keeps the last call's contents, none of which a call needs
+ * to start at zero.
+ */
+vlmce_status ce_fwd_bwd_noalloc(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                                int64_t V, int64_t row_stride, int64_t ignore_index,
+                                float label_smoothing, float softcap, int32_t reduction,
+                                float grad_scale, float *out_loss, int64_t *out_argmax,
+                                float *out_reduced, int64_t *out_counts, vlmce_stream_t stream);
+
+/* Rows ce_fwd_bwd_noalloc accepts (the size of its fixed scratch). */
+int64_t vlmce_ce_noalloc_max_rows(void);
+
+/*
  * Profiling hook: the next ce_fwd_bwd call made by this host thread records
  * `ev_begin` immediately before and `ev_end` immediately after its row kernel
  * (the dominant kernel) on the call's stream, then forgets both.  The two
