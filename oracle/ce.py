@@ -58,6 +58,9 @@ def _load():
             lib.oracle_ce_reduce.restype = None
             lib.oracle_round_bf16.argtypes = [vp, vp, i64]
             lib.oracle_round_bf16.restype = None
+            lib.oracle_ce_grad_columns.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp, vp, dbl,
+                                                   dbl, vp]
+            lib.oracle_ce_grad_columns.restype = None
             lib.oracle_default_threads.argtypes = []
             lib.oracle_default_threads.restype = i32
             _lib = lib
@@ -144,6 +147,24 @@ def ce_fwd_bwd(x: np.ndarray, dtype: str, V: int, labels: np.ndarray, *, ignore_
     red, acc, n_correct = reduce(loss, amax, labels, V, ignore_index, reduction)
     return dict(loss=loss, argmax=amax, grad=grad, reduced_loss=red, accuracy=acc,
                 n_valid=n_valid, n_correct=n_correct, n_bad=n_bad, row_scale=s)
+
+
+def grad_columns(x: np.ndarray, cols: np.ndarray, V: int, labels: np.ndarray, lse: np.ndarray,
+                 row_scale: np.ndarray, *, ignore_index: int = -100, label_smoothing: float = 0.0,
+                 softcap: float = 0.0) -> np.ndarray:
+    """Gradient of columns `cols` (fp64 logits x [n, len(cols)]) given each row's lse and scale."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    n, m = x.shape
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    sc = np.ascontiguousarray(row_scale, dtype=np.float64)
+    assert cols.shape == (m,) and lab.shape == (n,) and lse.shape == (n,) and sc.shape == (n,)
+    g = np.zeros((n, m), np.float64)
+    _load().oracle_ce_grad_columns(_ptr(x), n, m, _ptr(cols), V, _ptr(lab), ignore_index,
+                                   _ptr(lse), _ptr(sc), float(label_smoothing), float(softcap),
+                                   _ptr(g))
+    return g
 
 
 def round_bf16(values: np.ndarray) -> np.ndarray:

@@ -226,6 +226,40 @@ int oracle_ce_rows(const void *x, int dtype, int64_t n_rows, int64_t V, int64_t 
 }
 
 /*
+ * Gradient of some columns of some rows when the row's log-sum-exp is known
+ * (the full-vocabulary sum is formed elsewhere): the gradient line of
+ * one_row(), g_j = scale_r (exp(z_j - lse_r) - q_j) (T > 0 ? 1 - t_j^2 : 1),
+ * for x: n_rows x n_cols fp64 logits of columns col[0..n_cols) of a V-wide
+ * vocabulary; q_j = eps/V + (col[j] == y_r ? 1 - eps : 0).  Rows whose
+ * label is ignore_index or outside [0, V) get zeros.
+ */
+void oracle_ce_grad_columns(const double *x, int64_t n_rows, int64_t n_cols, const int64_t *col,
+                            int64_t V, const int64_t *labels, int64_t ignore_index,
+                            const double *lse, const double *scale, double eps, double softcap,
+                            double *grad) {
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t y = labels[r];
+        const int valid = y != ignore_index && y >= 0 && y < V;
+        for (int64_t j = 0; j < n_cols; ++j) {
+            double g = 0.0;
+            if (valid) {
+                const double xj = x[r * n_cols + j];
+                double t = 0.0, z = xj;
+                if (softcap > 0.0) {
+                    t = tanh(xj / softcap);
+                    z = softcap * t;
+                }
+                const double q = eps / (double)V + (col[j] == y ? 1.0 - eps : 0.0);
+                g = exp(z - lse[r]) - q;
+                if (softcap > 0.0) g *= 1.0 - t * t;
+                g *= scale[r];
+            }
+            grad[r * n_cols + j] = g;
+        }
+    }
+}
+
+/*
  * Label census: n_valid = #labels in [0, V); n_bad = #labels that are neither
  * ignore_index nor in [0, V).  The mean reduction divides by n_valid.
  */
