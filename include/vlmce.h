@@ -118,6 +118,57 @@ vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int6
                         int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
                         void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
 
+/* Bytes of device workspace flce_fwd_bwd needs (256-byte aligned): per-row
+ * statistics of every 256-column logits tile, a bf16 [N, 8192] gradient tile
+ * and an fp32 [N, H] grad_hidden accumulator. */
+size_t vlmce_flce_workspace_bytes(int64_t N, int64_t H, int64_t V);
+
+/*
+ * flce_fwd_bwd -- fused linear cross-entropy forward + backward: the logits
+ * S = h' W^T are formed tile by tile on the tensor cores and never stored as an
+ * [N, V] tensor ("Add Liger Kernel support for Muse Glimmer", Summary and
+ * Details: Softcap; its Memory section: grad_weight in fp32).
+ *
+ * hidden       bf16 [N, hidden_stride], rows of H valid elements: h' = m h, the
+ *              hidden states already multiplied by the logit multiplier m.
+ * weight       bf16 [V, weight_stride], rows of H valid elements (lm_head).
+ * labels, ignore_index, label_smoothing, softcap, reduction, grad_scale,
+ * out_loss, out_argmax, out_reduced, out_counts: as ce_fwd_bwd, applied to
+ *              the logits S (argmax over the fp32 S).
+ * grad_hidden  out: bf16 [N, hidden_stride], d(grad_scale * loss) / d h'
+ *              (the caller multiplies by m for d / d h).
+ * grad_weight  fp32 [V, H] contiguous: overwritten with d(...)/dW, or added
+ *              to when accumulate_grad_weight != 0.
+ * workspace    >= vlmce_flce_workspace_bytes(N, H, V) bytes, 256-byte aligned.
+ * H, hidden_stride, weight_stride must be multiples of 8; every pointer
+ * 16-byte aligned.  bf16 only (like the native Blackwell path on the pages).
+ * Deterministic: no floating-point atomics.
+ */
+vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, const void *weight,
+                          int64_t weight_stride, const int64_t *labels, int64_t N, int64_t H,
+                          int64_t V, int64_t ignore_index, float label_smoothing, float softcap,
+                          int32_t reduction, float grad_scale, float *out_loss,
+                          int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
+                          void *grad_hidden, float *grad_weight, int32_t accumulate_grad_weight,
+                          void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
+
+/*
+ * vlmce_gemm_bf16 -- the library's tcgen05 GEMM on its own:
+ * C[M, N] (+)= A[M, K] B[N, K]^T, bf16 inputs, fp32 accumulation and output.
+ * A is stored K-major ([M, lda], a_mn = 0) or M-major ([K, lda], a_mn = 1);
+ * B is stored K-major ([N, ldb], b_mn = 0) or N-major ([K, ldb], b_mn = 1);
+ * C is [M, ldc] fp32.  lda, ldb multiples of 8, ldc of 4, pointers 16-byte
+ * aligned.  accumulate != 0 adds to C.
+ */
+vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void *B, int32_t b_mn, float *C,
+                             int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                             int64_t ldc, int32_t accumulate, vlmce_stream_t stream);
+
+/* Profiling hook of flce_fwd_bwd: like vlmce_profile_events, the next call on
+ * this host thread records the two events around its tensor-core work (the
+ * statistics GEMM, the row merge and every chunk's three GEMMs). */
+void vlmce_flce_profile_events(void *ev_begin, void *ev_end);
+
 /*
  * ce_fwd_bwd_noalloc -- ce_fwd_bwd without a workspace argument, for callers
  * that cannot allocate device memory (for instance code inside a framework

@@ -49,6 +49,12 @@ SIGNATURES = {
     "ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32,
                                   _vp, _vp, _vp, _vp, _vp]),
     "vlmce_ce_noalloc_max_rows": (_i64, []),
+    "vlmce_flce_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "flce_fwd_bwd": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32,
+                            _f32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "vlmce_gemm_bf16": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
+                               _i32, _vp]),
+    "vlmce_flce_profile_events": (None, [_vp, _vp]),
 }
 
 

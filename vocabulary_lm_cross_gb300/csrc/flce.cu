@@ -1,0 +1,483 @@
+// flce.cu -- entry point flce_fwd_bwd: fused linear cross-entropy forward +
+// backward, and vlmce_gemm_bf16 (the tcgen05 GEMM engine on its own).
+//
+// Method ("Add Liger Kernel support for Muse Glimmer", Summary and Details):
+// the lm_head product h' W^T is never materialised as an [N, V] tensor; the
+// softcap multiplier is folded into the hidden states by the caller; grad
+// weight is accumulated in fp32.
+//
+// Schedule (V-chunked, logits recomputed; all products on tcgen05):
+//   1. label census                                            (1 CTA)
+//   2. S = h' W^T over the whole vocabulary, epilogue = per (row, 256-column
+//      tile) statistics: max / first argmax of S, online sum exp(z - m),
+//      sum z, z at the label                                   (GEMM, kStats)
+//   3. per row: merge the tile statistics in column order -> lse, loss,
+//      argmax, gradient scale                                  (1 warp / row)
+//   4. for each chunk of Vc = 8192 vocabulary columns:
+//        G_c = scale (softmax - q) (1 - t^2), recomputed from S_c = h' W_c^T
+//              and stored in bf16 [N, Vc]                      (GEMM, kGrad)
+//        grad_h  (+)= G_c W_c  (fp32 [N, H]; the last chunk writes bf16)
+//        grad_W_c (+)= G_c^T h' (fp32, rows of the chunk)
+//   5. reduced loss and accuracy                               (1 CTA)
+// Executed tensor work 8 N V H (the logits twice); algorithmic 6 N V H.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "ce_common.cuh"
+#include "gemm_launch.h"
+#include "host_util.h"
+#include "ptx.cuh"
+#include "vlmce.h"
+
+namespace vlmce {
+namespace flce {
+namespace {
+
+using ce::RowPart;
+
+constexpr int kChunk = 8192;  // vocabulary columns per gradient chunk
+constexpr int64_t kWsHeader = 256;
+
+// ----------------------------------------------------------------- kernels
+
+__global__ void __launch_bounds__(1024) flce_count_kernel(const int64_t *__restrict__ labels,
+                                                          int64_t N, int64_t V, int64_t ignore_index,
+                                                          int64_t *counts, int *err) {
+    long long nv = 0, nb = 0;
+    for (int64_t r = threadIdx.x; r < N; r += blockDim.x) {
+        const int64_t y = labels[r];
+        if (y == ignore_index) continue;
+        if (y >= 0 && y < V)
+            ++nv;
+        else
+            ++nb;
+    }
+    __shared__ long long sv[32], sb[32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        nv += __shfl_xor_sync(0xffffffffu, nv, off);
+        nb += __shfl_xor_sync(0xffffffffu, nb, off);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        sv[warp] = nv;
+        sb[warp] = nb;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        nv = lane < static_cast<int>(blockDim.x >> 5) ? sv[lane] : 0;
+        nb = lane < static_cast<int>(blockDim.x >> 5) ? sb[lane] : 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            nv += __shfl_xor_sync(0xffffffffu, nv, off);
+            nb += __shfl_xor_sync(0xffffffffu, nb, off);
+        }
+        if (lane == 0) {
+            counts[0] = nv;
+            counts[1] = nb;
+            *err = 0;
+        }
+    }
+}
+
+// One warp per row: merge the row's tile statistics (fixed order) into lse,
+// loss, argmax and the gradient scale of the row.
+__global__ void __launch_bounds__(256) flce_merge_kernel(
+    const RowPart *__restrict__ part, int64_t part_ld, int ntiles, const int64_t *__restrict__ labels,
+    int64_t N, int64_t V, int64_t ignore_index, float eps, float grad_scale, int reduction,
+    const int64_t *counts, float *lse, float *row_scale, float *loss, int64_t *argmax) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    RowPart a = ce::part_identity();
+    for (int t = lane; t < ntiles; t += 32) {
+        const RowPart p = part[static_cast<int64_t>(t) * part_ld + row];
+        ce::part_merge(a, p.mx, p.idx, p.mz, p.s, p.sz, p.zy);
+    }
+    ce::warp_allreduce(a);
+    if (lane == 0) {
+        const float l = a.mz + logf(a.s);
+        const int64_t y = labels[row];
+        const bool ignored = y == ignore_index;
+        const bool valid = !ignored && y >= 0 && y < V;
+        float sc = 0.f;
+        if (valid) {
+            sc = grad_scale;
+            if (reduction == VLMCE_MEAN) {
+                const long long nv = counts[0];
+                sc = nv > 0 ? grad_scale / static_cast<float>(nv) : 0.f;
+            }
+        }
+        lse[row] = l;
+        row_scale[row] = sc;
+        float lo = 0.f;
+        if (valid)
+            lo = l - fmaf(1.f - eps, a.zy, (eps / static_cast<float>(V)) * a.sz);
+        else if (!ignored)
+            lo = __int_as_float(0x7fc00000);
+        loss[row] = lo;
+        argmax[row] = a.idx;
+    }
+}
+
+__global__ void __launch_bounds__(1024) flce_finalize_kernel(
+    const float *__restrict__ loss, const int64_t *__restrict__ argmax,
+    const int64_t *__restrict__ labels, int64_t N, int64_t V, int64_t ignore_index, int reduction,
+    const int64_t *counts, const int *err, float *out_reduced, int64_t *out_counts) {
+    double acc = 0.0;
+    long long nc = 0;
+    for (int64_t r = threadIdx.x; r < N; r += blockDim.x) {
+        const int64_t y = labels[r];
+        if (y == ignore_index) continue;
+        acc += static_cast<double>(loss[r]);
+        if (y >= 0 && y < V && argmax[r] == y) ++nc;
+    }
+    __shared__ double sa[32];
+    __shared__ long long sc[32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        nc += __shfl_xor_sync(0xffffffffu, nc, off);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        sa[warp] = acc;
+        sc[warp] = nc;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        acc = lane < static_cast<int>(blockDim.x >> 5) ? sa[lane] : 0.0;
+        nc = lane < static_cast<int>(blockDim.x >> 5) ? sc[lane] : 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            nc += __shfl_xor_sync(0xffffffffu, nc, off);
+        }
+        if (lane == 0) {
+            const long long nv = counts[0];
+            double red = acc;
+            if (reduction == VLMCE_MEAN) red = nv > 0 ? acc / static_cast<double>(nv) : 0.0;
+            const double accuracy = nv > 0 ? static_cast<double>(nc) / static_cast<double>(nv) : 0.0;
+            if (out_reduced) {
+                out_reduced[0] = static_cast<float>(red);
+                out_reduced[1] = static_cast<float>(accuracy);
+            }
+            if (out_counts) {
+                out_counts[0] = nv;
+                out_counts[1] = nc;
+                out_counts[2] = counts[1];
+                out_counts[3] = *err;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- TMA maps
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static std::once_flag once;
+    static EncodeTiled fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// A bf16 matrix of `outer` rows of `inner` elements (row stride `stride`
+// elements), read in boxes of box_inner x box_outer with 128-byte swizzle;
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
+              uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand maps for C[M, N] = A[M, K] B[N, K]^T: K-major operands are boxes of
+// 64 K x rows; MN-major ones 64 M/N x 64 K (see gemm.cuh).
+bool map_a(CUtensorMap *m, const void *A, bool mn, int64_t M, int64_t K, int64_t ld) {
+    return mn ? make_map(m, A, M, K, ld, 64, 64) : make_map(m, A, K, M, ld, 64, gemm::BM);
+}
+bool map_b(CUtensorMap *m, const void *B, bool mn, int64_t N, int64_t K, int64_t ld) {
+    return mn ? make_map(m, B, N, K, ld, 64, 64) : make_map(m, B, K, N, ld, 64, gemm::BN);
+}
+
+cudaError_t launch(bool a_mn, bool b_mn, int mode, const CUtensorMap &ma, const CUtensorMap &mb,
+                   const gemm::Args &args, int sm_count, cudaStream_t s) {
+    const int64_t tiles = static_cast<int64_t>((args.M + gemm::BM - 1) / gemm::BM) *
+                          ((args.N + gemm::BN - 1) / gemm::BN);
+    const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+    if (grid < 1) return cudaSuccess;
+    if (!a_mn && !b_mn) return gemm::launch_kk(mode, ma, mb, args, grid, s);
+    if (!a_mn && b_mn) return gemm::launch_km(mode, ma, mb, args, grid, s);
+    if (a_mn && !b_mn) return gemm::launch_mk(mode, ma, mb, args, grid, s);
+    return gemm::launch_mm(mode, ma, mb, args, grid, s);
+}
+
+// ----------------------------------------------------------------- workspace
+struct Ws {
+    int64_t *counts;
+    int *err;
+    RowPart *part;  // [ntiles][N]
+    float *lse, *row_scale, *loss;
+    int64_t *argmax;
+    __nv_bfloat16 *g;  // [N, kChunk]
+    float *gh;         // [N, H] grad_h accumulator
+};
+
+int64_t ntiles_of(int64_t V) { return (V + gemm::BN - 1) / gemm::BN; }
+
+size_t ws_bytes(int64_t N, int64_t H, int64_t V) {
+    int64_t b = kWsHeader;
+    b += round_up(ntiles_of(V) * N * static_cast<int64_t>(sizeof(RowPart)), 256);
+    b += 3 * round_up(4 * N, 256) + round_up(8 * N, 256);
+    b += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
+    b += round_up(4 * N * H, 256);
+    return static_cast<size_t>(b);
+}
+
+Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
+    unsigned char *p = static_cast<unsigned char *>(ws);
+    Ws w;
+    w.counts = reinterpret_cast<int64_t *>(p);
+    w.err = reinterpret_cast<int *>(p + 64);
+    p += kWsHeader;
+    w.part = reinterpret_cast<RowPart *>(p);
+    p += round_up(ntiles_of(V) * N * static_cast<int64_t>(sizeof(RowPart)), 256);
+    w.lse = reinterpret_cast<float *>(p);
+    p += round_up(4 * N, 256);
+    w.row_scale = reinterpret_cast<float *>(p);
+    p += round_up(4 * N, 256);
+    w.loss = reinterpret_cast<float *>(p);
+    p += round_up(4 * N, 256);
+    w.argmax = reinterpret_cast<int64_t *>(p);
+    p += round_up(8 * N, 256);
+    w.g = reinterpret_cast<__nv_bfloat16 *>(p);
+    p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
+    w.gh = reinterpret_cast<float *>(p);
+    return w;
+}
+
+thread_local cudaEvent_t t_prof_begin = nullptr;
+thread_local cudaEvent_t t_prof_end = nullptr;
+
+}  // namespace
+}  // namespace flce
+}  // namespace vlmce
+
+using namespace vlmce;
+using namespace vlmce::flce;
+
+extern "C" void vlmce_flce_profile_events(void *ev_begin, void *ev_end) {
+    t_prof_begin = static_cast<cudaEvent_t>(ev_begin);
+    t_prof_end = static_cast<cudaEvent_t>(ev_end);
+}
+
+extern "C" size_t vlmce_flce_workspace_bytes(int64_t N, int64_t H, int64_t V) {
+    if (N < 0 || H < 1 || V < 1) return 0;
+    return ws_bytes(N, H, V);
+}
+
+extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void *B, int32_t b_mn,
+                                        float *C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                        int64_t ldb, int64_t ldc, int32_t accumulate,
+                                        vlmce_stream_t stream) {
+    if (!A || !B || !C || M < 1 || N < 1 || K < 1) return VLMCE_ERR_INVALID_ARG;
+    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+    if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N) return VLMCE_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || lda % 8 || ldb % 8 || ldc % 4)
+        return VLMCE_ERR_MISALIGNED;
+    DeviceInfo dev;
+    vlmce_status st = current_device(&dev);
+    if (st != VLMCE_OK) return st;
+    CUtensorMap ma, mb;
+    if (!map_a(&ma, A, a_mn != 0, M, K, lda) || !map_b(&mb, B, b_mn != 0, N, K, ldb)) {
+        record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+        return VLMCE_ERR_CUDA;
+    }
+    gemm::Args g = {};
+    g.M = static_cast<int>(M);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    g.C = C;
+    g.ldc = ldc;
+    g.err = nullptr;  // no device error word: a wait that gives up only ends the kernel
+    return launch_status(launch(a_mn != 0, b_mn != 0, accumulate ? gemm::kAccF32 : gemm::kStoreF32,
+                                ma, mb, g, dev.sm_count, reinterpret_cast<cudaStream_t>(stream)),
+                         "vlmce_gemm_kernel");
+}
+
+extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, const void *weight,
+                                     int64_t weight_stride, const int64_t *labels, int64_t N,
+                                     int64_t H, int64_t V, int64_t ignore_index,
+                                     float label_smoothing, float softcap, int32_t reduction,
+                                     float grad_scale, float *out_loss, int64_t *out_argmax,
+                                     float *out_reduced, int64_t *out_counts, void *grad_hidden,
+                                     float *grad_weight, int32_t accumulate_grad_weight,
+                                     void *workspace, size_t workspace_bytes_given,
+                                     vlmce_stream_t stream) {
+    // ---- host-side argument checks; nothing is enqueued on failure
+    if (N < 0 || H < 1 || V < 1) return VLMCE_ERR_INVALID_ARG;
+    if (N > INT_MAX || H > INT_MAX || V > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+    if (hidden_stride < H || weight_stride < H) return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && (!hidden || !weight || !labels || !grad_hidden || !grad_weight))
+        return VLMCE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
+    if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes_given < ws_bytes(N, H, V)) return VLMCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return VLMCE_ERR_MISALIGNED;
+    if (N > 0 && (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(grad_hidden, 16) ||
+                  !aligned(grad_weight, 16) || !aligned(labels, 8)))
+        return VLMCE_ERR_MISALIGNED;
+    if (H % 8 || hidden_stride % 8 || weight_stride % 8) return VLMCE_ERR_MISALIGNED;
+    if ((out_loss && !aligned(out_loss, 4)) || (out_argmax && !aligned(out_argmax, 8)) ||
+        (out_reduced && !aligned(out_reduced, 4)) || (out_counts && !aligned(out_counts, 8)))
+        return VLMCE_ERR_MISALIGNED;
+
+    DeviceInfo dev;
+    vlmce_status st = current_device(&dev);
+    if (st != VLMCE_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    Ws w = carve(workspace, N, H, V);
+    float *loss = out_loss ? out_loss : w.loss;
+    int64_t *amax = out_argmax ? out_argmax : w.argmax;
+
+    flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
+    st = launch_status(cudaSuccess, "flce_count_kernel");
+    if (st != VLMCE_OK) return st;
+
+    if (N > 0) {
+        const float T = softcap;
+        gemm::Args base = {};
+        base.labels = labels;
+        base.ignore_index = ignore_index;
+        base.V = static_cast<int>(V);
+        base.eps = label_smoothing;
+        base.T = T;
+        base.k2 = T > 0.f ? -2.f * ce::kLog2e / T : 0.f;
+        base.err = w.err;
+
+        cudaEvent_t eb = t_prof_begin, ee = t_prof_end;
+        t_prof_begin = t_prof_end = nullptr;
+        if (eb && (st = launch_status(cudaEventRecord(eb, cs), "cudaEventRecord")) != VLMCE_OK)
+            return st;
+
+        // ---- pass 1: statistics of S = h' W^T over the whole vocabulary
+        CUtensorMap m_h, m_w;
+        if (!map_a(&m_h, hidden, false, N, H, hidden_stride) ||
+            !map_b(&m_w, weight, false, V, H, weight_stride)) {
+            record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+            return VLMCE_ERR_CUDA;
+        }
+        gemm::Args s1 = base;
+        s1.M = static_cast<int>(N);
+        s1.N = static_cast<int>(V);
+        s1.K = static_cast<int>(H);
+        s1.col0 = 0;
+        s1.part = w.part;
+        s1.part_ld = N;
+        st = launch_status(launch(false, false, gemm::kStats, m_h, m_w, s1, dev.sm_count, cs),
+                           "vlmce_gemm_kernel(stats)");
+        if (st != VLMCE_OK) return st;
+
+        flce_merge_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, cs>>>(
+            w.part, N, static_cast<int>(ntiles_of(V)), labels, N, V, ignore_index, label_smoothing,
+            grad_scale, reduction, w.counts, w.lse, w.row_scale, loss, amax);
+        st = launch_status(cudaSuccess, "flce_merge_kernel");
+        if (st != VLMCE_OK) return st;
+
+        // ---- pass 2: per vocabulary chunk, the gradient tile and the two products
+        CUtensorMap m_ht;  // h' as the N(=H)-major B of grad_W = G^T h'
+        if (!map_b(&m_ht, hidden, true, H, N, hidden_stride)) {
+            record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+            return VLMCE_ERR_CUDA;
+        }
+        const int64_t nchunks = (V + kChunk - 1) / kChunk;
+        for (int64_t c = 0; c < nchunks; ++c) {
+            const int64_t v0 = c * kChunk;
+            const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
+            const __nv_bfloat16 *wc =
+                reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
+            CUtensorMap m_wc, m_g, m_wcn, m_gt;
+            if (!map_b(&m_wc, wc, false, vc, H, weight_stride) ||  // W_c, K-major B of S_c
+                !map_a(&m_g, w.g, false, N, vc, kChunk) ||         // G_c, K-major A of grad_h
+                !map_b(&m_wcn, wc, true, H, vc, weight_stride) ||  // W_c, N-major B of grad_h
+                !map_a(&m_gt, w.g, true, vc, N, kChunk)) {         // G_c^T, M-major A of grad_W
+                record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+                return VLMCE_ERR_CUDA;
+            }
+            // G_c = scale (softmax - q) (1 - t^2) from the recomputed logits
+            gemm::Args g1 = base;
+            g1.M = static_cast<int>(N);
+            g1.N = static_cast<int>(vc);
+            g1.K = static_cast<int>(H);
+            g1.col0 = static_cast<int>(v0);
+            g1.C16 = w.g;
+            g1.ldc16 = kChunk;
+            g1.lse = w.lse;
+            g1.row_scale = w.row_scale;
+            st = launch_status(launch(false, false, gemm::kGrad, m_h, m_wc, g1, dev.sm_count, cs),
+                               "vlmce_gemm_kernel(grad tile)");
+            if (st != VLMCE_OK) return st;
+            // grad_h (+)= G_c W_c
+            gemm::Args g3 = base;
+            g3.M = static_cast<int>(N);
+            g3.N = static_cast<int>(H);
+            g3.K = static_cast<int>(vc);
+            g3.C = w.gh;
+            g3.ldc = H;
+            g3.C16 = static_cast<__nv_bfloat16 *>(grad_hidden);
+            g3.ldc16 = hidden_stride;
+            const int mode3 = nchunks == 1 ? gemm::kStoreBF16
+                              : c == 0        ? gemm::kStoreF32
+                              : c == nchunks - 1 ? gemm::kAccToBF16
+                                                 : gemm::kAccF32;
+            st = launch_status(launch(false, true, mode3, m_g, m_wcn, g3, dev.sm_count, cs),
+                               "vlmce_gemm_kernel(grad_hidden)");
+            if (st != VLMCE_OK) return st;
+            // grad_W_c (+)= G_c^T h'
+            gemm::Args g2 = base;
+            g2.M = static_cast<int>(vc);
+            g2.N = static_cast<int>(H);
+            g2.K = static_cast<int>(N);
+            g2.C = grad_weight + v0 * H;
+            g2.ldc = H;
+            st = launch_status(launch(true, true, accumulate_grad_weight ? gemm::kAccF32
+                                                                         : gemm::kStoreF32,
+                                      m_gt, m_ht, g2, dev.sm_count, cs),
+                               "vlmce_gemm_kernel(grad_weight)");
+            if (st != VLMCE_OK) return st;
+        }
+        if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
+            return st;
+    }
+
+    flce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index, reduction,
+                                             w.counts, w.err, out_reduced, out_counts);
+    return launch_status(cudaSuccess, "flce_finalize_kernel");
+}

@@ -1,0 +1,35 @@
+// gemm_km.cu -- tcgen05 GEMM instantiations: A K-major, B MN-major.
+#include "gemm_launch.h"
+
+namespace vlmce {
+namespace gemm {
+namespace {
+template <int MODE>
+cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const Args &args, int grid,
+                       cudaStream_t s) {
+    auto kern = vlmce_gemm_kernel<MODE, false, true>;
+    static bool attr_set = false;  // per process; the attribute is per function
+    if (!attr_set) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<grid, kThreads, kSmemBytes, s>>>(a, b, args);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_km(int mode, const CUtensorMap &a, const CUtensorMap &b, const Args &args,
+                      int grid, cudaStream_t s) {
+    switch (mode) {
+        case kStoreF32: return launch_one<kStoreF32>(a, b, args, grid, s);
+        case kAccF32: return launch_one<kAccF32>(a, b, args, grid, s);
+        case kStoreBF16: return launch_one<kStoreBF16>(a, b, args, grid, s);
+        case kAccToBF16: return launch_one<kAccToBF16>(a, b, args, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gemm
+}  // namespace vlmce
