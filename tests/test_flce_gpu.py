@@ -1,0 +1,168 @@
+"""GPU parity of the tcgen05 GEMM engine and of flce_fwd_bwd (through the C
+ABI) against matmuls of the same bf16 values and the fp64 FLCE oracle.
+
+Tolerances: GEMM fp32 results within 1e-5 of the largest reference magnitude
+(fp32 accumulation of exact bf16 products); FLCE per-token loss 1e-4
+absolute; argmax exact except on rows whose two largest fp64 logits are
+closer than 1e-3 max(1, |top|) (fp32 accumulation may order such near-ties
+differently; such rows are counted and reported); gradients within 1e-2
+relative L2 (the gradient tile is rounded to bf16 before the two gradient
+products, as the pages' fused path does); reduced loss 1e-4 (mean) /
+1e-6 relative (sum).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import flce as of
+from tests.parity import bf16_bits_np, check_loss, check_reduced
+from vocabulary_lm_cross_gb300 import capi
+from vocabulary_lm_cross_gb300.flce import flce_fwd_bwd
+from vocabulary_lm_cross_gb300.workloads import (FLCE_WORKLOADS, IGNORE_INDEX, FLCEWorkload,
+                                                 make_flce_inputs)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from vocabulary_lm_cross_gb300 import build
+    build.build()
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def gemm(A, a_mn, B, b_mn, C, M, N, K, accumulate=False):
+    st = capi.lib().vlmce_gemm_bf16(A.data_ptr(), int(a_mn), B.data_ptr(), int(b_mn), C.data_ptr(),
+                                    M, N, K, A.stride(0), B.stride(0), C.stride(0), int(accumulate),
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    capi.check(st, "vlmce_gemm_bf16")
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (1000, 264, 1032)])
+def test_gemm_engine_against_matmul(a_mn, b_mn, M, N, K):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(M * 7 + N * 3 + K + 10 * a_mn + b_mn)
+    Al = torch.randn(M, K, generator=g, device=DEV).to(torch.bfloat16)  # logical A [M, K]
+    Bl = torch.randn(N, K, generator=g, device=DEV).to(torch.bfloat16)  # logical B [N, K]
+    A = Al.t().contiguous() if a_mn else Al
+    B = Bl.t().contiguous() if b_mn else Bl
+    ref = Al.double() @ Bl.double().t()
+    C = torch.full((M, N), 3.0, dtype=torch.float32, device=DEV)
+    gemm(A, a_mn, B, b_mn, C, M, N, K)
+    torch.cuda.synchronize()
+    err = (C.double() - ref).abs().max().item()
+    assert err <= 1e-5 * ref.abs().max().item(), err
+    gemm(A, a_mn, B, b_mn, C, M, N, K, accumulate=True)
+    torch.cuda.synchronize()
+    err = (C.double() - 2 * ref).abs().max().item()
+    assert err <= 2e-5 * ref.abs().max().item(), err
+
+
+def near_tie_rows(h64, W64, labels=None):
+    S = h64 @ W64.T
+    top2 = np.sort(S, axis=1)[:, -2:]
+    return np.abs(top2[:, 1] - top2[:, 0]) < 1e-3 * np.maximum(1.0, np.abs(top2[:, 1]))
+
+
+def run_small(w: FLCEWorkload, accumulate=False):
+    h, W, lab = make_flce_inputs(w, device=DEV)
+    gw0 = None
+    if accumulate:
+        gw0 = torch.randn(w.V, w.H, device=DEV, dtype=torch.float32)
+    res = flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                       reduction=w.reduction, grad_scale=w.grad_scale,
+                       grad_weight=gw0.clone() if accumulate else None,
+                       accumulate_grad_weight=accumulate)
+    torch.cuda.synchronize()
+    h64 = of.widen_bf16(bf16_bits_np(h))
+    W64 = of.widen_bf16(bf16_bits_np(W))
+    labh = lab.cpu().numpy()
+    ref = of.flce_fwd_bwd(h64, W64, labh, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                          reduction=w.reduction, grad_scale=w.grad_scale)
+    check_loss(res.loss.cpu().numpy(), ref["loss"])
+    ties = near_tie_rows(h64, W64)
+    amax = res.argmax.cpu().numpy()
+    mism = (amax != ref["argmax"])
+    assert not np.any(mism & ~ties), np.flatnonzero(mism & ~ties)
+    counts = res.counts.cpu().numpy()
+    assert counts[0] == ref["n_valid"] and counts[2] == ref["n_bad"] and counts[3] == 0
+    if not np.any(mism):
+        assert counts[1] == ref["n_correct"]
+    check_reduced(float(res.reduced[0]), ref["reduced_loss"], w.reduction)
+    gh = res.grad_hidden.float().cpu().numpy()
+    assert rel_l2(gh, ref["grad_hidden"]) < 1e-2
+    gw = res.grad_weight.cpu().numpy().astype(np.float64)
+    if accumulate:
+        gw = gw - gw0.cpu().numpy()
+    assert rel_l2(gw, ref["grad_weight"]) < 1e-2
+    return res, ref
+
+
+def small(N, H, V, T=0.0, eps=0.0, red="mean", gs=1.0, seed=11, wsig=0.05):
+    return FLCEWorkload(f"f{N}x{H}x{V}", N=N, H=H, V=V, hidden_sigma=1.0, weight_sigma=wsig,
+                        multiplier=0.5, ignore_frac=0.05, label_smoothing=eps, softcap=T,
+                        reduction=red, grad_scale=gs, seed=seed)
+
+
+@pytest.mark.parametrize("N,H,V", [(256, 512, 8192), (200, 264, 5000), (130, 128, 300)])
+@pytest.mark.parametrize("T,eps,red", [(0.0, 0.0, "mean"), (30.0, 0.1, "sum")])
+def test_flce_small_single_chunk(N, H, V, T, eps, red):
+    run_small(small(N, H, V, T=T, eps=eps, red=red, gs=0.5))
+
+
+def test_flce_several_chunks_and_accumulated_weight_gradient():
+    run_small(small(200, 264, 20000, T=30.0, eps=0.1), accumulate=False)
+    run_small(small(150, 136, 17000, T=0.0, eps=0.0, red="sum"), accumulate=True)
+
+
+def test_flce_deterministic():
+    w = small(256, 512, 9000, T=30.0)
+    outs = []
+    for _ in range(2):
+        h, W, lab = make_flce_inputs(w, device=DEV)
+        r = flce_fwd_bwd(h, W, lab, softcap=30.0)
+        torch.cuda.synchronize()
+        outs.append((r.grad_hidden.view(torch.int16).cpu(), r.grad_weight.cpu(), r.loss.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))
+    assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
+
+
+def test_flce_full_size_workload_sampled():
+    w = FLCE_WORKLOADS["flce-bf16-4096x6656x202048-softcap30"]
+    h, W, lab = make_flce_inputs(w, device=DEV)
+    hb = bf16_bits_np(h)
+    Wb = bf16_bits_np(W)
+    labh = lab.cpu().numpy()
+    res = flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                       reduction=w.reduction, grad_scale=w.grad_scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, w.N - 1], np.flatnonzero(labh == IGNORE_INDEX)[:2],
+                                     rng.choice(w.N, 28, replace=False)]))
+    cols = np.unique(np.concatenate([[0, w.V - 1, 8191, 8192], labh[labh >= 0][:6],
+                                     rng.choice(w.V, 22, replace=False)]))
+    ref = of.sampled(hb, Wb, labh, rows, cols, label_smoothing=w.label_smoothing,
+                     softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale)
+    check_loss(res.loss.cpu().numpy(), ref["loss"])
+    amax = res.argmax.cpu().numpy()
+    mism = np.flatnonzero(amax != ref["argmax"])
+    assert mism.size <= 8, mism  # near-ties only (fp32 vs fp64 logits); reported below
+    check_reduced(float(res.reduced[0]), ref["reduced_loss"], w.reduction)
+    gh = res.grad_hidden.float().cpu().numpy()[rows]
+    gw = res.grad_weight.cpu().numpy()[cols]
+    e_h = rel_l2(gh, ref["grad_hidden_rows"])
+    e_w = rel_l2(gw, ref["grad_weight_cols"])
+    print("full-size FLCE: argmax mismatches", mism.size, "rel-L2 grad_hidden", e_h,
+          "grad_weight", e_w)
+    assert e_h < 1e-2 and e_w < 1e-2

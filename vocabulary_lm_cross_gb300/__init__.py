@@ -5,3 +5,4 @@ C ABI in ``include/vlmce.h``); this package holds the build script, a thin
 ctypes/PyTorch binding and the seeded synthetic workloads.
 """
 from .ce import CEResult, ce_fwd_bwd, describe_plan, max_vocab, workspace_bytes  # noqa: F401
+from .flce import FLCEResult, flce_fwd_bwd  # noqa: F401
