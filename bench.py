@@ -4,9 +4,13 @@
 One "step" is one ce_fwd_bwd call (label census, row kernel, finalize) over
 one batch of seeded synthetic logits already resident in HBM.  The default
 workload is bf16 logits [N=2048, V=131072] (sequence 2048 x batch 1, the
-128K vocabulary) with label smoothing 0.1, argmax and token accuracy.
+128K vocabulary) with label smoothing 0.1, argmax and token accuracy.  The
+same run also times the fused linear cross-entropy (flce_fwd_bwd: hidden
+[4096, 6656] x weight [202048, 6656], softcap 30) and reports it in the
+line's "flce" object against the dense bf16 tensor roofline.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-flce]
+    python bench.py --workload flce-bf16-4096x6656x202048-softcap30   # FLCE as the headline
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
@@ -32,7 +36,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "CE fwd+bwd ms & HBM GB/s (N=2048,V=128K bf16); % of HBM roofline"
+FLCE_METRIC = "fused linear CE fwd+bwd TFLOP/s (6NVH, N=4096,H=6656,V=202048 bf16); % of dense bf16"
+FLCE_DEFAULT = "flce-bf16-4096x6656x202048-softcap30"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 # The pages' fastest prior art on this exact workload (context, another machine):
 # Transformer Engine CE fwd+bwd 0.711 ms on H100, BF16, seq 2048, batch 1, 128K vocab
 # = 2*2048*131072*2 bytes / 0.711 ms = 1510 GB/s.
@@ -56,12 +64,38 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_sha() -> str:
-    """sha256 over every CUDA source of the library (any change invalidates a capture)."""
-    import glob
+def load_tensor_peak(sustained: bool):
+    """Dense bf16 TFLOP/s: the burst figure for a kernel timed alone, the
+    sustained one (a seconds-long loop under the power cap) otherwise."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d[key]), f"measured ({key})"
+    except Exception:
+        return (FALLBACK_BF16_TFLOPS_SUSTAINED if sustained else FALLBACK_BF16_TFLOPS), "fallback"
+
+
+# The CUDA sources each profiled kernel is built from (its launch code included):
+# a change to any of them invalidates that kernel's recorded ncu traffic.
+KERNEL_SOURCES = {
+    "ce_rows_kernel": ["ce_rows.cuh", "ce_rows_bf16.cu", "ce_rows_f32.cu", "ce_common.cuh",
+                       "ptx.cuh", "host_util.h", "ce.cu"],
+    "ce_split_kernel": ["ce_split.cuh", "ce_split_bf16.cu", "ce_split_f32.cu", "ce_common.cuh",
+                        "ptx.cuh", "host_util.h", "ce.cu"],
+    "vlmce_gemm_kernel": ["gemm.cuh", "gemm_launch.h", "gemm_kk.cu", "gemm_km.cu", "gemm_mk.cu",
+                          "gemm_mm.cu", "tcgen05.cuh", "ce_common.cuh", "ptx.cuh", "host_util.h",
+                          "flce.cu"],
+}
+
+
+def kernel_sources_sha(kernel: str) -> str:
+    """sha256 over the CUDA sources of one kernel (file names and contents)."""
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(ROOT, "vocabulary_lm_cross_gb300", "csrc", "*"))):
-        h.update(os.path.basename(path).encode())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        path = os.path.join(ROOT, "vocabulary_lm_cross_gb300", "csrc", name)
+        h.update(name.encode())
         h.update(open(path, "rb").read())
     return h.hexdigest()
 
@@ -69,7 +103,7 @@ def kernel_sources_sha() -> str:
 def recorded_traffic(kernel: str, workload: str):
     """dram bytes per launch from the committed ncu summary, if the kernel
     source has not changed since the capture (else None)."""
-    sha = kernel_sources_sha()
+    sha = kernel_sources_sha(kernel)
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -294,7 +328,6 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier()
     t_timed1 = time.time()
-    sampler.stop()
     ms = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -355,6 +388,20 @@ def run_ours(args, w):
         e2e_ms = float(t.item())
     h2d = x_host.numel() * x_host.element_size() + lab_host.numel() * 8
     d2h = g_host.numel() * g_host.element_size() + w.N * 4 + w.N * 8 + 8
+    buf_gb = buf_bytes * n_buf / 1e9
+    del bufs, dbuf, x_host, g_host
+    torch.cuda.empty_cache()
+
+    flce = None
+    if not args.no_flce:
+        from vocabulary_lm_cross_gb300.workloads import FLCE_WORKLOADS
+        fw = FLCE_WORKLOADS[FLCE_DEFAULT]
+        f = run_flce(args, fw, min(args.steps, 10), dev, world, barrier, sampler)
+        flce = {"metric": FLCE_METRIC, "value": f["value"], "unit": "TFLOP/s",
+                "ms_per_step": f["ms"], "steps": f["steps"], "roofline": f["roofline"],
+                "e2e": f["e2e"], "gpu_launches": f["gpu_launches"], "clocks": f["clocks"],
+                "config": f["config"], "device_status_ok": f["ok_status"]}
+    sampler.stop()
 
     if rank != 0:
         if world > 1:
@@ -379,8 +426,8 @@ def run_ours(args, w):
                    "label_smoothing": w.label_smoothing, "softcap": w.softcap,
                    "reduction": w.reduction, "parallelism": f"replicas x{world}",
                    "l2": ("inputs larger than L2: each timed step consumes its own fresh copy "
-                          f"of the {buf_bytes / 1e6:.0f} MB logits") if fresh else
-                         f"ring of {n_buf} buffers of {buf_bytes / 1e6:.0f} MB (> L2)",
+                          f"of the {buf_bytes / 1e6:.0f} MB logits ({buf_gb:.1f} GB)") if fresh
+                         else f"ring of {n_buf} buffers of {buf_bytes / 1e6:.0f} MB (> L2)",
                    "vs_baseline_is": "value per GPU / 1510 GB/s = TE CE 0.711 ms on H100 "
                                      "(the pages' number, another machine: context)",
                    "device_status_ok": ok_status,
@@ -395,10 +442,240 @@ def run_ours(args, w):
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "flce": flce,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def flce_oracle_sample(w, budget_s=10.0):
+    """Oracle throughput (TFLOP/s of 6 n v H) on a bounded sub-problem: the
+    workload's recipe at n rows and v vocabulary rows, H unchanged."""
+    import numpy as np
+    from oracle import flce as of
+    from vocabulary_lm_cross_gb300.workloads import bf16_bits, make_flce_inputs
+
+    def one(n, v):
+        ws = w.resized(N=n, V=v)
+        h, W, lab = make_flce_inputs(ws, device="cpu")
+        h64 = of.widen_bf16(bf16_bits(h))
+        W64 = of.widen_bf16(bf16_bits(W))
+        labh = lab.numpy().astype(np.int64)
+        t0 = time.perf_counter()
+        of.flce_fwd_bwd(h64, W64, labh, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                        reduction=w.reduction, grad_scale=w.grad_scale)
+        dt = time.perf_counter() - t0
+        return ws.algorithmic_flops / dt / 1e12, dt, ws
+
+    n = min(w.N, 256)
+    _, dt0, _ = one(n, 1024)
+    v = int(min(w.V, 32768, max(1024, 1024 * budget_s / max(dt0, 1e-6))))
+    tf, dt, ws = one(n, v)
+    return {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 oracle (numpy BLAS on all host cores + the C CE oracle) on the "
+                      f"workload's recipe at N={ws.N}, V={ws.V}, H={ws.H}: "
+                      f"{ws.algorithmic_flops / 1e9:.1f} GFLOP (6NVH) in {dt:.2f} s"}
+
+
+def run_flce(args, w, steps, dev, world, barrier, sampler):
+    """Time flce_fwd_bwd on resident inputs; returns the measurements (rank-local)."""
+    import torch
+
+    import vocabulary_lm_cross_gb300 as v
+    from vocabulary_lm_cross_gb300 import capi
+    from vocabulary_lm_cross_gb300.workloads import make_flce_inputs
+
+    rank = env_int("RANK", 0)
+    lib = capi.lib()
+    h, W, lab = make_flce_inputs(w.resized(seed=w.seed + 1000 * rank), device=dev)
+    gw = torch.empty((w.V, w.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(v.flce.workspace_bytes(w.N, w.H, w.V), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(label_smoothing=w.label_smoothing, softcap=w.softcap, reduction=w.reduction,
+              grad_scale=w.grad_scale, grad_weight=gw, workspace=ws)
+
+    def step():
+        return v.flce_fwd_bwd(h, W, lab, **kw)
+
+    t_w0 = time.time()
+    for _ in range(args.warmup):
+        res = step()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        res = step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_w1 = time.time()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ok_status = int(res.counts[3].item()) == 0
+
+    # the tensor-core region of each call (statistics GEMM, row merge, every
+    # chunk's three GEMMs), events recorded by the library on its stream
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        lib.vlmce_flce_profile_events(ctypes_handle(kb[i], stream), ctypes_handle(ke[i], stream))
+        step()
+    torch.cuda.synchronize()
+    kern_ms = statistics.fmean(kb[i].elapsed_time(ke[i]) for i in range(steps))
+
+    # end to end through the public API with host buffers
+    h_host = h.cpu().pin_memory()
+    W_host = W.cpu().pin_memory()
+    lab_host = lab.cpu().pin_memory()
+    gh_host = torch.empty((w.N, w.H), dtype=torch.bfloat16).pin_memory()
+    gw_host = torch.empty((w.V, w.H), dtype=torch.float32).pin_memory()
+    loss_host = torch.empty(w.N, dtype=torch.float32).pin_memory()
+    red_host = torch.empty(2, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        h.copy_(h_host, non_blocking=True)
+        W.copy_(W_host, non_blocking=True)
+        lab.copy_(lab_host, non_blocking=True)
+        r = step()
+        gh_host.copy_(r.grad_hidden, non_blocking=True)
+        gw_host.copy_(gw, non_blocking=True)
+        loss_host.copy_(r.loss, non_blocking=True)
+        red_host.copy_(r.reduced, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = 3
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (h_host.numel() + W_host.numel()) * 2 + lab_host.numel() * 8
+    d2h = gh_host.numel() * 2 + gw_host.numel() * 4 + w.N * 4 + 8
+    nchunks = (w.V + 8191) // 8192
+    flops = w.algorithmic_flops
+    peak, peak_src = load_tensor_peak(sustained=True)
+    peak_b, _ = load_tensor_peak(sustained=False)
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    return {
+        "ms": ms / steps, "value": world * flops * steps / (ms * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": "vlmce_gemm_kernel",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_src,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst": achieved / peak_b,
+                     "kernel_ms": kern_ms, "flops_per_launch": flops,
+                     "executed_flops": 8 * w.N * w.V * w.H,
+                     "measured_over": "the call's tensor-core region: 1 statistics GEMM, the "
+                                      f"row merge and {nchunks} x 3 chunk GEMMs",
+                     "traffic": recorded_traffic("vlmce_gemm_kernel", w.name)},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": (4 + 3 * nchunks) * steps, "ok_status": ok_status,
+        "clocks": sampler.summary(t_w0, t_w1),
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "softcap": w.softcap,
+                   "label_smoothing": w.label_smoothing, "reduction": w.reduction,
+                   "grad_weight": "fp32, overwritten", "chunk": 8192,
+                   "l2": "inputs larger than L2 (weight 2.69 GB streamed three times a step)"},
+        "steps": steps,
+    }
+
+
+def run_ours_flce(args, w):
+    """The fused linear cross-entropy as the line's headline (--workload flce-...)."""
+    import torch
+    import torch.distributed as dist
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local = env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    f = run_flce(args, w, args.steps, dev, world, barrier, sampler)
+    sampler.stop()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cfg = dict(f["config"])
+    cfg["parallelism"] = f"replicas x{world}"
+    cfg["device_status_ok"] = f["ok_status"]
+    line = {"metric": FLCE_METRIC, "value": f["value"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": f["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded normal hidden states and weight, uniform labels)",
+            "config": cfg, "roofline": f["roofline"],
+            "cpu_baseline": flce_oracle_sample(w) if world == 1 else None,
+            "e2e": f["e2e"], "gpu_launches": f["gpu_launches"], "clocks": f["clocks"]}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_flce(args, w):
+    """The FLCE oracle on the host cores: each step a bounded sub-problem."""
+    import numpy as np
+    from oracle import flce as of
+    from vocabulary_lm_cross_gb300.workloads import bf16_bits, make_flce_inputs
+    if env_int("RANK", 0) != 0:
+        return
+    ws = w.resized(N=min(w.N, 128), V=min(w.V, 2048))
+    h, W, lab = make_flce_inputs(ws, device="cpu")
+    h64 = of.widen_bf16(bf16_bits(h))
+    W64 = of.widen_bf16(bf16_bits(W))
+    labh = lab.numpy().astype(np.int64)
+
+    def one():
+        of.flce_fwd_bwd(h64, W64, labh, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                        reduction=w.reduction, grad_scale=w.grad_scale)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    value = ws.algorithmic_flops * args.steps / dt / 1e12
+    sample = (f"fp64 FLCE oracle on the workload's recipe at N={ws.N}, V={ws.V}, H={ws.H} "
+              "per step")
+    line = {"impl": "reference", "metric": FLCE_METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V,
+                       "sample_N": ws.N, "sample_V": ws.V},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
 
 
 def ctypes_handle(ev, stream):
@@ -415,10 +692,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ce-bf16-2048x131072-ls0.1-argmax")
+    ap.add_argument("--no-flce", action="store_true",
+                    help="skip the fused linear cross-entropy leg of a cross-entropy run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    from vocabulary_lm_cross_gb300.workloads import CE_WORKLOADS
+    from vocabulary_lm_cross_gb300.workloads import CE_WORKLOADS, FLCE_WORKLOADS
+    if args.workload in FLCE_WORKLOADS:
+        w = FLCE_WORKLOADS[args.workload]
+        (run_reference_flce if args.impl == "reference" else run_ours_flce)(args, w)
+        return
     w = CE_WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -121,6 +121,11 @@ FLCE_WORKLOADS = {
                      hidden_sigma=1.0, weight_sigma=0.02, multiplier=0.5, ignore_frac=0.02,
                      label_smoothing=0.0, softcap=30.0, reduction="mean", grad_scale=1.0,
                      seed=1005),
+        # the same recipe at a profiling size (weight 436 MB, still larger than L2)
+        FLCEWorkload("flce-bf16-1024x6656x32768-softcap30", N=1024, H=6656, V=32768,
+                     hidden_sigma=1.0, weight_sigma=0.02, multiplier=0.5, ignore_frac=0.02,
+                     label_smoothing=0.0, softcap=30.0, reduction="mean", grad_scale=1.0,
+                     seed=1006),
     ]
 }
 
