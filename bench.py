@@ -84,9 +84,8 @@ KERNEL_SOURCES = {
                        "ptx.cuh", "host_util.h", "ce.cu"],
     "ce_split_kernel": ["ce_split.cuh", "ce_split_bf16.cu", "ce_split_f32.cu", "ce_common.cuh",
                         "ptx.cuh", "host_util.h", "ce.cu"],
-    "vlmce_gemm_kernel": ["gemm.cuh", "gemm_launch.h", "gemm_kk.cu", "gemm_km.cu", "gemm_mk.cu",
-                          "gemm_mm.cu", "tcgen05.cuh", "ce_common.cuh", "ptx.cuh", "host_util.h",
-                          "flce.cu"],
+    "vlmce_gemm_kernel": ["gemm.cuh", "gemm_types.h", "gemm_launch.h", "gemm.cu", "tcgen05.cuh",
+                          "ce_common.cuh", "ptx.cuh", "host_util.h", "flce.cu"],
 }
 
 
@@ -96,7 +95,7 @@ def kernel_sources_sha(kernel: str) -> str:
     for name in sorted(KERNEL_SOURCES[kernel]):
         path = os.path.join(ROOT, "vocabulary_lm_cross_gb300", "csrc", name)
         h.update(name.encode())
-        h.update(open(path, "rb").read())
+        h.update(open(path, "rb").read() if os.path.exists(path) else b"<missing>")
     return h.hexdigest()
 
 

@@ -13,11 +13,14 @@
 //      sum z, z at the label                                   (GEMM, kStats)
 //   3. per row: merge the tile statistics in column order -> lse, loss,
 //      argmax, gradient scale                                  (1 warp / row)
-//   4. for each chunk of Vc = 8192 vocabulary columns:
+//   4. for chunk c = 0 .. C of Vc = 8192 vocabulary columns, one grouped
+//      GEMM launch each:
+//        grad_h  (+)= G_{c-1} W_{c-1}   (fp32 [N, H]; the last chunk writes bf16)
+//        grad_W_{c-1} (+)= G_{c-1}^T h' (fp32, rows of the chunk)
 //        G_c = scale (softmax - q) (1 - t^2), recomputed from S_c = h' W_c^T
-//              and stored in bf16 [N, Vc]                      (GEMM, kGrad)
-//        grad_h  (+)= G_c W_c  (fp32 [N, H]; the last chunk writes bf16)
-//        grad_W_c (+)= G_c^T h' (fp32, rows of the chunk)
+//              and stored in bf16 [N, Vc] (two buffers, alternating)
+//      so the two products of a chunk share a launch with the next chunk's
+//      gradient tile and every launch has one tail.
 //   5. reduced loss and accuracy                               (1 CTA)
 // Executed tensor work 8 N V H (the logits twice); algorithmic 6 N V H.
 #include <cuda.h>
@@ -26,7 +29,6 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "ce_common.cuh"
 #include "gemm_launch.h"
@@ -177,66 +179,6 @@ __global__ void __launch_bounds__(1024) flce_finalize_kernel(
     }
 }
 
-// ----------------------------------------------------------------- TMA maps
-
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-    static std::once_flag once;
-    static EncodeTiled fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
-// A bf16 matrix of `outer` rows of `inner` elements (row stride `stride`
-// elements), read in boxes of box_inner x box_outer with 128-byte swizzle;
-// out-of-range elements read as zero.
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
-              uint32_t box_inner, uint32_t box_outer) {
-    EncodeTiled enc = encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {stride * 2};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Operand maps for C[M, N] = A[M, K] B[N, K]^T: K-major operands are boxes of
-// 64 K x rows; MN-major ones 64 M/N x 64 K (see gemm.cuh).
-bool map_a(CUtensorMap *m, const void *A, bool mn, int64_t M, int64_t K, int64_t ld) {
-    return mn ? make_map(m, A, M, K, ld, 64, 64) : make_map(m, A, K, M, ld, 64, gemm::BM);
-}
-bool map_b(CUtensorMap *m, const void *B, bool mn, int64_t N, int64_t K, int64_t ld) {
-    return mn ? make_map(m, B, N, K, ld, 64, 64) : make_map(m, B, K, N, ld, 64, gemm::BN);
-}
-
-cudaError_t launch(bool a_mn, bool b_mn, int mode, const CUtensorMap &ma, const CUtensorMap &mb,
-                   const gemm::Args &args, int sm_count, cudaStream_t s) {
-    const int64_t tiles = static_cast<int64_t>((args.M + gemm::BM - 1) / gemm::BM) *
-                          ((args.N + gemm::BN - 1) / gemm::BN);
-    const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
-    if (grid < 1) return cudaSuccess;
-    if (!a_mn && !b_mn) return gemm::launch_kk(mode, ma, mb, args, grid, s);
-    if (!a_mn && b_mn) return gemm::launch_km(mode, ma, mb, args, grid, s);
-    if (a_mn && !b_mn) return gemm::launch_mk(mode, ma, mb, args, grid, s);
-    return gemm::launch_mm(mode, ma, mb, args, grid, s);
-}
-
 // ----------------------------------------------------------------- workspace
 struct Ws {
     int64_t *counts;
@@ -244,8 +186,8 @@ struct Ws {
     RowPart *part;  // [ntiles][N]
     float *lse, *row_scale, *loss;
     int64_t *argmax;
-    __nv_bfloat16 *g;  // [N, kChunk]
-    float *gh;         // [N, H] grad_h accumulator
+    __nv_bfloat16 *g[2];  // two [N, kChunk] gradient tiles
+    float *gh;            // [N, H] grad_h accumulator
 };
 
 int64_t ntiles_of(int64_t V) { return (V + gemm::BN - 1) / gemm::BN; }
@@ -254,7 +196,7 @@ size_t ws_bytes(int64_t N, int64_t H, int64_t V) {
     int64_t b = kWsHeader;
     b += round_up(ntiles_of(V) * N * static_cast<int64_t>(sizeof(RowPart)), 256);
     b += 3 * round_up(4 * N, 256) + round_up(8 * N, 256);
-    b += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
+    b += 2 * round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     b += round_up(4 * N * H, 256);
     return static_cast<size_t>(b);
 }
@@ -275,8 +217,10 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
     p += round_up(4 * N, 256);
     w.argmax = reinterpret_cast<int64_t *>(p);
     p += round_up(8 * N, 256);
-    w.g = reinterpret_cast<__nv_bfloat16 *>(p);
-    p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
+    for (int i = 0; i < 2; ++i) {
+        w.g[i] = reinterpret_cast<__nv_bfloat16 *>(p);
+        p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
+    }
     w.gh = reinterpret_cast<float *>(p);
     return w;
 }
@@ -313,20 +257,25 @@ extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void 
     DeviceInfo dev;
     vlmce_status st = current_device(&dev);
     if (st != VLMCE_OK) return st;
-    CUtensorMap ma, mb;
-    if (!map_a(&ma, A, a_mn != 0, M, K, lda) || !map_b(&mb, B, b_mn != 0, N, K, ldb)) {
+    gemm::Maps maps;
+    if (!gemm::make_operand_map(&maps.a[0], A, a_mn != 0, M, K, lda) ||
+        !gemm::make_operand_map(&maps.b[0], B, b_mn != 0, N, K, ldb)) {
         record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
         return VLMCE_ERR_CUDA;
     }
-    gemm::Args g = {};
-    g.M = static_cast<int>(M);
-    g.N = static_cast<int>(N);
-    g.K = static_cast<int>(K);
-    g.C = C;
-    g.ldc = ldc;
+    gemm::Params g = {};
+    g.nprob = 1;
+    gemm::Problem &p = g.p[0];
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.mode = accumulate ? gemm::kAccF32 : gemm::kStoreF32;
+    p.a_mn = a_mn != 0;
+    p.b_mn = b_mn != 0;
+    p.C = C;
+    p.ldc = ldc;
     g.err = nullptr;  // no device error word: a wait that gives up only ends the kernel
-    return launch_status(launch(a_mn != 0, b_mn != 0, accumulate ? gemm::kAccF32 : gemm::kStoreF32,
-                                ma, mb, g, dev.sm_count, reinterpret_cast<cudaStream_t>(stream)),
+    return launch_status(gemm::launch_group(maps, g, reinterpret_cast<cudaStream_t>(stream)),
                          "vlmce_gemm_kernel");
 }
 
@@ -373,37 +322,45 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
 
     if (N > 0) {
         const float T = softcap;
-        gemm::Args base = {};
+        gemm::Params base = {};
         base.labels = labels;
         base.ignore_index = ignore_index;
         base.V = static_cast<int>(V);
         base.eps = label_smoothing;
         base.T = T;
         base.k2 = T > 0.f ? -2.f * ce::kLog2e / T : 0.f;
+        base.lse = w.lse;
+        base.row_scale = w.row_scale;
         base.err = w.err;
 
         cudaEvent_t eb = t_prof_begin, ee = t_prof_end;
         t_prof_begin = t_prof_end = nullptr;
         if (eb && (st = launch_status(cudaEventRecord(eb, cs), "cudaEventRecord")) != VLMCE_OK)
             return st;
-
-        // ---- pass 1: statistics of S = h' W^T over the whole vocabulary
-        CUtensorMap m_h, m_w;
-        if (!map_a(&m_h, hidden, false, N, H, hidden_stride) ||
-            !map_b(&m_w, weight, false, V, H, weight_stride)) {
+        auto map_fail = [] {
             record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
             return VLMCE_ERR_CUDA;
+        };
+
+        // ---- pass 1: statistics of S = h' W^T over the whole vocabulary
+        {
+            gemm::Maps maps;
+            if (!gemm::make_operand_map(&maps.a[0], hidden, false, N, H, hidden_stride) ||
+                !gemm::make_operand_map(&maps.b[0], weight, false, V, H, weight_stride))
+                return map_fail();
+            gemm::Params g = base;
+            g.nprob = 1;
+            gemm::Problem &p = g.p[0];
+            p.M = static_cast<int>(N);
+            p.N = static_cast<int>(V);
+            p.K = static_cast<int>(H);
+            p.mode = gemm::kStats;
+            p.col0 = 0;
+            p.part = w.part;
+            p.part_ld = N;
+            st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(stats)");
+            if (st != VLMCE_OK) return st;
         }
-        gemm::Args s1 = base;
-        s1.M = static_cast<int>(N);
-        s1.N = static_cast<int>(V);
-        s1.K = static_cast<int>(H);
-        s1.col0 = 0;
-        s1.part = w.part;
-        s1.part_ld = N;
-        st = launch_status(launch(false, false, gemm::kStats, m_h, m_w, s1, dev.sm_count, cs),
-                           "vlmce_gemm_kernel(stats)");
-        if (st != VLMCE_OK) return st;
 
         flce_merge_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, cs>>>(
             w.part, N, static_cast<int>(ntiles_of(V)), labels, N, V, ignore_index, label_smoothing,
@@ -411,66 +368,71 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
         st = launch_status(cudaSuccess, "flce_merge_kernel");
         if (st != VLMCE_OK) return st;
 
-        // ---- pass 2: per vocabulary chunk, the gradient tile and the two products
-        CUtensorMap m_ht;  // h' as the N(=H)-major B of grad_W = G^T h'
-        if (!map_b(&m_ht, hidden, true, H, N, hidden_stride)) {
-            record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-            return VLMCE_ERR_CUDA;
-        }
+        // ---- pass 2: launch c = the products of chunk c - 1 and the gradient tile of chunk c
         const int64_t nchunks = (V + kChunk - 1) / kChunk;
-        for (int64_t c = 0; c < nchunks; ++c) {
-            const int64_t v0 = c * kChunk;
-            const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
-            const __nv_bfloat16 *wc =
-                reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
-            CUtensorMap m_wc, m_g, m_wcn, m_gt;
-            if (!map_b(&m_wc, wc, false, vc, H, weight_stride) ||  // W_c, K-major B of S_c
-                !map_a(&m_g, w.g, false, N, vc, kChunk) ||         // G_c, K-major A of grad_h
-                !map_b(&m_wcn, wc, true, H, vc, weight_stride) ||  // W_c, N-major B of grad_h
-                !map_a(&m_gt, w.g, true, vc, N, kChunk)) {         // G_c^T, M-major A of grad_W
-                record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-                return VLMCE_ERR_CUDA;
+        for (int64_t c = 0; c <= nchunks; ++c) {
+            gemm::Maps maps;
+            gemm::Params g = base;
+            int n = 0;
+            if (c >= 1) {
+                const int64_t cp = c - 1;
+                const int64_t v0 = cp * kChunk;
+                const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
+                const __nv_bfloat16 *wc =
+                    reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
+                const __nv_bfloat16 *gc = w.g[cp & 1];
+                // grad_h (+)= G_c W_c: A = G_c K-major [N, Vc], B = W_c N(=H)-major
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, N, vc, kChunk) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, H, vc, weight_stride))
+                    return map_fail();
+                gemm::Problem &ph = g.p[n++];
+                ph.M = static_cast<int>(N);
+                ph.N = static_cast<int>(H);
+                ph.K = static_cast<int>(vc);
+                ph.mode = nchunks == 1       ? gemm::kStoreBF16
+                          : cp == 0           ? gemm::kStoreF32
+                          : cp == nchunks - 1 ? gemm::kAccToBF16
+                                              : gemm::kAccF32;
+                ph.a_mn = 0;
+                ph.b_mn = 1;
+                ph.C = w.gh;
+                ph.ldc = H;
+                ph.C16 = static_cast<__nv_bfloat16 *>(grad_hidden);
+                ph.ldc16 = hidden_stride;
+                // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
+                if (!gemm::make_operand_map(&maps.a[n], gc, true, vc, N, kChunk) ||
+                    !gemm::make_operand_map(&maps.b[n], hidden, true, H, N, hidden_stride))
+                    return map_fail();
+                gemm::Problem &pw = g.p[n++];
+                pw.M = static_cast<int>(vc);
+                pw.N = static_cast<int>(H);
+                pw.K = static_cast<int>(N);
+                pw.mode = accumulate_grad_weight ? gemm::kAccF32 : gemm::kStoreF32;
+                pw.a_mn = 1;
+                pw.b_mn = 1;
+                pw.C = grad_weight + v0 * H;
+                pw.ldc = H;
             }
-            // G_c = scale (softmax - q) (1 - t^2) from the recomputed logits
-            gemm::Args g1 = base;
-            g1.M = static_cast<int>(N);
-            g1.N = static_cast<int>(vc);
-            g1.K = static_cast<int>(H);
-            g1.col0 = static_cast<int>(v0);
-            g1.C16 = w.g;
-            g1.ldc16 = kChunk;
-            g1.lse = w.lse;
-            g1.row_scale = w.row_scale;
-            st = launch_status(launch(false, false, gemm::kGrad, m_h, m_wc, g1, dev.sm_count, cs),
-                               "vlmce_gemm_kernel(grad tile)");
-            if (st != VLMCE_OK) return st;
-            // grad_h (+)= G_c W_c
-            gemm::Args g3 = base;
-            g3.M = static_cast<int>(N);
-            g3.N = static_cast<int>(H);
-            g3.K = static_cast<int>(vc);
-            g3.C = w.gh;
-            g3.ldc = H;
-            g3.C16 = static_cast<__nv_bfloat16 *>(grad_hidden);
-            g3.ldc16 = hidden_stride;
-            const int mode3 = nchunks == 1 ? gemm::kStoreBF16
-                              : c == 0        ? gemm::kStoreF32
-                              : c == nchunks - 1 ? gemm::kAccToBF16
-                                                 : gemm::kAccF32;
-            st = launch_status(launch(false, true, mode3, m_g, m_wcn, g3, dev.sm_count, cs),
-                               "vlmce_gemm_kernel(grad_hidden)");
-            if (st != VLMCE_OK) return st;
-            // grad_W_c (+)= G_c^T h'
-            gemm::Args g2 = base;
-            g2.M = static_cast<int>(vc);
-            g2.N = static_cast<int>(H);
-            g2.K = static_cast<int>(N);
-            g2.C = grad_weight + v0 * H;
-            g2.ldc = H;
-            st = launch_status(launch(true, true, accumulate_grad_weight ? gemm::kAccF32
-                                                                         : gemm::kStoreF32,
-                                      m_gt, m_ht, g2, dev.sm_count, cs),
-                               "vlmce_gemm_kernel(grad_weight)");
+            if (c < nchunks) {
+                const int64_t v0 = c * kChunk;
+                const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
+                const __nv_bfloat16 *wc =
+                    reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
+                // G_c = scale (softmax - q) (1 - t^2) from the recomputed S_c = h' W_c^T
+                if (!gemm::make_operand_map(&maps.a[n], hidden, false, N, H, hidden_stride) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, false, vc, H, weight_stride))
+                    return map_fail();
+                gemm::Problem &pg = g.p[n++];
+                pg.M = static_cast<int>(N);
+                pg.N = static_cast<int>(vc);
+                pg.K = static_cast<int>(H);
+                pg.mode = gemm::kGrad;
+                pg.col0 = static_cast<int>(v0);
+                pg.C16 = w.g[c & 1];
+                pg.ldc16 = kChunk;
+            }
+            g.nprob = n;
+            st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(chunk)");
             if (st != VLMCE_OK) return st;
         }
         if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)

@@ -1,5 +1,5 @@
-// gemm.cuh -- persistent tcgen05 GEMM for sm_103a with the fused
-// linear-cross-entropy epilogues.
+// gemm.cuh -- persistent tcgen05 GEMM for sm_103a, run by CTA pairs, with the
+// fused linear-cross-entropy epilogues.
 //
 // C[M, N] = A[M, K] * B[N, K]^T with bf16 operands and fp32 accumulation in
 // tensor memory.  Either operand may be stored K-major (K contiguous) or
@@ -9,86 +9,66 @@
 //   grad_h     += G_c W_c      A = G_c [N, Vc] K-major,  B = W_c: N(=H)-major
 //   grad_W_c    = G_c^T h'     A = G_c: M(=Vc)-major,    B = h': N(=H)-major
 //
-// CTA = 6 warps, one per SM (persistent, tiles strided over the grid):
-//   warp 0      one lane issues the TMA loads of A and B tiles (128x64 and
-//               256x64 bf16, 128-byte swizzle) into a 4-stage ring;
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and one lane issues tcgen05.mma (M=128, N=256, K=16 per
-//               instruction), committing to the ring's empty barriers and,
-//               per tile, to the accumulator's full barrier;
+// One launch runs up to kMaxProblems independent products ("problems") over
+// one persistent grid: their 256 x 256 tiles are numbered one after the
+// other and strided over the clusters, so a launch has a single tail.
+//
+// Cluster = 2 CTAs on two SMs ("pair"); the pair computes one 256 x 256 tile
+// with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction).
+// Each CTA stages its own 128 rows of A and its own 128 rows of B (K = 64
+// per stage, 128-byte swizzle) in a 6-stage ring, so a CTA moves a third
+// less operand data per flop than a single-SM 128 x 256 tile would, and each
+// CTA's TMEM receives its 128 rows of the tile.  CTA = 6 warps:
+//   warp 0      one lane issues the TMA loads of this CTA's halves; the
+//               copies of both CTAs count on the leader's "full" barrier;
+//   warp 1      allocates 512 TMEM columns per SM (two 128 x 256 fp32
+//               accumulators) with its peer; in the leader one lane issues
+//               the pair MMAs and commits them to both CTAs' barriers;
 //   warps 2-5   epilogue: each reads its 32-lane TMEM subpartition (one
 //               accumulator row per thread) in 32-column chunks while the
-//               MMA fills the other accumulator.
+//               MMA fills the other accumulator; both CTAs' epilogue warps
+//               release an accumulator on the leader's "tmem empty" barrier.
 //
-// Operand tile layouts in shared memory (bf16, 128-byte swizzle atoms of
-// 8 rows x 128 bytes):
-//   K-major  (rows = M or N, 64 K-elements = 128 B per row): consecutive
-//            8-row groups 1024 B apart (SBO); one K-step of 16 elements
-//            advances the start address by 32 B.
-//   MN-major (rows = K, 64 M/N-elements = 128 B per row, one TMA box of
-//            64 x 64 per 64 M/N): 8-row (K) groups 1024 B apart (SBO), 64-wide
-//            M/N groups 8192 B apart (LBO); a K-step of 16 rows advances by
-//            2048 B.
+// Operand tile layouts in shared memory (per CTA, bf16, 128-byte swizzle
+// atoms of 8 rows x 128 bytes):
+//   K-major  (128 rows of M or N, 64 K-elements = 128 B per row): 8-row
+//            groups 1024 B apart (SBO); a K-step of 16 elements advances the
+//            start address by 32 B.
+//   MN-major (64 rows of K, 128 B = 64 M/N-elements per row, one TMA box of
+//            64 x 64 per 64 M/N): 8-row (K) groups 1024 B apart (SBO), the
+//            two 64-wide M/N groups 8192 B apart (LBO); a K-step of 16 rows
+//            advances by 2048 B.
+//
+// Every wait on an mbarrier is bounded (kWaitLimitNs); a wait that gives up
+// sets VLMCE_DEVERR_TIMEOUT in the device error word and the CTA runs its
+// remaining loops without waiting, so the launch always ends.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "ce_common.cuh"
+#include "gemm_types.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
 
 namespace vlmce {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 2 * BN;
-constexpr int kBarriers = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kBarriers + 16;
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;
-
-enum Mode : int {
-    kStoreF32 = 0,   // C = acc (fp32)
-    kAccF32 = 1,     // C += acc (fp32)
-    kStats = 2,      // row statistics of the logits tile (fused linear CE, pass 1)
-    kGrad = 3,       // gradient tile G = scale (p - q) (1 - t^2) -> bf16 (pass 2)
-    kStoreBF16 = 4,  // C16 = bf16(acc)
-    kAccToBF16 = 5,  // C16 = bf16(C + acc)
-};
-
-struct Args {
-    int M, N, K;
-    float *C;                  // fp32 [M, ldc]
-    int64_t ldc;
-    __nv_bfloat16 *C16;        // bf16 [M, ldc16]
-    int64_t ldc16;
-    // cross-entropy epilogues
-    const int64_t *labels;     // [M]
-    int64_t ignore_index;
-    int col0;                  // vocabulary column of n = 0
-    int V;                     // vocabulary size
-    float eps, T, k2;          // smoothing, softcap (0 = off), -2 log2e / T
-    ce::RowPart *part;         // kStats: part[n_tile * part_ld + row]
-    int64_t part_ld;
-    const float *lse;          // kGrad: [M]
-    const float *row_scale;    // kGrad: [M] scale of a valid row, 0 otherwise
-    int *err;                  // device error word
-};
-
 // ------------------------------------------------------------ barriers
+template <bool CLUSTER_ACQUIRE = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort,
                                          int *err) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto try_once = [&] {
+        return CLUSTER_ACQUIRE ? ptx::mbar_try_wait_cluster(bar, parity)
+                               : ptx::mbar_try_wait(bar, parity);
+    };
+    if (try_once()) return true;
     if (*abort) return false;
     const unsigned long long t0 = ptx::globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 64; ++i)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (try_once()) return true;
         if (*abort) return false;
         if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
@@ -103,8 +83,18 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int *er
     wait_bar(bar, parity, &no_abort, err);
 }
 
-__device__ __forceinline__ void bar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+// ------------------------------------------------------------ tiles
+struct Tile {
+    int p, m0, n0;
+};
+__device__ __forceinline__ Tile tile_of(const Params &a, int t) {
+    int p = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxProblems; ++i)
+        if (i < a.nprob && t >= a.p[i].tile0) p = i;
+    const int lt = t - a.p[p].tile0;
+    const int mt = a.p[p].mt;
+    return Tile{p, (lt % mt) * BM, (lt / mt) * BN};
 }
 
 // ------------------------------------------------------------ epilogues
@@ -119,14 +109,12 @@ struct StatAcc {
     float mz, s, sz, zy;
 };
 
+// fp32 / bf16 output modes on one 32-column chunk of one row.
 template <int MODE>
-__device__ __forceinline__ void epilogue_chunk(const Args &a, const float (&v)[32], int row,
-                                               int cbase, StatAcc &st, int64_t y, float rscale,
-                                               float nlseL) {
-    const int nvalid = min(32, a.N - cbase);
-    if (nvalid <= 0 || row >= a.M) return;
+__device__ __forceinline__ void store_chunk(const Problem &P, const float (&v)[32], int row,
+                                            int cbase, int nvalid) {
     if constexpr (MODE == kStoreF32 || MODE == kAccF32 || MODE == kAccToBF16) {
-        float *c = a.C + static_cast<int64_t>(row) * a.ldc + cbase;
+        float *c = P.C + static_cast<int64_t>(row) * P.ldc + cbase;
         float o[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = v[j];
@@ -147,14 +135,13 @@ __device__ __forceinline__ void epilogue_chunk(const Args &a, const float (&v)[3
             }
         }
         if constexpr (MODE == kAccToBF16) {
-            __nv_bfloat16 *c16 = a.C16 + static_cast<int64_t>(row) * a.ldc16 + cbase;
+            __nv_bfloat16 *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
             if (nvalid == 32) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    *reinterpret_cast<uint4 *>(c16 + j) =
-                        make_uint4(ce::pack_bf16x2(o[j], o[j + 1]), ce::pack_bf16x2(o[j + 2], o[j + 3]),
-                                   ce::pack_bf16x2(o[j + 4], o[j + 5]), ce::pack_bf16x2(o[j + 6], o[j + 7]));
-                }
+                for (int j = 0; j < 32; j += 8)
+                    *reinterpret_cast<uint4 *>(c16 + j) = make_uint4(
+                        ce::pack_bf16x2(o[j], o[j + 1]), ce::pack_bf16x2(o[j + 2], o[j + 3]),
+                        ce::pack_bf16x2(o[j + 4], o[j + 5]), ce::pack_bf16x2(o[j + 6], o[j + 7]));
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -170,107 +157,124 @@ __device__ __forceinline__ void epilogue_chunk(const Args &a, const float (&v)[3
                     if (j < nvalid) c[j] = o[j];
             }
         }
-    } else if constexpr (MODE == kStoreBF16) {
-        __nv_bfloat16 *c16 = a.C16 + static_cast<int64_t>(row) * a.ldc16 + cbase;
+    } else {  // kStoreBF16
+        __nv_bfloat16 *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
+        if (nvalid == 32 && (P.ldc16 % 8) == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < nvalid) c16[j] = __float2bfloat16_rn(v[j]);
-    } else if constexpr (MODE == kStats) {
-        // chunk max and its first column among the valid ones
-        float cm = -INFINITY;
-        int ci = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < nvalid && v[j] > cm) {
-                cm = v[j];
-                ci = j;
-            }
-        const bool cap = a.T > 0.f;
-        if (cm > st.mx) {
-            const float nz = cap ? ce::softcap_z<true>(cm, a.T, a.k2).z : cm;
-            const float f = ptx::ex2((st.mz - nz) * ce::kLog2e);
-            st.s = (st.s == 0.f) ? 0.f : st.s * f;
-            st.mx = cm;
-            st.idx = a.col0 + cbase + ci;
-            st.mz = nz;
-        }
-        const float nm = -st.mz * ce::kLog2e;
-        float s0 = 0.f, s1 = 0.f, z0 = 0.f, z1 = 0.f;
-        if (cap) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const float za = ce::softcap_z<true>(v[j], a.T, a.k2).z;
-                const float zb = ce::softcap_z<true>(v[j + 1], a.T, a.k2).z;
-                if (j < nvalid) {
-                    s0 += ptx::ex2(fmaf(za, ce::kLog2e, nm));
-                    z0 += za;
-                }
-                if (j + 1 < nvalid) {
-                    s1 += ptx::ex2(fmaf(zb, ce::kLog2e, nm));
-                    z1 += zb;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                if (j < nvalid) {
-                    s0 += ptx::ex2(fmaf(v[j], ce::kLog2e, nm));
-                    z0 += v[j];
-                }
-                if (j + 1 < nvalid) {
-                    s1 += ptx::ex2(fmaf(v[j + 1], ce::kLog2e, nm));
-                    z1 += v[j + 1];
-                }
-            }
-        }
-        st.s += s0 + s1;
-        st.sz += z0 + z1;
-        const int64_t yl = y - a.col0 - cbase;  // label column within this chunk
-        if (yl >= 0 && yl < nvalid) {
-            float xy = v[0];
-#pragma unroll
-            for (int j = 1; j < 32; ++j)
-                if (j == yl) xy = v[j];
-            st.zy = cap ? ce::softcap_z<true>(xy, a.T, a.k2).z : xy;
-        }
-    } else if constexpr (MODE == kGrad) {
-        const bool cap = a.T > 0.f;
-        const float c_smooth = rscale * (a.eps / static_cast<float>(a.V));
-        const float c_label = c_smooth + rscale * (1.f - a.eps);
-        const int64_t yl = y - a.col0 - cbase;
-        float g[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            float z = v[j], dz = 1.f;
-            if (cap) {
-                const ce::Capped cz = ce::softcap_z<true>(v[j], a.T, a.k2);
-                z = cz.z;
-                dz = cz.dz;
-            }
-            const float pr = ptx::ex2(fmaf(z, ce::kLog2e, nlseL));
-            g[j] = fmaf(pr, rscale, (j == yl) ? -c_label : -c_smooth) * dz;
-        }
-        __nv_bfloat16 *c16 = a.C16 + static_cast<int64_t>(row) * a.ldc16 + cbase;
-        if (nvalid == 32) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-                *reinterpret_cast<uint4 *>(c16 + j) =
-                    make_uint4(ce::pack_bf16x2(g[j], g[j + 1]), ce::pack_bf16x2(g[j + 2], g[j + 3]),
-                               ce::pack_bf16x2(g[j + 4], g[j + 5]), ce::pack_bf16x2(g[j + 6], g[j + 7]));
-            }
+            for (int j = 0; j < 32; j += 8)
+                *reinterpret_cast<uint4 *>(c16 + j) = make_uint4(
+                    ce::pack_bf16x2(v[j], v[j + 1]), ce::pack_bf16x2(v[j + 2], v[j + 3]),
+                    ce::pack_bf16x2(v[j + 4], v[j + 5]), ce::pack_bf16x2(v[j + 6], v[j + 7]));
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (j < nvalid) c16[j] = __float2bfloat16_rn(g[j]);
+                if (j < nvalid) c16[j] = __float2bfloat16_rn(v[j]);
         }
     }
 }
 
+// Statistics of one 32-column chunk of a logits row (max / first argmax of
+// S, online sum of exp(z - m_z), sum of z, z at the label).
+__device__ __forceinline__ void stats_chunk(const Params &a, const Problem &P,
+                                            const float (&v)[32], int cbase, int nvalid,
+                                            StatAcc &st, int64_t y) {
+    float cm = -INFINITY;
+    int ci = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j < nvalid && v[j] > cm) {
+            cm = v[j];
+            ci = j;
+        }
+    const bool cap = a.T > 0.f;
+    if (cm > st.mx) {
+        const float nz = cap ? ce::softcap_z<true>(cm, a.T, a.k2).z : cm;
+        const float f = ptx::ex2((st.mz - nz) * ce::kLog2e);
+        st.s = (st.s == 0.f) ? 0.f : st.s * f;
+        st.mx = cm;
+        st.idx = P.col0 + cbase + ci;
+        st.mz = nz;
+    }
+    const float nm = -st.mz * ce::kLog2e;
+    float s0 = 0.f, s1 = 0.f, z0 = 0.f, z1 = 0.f;
+    if (cap) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float za = ce::softcap_z<true>(v[j], a.T, a.k2).z;
+            const float zb = ce::softcap_z<true>(v[j + 1], a.T, a.k2).z;
+            if (j < nvalid) {
+                s0 += ptx::ex2(fmaf(za, ce::kLog2e, nm));
+                z0 += za;
+            }
+            if (j + 1 < nvalid) {
+                s1 += ptx::ex2(fmaf(zb, ce::kLog2e, nm));
+                z1 += zb;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            if (j < nvalid) {
+                s0 += ptx::ex2(fmaf(v[j], ce::kLog2e, nm));
+                z0 += v[j];
+            }
+            if (j + 1 < nvalid) {
+                s1 += ptx::ex2(fmaf(v[j + 1], ce::kLog2e, nm));
+                z1 += v[j + 1];
+            }
+        }
+    }
+    st.s += s0 + s1;
+    st.sz += z0 + z1;
+    const int64_t yl = y - P.col0 - cbase;  // label column within this chunk
+    if (yl >= 0 && yl < nvalid) {
+        float xy = v[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j)
+            if (j == yl) xy = v[j];
+        st.zy = cap ? ce::softcap_z<true>(xy, a.T, a.k2).z : xy;
+    }
+}
+
+// Gradient tile: G = rscale (softmax - q) (1 - t^2) of one 32-column chunk -> bf16.
+__device__ __forceinline__ void grad_chunk(const Params &a, const Problem &P, const float (&v)[32],
+                                           int row, int cbase, int nvalid, int64_t y,
+                                           float rscale, float nlseL) {
+    const bool cap = a.T > 0.f;
+    const float c_smooth = rscale * (a.eps / static_cast<float>(a.V));
+    const float c_label = c_smooth + rscale * (1.f - a.eps);
+    const int64_t yl = y - P.col0 - cbase;
+    float g[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float z = v[j], dz = 1.f;
+        if (cap) {
+            const ce::Capped cz = ce::softcap_z<true>(v[j], a.T, a.k2);
+            z = cz.z;
+            dz = cz.dz;
+        }
+        const float pr = ptx::ex2(fmaf(z, ce::kLog2e, nlseL));
+        g[j] = fmaf(pr, rscale, (j == yl) ? -c_label : -c_smooth) * dz;
+    }
+    __nv_bfloat16 *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
+    if (nvalid == 32) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+            *reinterpret_cast<uint4 *>(c16 + j) =
+                make_uint4(ce::pack_bf16x2(g[j], g[j + 1]), ce::pack_bf16x2(g[j + 2], g[j + 3]),
+                           ce::pack_bf16x2(g[j + 4], g[j + 5]), ce::pack_bf16x2(g[j + 6], g[j + 7]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < nvalid) c16[j] = __float2bfloat16_rn(g[j]);
+    }
+}
+
 // ------------------------------------------------------------ the kernel
-template <int MODE, bool A_MN, bool B_MN>
+// Launched with clusters of 2 CTAs (rank 0 = leader) and a grid of 2 x
+// (co-resident clusters); needs kSmemBytes of dynamic shared memory.
 __global__ void __launch_bounds__(kThreads, 1)
-    vlmce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const Args a) {
+    vlmce_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -286,60 +290,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Mt = (a.M + BM - 1) / BM, Nt = (a.N + BN - 1) / BN;
-    const int tiles = Mt * Nt;
-    const int kblocks = (a.K + BK - 1) / BK;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cluster = static_cast<int>(ptx::cluster_id_x());
+    const int nclusters = static_cast<int>(ptx::ncluster_x());
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), 1);
+            ptx::mbar_init(full(s), 1);   // leader: its arrive + both CTAs' bytes
+            ptx::mbar_init(empty(s), 1);  // one multicast commit per use
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull(b), 1);
-            ptx::mbar_init(tempty(b), 4);
+            ptx::mbar_init(tempty(b), 8);  // leader: 4 epilogue warps x 2 CTAs
         }
         ptx::mbar_init(drain, 1);
         *abort = 0;
         ptx::fence_mbar_init_cluster();
     }
     if (warp == 0 && lane == 0) {
-        tc::prefetch_tensormap(&tmA);
-        tc::prefetch_tensormap(&tmB);
+        for (int i = 0; i < a.nprob; ++i) {
+            tc::prefetch_tensormap(&maps.a[i]);
+            tc::prefetch_tensormap(&maps.b[i]);
+        }
     }
     if (warp == 1) {
-        tc::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
-        tc::tmem_relinquish();
+        tc::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+        tc::tmem_relinquish_pair();
     }
     tc::fence_before_sync();
-    __syncthreads();
+    ptx::cluster_sync_any();  // barrier inits and the TMEM address visible to the pair
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---- TMA producer
+        // ---- TMA producer (both CTAs): this CTA's 128 rows of A and of B
         if (lane == 0) {
+            const uint32_t full_leader = ptx::mapa(full(0), 0);
             int s = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
-            for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-                const int m0 = (t % Mt) * BM, n0 = (t / Mt) * BN;
+            for (int t = cluster; t < a.tiles; t += nclusters) {
+                const Tile tl = tile_of(a, t);
+                const Problem &P = a.p[tl.p];
+                const CUtensorMap *ma = &maps.a[tl.p];
+                const CUtensorMap *mb = &maps.b[tl.p];
+                const int ar = tl.m0 + kHalf * static_cast<int>(rank);
+                const int br = tl.n0 + kHalf * static_cast<int>(rank);
+                const int kblocks = (P.K + BK - 1) / BK;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     wait_bar(empty(s), ph ^ 1, abort, a.err);
-                    ptx::mbar_arrive_expect_tx(full(s), kStageBytes);
-                    const uint32_t sa = ring + s * kStageBytes, sb = sa + kABytes;
-                    if constexpr (!A_MN) {
-                        tc::tma_load_2d(sa, &tmA, kb * BK, m0, full(s));
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(full(s), 2 * kStageBytes);
+                    const uint32_t sa = ring + s * kStageBytes, sb = sa + kOpBytes;
+                    const uint32_t fb = full_leader + 8u * s;
+                    if (!P.a_mn) {
+                        tc::tma_load_2d_pair(sa, ma, kb * BK, ar, fb);
                     } else {
-                        tc::tma_load_2d(sa, &tmA, m0, kb * BK, full(s));
-                        tc::tma_load_2d(sa + 8192, &tmA, m0 + 64, kb * BK, full(s));
+                        tc::tma_load_2d_pair(sa, ma, ar, kb * BK, fb);
+                        tc::tma_load_2d_pair(sa + 8192, ma, ar + 64, kb * BK, fb);
                     }
-                    if constexpr (!B_MN) {
-                        tc::tma_load_2d(sb, &tmB, kb * BK, n0, full(s));
+                    if (!P.b_mn) {
+                        tc::tma_load_2d_pair(sb, mb, kb * BK, br, fb);
                     } else {
-#pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tc::tma_load_2d(sb + 8192 * i, &tmB, n0 + 64 * i, kb * BK, full(s));
+                        tc::tma_load_2d_pair(sb, mb, br, kb * BK, fb);
+                        tc::tma_load_2d_pair(sb + 8192, mb, br + 64, kb * BK, fb);
                     }
                     ++issued;
                     if (++s == kStages) {
@@ -348,68 +361,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // every issued copy has landed before teardown
-            for (int i = 0; i < kStages && i < issued; ++i) {
-                const int64_t q = issued - 1 - i;
-                drain_bar(full(static_cast<int>(q % kStages)),
-                          static_cast<uint32_t>((q / kStages) & 1), a.err);
+            // the leader's full barriers count both CTAs' copies: every issued
+            // copy has landed once its phase completed
+            if (rank == 0) {
+                for (int i = 0; i < kStages && i < issued; ++i) {
+                    const int64_t q = issued - 1 - i;
+                    drain_bar(full(static_cast<int>(q % kStages)),
+                              static_cast<uint32_t>((q / kStages) & 1), a.err);
+                }
             }
         }
     } else if (warp == 1) {
-        // ---- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+        // ---- MMA issuer (leader only)
+        if (rank == 0 && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
-            for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+            for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
+                const Tile tl = tile_of(a, t);
+                const Problem &P = a.p[tl.p];
+                const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, P.a_mn != 0, P.b_mn != 0);
+                const int kblocks = (P.K + BK - 1) / BK;
                 const int b = it & 1;
-                wait_bar(tempty(b), ((it >> 1) & 1) ^ 1, abort, a.err);
+                wait_bar<true>(tempty(b), ((it >> 1) & 1) ^ 1, abort, a.err);
                 tc::fence_after_sync();
                 const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     wait_bar(full(s), ph, abort, a.err);
                     tc::fence_after_sync();
-                    const uint32_t sa = ring + s * kStageBytes, sb = sa + kABytes;
+                    const uint32_t sa = ring + s * kStageBytes, sb = sa + kOpBytes;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = A_MN ? tc::smem_desc_sw128(sa + 2048 * kk, 8192, 1024)
-                                                 : tc::smem_desc_sw128(sa + 32 * kk, 16, 1024);
-                        const uint64_t bd = B_MN ? tc::smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
-                                                 : tc::smem_desc_sw128(sb + 32 * kk, 16, 1024);
-                        tc::mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+                        const uint64_t ad = P.a_mn ? tc::smem_desc_sw128(sa + 2048 * kk, 8192, 1024)
+                                                   : tc::smem_desc_sw128(sa + 32 * kk, 16, 1024);
+                        const uint64_t bd = P.b_mn ? tc::smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
+                                                   : tc::smem_desc_sw128(sb + 32 * kk, 16, 1024);
+                        tc::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    tc::mma_commit(empty(s));
+                    tc::mma_commit_pair(empty(s), 0x3);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1;
                     }
                 }
-                tc::mma_commit(tfull(b));
+                tc::mma_commit_pair(tfull(b), 0x3);
             }
-            tc::mma_commit(drain);
+            tc::mma_commit_pair(drain, 0x1);
             drain_bar(drain, 0, a.err);
         }
     } else {
-        // ---- epilogue: warps 2-5, TMEM subpartition warp % 4
+        // ---- epilogue: warps 2-5 of both CTAs, TMEM subpartition warp % 4
         const int q = warp & 3;
-        const int rl = q * 32 + lane;
+        const int rl = static_cast<int>(rank) * kHalf + q * 32 + lane;
+        const uint32_t tempty_leader = ptx::mapa(tempty(0), 0);
         int it = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+        for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
+            const Tile tl = tile_of(a, t);
+            const Problem &P = a.p[tl.p];
             const int b = it & 1;
-            const int m0 = (t % Mt) * BM, n0 = (t / Mt) * BN;
             wait_bar(tfull(b), (it >> 1) & 1, abort, a.err);
             tc::fence_after_sync();
-            const int row = m0 + rl;
+            const int row = tl.m0 + rl;
+            const bool row_ok = row < P.M;
             int64_t y = -1;
             float rscale = 0.f, nlseL = 0.f;
-            if constexpr (MODE == kStats || MODE == kGrad) {
-                if (row < a.M) {
-                    y = a.labels[row];
-                    if constexpr (MODE == kGrad) {
-                        rscale = a.row_scale[row];
-                        nlseL = -a.lse[row] * ce::kLog2e;
-                    }
+            if ((P.mode == kStats || P.mode == kGrad) && row_ok) {
+                y = a.labels[row];
+                if (P.mode == kGrad) {
+                    rscale = a.row_scale[row];
+                    nlseL = -a.lse[row] * ce::kLog2e;
                 }
             }
             StatAcc st;
@@ -428,31 +448,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                epilogue_chunk<MODE>(a, v, row, n0 + 32 * c, st, y, rscale, nlseL);
-            }
-            if constexpr (MODE == kStats) {
-                if (row < a.M) {
-                    ce::RowPart p;
-                    p.mx = st.mx;
-                    p.idx = st.idx;
-                    p.mz = st.mz;
-                    p.s = st.s;
-                    p.sz = st.sz;
-                    p.zy = st.zy;
-                    p.pad0 = p.pad1 = 0.f;
-                    a.part[static_cast<int64_t>(t / Mt) * a.part_ld + row] = p;
+                const int cbase = tl.n0 + 32 * c;
+                const int nvalid = min(32, P.N - cbase);
+                if (nvalid <= 0 || !row_ok) continue;
+                switch (P.mode) {
+                    case kStats: stats_chunk(a, P, v, cbase, nvalid, st, y); break;
+                    case kGrad: grad_chunk(a, P, v, row, cbase, nvalid, y, rscale, nlseL); break;
+                    case kStoreF32: store_chunk<kStoreF32>(P, v, row, cbase, nvalid); break;
+                    case kAccF32: store_chunk<kAccF32>(P, v, row, cbase, nvalid); break;
+                    case kStoreBF16: store_chunk<kStoreBF16>(P, v, row, cbase, nvalid); break;
+                    default: store_chunk<kAccToBF16>(P, v, row, cbase, nvalid); break;
                 }
+            }
+            if (P.mode == kStats && row_ok) {
+                ce::RowPart p;
+                p.mx = st.mx;
+                p.idx = st.idx;
+                p.mz = st.mz;
+                p.s = st.s;
+                p.sz = st.sz;
+                p.zy = st.zy;
+                p.pad0 = p.pad1 = 0.f;
+                P.part[static_cast<int64_t>(tl.n0 / BN) * P.part_ld + row] = p;
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) bar_arrive(tempty(b));
+            if (lane == 0) ptx::mbar_remote_arrive_release(tempty_leader + 8u * b);
         }
     }
+    // teardown: the leader's MMAs have completed (drain) and its copies have
+    // landed; the pair meets before TMEM is released and either CTA exits
     tc::fence_before_sync();
     __syncthreads();
+    ptx::cluster_sync_any();
     if (warp == 1) {
+        __syncwarp();
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 

@@ -1,24 +1,27 @@
-// gemm_launch.h -- host-side launchers of the tcgen05 GEMM instantiations
-// (gemm_kk.cu, gemm_km.cu, gemm_mk.cu, gemm_mm.cu: K- or MN-major A and B).
+// gemm_launch.h -- host side of the tcgen05 GEMM (gemm.cuh): tensor maps of
+// the operands and the launch of a group of up to kMaxProblems products.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "gemm.cuh"
+#include <cstdint>
+
+#include "gemm_types.h"
 
 namespace vlmce {
 namespace gemm {
 
-// Launch mode `mode` (gemm::Mode) on `grid` CTAs; returns the launch error.
-cudaError_t launch_kk(int mode, const CUtensorMap &a, const CUtensorMap &b, const Args &args,
-                      int grid, cudaStream_t s);
-cudaError_t launch_km(int mode, const CUtensorMap &a, const CUtensorMap &b, const Args &args,
-                      int grid, cudaStream_t s);
-cudaError_t launch_mk(int mode, const CUtensorMap &a, const CUtensorMap &b, const Args &args,
-                      int grid, cudaStream_t s);
-cudaError_t launch_mm(int mode, const CUtensorMap &a, const CUtensorMap &b, const Args &args,
-                      int grid, cudaStream_t s);
+// Tensor map of operand A (rows = M) or B (rows = N) of C = A B^T, bf16:
+// K-major ([rows, ld], K contiguous) or MN-major ([K, ld], rows contiguous).
+// Out-of-range elements read as zero.  False if the driver refuses it.
+bool make_operand_map(CUtensorMap *m, const void *base, bool mn, int64_t rows, int64_t K,
+                      int64_t ld);
+
+// Fill p.mt / p.tile0 / a.tiles from the problems' shapes and launch them on
+// `s` as one persistent grid of CTA pairs (a.nprob problems, maps.a/b[i]
+// for problem i).  Returns the launch error.
+cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s);
 
 }  // namespace gemm
 }  // namespace vlmce

@@ -1,0 +1,72 @@
+// gemm_types.h -- shapes, modes and launch parameters of the tcgen05 GEMM
+// (the kernel is in gemm.cuh, its host side in gemm.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "ce_common.cuh"
+
+namespace vlmce {
+namespace gemm {
+
+constexpr int BM = 256, BN = 256, BK = 64;  // pair tile
+constexpr int kHalf = 128;                  // rows of A and of B held by one CTA
+constexpr int kStages = 6;
+constexpr int kOpBytes = kHalf * BK * 2;    // 16 KB per operand per stage
+constexpr int kStageBytes = 2 * kOpBytes;   // 32 KB per CTA
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 2 * BN;
+constexpr int kBarriers = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kBarriers + 16;
+constexpr int kMaxProblems = 3;
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
+enum Mode : int {
+    kStoreF32 = 0,   // C = acc (fp32)
+    kAccF32 = 1,     // C += acc (fp32)
+    kStats = 2,      // row statistics of the logits tile (fused linear CE, pass 1)
+    kGrad = 3,       // gradient tile G = scale (p - q) (1 - t^2) -> bf16 (pass 2)
+    kStoreBF16 = 4,  // C16 = bf16(acc)
+    kAccToBF16 = 5,  // C16 = bf16(C + acc)
+};
+
+// One product of a launch.
+struct Problem {
+    int M, N, K;
+    int mode;                  // Mode
+    int a_mn, b_mn;            // operand stored MN-major
+    int mt;                    // tiles along M
+    int tile0;                 // number of the problem's first tile in the launch
+    float *C;                  // fp32 [M, ldc]
+    int64_t ldc;
+    __nv_bfloat16 *C16;        // bf16 [M, ldc16]
+    int64_t ldc16;
+    int col0;                  // kStats / kGrad: vocabulary column of n = 0
+    ce::RowPart *part;         // kStats: part[n_tile * part_ld + row]
+    int64_t part_ld;
+};
+
+struct Params {
+    Problem p[kMaxProblems];
+    int nprob;
+    int tiles;                 // all problems' tiles
+    // cross-entropy epilogues (shared by the problems of a launch)
+    const int64_t *labels;     // [M]
+    int64_t ignore_index;
+    int V;                     // vocabulary size
+    float eps, T, k2;          // smoothing, softcap (0 = off), -2 log2e / T
+    const float *lse;          // kGrad: [M]
+    const float *row_scale;    // kGrad: [M] scale of a valid row, 0 otherwise
+    int *err;                  // device error word (may be null)
+};
+
+struct Maps {
+    CUtensorMap a[kMaxProblems];  // K-major: box 64 K x 128 rows; MN-major: 64 x 64
+    CUtensorMap b[kMaxProblems];
+};
+
+}  // namespace gemm
+}  // namespace vlmce

@@ -1,7 +1,10 @@
-// tcgen05.cuh -- inline-PTX wrappers for the sm_100-family tensor cores:
-// tensor-memory (TMEM) allocation, tcgen05.mma with bf16 operands and fp32
-// accumulators, commits to mbarriers, TMEM loads, tiled TMA loads, and the
-// shared-memory / instruction descriptors the MMA consumes.
+// tcgen05.cuh -- inline-PTX wrappers for the sm_100-family tensor cores,
+// in their CTA-pair form (.cta_group::2: one MMA spans the tensor cores of
+// two SMs of a cluster): tensor-memory (TMEM) allocation, tcgen05.mma with
+// bf16 operands and fp32 accumulators, commits multicast to mbarriers of
+// both CTAs, TMEM loads, tiled TMA loads that signal the pair's leader, and
+// the shared-memory / instruction descriptors the MMA consumes.  Every
+// tcgen05 instruction of a kernel must use the same .cta_group.
 #pragma once
 
 #include <cuda.h>
@@ -12,18 +15,19 @@ namespace vlmce {
 namespace tc {
 
 // ------------------------------------------------------------------- TMEM
-// Allocate `ncols` TMEM columns (power of two >= 32) for this CTA; the
-// address is written to shared memory at `dst`.  Whole warp.
-__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+// Allocate `ncols` TMEM columns (power of two >= 32) in both SMs of the CTA
+// pair; one warp of each CTA executes it, and each gets the (common) address
+// in its own shared memory at `dst`.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
                  "r"(ncols)
                  : "memory");
 }
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
 __device__ __forceinline__ void fence_before_sync() {
@@ -34,21 +38,27 @@ __device__ __forceinline__ void fence_after_sync() {
 }
 
 // ------------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 x bf16 -> fp32, shape from idesc.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// Pair MMA, issued by one thread of the leader CTA: D (+)= A B^T with A's M
+// rows split between the two CTAs (each CTA's half at the same shared-memory
+// offset, described by a_desc) and B's N rows likewise (b_desc); each CTA's
+// TMEM receives its own M half x all N columns.  bf16 x bf16 -> fp32.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Arrive on an mbarrier once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     mbar)
-                 : "memory");
+// Once every pair MMA this thread issued so far has completed, arrive once on
+// the mbarrier at shared-memory offset `mbar` of each CTA in `cta_mask`.
+__device__ __forceinline__ void mma_commit_pair(uint32_t mbar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(mbar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns of TMEM into 32 registers per thread
@@ -70,14 +80,16 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 // ------------------------------------------------------------------- TMA
-// 2-D tiled bulk tensor load into this CTA's shared memory; c0 is the
+// 2-D tiled bulk tensor load into this CTA's shared memory at `dst`; the
+// completed bytes are counted on the mbarrier at shared::cluster address
+// `mbar_cluster`, which may be in this CTA or its pair peer.  c0 is the
 // innermost coordinate (elements; its byte offset must be a multiple of 16).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
-                                            uint32_t mbar) {
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *tm, int c0,
+                                                 int c1, uint32_t mbar_cluster) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(tm), "r"(c0), "r"(c1), "r"(mbar)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tm), "r"(c0), "r"(c1), "r"(mbar_cluster)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
