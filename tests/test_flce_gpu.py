@@ -48,7 +48,8 @@ def gemm(A, a_mn, B, b_mn, C, M, N, K, accumulate=False):
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (1000, 264, 1032)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (1000, 264, 1032),
+                                   (520, 136, 72)])
 def test_gemm_engine_against_matmul(a_mn, b_mn, M, N, K):
     g = torch.Generator(device=DEV)
     g.manual_seed(M * 7 + N * 3 + K + 10 * a_mn + b_mn)
@@ -123,6 +124,14 @@ def test_flce_small_single_chunk(N, H, V, T, eps, red):
 def test_flce_several_chunks_and_accumulated_weight_gradient():
     run_small(small(200, 264, 20000, T=30.0, eps=0.1), accumulate=False)
     run_small(small(150, 136, 17000, T=0.0, eps=0.0, red="sum"), accumulate=True)
+
+
+@pytest.mark.parametrize("N,H,V,T,eps", [(600, 264, 17000, 30.0, 0.1), (520, 128, 9000, 0.0, 0.0),
+                                         (1030, 200, 700, 5.0, 0.2)])
+def test_flce_two_pairs_per_cluster(N, H, V, T, eps):
+    # more than one 256-row pair tile: clusters of two CTA pairs share each
+    # weight tile; ragged rows in the second pair, several vocabulary chunks
+    run_small(small(N, H, V, T=T, eps=eps, red="sum", gs=0.25, seed=N), accumulate=(N == 520))
 
 
 def test_flce_deterministic():

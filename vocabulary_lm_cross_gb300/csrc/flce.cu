@@ -258,8 +258,8 @@ extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void 
     vlmce_status st = current_device(&dev);
     if (st != VLMCE_OK) return st;
     gemm::Maps maps;
-    if (!gemm::make_operand_map(&maps.a[0], A, a_mn != 0, M, K, lda) ||
-        !gemm::make_operand_map(&maps.b[0], B, b_mn != 0, N, K, ldb)) {
+    if (!gemm::make_operand_map(&maps.a[0], A, false, a_mn != 0, M, K, lda) ||
+        !gemm::make_operand_map(&maps.b[0], B, true, b_mn != 0, N, K, ldb)) {
         record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
         return VLMCE_ERR_CUDA;
     }
@@ -345,8 +345,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
         // ---- pass 1: statistics of S = h' W^T over the whole vocabulary
         {
             gemm::Maps maps;
-            if (!gemm::make_operand_map(&maps.a[0], hidden, false, N, H, hidden_stride) ||
-                !gemm::make_operand_map(&maps.b[0], weight, false, V, H, weight_stride))
+            if (!gemm::make_operand_map(&maps.a[0], hidden, false, false, N, H, hidden_stride) ||
+                !gemm::make_operand_map(&maps.b[0], weight, true, false, V, H, weight_stride))
                 return map_fail();
             gemm::Params g = base;
             g.nprob = 1;
@@ -382,8 +382,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                     reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
                 const __nv_bfloat16 *gc = w.g[cp & 1];
                 // grad_h (+)= G_c W_c: A = G_c K-major [N, Vc], B = W_c N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, N, vc, kChunk) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, true, H, vc, weight_stride))
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, false, N, vc, kChunk) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, true, H, vc, weight_stride))
                     return map_fail();
                 gemm::Problem &ph = g.p[n++];
                 ph.M = static_cast<int>(N);
@@ -400,8 +400,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                 ph.C16 = static_cast<__nv_bfloat16 *>(grad_hidden);
                 ph.ldc16 = hidden_stride;
                 // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, true, vc, N, kChunk) ||
-                    !gemm::make_operand_map(&maps.b[n], hidden, true, H, N, hidden_stride))
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, true, vc, N, kChunk) ||
+                    !gemm::make_operand_map(&maps.b[n], hidden, true, true, H, N, hidden_stride))
                     return map_fail();
                 gemm::Problem &pw = g.p[n++];
                 pw.M = static_cast<int>(vc);
@@ -419,8 +419,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                 const __nv_bfloat16 *wc =
                     reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
                 // G_c = scale (softmax - q) (1 - t^2) from the recomputed S_c = h' W_c^T
-                if (!gemm::make_operand_map(&maps.a[n], hidden, false, N, H, hidden_stride) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, false, vc, H, weight_stride))
+                if (!gemm::make_operand_map(&maps.a[n], hidden, false, false, N, H, hidden_stride) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, false, vc, H, weight_stride))
                     return map_fail();
                 gemm::Problem &pg = g.p[n++];
                 pg.M = static_cast<int>(N);

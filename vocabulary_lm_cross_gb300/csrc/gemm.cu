@@ -50,11 +50,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
 
 constexpr int kMaxDevices = 64;
 
-// Clusters of 2 CTAs that fit on the device at once (an SM of a GPC whose
-// SM count is odd cannot take part in a pair); cached per device.
-int co_resident_clusters(int device, cudaError_t *err) {
+// Clusters of `csize` CTAs that fit on the device at once (SMs of a GPC
+// that cannot complete a cluster stay idle); cached per device and size.
+int co_resident_clusters(int device, int csize, cudaError_t *err) {
     static std::mutex mu;
-    static int cached[kMaxDevices] = {};
+    static int cached[kMaxDevices][2] = {};
     static bool attr_done = false;
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_done) {
@@ -66,14 +66,16 @@ int co_resident_clusters(int device, cudaError_t *err) {
         }
         attr_done = true;
     }
-    if (device >= 0 && device < kMaxDevices && cached[device] > 0) return cached[device];
+    const int slot = csize == 4 ? 1 : 0;
+    if (device >= 0 && device < kMaxDevices && cached[device][slot] > 0)
+        return cached[device][slot];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(csize, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.attrs = attr;
@@ -84,22 +86,28 @@ int co_resident_clusters(int device, cudaError_t *err) {
         *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
         return 0;
     }
-    if (device >= 0 && device < kMaxDevices) cached[device] = n;
+    if (device >= 0 && device < kMaxDevices) cached[device][slot] = n;
     return n;
 }
 
 }  // namespace
 
-bool make_operand_map(CUtensorMap *m, const void *base, bool mn, int64_t rows, int64_t K,
-                      int64_t ld) {
-    return mn ? make_map(m, base, rows, K, ld, 64, 64) : make_map(m, base, K, rows, ld, 64, kHalf);
+bool make_operand_map(CUtensorMap *m, const void *base, bool is_b, bool mn, int64_t rows,
+                      int64_t K, int64_t ld) {
+    if (mn) return make_map(m, base, rows, K, ld, 64, 64);
+    return make_map(m, base, K, rows, ld, 64, is_b ? 64 : kHalf);
 }
 
 cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s) {
+    // two pairs per cluster (sharing each B tile) unless a problem is at
+    // most one pair tile high
+    int npairs = 2;
+    for (int i = 0; i < a.nprob; ++i)
+        if (a.p[i].M <= BM) npairs = 1;
     int tiles = 0;
     for (int i = 0; i < a.nprob; ++i) {
         Problem &p = a.p[i];
-        p.mt = (p.M + BM - 1) / BM;
+        p.mt = (p.M + BM * npairs - 1) / (BM * npairs);
         p.tile0 = tiles;
         tiles += p.mt * ((p.N + BN - 1) / BN);
     }
@@ -109,17 +117,18 @@ cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     e = cudaSuccess;
-    const int clusters_max = co_resident_clusters(device, &e);
+    const int csize = 2 * npairs;
+    const int clusters_max = co_resident_clusters(device, csize, &e);
     if (clusters_max < 1) return e;
     const int clusters = tiles < clusters_max ? tiles : clusters_max;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.gridDim = dim3(csize * clusters, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;

@@ -87,14 +87,15 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int *er
 struct Tile {
     int p, m0, n0;
 };
-__device__ __forceinline__ Tile tile_of(const Params &a, int t) {
+// Cluster tile t of the launch: problem, first row (BM x npairs rows), first column.
+__device__ __forceinline__ Tile tile_of(const Params &a, int t, int npairs) {
     int p = 0;
 #pragma unroll
     for (int i = 1; i < kMaxProblems; ++i)
         if (i < a.nprob && t >= a.p[i].tile0) p = i;
     const int lt = t - a.p[p].tile0;
     const int mt = a.p[p].mt;
-    return Tile{p, (lt % mt) * BM, (lt / mt) * BN};
+    return Tile{p, (lt % mt) * (BM * npairs), (lt / mt) * BN};
 }
 
 // ------------------------------------------------------------ epilogues
@@ -271,8 +272,9 @@ __device__ __forceinline__ void grad_chunk(const Params &a, const Problem &P, co
 }
 
 // ------------------------------------------------------------ the kernel
-// Launched with clusters of 2 CTAs (rank 0 = leader) and a grid of 2 x
-// (co-resident clusters); needs kSmemBytes of dynamic shared memory.
+// Launched with clusters of 2 or 4 CTAs (one or two pairs; the even CTA of
+// a pair is its leader) and a grid of co-resident clusters; needs
+// kSmemBytes of dynamic shared memory.
 __global__ void __launch_bounds__(kThreads, 1)
     vlmce_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params a) {
     extern __shared__ unsigned char smem_raw[];
@@ -290,14 +292,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t crank = ptx::cluster_ctarank();
+    const int npairs = static_cast<int>(ptx::cluster_nctarank()) >> 1;  // 1 or 2
+    const int pair = static_cast<int>(crank >> 1);
+    const uint32_t prank = crank & 1u;  // 0: the pair's leader
+    const uint32_t leader = crank & ~1u;
+    const uint16_t all_ctas = static_cast<uint16_t>((1u << (2 * npairs)) - 1u);
+    const uint16_t pair_ctas = static_cast<uint16_t>(3u << (2 * pair));
     const int cluster = static_cast<int>(ptx::cluster_id_x());
     const int nclusters = static_cast<int>(ptx::ncluster_x());
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(full(s), 1);   // leader: its arrive + both CTAs' bytes
-            ptx::mbar_init(empty(s), 1);  // one multicast commit per use
+            // leader: its producer's arrival + the bytes of both CTAs of the pair
+            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(empty(s), npairs);  // one commit from every pair's leader
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull(b), 1);
@@ -318,28 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_relinquish_pair();
     }
     tc::fence_before_sync();
-    ptx::cluster_sync_any();  // barrier inits and the TMEM address visible to the pair
+    ptx::cluster_sync_any();  // barrier inits and the TMEM address visible to the cluster
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---- TMA producer (both CTAs): this CTA's 128 rows of A and of B
+        // ---- TMA producer (every CTA).  A: this CTA's 128 rows.  B: this
+        // CTA's 128-row half of the pair's B tile, made of two 64-row slices;
+        // with two pairs each CTA loads one slice and multicasts it to the
+        // CTA of the other pair that holds the same half.  Every copy counts
+        // on the full barrier of the receiving CTA's pair leader.
         if (lane == 0) {
-            const uint32_t full_leader = ptx::mapa(full(0), 0);
+            const uint32_t full_leader = ptx::mapa(full(0), leader);
+            const uint16_t b_mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
             int s = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
             for (int t = cluster; t < a.tiles; t += nclusters) {
-                const Tile tl = tile_of(a, t);
+                const Tile tl = tile_of(a, t, npairs);
                 const Problem &P = a.p[tl.p];
                 const CUtensorMap *ma = &maps.a[tl.p];
                 const CUtensorMap *mb = &maps.b[tl.p];
-                const int ar = tl.m0 + kHalf * static_cast<int>(rank);
-                const int br = tl.n0 + kHalf * static_cast<int>(rank);
+                const int ar = tl.m0 + BM * pair + kHalf * static_cast<int>(prank);
+                const int br = tl.n0 + kHalf * static_cast<int>(prank);
                 const int kblocks = (P.K + BK - 1) / BK;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     wait_bar(empty(s), ph ^ 1, abort, a.err);
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(full(s), 2 * kStageBytes);
+                    if (prank == 0) ptx::mbar_arrive_expect_tx(full(s), 2 * kStageBytes);
                     const uint32_t sa = ring + s * kStageBytes, sb = sa + kOpBytes;
                     const uint32_t fb = full_leader + 8u * s;
                     if (!P.a_mn) {
@@ -348,11 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::tma_load_2d_pair(sa, ma, ar, kb * BK, fb);
                         tc::tma_load_2d_pair(sa + 8192, ma, ar + 64, kb * BK, fb);
                     }
-                    if (!P.b_mn) {
-                        tc::tma_load_2d_pair(sb, mb, kb * BK, br, fb);
-                    } else {
-                        tc::tma_load_2d_pair(sb, mb, br, kb * BK, fb);
-                        tc::tma_load_2d_pair(sb + 8192, mb, br + 64, kb * BK, fb);
+                    for (int q = (npairs == 2 ? pair : 0); q < 2; q += npairs) {
+                        const int c0 = P.b_mn ? br + 64 * q : kb * BK;
+                        const int c1 = P.b_mn ? kb * BK : br + 64 * q;
+                        if (npairs == 2)
+                            tc::tma_load_2d_pair_multicast(sb + 8192 * q, mb, c0, c1, fb, b_mask);
+                        else
+                            tc::tma_load_2d_pair(sb + 8192 * q, mb, c0, c1, fb);
                     }
                     ++issued;
                     if (++s == kStages) {
@@ -361,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // the leader's full barriers count both CTAs' copies: every issued
-            // copy has landed once its phase completed
-            if (rank == 0) {
+            // at a leader, every copy into its pair has landed once the full
+            // phases of the last kStages loads completed
+            if (prank == 0) {
                 for (int i = 0; i < kStages && i < issued; ++i) {
                     const int64_t q = issued - 1 - i;
                     drain_bar(full(static_cast<int>(q % kStages)),
@@ -372,13 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ---- MMA issuer (leader only)
-        if (rank == 0 && lane == 0) {
+        // ---- MMA issuer (pair leader)
+        if (prank == 0 && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
-                const Tile tl = tile_of(a, t);
+                const Tile tl = tile_of(a, t, npairs);
                 const Problem &P = a.p[tl.p];
                 const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, P.a_mn != 0, P.b_mn != 0);
                 const int kblocks = (P.K + BK - 1) / BK;
@@ -398,25 +414,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    : tc::smem_desc_sw128(sb + 32 * kk, 16, 1024);
                         tc::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    tc::mma_commit_pair(empty(s), 0x3);
+                    tc::mma_commit_pair(empty(s), all_ctas);  // the stage is free everywhere
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1;
                     }
                 }
-                tc::mma_commit_pair(tfull(b), 0x3);
+                tc::mma_commit_pair(tfull(b), pair_ctas);
             }
-            tc::mma_commit_pair(drain, 0x1);
+            tc::mma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
             drain_bar(drain, 0, a.err);
         }
     } else {
-        // ---- epilogue: warps 2-5 of both CTAs, TMEM subpartition warp % 4
+        // ---- epilogue: warps 2-5 of every CTA, TMEM subpartition warp % 4
         const int q = warp & 3;
-        const int rl = static_cast<int>(rank) * kHalf + q * 32 + lane;
-        const uint32_t tempty_leader = ptx::mapa(tempty(0), 0);
+        const int rl = BM * pair + static_cast<int>(prank) * kHalf + q * 32 + lane;
+        const uint32_t tempty_leader = ptx::mapa(tempty(0), leader);
         int it = 0;
         for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
-            const Tile tl = tile_of(a, t);
+            const Tile tl = tile_of(a, t, npairs);
             const Problem &P = a.p[tl.p];
             const int b = it & 1;
             wait_bar(tfull(b), (it >> 1) & 1, abort, a.err);
@@ -476,8 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::mbar_remote_arrive_release(tempty_leader + 8u * b);
         }
     }
-    // teardown: the leader's MMAs have completed (drain) and its copies have
-    // landed; the pair meets before TMEM is released and either CTA exits
+    // teardown: every MMA of the cluster has completed (drain) and every copy
+    // into it has landed; the cluster meets before TMEM is released and any
+    // CTA exits
     tc::fence_before_sync();
     __syncthreads();
     ptx::cluster_sync_any();

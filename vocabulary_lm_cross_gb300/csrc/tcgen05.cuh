@@ -2,9 +2,9 @@
 // in their CTA-pair form (.cta_group::2: one MMA spans the tensor cores of
 // two SMs of a cluster): tensor-memory (TMEM) allocation, tcgen05.mma with
 // bf16 operands and fp32 accumulators, commits multicast to mbarriers of
-// both CTAs, TMEM loads, tiled TMA loads that signal the pair's leader, and
-// the shared-memory / instruction descriptors the MMA consumes.  Every
-// tcgen05 instruction of a kernel must use the same .cta_group.
+// several CTAs, TMEM loads, tiled TMA loads (plain and multicast), and the
+// shared-memory / instruction descriptors the MMA consumes.  Every tcgen05
+// instruction of a kernel must use the same .cta_group.
 #pragma once
 
 #include <cuda.h>
@@ -80,16 +80,30 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 // ------------------------------------------------------------------- TMA
-// 2-D tiled bulk tensor load into this CTA's shared memory at `dst`; the
-// completed bytes are counted on the mbarrier at shared::cluster address
-// `mbar_cluster`, which may be in this CTA or its pair peer.  c0 is the
-// innermost coordinate (elements; its byte offset must be a multiple of 16).
+// 2-D tiled bulk tensor loads into this CTA's shared memory at `dst`.  c0 is
+// the innermost coordinate (elements; its byte offset must be a multiple of
+// 16).
+// Pair form: the completed bytes are counted on the mbarrier at
+// shared::cluster address `mbar_leader`, the barrier of the pair's leader
+// (even) CTA.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *tm, int c0,
-                                                 int c1, uint32_t mbar_cluster) {
+                                                 int c1, uint32_t mbar_leader) {
     asm volatile(
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
         ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(tm), "r"(c0), "r"(c1), "r"(mbar_cluster)
+        "l"(tm), "r"(c0), "r"(c1), "r"(mbar_leader)
+        : "memory");
+}
+// Pair form, multicast: the box goes to shared-memory offset `dst` of every
+// CTA in `cta_mask`; the bytes each CTA receives are counted on the barrier
+// at the offset of `mbar_leader` in the leader CTA of that CTA's pair.
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap *tm,
+                                                           int c0, int c1, uint32_t mbar_leader,
+                                                           uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tm), "r"(c0), "r"(c1), "r"(mbar_leader), "h"(cta_mask)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
