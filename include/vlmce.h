@@ -118,9 +118,49 @@ vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int6
                         int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
                         void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
 
+/*
+ * ce_fwd_bwd_host -- ce_fwd_bwd for data that lives in host memory.  logits
+ * (read, then overwritten by the gradient), labels and the outputs may be
+ * page-locked host memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister)
+ * as well as device memory.  The pages have no counterpart: it serves callers
+ * whose logits are produced or consumed on the host.
+ *
+ * Host logits pass through the device in chunks of about 32 MB of rows: a
+ * copy in on a library-owned stream, the row kernel on `stream`, a copy of
+ * the gradient columns [0, V) back on a second library-owned stream, three
+ * chunks in flight, so both directions of the host-device link (NVLink-C2C on
+ * GB300) stay busy.  Labels and the outputs are read and written in place by
+ * the kernels.  Results are those of ce_fwd_bwd with its row kernel (bit-
+ * identical on the same inputs).  Device logits are handled by ce_fwd_bwd
+ * itself (host labels / outputs still allowed).
+ *
+ * Arguments, layout, results and errors are those of ce_fwd_bwd, except:
+ *   - every non-NULL pointer but the workspace is checked with
+ *     cudaPointerGetAttributes before anything is enqueued; one the device
+ *     cannot address (pageable host memory) gives VLMCE_ERR_INVALID_ARG;
+ *   - with host logits the workspace (device, 256-byte aligned) must hold
+ *     vlmce_ce_host_workspace_bytes(N, V, row_stride, dtype) bytes (it
+ *     includes the staging ring);
+ *   - the library creates, once per device, two non-blocking streams and a
+ *     few events for the pipeline, and enqueue is serialised by a mutex.
+ * The host buffers hold the results once `stream` has reached the end of the
+ * call (synchronise it before reading them).
+ */
+vlmce_status ce_fwd_bwd_host(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                             int64_t V, int64_t row_stride, int64_t ignore_index,
+                             float label_smoothing, float softcap, int32_t reduction,
+                             float grad_scale, float *out_loss, int64_t *out_argmax,
+                             float *out_reduced, int64_t *out_counts, void *workspace,
+                             size_t workspace_bytes, vlmce_stream_t stream);
+
+/* Bytes of device workspace ce_fwd_bwd_host needs when the logits are in
+ * host memory: ce_fwd_bwd's workspace and a ring of three chunk buffers of
+ * whole rows (row_stride elements each, about 32 MB per chunk). */
+size_t vlmce_ce_host_workspace_bytes(int64_t N, int64_t V, int64_t row_stride, int32_t dtype);
+
 /* Bytes of device workspace flce_fwd_bwd needs (256-byte aligned): per-row
- * statistics of every 256-column logits tile, a bf16 [N, 8192] gradient tile
- * and an fp32 [N, H] grad_hidden accumulator. */
+ * statistics of every 256-column logits tile, two bf16 [N, 8192] gradient
+ * tiles and an fp32 [N, H] grad_hidden accumulator. */
 size_t vlmce_flce_workspace_bytes(int64_t N, int64_t H, int64_t V);
 
 /*

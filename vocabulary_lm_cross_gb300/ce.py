@@ -95,3 +95,55 @@ def ce_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, *, ignore_index: int 
     except Exception:  # older/newer torch without the helper: nothing to bump
         pass
     return out
+
+
+def host_workspace_bytes(N: int, V: int, row_stride: int, dtype: torch.dtype) -> int:
+    """Device workspace of ce_fwd_bwd_host with host logits (includes its staging ring)."""
+    return int(capi.lib().vlmce_ce_host_workspace_bytes(N, V, row_stride, _DTYPES[dtype]))
+
+
+def ce_fwd_bwd_host(logits: torch.Tensor, labels: torch.Tensor, *, device: torch.device | str = "cuda",
+                    ignore_index: int = -100, label_smoothing: float = 0.0, softcap: float = 0.0,
+                    reduction: str = "mean", grad_scale: float = 1.0, out: CEResult | None = None,
+                    workspace: torch.Tensor | None = None) -> CEResult:
+    """``ce_fwd_bwd`` on page-locked host tensors: the logits stream through
+    ``device`` in chunks of rows (copy in, row kernel, gradient copied back
+    into ``logits``), labels and outputs are read and written in place.
+
+    logits: pinned CPU tensor [N, V] (fp32 or bf16, rows may be strided);
+    labels: pinned int64 CPU tensor [N]; ``out`` tensors (allocated pinned on
+    the host unless given) and the gradient in ``logits`` are valid once the
+    device's current stream has been synchronised.
+    """
+    if logits.dim() != 2 or labels.dim() != 1 or labels.shape[0] != logits.shape[0]:
+        raise ValueError("logits must be [N, V] and labels [N]")
+    if logits.dtype not in _DTYPES:
+        raise TypeError(f"unsupported logits dtype {logits.dtype}")
+    if labels.dtype != torch.int64:
+        raise TypeError("labels must be int64")
+    if logits.is_cuda or labels.is_cuda or not logits.is_pinned() or not labels.is_pinned():
+        raise ValueError("logits and labels must be page-locked (pinned) CPU tensors")
+    N, V = logits.shape
+    if V > 1 and logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous (stride(1) == 1)")
+    if not labels.is_contiguous():
+        raise ValueError("labels must be contiguous")
+    row_stride = logits.stride(0) if N > 1 else V
+    dev = torch.device(device)
+    if out is None:
+        out = CEResult(loss=torch.empty(N, dtype=torch.float32).pin_memory(),
+                       argmax=torch.empty(N, dtype=torch.int64).pin_memory(),
+                       reduced=torch.empty(2, dtype=torch.float32).pin_memory(),
+                       counts=torch.empty(4, dtype=torch.int64).pin_memory())
+    need = host_workspace_bytes(N, V, row_stride, logits.dtype)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = capi.lib().ce_fwd_bwd_host(
+            logits.data_ptr(), _DTYPES[logits.dtype], labels.data_ptr(), N, V, row_stride,
+            ignore_index, float(label_smoothing), float(softcap), _REDUCTIONS[reduction],
+            float(grad_scale), out.loss.data_ptr(), out.argmax.data_ptr(), out.reduced.data_ptr(),
+            out.counts.data_ptr(), workspace.data_ptr(), workspace.numel(), stream)
+    capi.check(st, "ce_fwd_bwd_host")
+    return out

@@ -327,12 +327,17 @@ extern "C" size_t vlmce_ce_workspace_bytes(int64_t N, int64_t V, int32_t dtype) 
     return workspace_bytes(N);
 }
 
-extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
-                                   int64_t V, int64_t row_stride, int64_t ignore_index,
-                                   float label_smoothing, float softcap, int32_t reduction,
-                                   float grad_scale, float *out_loss, int64_t *out_argmax,
-                                   float *out_reduced, int64_t *out_counts, void *workspace,
-                                   size_t workspace_bytes_given, vlmce_stream_t stream) {
+namespace vlmce {
+namespace ce {
+namespace {
+
+// ce_fwd_bwd itself; allow_split = false keeps the row work on the row kernel
+// (plain loads and stores only), for logits in host memory.
+vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t N, int64_t V,
+                    int64_t row_stride, int64_t ignore_index, float label_smoothing, float softcap,
+                    int32_t reduction, float grad_scale, float *out_loss, int64_t *out_argmax,
+                    float *out_reduced, int64_t *out_counts, void *workspace,
+                    size_t workspace_bytes_given, vlmce_stream_t stream, bool allow_split) {
     // ---- host-side argument checks; nothing is enqueued on failure
     if (dtype != VLMCE_F32 && dtype != VLMCE_BF16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
     if (N < 0 || V < 1 || row_stride < V) return VLMCE_ERR_INVALID_ARG;
@@ -360,7 +365,7 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
     const bool bf16 = dtype == VLMCE_BF16;
     const bool capped = softcap > 0.f;
     const int64_t G = row_granules(bf16, V, rows_aligned(logits, row_stride, elt));
-    const bool split_path = N > 0 && use_split(N, G, dev);
+    const bool split_path = allow_split && N > 0 && use_split(N, G, dev);
     SplitPlan pl;
     if (split_path) {
         st = get_split_plan(dev, bf16, capped, G, &pl);
@@ -459,4 +464,249 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
                            static_cast<int>(reduction), static_cast<const int64_t *>(w.counts),
                            static_cast<const int *>(w.err), out_reduced, out_counts),
         "ce_finalize_kernel");
+}
+
+}  // namespace
+}  // namespace ce
+}  // namespace vlmce
+
+extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                                   int64_t V, int64_t row_stride, int64_t ignore_index,
+                                   float label_smoothing, float softcap, int32_t reduction,
+                                   float grad_scale, float *out_loss, int64_t *out_argmax,
+                                   float *out_reduced, int64_t *out_counts, void *workspace,
+                                   size_t workspace_bytes_given, vlmce_stream_t stream) {
+    return run_ce(logits, dtype, labels, N, V, row_stride, ignore_index, label_smoothing, softcap,
+                  reduction, grad_scale, out_loss, out_argmax, out_reduced, out_counts, workspace,
+                  workspace_bytes_given, stream, true);
+}
+
+namespace vlmce {
+namespace ce {
+namespace {
+
+// The device address of a pointer the kernels may dereference: device or
+// managed memory as is, page-locked host memory through its device mapping.
+// False for memory the device cannot address (pageable host memory).
+bool device_alias(const void *p, void **out, bool *is_host) {
+    *is_host = false;
+    if (!p) {
+        *out = nullptr;
+        return true;
+    }
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *out = const_cast<void *>(p);
+        return true;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+        // the mapping of this address within its page-locked allocation
+        *out = static_cast<char *>(a.devicePointer) +
+               (static_cast<const char *>(p) - static_cast<const char *>(a.hostPointer));
+        *is_host = true;
+        return true;
+    }
+    return false;
+}
+
+// ---- staged pipeline for logits in host memory
+constexpr int kRing = 3;                       // staging slots
+constexpr int64_t kChunkTarget = 32ll << 20;   // bytes of logits per chunk
+constexpr int kMaxPipeDevices = 64;
+
+int64_t chunk_rows(int64_t N, int64_t row_stride, int64_t elt) {
+    int64_t r = kChunkTarget / (row_stride * elt);
+    if (r < 1) r = 1;
+    return r < N ? r : (N > 0 ? N : 1);
+}
+int64_t slot_bytes(int64_t rows, int64_t row_stride, int64_t elt) {
+    return round_up(16 + rows * row_stride * elt, 256);
+}
+size_t host_workspace_bytes(int64_t N, int64_t row_stride, int64_t elt) {
+    return workspace_bytes(N) +
+           static_cast<size_t>(kRing * slot_bytes(chunk_rows(N, row_stride, elt), row_stride, elt));
+}
+
+// Per device: the copy-in and copy-out streams and the ring's events.
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t loaded[kRing] = {}, computed[kRing] = {}, stored[kRing] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipes[kMaxPipeDevices];
+
+vlmce_status get_pipe(int device, HostPipe **out) {
+    if (device < 0 || device >= kMaxPipeDevices) return VLMCE_ERR_UNSUPPORTED_DEVICE;
+    HostPipe &hp = g_pipes[device];
+    if (!hp.ready) {
+        const unsigned f = cudaEventDisableTiming;
+        cudaError_t e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, f);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done, f);
+        for (int b = 0; b < kRing && e == cudaSuccess; ++b) {
+            e = cudaEventCreateWithFlags(&hp.loaded[b], f);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.computed[b], f);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.stored[b], f);
+        }
+        if (record_cuda(e, "host pipeline streams and events") != cudaSuccess) return VLMCE_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return VLMCE_OK;
+}
+
+// Same checks and results as run_ce (row kernel); the logits live in host
+// memory and pass through the device in chunks of rows: copy in (stream
+// `in`), compute (the caller's stream), copy the gradient columns back
+// (stream `out`), three chunks in flight.  Staged rows keep the caller's row
+// stride and 16-byte phase, so the kernel sees the same layout.
+vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labels, int64_t N,
+                           int64_t V, int64_t row_stride, int64_t ignore_index,
+                           float label_smoothing, float softcap, int32_t reduction,
+                           float grad_scale, float *loss_out, int64_t *amax_out,
+                           float *out_reduced, int64_t *out_counts, void *workspace,
+                           size_t workspace_bytes_given, cudaStream_t cs) {
+    if (dtype != VLMCE_F32 && dtype != VLMCE_BF16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
+    if (N < 0 || V < 1 || row_stride < V) return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && (!host_logits || !labels)) return VLMCE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
+    if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (V > kMaxVocab || N > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+    const int64_t elt = dtype == VLMCE_BF16 ? 2 : 4;
+    if (N > 0 && row_stride > (INT64_MAX / elt) / N) return VLMCE_ERR_TOO_LARGE;
+    if (!workspace || workspace_bytes_given < host_workspace_bytes(N, row_stride, elt))
+        return VLMCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return VLMCE_ERR_MISALIGNED;
+    if (!aligned(host_logits, static_cast<uintptr_t>(elt))) return VLMCE_ERR_MISALIGNED;
+    if (labels && !aligned(labels, 8)) return VLMCE_ERR_MISALIGNED;
+    if (loss_out && !aligned(loss_out, 4)) return VLMCE_ERR_MISALIGNED;
+    if (amax_out && !aligned(amax_out, 8)) return VLMCE_ERR_MISALIGNED;
+    if (out_reduced && !aligned(out_reduced, 4)) return VLMCE_ERR_MISALIGNED;
+    if (out_counts && !aligned(out_counts, 8)) return VLMCE_ERR_MISALIGNED;
+
+    DeviceInfo dev;
+    vlmce_status st = current_device(&dev);
+    if (st != VLMCE_OK) return st;
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    if ((st = get_pipe(dev.device, &hp)) != VLMCE_OK) return st;
+
+    const bool bf16 = dtype == VLMCE_BF16;
+    const int64_t stride_bytes = row_stride * elt;
+    const int64_t R = chunk_rows(N, row_stride, elt);
+    const int64_t sb = slot_bytes(R, row_stride, elt);
+    Workspace w = carve(workspace, N);
+    unsigned char *ring = static_cast<unsigned char *>(workspace) + workspace_bytes(N);
+    float *loss = loss_out ? loss_out : w.loss;
+    int64_t *amax = amax_out ? amax_out : w.argmax;
+    unsigned char *hbase = static_cast<unsigned char *>(host_logits);
+
+    auto fail = [](cudaError_t e, const char *where) { return launch_status(e, where); };
+    if ((st = fail(cudaEventRecord(hp->start, cs), "cudaEventRecord")) != VLMCE_OK) return st;
+    if ((st = fail(cudaStreamWaitEvent(hp->in, hp->start, 0), "cudaStreamWaitEvent")) != VLMCE_OK)
+        return st;
+    if ((st = fail(cudaStreamWaitEvent(hp->out, hp->start, 0), "cudaStreamWaitEvent")) != VLMCE_OK)
+        return st;
+
+    ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
+    if ((st = launch_status(cudaSuccess, "ce_count_kernel")) != VLMCE_OK) return st;
+
+    const rows::Kernel kern = bf16 ? rows::kernel_bf16(softcap > 0.f) : rows::kernel_f32(softcap > 0.f);
+    const int64_t nchunks = N > 0 ? (N + R - 1) / R : 0;
+    for (int64_t i = 0; i < nchunks; ++i) {
+        const int b = static_cast<int>(i % kRing);
+        const int64_t r0 = i * R;
+        const int64_t rows_i = (N - r0) < R ? (N - r0) : R;
+        unsigned char *hrow = hbase + r0 * stride_bytes;
+        // the chunk's first row keeps its 16-byte phase in the slot
+        unsigned char *slot = ring + b * sb + (reinterpret_cast<uintptr_t>(hrow) & 15u);
+        // copy in: whole rows, but not past the last row's V columns
+        if (i >= kRing &&
+            (st = fail(cudaStreamWaitEvent(hp->in, hp->stored[b], 0), "cudaStreamWaitEvent")) != VLMCE_OK)
+            return st;
+        if ((st = fail(cudaMemcpyAsync(slot, hrow, (rows_i - 1) * stride_bytes + V * elt,
+                                       cudaMemcpyDefault, hp->in),
+                       "cudaMemcpyAsync(host to device)")) != VLMCE_OK)
+            return st;
+        if ((st = fail(cudaEventRecord(hp->loaded[b], hp->in), "cudaEventRecord")) != VLMCE_OK) return st;
+        // compute on the caller's stream
+        if ((st = fail(cudaStreamWaitEvent(cs, hp->loaded[b], 0), "cudaStreamWaitEvent")) != VLMCE_OK)
+            return st;
+        rows::Params p;
+        p.logits = slot;
+        p.labels = labels + r0;
+        p.V = static_cast<int>(V);
+        p.stride_bytes = stride_bytes;
+        p.ignore_index = ignore_index;
+        p.eps = label_smoothing;
+        p.softcap = softcap;
+        p.grad_scale = grad_scale;
+        p.reduction = reduction;
+        p.loss = loss + r0;
+        p.argmax = amax + r0;
+        p.counts = w.counts;
+        kern<<<static_cast<unsigned>(rows_i), rows::kThreads, 0, cs>>>(p);
+        if ((st = launch_status(cudaSuccess, "ce_rows_kernel")) != VLMCE_OK) return st;
+        if ((st = fail(cudaEventRecord(hp->computed[b], cs), "cudaEventRecord")) != VLMCE_OK) return st;
+        // copy the gradient columns [0, V) of each row back
+        if ((st = fail(cudaStreamWaitEvent(hp->out, hp->computed[b], 0), "cudaStreamWaitEvent")) !=
+            VLMCE_OK)
+            return st;
+        if ((st = fail(cudaMemcpy2DAsync(hrow, stride_bytes, slot, stride_bytes, V * elt, rows_i,
+                                         cudaMemcpyDefault, hp->out),
+                       "cudaMemcpy2DAsync(device to host)")) != VLMCE_OK)
+            return st;
+        if ((st = fail(cudaEventRecord(hp->stored[b], hp->out), "cudaEventRecord")) != VLMCE_OK) return st;
+    }
+    if ((st = fail(cudaEventRecord(hp->done, hp->out), "cudaEventRecord")) != VLMCE_OK) return st;
+    if ((st = fail(cudaStreamWaitEvent(cs, hp->done, 0), "cudaStreamWaitEvent")) != VLMCE_OK) return st;
+
+    ce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index,
+                                           static_cast<int>(reduction), w.counts, w.err,
+                                           out_reduced, out_counts);
+    return launch_status(cudaSuccess, "ce_finalize_kernel");
+}
+
+}  // namespace
+}  // namespace ce
+}  // namespace vlmce
+
+extern "C" size_t vlmce_ce_host_workspace_bytes(int64_t N, int64_t V, int64_t row_stride,
+                                                int32_t dtype) {
+    if (N < 0 || V < 1 || row_stride < V || (dtype != VLMCE_F32 && dtype != VLMCE_BF16)) return 0;
+    return host_workspace_bytes(N, row_stride, dtype == VLMCE_BF16 ? 2 : 4);
+}
+
+extern "C" vlmce_status ce_fwd_bwd_host(void *logits, int32_t dtype, const int64_t *labels,
+                                        int64_t N, int64_t V, int64_t row_stride,
+                                        int64_t ignore_index, float label_smoothing, float softcap,
+                                        int32_t reduction, float grad_scale, float *out_loss,
+                                        int64_t *out_argmax, float *out_reduced,
+                                        int64_t *out_counts, void *workspace,
+                                        size_t workspace_bytes_given, vlmce_stream_t stream) {
+    void *d[6];
+    bool host[6];
+    const void *h[6] = {logits, labels, out_loss, out_argmax, out_reduced, out_counts};
+    for (int i = 0; i < 6; ++i)
+        if (!device_alias(h[i], &d[i], &host[i])) return VLMCE_ERR_INVALID_ARG;
+    if (!host[0])  // device logits: ce_fwd_bwd, with host labels / outputs read and written in place
+        return run_ce(d[0], dtype, static_cast<const int64_t *>(d[1]), N, V, row_stride,
+                      ignore_index, label_smoothing, softcap, reduction, grad_scale,
+                      static_cast<float *>(d[2]), static_cast<int64_t *>(d[3]),
+                      static_cast<float *>(d[4]), static_cast<int64_t *>(d[5]), workspace,
+                      workspace_bytes_given, stream, true);
+    return run_ce_staged(logits, dtype, static_cast<const int64_t *>(d[1]), N, V, row_stride,
+                         ignore_index, label_smoothing, softcap, reduction, grad_scale,
+                         static_cast<float *>(d[2]), static_cast<int64_t *>(d[3]),
+                         static_cast<float *>(d[4]), static_cast<int64_t *>(d[5]), workspace,
+                         workspace_bytes_given, reinterpret_cast<cudaStream_t>(stream));
 }
