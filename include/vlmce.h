@@ -158,6 +158,63 @@ vlmce_status ce_fwd_bwd_host(void *logits, int32_t dtype, const int64_t *labels,
  * whole rows (row_stride elements each, about 32 MB per chunk). */
 size_t vlmce_ce_host_workspace_bytes(int64_t N, int64_t V, int64_t row_stride, int32_t dtype);
 
+/*
+ * Vocabulary-sharded cross-entropy ("Add Megatron-LM cross-entropy
+ * integration", Summary; "Add opt-in Liger vocab-parallel cross entropy
+ * through ops/loss", What does this PR do): each rank of a tensor-parallel
+ * group holds the columns [vocab_start, vocab_start + V_local) of every row
+ * (V = the whole vocabulary).  Per call sequence on each rank:
+ *   ce_shard_stats  -> this shard's row statistics [N];
+ *   (the caller gathers all k shards' statistics, e.g. an all-gather, as a
+ *    [k][N] array in shard order);
+ *   ce_merge_stats  -> the whole vocabulary's statistics [N] (identical bits
+ *                      on every rank that merges the same array);
+ *   ce_shard_fwd_bwd -> per-token loss / argmax / reduced loss and accuracy
+ *                      (the same on every rank) and the gradient of this
+ *                      shard's columns, written in place.
+ * With one shard (vocab_start 0, V_local = V) this is ce_fwd_bwd.
+ */
+typedef struct vlmce_row_stats {
+    float x_max;     /* largest raw logit of the columns merged so far */
+    int32_t argmax;  /* its smallest global column (INT32_MAX before any column) */
+    float m;         /* reference of s: z at x_max (z = T tanh(x/T), or x) */
+    float s;         /* sum over the columns of exp(z_j - m) */
+    float sum_z;     /* sum over the columns of z_j */
+    float z_y;       /* z at the row's label column if merged so far, else 0 */
+    float reserved[2];
+} vlmce_row_stats;   /* 32 bytes; lse = m + log(s) */
+
+/* Statistics of one shard.  logits: device, N rows of row_stride elements
+ * (>= V_local) holding the shard's V_local columns (not modified); labels:
+ * [N] int64 global labels; 0 <= vocab_start, vocab_start + V_local <= V <=
+ * vlmce_ce_max_vocab(dtype); softcap as in ce_fwd_bwd.  out_stats: device
+ * [N], 16-byte aligned.  Argument errors as ce_fwd_bwd. */
+vlmce_status ce_shard_stats(const void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                            int64_t V_local, int64_t row_stride, int64_t vocab_start, int64_t V,
+                            float softcap, vlmce_row_stats *out_stats, vlmce_stream_t stream);
+
+/* out[r] = merge of shards[0][r] .. shards[k-1][r] in that order: the
+ * largest x_max (smallest argmax on ties), the sums of exp rescaled to the
+ * larger reference, the sums of sum_z and z_y.  shards: device [k][N]
+ * (contiguous), k >= 1; out: device [N], may be shards itself (block 0). */
+vlmce_status ce_merge_stats(const vlmce_row_stats *shards, int32_t k, int64_t N,
+                            vlmce_row_stats *out, vlmce_stream_t stream);
+
+/* Loss and this shard's gradient from the whole vocabulary's statistics.
+ * Arguments as ce_fwd_bwd (logits: the shard, overwritten by the gradient of
+ * its V_local columns; label validity, the mean's n_valid and eps / V use
+ * the global V), plus vocab_start, V and global_stats (device [N], the merge
+ * of every shard's statistics).  workspace: vlmce_ce_workspace_bytes(N, V,
+ * dtype) bytes of device memory.  out_* as ce_fwd_bwd; their values are the
+ * same on every rank. */
+vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                              int64_t V_local, int64_t row_stride, int64_t vocab_start, int64_t V,
+                              int64_t ignore_index, float label_smoothing, float softcap,
+                              int32_t reduction, float grad_scale,
+                              const vlmce_row_stats *global_stats, float *out_loss,
+                              int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
+                              void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
+
 /* Bytes of device workspace flce_fwd_bwd needs (256-byte aligned): per-row
  * statistics of every 256-column logits tile, two bf16 [N, 8192] gradient
  * tiles and an fp32 [N, H] grad_hidden accumulator. */

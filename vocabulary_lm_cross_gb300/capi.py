@@ -49,6 +49,10 @@ SIGNATURES = {
     "ce_fwd_bwd_host": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32, _vp,
                                _vp, _vp, _vp, _vp, _sz, _vp]),
     "vlmce_ce_host_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
+    "ce_shard_stats": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp]),
+    "ce_merge_stats": (_i32, [_vp, _i32, _i64, _vp, _vp]),
+    "ce_shard_fwd_bwd": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _i32,
+                                _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32,
                                   _vp, _vp, _vp, _vp, _vp]),
     "vlmce_ce_noalloc_max_rows": (_i64, []),

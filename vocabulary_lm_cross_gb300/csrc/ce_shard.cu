@@ -1,0 +1,361 @@
+// ce_shard.cu -- the vocabulary-sharded cross-entropy: the kernels each rank
+// of a tensor-parallel group runs on its shard of the logits (columns
+// [vocab_start, vocab_start + V_local) of every row), with the exchange of the
+// per-row statistics left to the caller.
+//
+// Method ("Add Megatron-LM cross-entropy integration", Summary; "Add opt-in
+// Liger vocab-parallel cross entropy through ops/loss", What does this PR do):
+//   1. ce_shard_stats   -- per row of the shard: largest raw logit and its
+//                          smallest global column, online sum of exp(z - m),
+//                          sum of z, z at the label when the shard holds it;
+//                          the row kernel's first pass, one CTA per row.
+//   2. (caller)         -- gather every shard's statistics.
+//   3. ce_merge_stats   -- merge k shards' statistics in shard order (the same
+//                          operator the kernels use between warps), so every
+//                          rank obtains bit-identical global statistics.
+//   4. ce_shard_fwd_bwd -- label census; per row the loss from the global
+//                          statistics and the gradient of the shard's columns
+//                          written in place (the row kernel's second pass with
+//                          the global lse and the global V); reduced loss.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "ce_census.cuh"
+#include "ce_rows.cuh"
+#include "host_util.h"
+#include "ptx.cuh"
+#include "vlmce.h"
+
+namespace vlmce {
+namespace ce {
+namespace shard {
+namespace {
+
+static_assert(sizeof(RowPart) == sizeof(vlmce_row_stats), "row statistics layout");
+
+struct ShardParams {
+    unsigned char *logits;
+    const int64_t *labels;
+    int V_local;
+    int64_t vocab_start;
+    int V;                  // global vocabulary
+    int64_t stride_bytes;
+    int64_t ignore_index;
+    float eps, softcap, grad_scale;
+    int reduction;
+    RowPart *stats;         // stats kernel: out [N]; grad kernel: global stats in [N]
+    float *loss;
+    int64_t *argmax;
+    const int64_t *counts;
+};
+
+// Row geometry in 16-byte granules (as the row kernel): whole granules are
+// [gs, ge); granule 0 is partial when the row starts inside a granule, G - 1
+// when it ends inside one.
+struct Geo {
+    const uint4 *row;
+    unsigned char *gbase;
+    uintptr_t a0;
+    int lead, G, gs, ge, tail_tid;
+    bool head;
+};
+template <bool BF16>
+__device__ __forceinline__ Geo geometry(const ShardParams &p) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    constexpr int ELT = Elem<BF16>::kBytes;
+    Geo g;
+    g.a0 = reinterpret_cast<uintptr_t>(p.logits) + static_cast<int64_t>(blockIdx.x) * p.stride_bytes;
+    g.gbase = reinterpret_cast<unsigned char *>(g.a0 & ~static_cast<uintptr_t>(15));
+    g.row = reinterpret_cast<const uint4 *>(g.gbase);
+    g.lead = static_cast<int>((g.a0 & 15) / ELT);
+    g.G = (g.lead + p.V_local + EPG - 1) / EPG;
+    g.gs = g.lead > 0 ? 1 : 0;
+    g.ge = ((g.lead + p.V_local) % EPG != 0) ? g.G - 1 : g.G;
+    g.head = g.gs == 1;
+    const bool tail = g.ge == g.G - 1 && g.G - 1 >= g.gs;
+    g.tail_tid = tail ? (g.G - 1 - g.gs) % rows::kThreads : -1;
+    return g;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load_x(uintptr_t a0, int64_t col) {
+    const unsigned char *py = reinterpret_cast<const unsigned char *>(a0) + Elem<BF16>::kBytes * col;
+    if constexpr (BF16)
+        return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
+    else
+        return *reinterpret_cast<const float *>(py);
+}
+
+template <bool BF16, bool SOFTCAP>
+__global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
+    ce_shard_stats_kernel(const ShardParams p) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    __shared__ RowPart wpart[rows::kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const Geo g = geometry<BF16>(p);
+    const float T = p.softcap;
+    const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    rows::Acc a;
+    a.mv = -INFINITY;
+    a.midx = INT_MAX;
+    a.mz = -INFINITY;
+    a.nmL = INFINITY;
+    a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
+    if (g.head && tid == 0)
+        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row), -g.lead, p.V_local, T, k2);
+    for (int gl = g.gs + tid; gl < g.ge; gl += rows::kThreads)
+        rows::fold_full<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row + gl), gl * EPG - g.lead,
+                                             p.V_local, T, k2);
+    if (tid == g.tail_tid)
+        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row + (g.G - 1)),
+                                          (g.G - 1) * EPG - g.lead, p.V_local, T, k2);
+    RowPart pt = part_identity();
+    pt.mx = a.mv;
+    pt.idx = a.midx;
+    pt.mz = a.mz;
+    pt.s = a.s0 + a.s1;
+    pt.sz = a.z0 + a.z1;
+    warp_allreduce(pt);
+    if (lane == 0) wpart[warp] = pt;
+    __syncthreads();
+    if (warp == 0) {
+        RowPart q = lane < rows::kWarps ? wpart[lane] : part_identity();
+        warp_allreduce(q);
+        if (lane == 0) {
+            const int64_t yl = p.labels[blockIdx.x] - p.vocab_start;
+            q.zy = 0.f;
+            if (yl >= 0 && yl < p.V_local)
+                q.zy = softcap_z<SOFTCAP>(load_x<BF16>(g.a0, yl), T, k2).z;
+            q.idx = q.idx == INT_MAX ? INT_MAX : static_cast<int>(q.idx + p.vocab_start);
+            q.pad0 = q.pad1 = 0.f;
+            p.stats[blockIdx.x] = q;
+        }
+    }
+}
+
+// One thread per row: out[r] = merge of shards[0][r], ..., shards[k-1][r]
+// in that order (out may be shards[0]).
+__global__ void __launch_bounds__(256) ce_merge_stats_kernel(const RowPart *shards, int k,
+                                                            int64_t N, RowPart *out) {
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r >= N) return;
+    RowPart a = shards[r];
+    for (int i = 1; i < k; ++i) {
+        const RowPart b = shards[static_cast<int64_t>(i) * N + r];
+        part_merge(a, b.mx, b.idx, b.mz, b.s, b.sz, b.zy);
+    }
+    out[r] = a;
+}
+
+template <bool BF16, bool SOFTCAP>
+__global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
+    ce_shard_grad_kernel(const ShardParams p) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    const int tid = threadIdx.x;
+    const int64_t r = blockIdx.x;
+    const Geo g = geometry<BF16>(p);
+    const float T = p.softcap;
+    const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    const RowPart st = p.stats[r];
+    const float lse = st.mz + logf(st.s);
+    const int64_t y = p.labels[r];
+    const bool ignored = y == p.ignore_index;
+    const bool valid = !ignored && y >= 0 && y < p.V;
+    if (tid == 0) {
+        float l = 0.f;
+        if (valid)
+            l = lse - fmaf(1.f - p.eps, st.zy, (p.eps / static_cast<float>(p.V)) * st.sz);
+        else if (!ignored)
+            l = __int_as_float(0x7fc00000);  // bad label: NaN
+        if (p.loss) p.loss[r] = l;
+        if (p.argmax) p.argmax[r] = st.idx;
+    }
+    if (valid) {
+        const int64_t n_valid = p.counts[0];
+        rows::GradCoef c;
+        c.scale = p.grad_scale;
+        if (p.reduction == VLMCE_MEAN)
+            c.scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
+        c.c_smooth = c.scale * (p.eps / static_cast<float>(p.V));
+        c.c_label = c.c_smooth + c.scale * (1.f - p.eps);
+        c.nlseL = -lse * kLog2e;
+        c.T = T;
+        c.k2 = k2;
+        // the label's granule and lane when this shard holds it
+        const int64_t yl = y - p.vocab_start;
+        const bool mine = yl >= 0 && yl < p.V_local;
+        const int gy = mine ? static_cast<int>((yl + g.lead) / EPG) : -1;
+        const int ly = mine ? static_cast<int>((yl + g.lead) % EPG) : -1;
+        float gr[EPG];
+        if (g.head && tid == 0) {
+            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row), c, gy == 0 ? ly : -1, gr);
+            rows::store_partial<BF16>(g.gbase, -g.lead, p.V_local, gr);
+        }
+        for (int gl = g.gs + tid; gl < g.ge; gl += rows::kThreads) {
+            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row + gl), c, gl == gy ? ly : -1, gr);
+            ptx::st_global_cs_v4(g.gbase + 16 * gl, rows::pack_granule<BF16>(gr));
+        }
+        if (tid == g.tail_tid) {
+            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row + (g.G - 1)), c,
+                                             gy == g.G - 1 ? ly : -1, gr);
+            rows::store_partial<BF16>(g.gbase + 16 * (g.G - 1), (g.G - 1) * EPG - g.lead,
+                                      p.V_local, gr);
+        }
+    } else {
+        float z[EPG];
+#pragma unroll
+        for (int l = 0; l < EPG; ++l) z[l] = 0.f;
+        if (g.head && tid == 0) rows::store_partial<BF16>(g.gbase, -g.lead, p.V_local, z);
+        for (int gl = g.gs + tid; gl < g.ge; gl += rows::kThreads)
+            ptx::st_global_cs_v4(g.gbase + 16 * gl, make_uint4(0u, 0u, 0u, 0u));
+        if (tid == g.tail_tid)
+            rows::store_partial<BF16>(g.gbase + 16 * (g.G - 1), (g.G - 1) * EPG - g.lead,
+                                      p.V_local, z);
+    }
+}
+
+using ShardKernel = void (*)(ShardParams);
+ShardKernel stats_kernel(bool bf16, bool softcap) {
+    if (bf16) return softcap ? ce_shard_stats_kernel<true, true> : ce_shard_stats_kernel<true, false>;
+    return softcap ? ce_shard_stats_kernel<false, true> : ce_shard_stats_kernel<false, false>;
+}
+ShardKernel grad_kernel(bool bf16, bool softcap) {
+    if (bf16) return softcap ? ce_shard_grad_kernel<true, true> : ce_shard_grad_kernel<true, false>;
+    return softcap ? ce_shard_grad_kernel<false, true> : ce_shard_grad_kernel<false, false>;
+}
+
+constexpr int64_t kMaxVocab = int64_t(1) << 28;
+
+// Checks shared by the shard entry points (nothing is enqueued on failure).
+vlmce_status check_shard(const void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                         int64_t V_local, int64_t row_stride, int64_t vocab_start, int64_t V,
+                         float softcap) {
+    if (dtype != VLMCE_F32 && dtype != VLMCE_BF16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
+    if (N < 0 || V_local < 1 || row_stride < V_local || vocab_start < 0 || V < 1 ||
+        vocab_start + V_local > V)
+        return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && (!logits || !labels)) return VLMCE_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
+    if (V > kMaxVocab || N > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+    const int64_t elt = dtype == VLMCE_BF16 ? 2 : 4;
+    if (N > 0 && row_stride > (INT64_MAX / elt) / N) return VLMCE_ERR_TOO_LARGE;
+    if (logits && !aligned(logits, static_cast<uintptr_t>(elt))) return VLMCE_ERR_MISALIGNED;
+    if (labels && !aligned(labels, 8)) return VLMCE_ERR_MISALIGNED;
+    return VLMCE_OK;
+}
+
+}  // namespace
+}  // namespace shard
+}  // namespace ce
+}  // namespace vlmce
+
+using namespace vlmce;
+using namespace vlmce::ce;
+using namespace vlmce::ce::shard;
+
+extern "C" vlmce_status ce_shard_stats(const void *logits, int32_t dtype, const int64_t *labels,
+                                       int64_t N, int64_t V_local, int64_t row_stride,
+                                       int64_t vocab_start, int64_t V, float softcap,
+                                       vlmce_row_stats *out_stats, vlmce_stream_t stream) {
+    vlmce_status st = check_shard(logits, dtype, labels, N, V_local, row_stride, vocab_start, V,
+                                  softcap);
+    if (st != VLMCE_OK) return st;
+    if (N > 0 && !out_stats) return VLMCE_ERR_INVALID_ARG;
+    if (out_stats && !aligned(out_stats, 16)) return VLMCE_ERR_MISALIGNED;
+    if (N == 0) return VLMCE_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != VLMCE_OK) return st;
+    ShardParams p = {};
+    p.logits = static_cast<unsigned char *>(const_cast<void *>(logits));
+    p.labels = labels;
+    p.V_local = static_cast<int>(V_local);
+    p.vocab_start = vocab_start;
+    p.V = static_cast<int>(V);
+    p.stride_bytes = row_stride * (dtype == VLMCE_BF16 ? 2 : 4);
+    p.softcap = softcap;
+    p.stats = reinterpret_cast<RowPart *>(out_stats);
+    stats_kernel(dtype == VLMCE_BF16, softcap > 0.f)
+        <<<static_cast<unsigned>(N), rows::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    return launch_status(cudaSuccess, "ce_shard_stats_kernel");
+}
+
+extern "C" vlmce_status ce_merge_stats(const vlmce_row_stats *shards, int32_t k, int64_t N,
+                                       vlmce_row_stats *out, vlmce_stream_t stream) {
+    if (k < 1 || N < 0) return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && (!shards || !out)) return VLMCE_ERR_INVALID_ARG;
+    if (N > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+    if ((shards && !aligned(shards, 16)) || (out && !aligned(out, 16))) return VLMCE_ERR_MISALIGNED;
+    if (N == 0) return VLMCE_OK;
+    DeviceInfo dev;
+    vlmce_status st = current_device(&dev);
+    if (st != VLMCE_OK) return st;
+    ce_merge_stats_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0,
+                            reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const RowPart *>(shards), k, N, reinterpret_cast<RowPart *>(out));
+    return launch_status(cudaSuccess, "ce_merge_stats_kernel");
+}
+
+extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels,
+                                         int64_t N, int64_t V_local, int64_t row_stride,
+                                         int64_t vocab_start, int64_t V, int64_t ignore_index,
+                                         float label_smoothing, float softcap, int32_t reduction,
+                                         float grad_scale, const vlmce_row_stats *global_stats,
+                                         float *out_loss, int64_t *out_argmax, float *out_reduced,
+                                         int64_t *out_counts, void *workspace,
+                                         size_t workspace_bytes_given, vlmce_stream_t stream) {
+    vlmce_status st = check_shard(logits, dtype, labels, N, V_local, row_stride, vocab_start, V,
+                                  softcap);
+    if (st != VLMCE_OK) return st;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
+    if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && !global_stats) return VLMCE_ERR_INVALID_ARG;
+    if (global_stats && !aligned(global_stats, 16)) return VLMCE_ERR_MISALIGNED;
+    const size_t need = vlmce_ce_workspace_bytes(N, V, dtype);
+    if (!workspace || workspace_bytes_given < need) return VLMCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return VLMCE_ERR_MISALIGNED;
+    if ((out_loss && !aligned(out_loss, 4)) || (out_argmax && !aligned(out_argmax, 8)) ||
+        (out_reduced && !aligned(out_reduced, 4)) || (out_counts && !aligned(out_counts, 8)))
+        return VLMCE_ERR_MISALIGNED;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != VLMCE_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // workspace: counts [4] and the error word at the front, then loss / argmax
+    unsigned char *wb = static_cast<unsigned char *>(workspace);
+    int64_t *counts = reinterpret_cast<int64_t *>(wb);
+    int *err = reinterpret_cast<int *>(wb + 64);
+    float *loss = out_loss ? out_loss : reinterpret_cast<float *>(wb + 256);
+    int64_t *amax = out_argmax ? out_argmax
+                               : reinterpret_cast<int64_t *>(wb + 256 + round_up(4 * N, 256));
+
+    ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, counts, err);
+    if ((st = launch_status(cudaSuccess, "ce_count_kernel")) != VLMCE_OK) return st;
+    if (N > 0) {
+        ShardParams p = {};
+        p.logits = static_cast<unsigned char *>(logits);
+        p.labels = labels;
+        p.V_local = static_cast<int>(V_local);
+        p.vocab_start = vocab_start;
+        p.V = static_cast<int>(V);
+        p.stride_bytes = row_stride * (dtype == VLMCE_BF16 ? 2 : 4);
+        p.ignore_index = ignore_index;
+        p.eps = label_smoothing;
+        p.softcap = softcap;
+        p.grad_scale = grad_scale;
+        p.reduction = reduction;
+        p.stats = reinterpret_cast<RowPart *>(const_cast<vlmce_row_stats *>(global_stats));
+        p.loss = loss;
+        p.argmax = amax;
+        p.counts = counts;
+        grad_kernel(dtype == VLMCE_BF16, softcap > 0.f)
+            <<<static_cast<unsigned>(N), rows::kThreads, 0, cs>>>(p);
+        if ((st = launch_status(cudaSuccess, "ce_shard_grad_kernel")) != VLMCE_OK) return st;
+    }
+    ce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index,
+                                           static_cast<int>(reduction), counts, err, out_reduced,
+                                           out_counts);
+    return launch_status(cudaSuccess, "ce_finalize_kernel");
+}
