@@ -81,9 +81,9 @@ def load_tensor_peak(sustained: bool):
 # a change to any of them invalidates that kernel's recorded ncu traffic.
 KERNEL_SOURCES = {
     "ce_rows_kernel": ["ce_rows.cuh", "ce_rows_bf16.cu", "ce_rows_f32.cu", "ce_common.cuh",
-                       "ptx.cuh", "host_util.h", "ce.cu"],
+                       "ce_census.cuh", "ptx.cuh", "host_util.h", "ce.cu"],
     "ce_split_kernel": ["ce_split.cuh", "ce_split_bf16.cu", "ce_split_f32.cu", "ce_common.cuh",
-                        "ptx.cuh", "host_util.h", "ce.cu"],
+                        "ce_census.cuh", "ptx.cuh", "host_util.h", "ce.cu"],
     "vlmce_gemm_kernel": ["gemm.cuh", "gemm_types.h", "gemm_launch.h", "gemm.cu", "tcgen05.cuh",
                           "ce_common.cuh", "ptx.cuh", "host_util.h", "flce.cu"],
 }
@@ -398,6 +398,9 @@ def run_ours(args, w):
     del bufs
     torch.cuda.empty_cache()
 
+    shard = run_shard(args, w, dev, world, barrier, sampler) if w.V % 8 == 0 else None
+    torch.cuda.empty_cache()
+
     flce = None
     if not args.no_flce:
         from vocabulary_lm_cross_gb300.workloads import FLCE_WORKLOADS
@@ -450,11 +453,110 @@ def run_ours(args, w):
                 "device_status_ok": e2e_ok},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "shard": shard,
         "flce": flce,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_shard(args, w, dev, world, barrier, sampler, tp=8):
+    """One rank's step of the vocabulary-sharded CE in a TP = `tp` layout of
+    the workload: statistics of its shard, merge of the `tp` gathered records,
+    loss and in-place gradient of its shard.  The other ranks' records are
+    formed beforehand (on a real group they arrive by an all-gather of
+    N x 32 bytes each).  Each timed step works on a fresh copy of the shard."""
+    import torch
+
+    from vocabulary_lm_cross_gb300 import shard as sh
+    from vocabulary_lm_cross_gb300.ce import workspace_bytes as v_ws_bytes
+    from vocabulary_lm_cross_gb300.workloads import make_ce_inputs
+
+    x0, lab = make_ce_inputs(w, device=dev)
+    V = w.V
+    vl = V // tp
+    shards = [x0[:, i * vl:(i + 1) * vl].contiguous() for i in range(tp)]
+    del x0
+    others = torch.stack([sh.shard_stats(s_, lab, i * vl, V, softcap=w.softcap)
+                          for i, s_ in enumerate(shards)]).contiguous()
+    mine0 = shards[0]
+    del shards
+    nb = max(2, int(2 * 129e6 // (mine0.numel() * mine0.element_size())) + 2)
+    steps = min(args.steps, 30)
+    bufs = [mine0.clone() for _ in range(nb)]
+    from vocabulary_lm_cross_gb300.ce import CEResult
+    out = CEResult(loss=torch.empty(w.N, dtype=torch.float32, device=dev),
+                   argmax=torch.empty(w.N, dtype=torch.int64, device=dev),
+                   reduced=torch.empty(2, dtype=torch.float32, device=dev),
+                   counts=torch.empty(4, dtype=torch.int64, device=dev))
+    gathered = others.clone()
+    merged = torch.empty((w.N, 8), dtype=torch.float32, device=dev)
+    ws = torch.empty(v_ws_bytes(w.N, V, mine0.dtype), dtype=torch.uint8, device=dev)
+
+    def step(b):
+        sh.shard_stats(b, lab, 0, V, softcap=w.softcap, out=gathered[0])
+        sh.merge_stats(gathered, out=merged)
+        sh.shard_fwd_bwd(b, lab, 0, V, merged, label_smoothing=w.label_smoothing,
+                         softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
+                         out=out, workspace=ws)
+
+    # the rank step is five short launches: replay it as a CUDA graph, one per
+    # buffer of the ring, so that host-side launch overhead is not timed
+    for i in range(args.warmup):
+        step(bufs[i % nb])
+    torch.cuda.synchronize()
+    graphs = []
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for b in bufs:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=side):
+                step(b)
+            graphs.append(gr)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    for b in bufs:
+        b.copy_(mine0)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0 = time.time()
+    ms = 0.0
+    done = 0
+    while done < steps:
+        k = min(nb, steps - done)  # each timed step on a pristine buffer
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(k):
+            graphs[i].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms += ev0.elapsed_time(ev1)
+        done += k
+        for b in bufs[:k]:
+            b.copy_(mine0)
+    t1 = time.time()
+    ms /= steps
+    ok = int(out.counts[3]) == 0
+    bytes_step = 2 * w.N * vl * mine0.element_size()
+    peak, peak_src = load_peaks()
+    return {"workload": f"{w.name}, vocabulary shard 0 of {tp} ([{w.N}, {vl}])",
+            "metric": "vocab-sharded CE rank step GB/s (shard read + gradient write)",
+            "value": bytes_step / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "steps": steps, "bytes_per_step": bytes_step,
+            "roofline": {"bound": "hbm", "achieved": bytes_step / (ms * 1e-3) / 1e9,
+                         "peak": peak, "peak_source": f"{peak_src} (copy GB/s)", "unit": "GB/s",
+                         "frac": bytes_step / (ms * 1e-3) / 1e9 / peak,
+                         "measured_over": "the whole rank step (stats, merge, count, gradient, "
+                                          "finalize: 5 launches), replayed as a CUDA graph"},
+            "gpu_launches": 5 * steps, "device_status_ok": ok,
+            "clocks": sampler.summary(t0, t1),
+            "l2": f"ring of {nb} shard copies ({nb * bytes_step / 2 / 1e6:.0f} MB > 2 x L2); the "
+                  "gradient pass re-reads the shard from L2"}
 
 
 def flce_oracle_sample(w, budget_s=10.0):

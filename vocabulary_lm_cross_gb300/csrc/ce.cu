@@ -72,16 +72,8 @@ Workspace carve(void *ws, int64_t N) {
     return w;
 }
 
-// Granules (16 B) of a row: exact when every row starts on a 16-byte boundary,
-// else the worst case over the possible offsets of its first element.
-int64_t row_granules(bool bf16, int64_t V, bool aligned_rows) {
-    const int64_t epg = bf16 ? 8 : 4;
-    return aligned_rows ? (V + epg - 1) / epg : (epg - 1 + V + epg - 1) / epg;
-}
-
-bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
-    return aligned(logits, 16) && ((row_stride * elt) % 16) == 0;
-}
+using rows::row_granules;
+using rows::rows_aligned;
 
 // ---- V-split plans (cluster per row)
 
@@ -218,8 +210,9 @@ extern "C" int32_t vlmce_ce_describe_plan(int64_t N, int64_t V, int32_t dtype, f
         out[0] = 0;
         out[1] = 1;
         out[2] = static_cast<int32_t>(G);
-        out[3] = 2 * dev.sm_count;
-        out[4] = rows::kThreads;
+        const int th = rows::threads_for(G);
+        out[3] = rows::min_blocks(th, softcap > 0.f) * dev.sm_count;
+        out[4] = th;
         out[5] = 0;
     }
     return VLMCE_OK;
@@ -339,15 +332,16 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
             p.loss = loss;
             p.argmax = amax;
             p.counts = w.counts;
+            const int th = rows::threads_for(G);
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(static_cast<unsigned>(N), 1, 1);
-            cfg.blockDim = dim3(rows::kThreads, 1, 1);
+            cfg.blockDim = dim3(th, 1, 1);
             cfg.dynamicSmemBytes = 0;
             cfg.stream = cs;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            st = launch_status(cudaLaunchKernelEx(&cfg, bf16 ? rows::kernel_bf16(capped)
-                                                             : rows::kernel_f32(capped),
+            st = launch_status(cudaLaunchKernelEx(&cfg, bf16 ? rows::kernel_bf16(capped, th)
+                                                             : rows::kernel_f32(capped, th),
                                                   p),
                                "ce_rows_kernel");
         }
@@ -525,7 +519,11 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
     ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
     if ((st = launch_status(cudaSuccess, "ce_count_kernel")) != VLMCE_OK) return st;
 
-    const rows::Kernel kern = bf16 ? rows::kernel_bf16(softcap > 0.f) : rows::kernel_f32(softcap > 0.f);
+    // the CTA size ce_fwd_bwd would pick for these rows (the same arithmetic order)
+    const int th = rows::threads_for(
+        rows::row_granules(bf16, V, rows::rows_aligned(host_logits, row_stride, elt)));
+    const rows::Kernel kern =
+        bf16 ? rows::kernel_bf16(softcap > 0.f, th) : rows::kernel_f32(softcap > 0.f, th);
     const int64_t nchunks = N > 0 ? (N + R - 1) / R : 0;
     for (int64_t i = 0; i < nchunks; ++i) {
         const int b = static_cast<int>(i % kRing);
@@ -559,7 +557,7 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
         p.loss = loss + r0;
         p.argmax = amax + r0;
         p.counts = w.counts;
-        kern<<<static_cast<unsigned>(rows_i), rows::kThreads, 0, cs>>>(p);
+        kern<<<static_cast<unsigned>(rows_i), th, 0, cs>>>(p);
         if ((st = launch_status(cudaSuccess, "ce_rows_kernel")) != VLMCE_OK) return st;
         if ((st = fail(cudaEventRecord(hp->computed[b], cs), "cudaEventRecord")) != VLMCE_OK) return st;
         // copy the gradient columns [0, V) of each row back

@@ -26,8 +26,17 @@ namespace vlmce {
 namespace ce {
 namespace rows {
 
+// CTA sizes: 1024 threads for long rows, 256 (eight CTAs per SM) for rows of
+// at most kShortGranules 16-byte granules, so that every thread still folds
+// several granules per row.
 constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kShortThreads = 256;
+constexpr int kShortGranules = 8192;
+// CTAs per SM the launch bounds ask for (the softcap variants need more
+// registers per thread).
+constexpr int min_blocks(int threads, bool softcap) {
+    return threads == kThreads ? (softcap ? 1 : 2) : (softcap ? 4 : 8);
+}
 
 struct Params {
     unsigned char *logits;
@@ -184,8 +193,9 @@ __device__ __forceinline__ void store_partial(unsigned char *dst, int jg, int V,
         if (jg + l >= 0 && jg + l < V) store_elem<BF16>(dst + ELT * l, g[l]);
 }
 
-template <bool BF16, bool SOFTCAP, bool SUMZ>
+template <bool BF16, bool SOFTCAP, bool SUMZ, int THREADS>
 __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float *bcast) {
+    constexpr int kWarps = THREADS / 32;
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
     const int tid = threadIdx.x;
@@ -202,7 +212,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const int ge = ((lead + p.V) % EPG != 0) ? G - 1 : G;
     const bool head = gs == 1;                     // granule 0 partial (thread 0)
     const bool tail = ge == G - 1 && G - 1 >= gs;  // granule G-1 partial, distinct from 0
-    const int tail_tid = tail ? (G - 1 - gs) % kThreads : -1;
+    const int tail_tid = tail ? (G - 1 - gs) % THREADS : -1;
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
 
@@ -214,7 +224,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     a.nmL = INFINITY;
     a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
     if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, T, k2);
-    for (int gl = gs + tid; gl < ge; gl += kThreads)
+    for (int gl = gs + tid; gl < ge; gl += THREADS)
         fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
     if (tid == tail_tid)
         fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, T, k2);
@@ -277,7 +287,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
             grad_values<BF16, SOFTCAP>(ld_v4(row), c, gy == 0 ? ly : -1, g);
             store_partial<BF16>(gbase, -lead, p.V, g);
         }
-        for (int gl = gs + tid; gl < ge; gl += kThreads) {
+        for (int gl = gs + tid; gl < ge; gl += THREADS) {
             grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, gl == gy ? ly : -1, g);
             ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
         }
@@ -290,29 +300,43 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
 #pragma unroll
         for (int l = 0; l < EPG; ++l) z[l] = 0.f;
         if (head && tid == 0) store_partial<BF16>(gbase, -lead, p.V, z);
-        for (int gl = gs + tid; gl < ge; gl += kThreads)
+        for (int gl = gs + tid; gl < ge; gl += THREADS)
             ptx::st_global_cs_v4(gbase + 16 * gl, make_uint4(0u, 0u, 0u, 0u));
         if (tid == tail_tid) store_partial<BF16>(gbase + 16 * (G - 1), (G - 1) * EPG - lead, p.V, z);
     }
 }
 
-// Two CTAs per SM (32 registers per thread); the softcap's extra arithmetic
-// needs more registers than that, so its kernels run one CTA per SM.
-template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(kThreads, SOFTCAP ? 1 : 2) ce_rows_kernel(const Params p) {
-    __shared__ RowPart wpart[kWarps];
+// Long rows: two CTAs of 1024 threads per SM (32 registers per thread); short
+// rows: eight CTAs of 256.  The softcap's extra arithmetic needs more
+// registers, so its kernels run a quarter as many CTAs per SM.
+template <bool BF16, bool SOFTCAP, int THREADS>
+__global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
+    __shared__ RowPart wpart[THREADS / 32];
     __shared__ float bcast;
     // sum z only matters with label smoothing; skip the adds without it
     if (p.eps > 0.f)
-        row_work<BF16, SOFTCAP, true>(p, wpart, &bcast);
+        row_work<BF16, SOFTCAP, true, THREADS>(p, wpart, &bcast);
     else
-        row_work<BF16, SOFTCAP, false>(p, wpart, &bcast);
+        row_work<BF16, SOFTCAP, false, THREADS>(p, wpart, &bcast);
 }
 
-// The row kernel for the given softcap, per element type (ce_rows_bf16.cu,
-// ce_rows_f32.cu).
-Kernel kernel_bf16(bool softcap);
-Kernel kernel_f32(bool softcap);
+// Granules (16 B) of a row: exact when every row starts on a 16-byte boundary,
+// else the worst case over the possible offsets of its first element.
+inline int64_t row_granules(bool bf16, int64_t V, bool aligned_rows) {
+    const int64_t epg = bf16 ? 8 : 4;
+    return aligned_rows ? (V + epg - 1) / epg : (epg - 1 + V + epg - 1) / epg;
+}
+inline bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
+    return (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((row_stride * elt) % 16) == 0;
+}
+
+// CTA size of the row kernel for rows of G granules.
+inline int threads_for(int64_t G) { return G <= kShortGranules ? kShortThreads : kThreads; }
+
+// The row kernel for the given softcap and CTA size, per element type
+// (ce_rows_bf16.cu, ce_rows_f32.cu).
+Kernel kernel_bf16(bool softcap, int threads);
+Kernel kernel_f32(bool softcap, int threads);
 
 }  // namespace rows
 }  // namespace ce

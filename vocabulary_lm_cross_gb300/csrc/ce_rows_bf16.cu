@@ -4,7 +4,11 @@
 namespace vlmce {
 namespace ce {
 namespace rows {
-Kernel kernel_bf16(bool softcap) { return softcap ? ce_rows_kernel<true, true> : ce_rows_kernel<true, false>; }
+Kernel kernel_bf16(bool softcap, int threads) {
+    if (threads == kShortThreads)
+        return softcap ? ce_rows_kernel<true, true, kShortThreads> : ce_rows_kernel<true, false, kShortThreads>;
+    return softcap ? ce_rows_kernel<true, true, kThreads> : ce_rows_kernel<true, false, kThreads>;
+}
 }  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

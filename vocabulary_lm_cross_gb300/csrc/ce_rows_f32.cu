@@ -4,7 +4,11 @@
 namespace vlmce {
 namespace ce {
 namespace rows {
-Kernel kernel_f32(bool softcap) { return softcap ? ce_rows_kernel<false, true> : ce_rows_kernel<false, false>; }
+Kernel kernel_f32(bool softcap, int threads) {
+    if (threads == kShortThreads)
+        return softcap ? ce_rows_kernel<false, true, kShortThreads> : ce_rows_kernel<false, false, kShortThreads>;
+    return softcap ? ce_rows_kernel<false, true, kThreads> : ce_rows_kernel<false, false, kThreads>;
+}
 }  // namespace rows
 }  // namespace ce
 }  // namespace vlmce

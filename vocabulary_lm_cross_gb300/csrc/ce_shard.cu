@@ -56,27 +56,30 @@ struct ShardParams {
 // [gs, ge); granule 0 is partial when the row starts inside a granule, G - 1
 // when it ends inside one.
 struct Geo {
-    const uint4 *row;
-    unsigned char *gbase;
-    uintptr_t a0;
+    unsigned char *gbase;  // the row's first 16-byte granule
     int lead, G, gs, ge, tail_tid;
     bool head;
+    __device__ __forceinline__ const uint4 *row() const {
+        return reinterpret_cast<const uint4 *>(gbase);
+    }
 };
-template <bool BF16>
+__device__ __forceinline__ uintptr_t row_addr(const ShardParams &p) {
+    return reinterpret_cast<uintptr_t>(p.logits) + static_cast<int64_t>(blockIdx.x) * p.stride_bytes;
+}
+template <bool BF16, int THREADS>
 __device__ __forceinline__ Geo geometry(const ShardParams &p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
     Geo g;
-    g.a0 = reinterpret_cast<uintptr_t>(p.logits) + static_cast<int64_t>(blockIdx.x) * p.stride_bytes;
-    g.gbase = reinterpret_cast<unsigned char *>(g.a0 & ~static_cast<uintptr_t>(15));
-    g.row = reinterpret_cast<const uint4 *>(g.gbase);
-    g.lead = static_cast<int>((g.a0 & 15) / ELT);
+    const uintptr_t a0 = row_addr(p);
+    g.gbase = reinterpret_cast<unsigned char *>(a0 & ~static_cast<uintptr_t>(15));
+    g.lead = static_cast<int>((a0 & 15) / ELT);
     g.G = (g.lead + p.V_local + EPG - 1) / EPG;
     g.gs = g.lead > 0 ? 1 : 0;
     g.ge = ((g.lead + p.V_local) % EPG != 0) ? g.G - 1 : g.G;
     g.head = g.gs == 1;
     const bool tail = g.ge == g.G - 1 && g.G - 1 >= g.gs;
-    g.tail_tid = tail ? (g.G - 1 - g.gs) % rows::kThreads : -1;
+    g.tail_tid = tail ? (g.G - 1 - g.gs) % THREADS : -1;
     return g;
 }
 
@@ -89,13 +92,14 @@ __device__ __forceinline__ float load_x(uintptr_t a0, int64_t col) {
         return *reinterpret_cast<const float *>(py);
 }
 
-template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
+template <bool BF16, bool SOFTCAP, int THREADS>
+__global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
     ce_shard_stats_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
-    __shared__ RowPart wpart[rows::kWarps];
+    constexpr int kWarps = THREADS / 32;
+    __shared__ RowPart wpart[kWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const Geo g = geometry<BF16>(p);
+    const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
     rows::Acc a;
@@ -105,12 +109,12 @@ __global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
     a.nmL = INFINITY;
     a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
     if (g.head && tid == 0)
-        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row), -g.lead, p.V_local, T, k2);
-    for (int gl = g.gs + tid; gl < g.ge; gl += rows::kThreads)
-        rows::fold_full<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row + gl), gl * EPG - g.lead,
+        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, T, k2);
+    for (int gl = g.gs + tid; gl < g.ge; gl += THREADS)
+        rows::fold_full<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row() + gl), gl * EPG - g.lead,
                                              p.V_local, T, k2);
     if (tid == g.tail_tid)
-        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row + (g.G - 1)),
+        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row() + (g.G - 1)),
                                           (g.G - 1) * EPG - g.lead, p.V_local, T, k2);
     RowPart pt = part_identity();
     pt.mx = a.mv;
@@ -122,13 +126,13 @@ __global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
     if (lane == 0) wpart[warp] = pt;
     __syncthreads();
     if (warp == 0) {
-        RowPart q = lane < rows::kWarps ? wpart[lane] : part_identity();
+        RowPart q = lane < kWarps ? wpart[lane] : part_identity();
         warp_allreduce(q);
         if (lane == 0) {
             const int64_t yl = p.labels[blockIdx.x] - p.vocab_start;
             q.zy = 0.f;
             if (yl >= 0 && yl < p.V_local)
-                q.zy = softcap_z<SOFTCAP>(load_x<BF16>(g.a0, yl), T, k2).z;
+                q.zy = softcap_z<SOFTCAP>(load_x<BF16>(row_addr(p), yl), T, k2).z;
             q.idx = q.idx == INT_MAX ? INT_MAX : static_cast<int>(q.idx + p.vocab_start);
             q.pad0 = q.pad1 = 0.f;
             p.stats[blockIdx.x] = q;
@@ -150,29 +154,20 @@ __global__ void __launch_bounds__(256) ce_merge_stats_kernel(const RowPart *shar
     out[r] = a;
 }
 
-template <bool BF16, bool SOFTCAP>
-__global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
+template <bool BF16, bool SOFTCAP, int THREADS>
+__global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
     ce_shard_grad_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
-    const Geo g = geometry<BF16>(p);
+    const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
-    const RowPart st = p.stats[r];
-    const float lse = st.mz + logf(st.s);
+    const RowPart *st = p.stats + r;
+    const float lse = st->mz + logf(st->s);
     const int64_t y = p.labels[r];
     const bool ignored = y == p.ignore_index;
     const bool valid = !ignored && y >= 0 && y < p.V;
-    if (tid == 0) {
-        float l = 0.f;
-        if (valid)
-            l = lse - fmaf(1.f - p.eps, st.zy, (p.eps / static_cast<float>(p.V)) * st.sz);
-        else if (!ignored)
-            l = __int_as_float(0x7fc00000);  // bad label: NaN
-        if (p.loss) p.loss[r] = l;
-        if (p.argmax) p.argmax[r] = st.idx;
-    }
     if (valid) {
         const int64_t n_valid = p.counts[0];
         rows::GradCoef c;
@@ -191,15 +186,15 @@ __global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
         const int ly = mine ? static_cast<int>((yl + g.lead) % EPG) : -1;
         float gr[EPG];
         if (g.head && tid == 0) {
-            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row), c, gy == 0 ? ly : -1, gr);
+            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row()), c, gy == 0 ? ly : -1, gr);
             rows::store_partial<BF16>(g.gbase, -g.lead, p.V_local, gr);
         }
-        for (int gl = g.gs + tid; gl < g.ge; gl += rows::kThreads) {
-            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row + gl), c, gl == gy ? ly : -1, gr);
+        for (int gl = g.gs + tid; gl < g.ge; gl += THREADS) {
+            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row() + gl), c, gl == gy ? ly : -1, gr);
             ptx::st_global_cs_v4(g.gbase + 16 * gl, rows::pack_granule<BF16>(gr));
         }
         if (tid == g.tail_tid) {
-            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row + (g.G - 1)), c,
+            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row() + (g.G - 1)), c,
                                              gy == g.G - 1 ? ly : -1, gr);
             rows::store_partial<BF16>(g.gbase + 16 * (g.G - 1), (g.G - 1) * EPG - g.lead,
                                       p.V_local, gr);
@@ -209,22 +204,47 @@ __global__ void __launch_bounds__(rows::kThreads, SOFTCAP ? 1 : 2)
 #pragma unroll
         for (int l = 0; l < EPG; ++l) z[l] = 0.f;
         if (g.head && tid == 0) rows::store_partial<BF16>(g.gbase, -g.lead, p.V_local, z);
-        for (int gl = g.gs + tid; gl < g.ge; gl += rows::kThreads)
+        for (int gl = g.gs + tid; gl < g.ge; gl += THREADS)
             ptx::st_global_cs_v4(g.gbase + 16 * gl, make_uint4(0u, 0u, 0u, 0u));
         if (tid == g.tail_tid)
             rows::store_partial<BF16>(g.gbase + 16 * (g.G - 1), (g.G - 1) * EPG - g.lead,
                                       p.V_local, z);
     }
+    if (tid == 0) {  // the row's loss and argmax (the same on every shard)
+        float l = 0.f;
+        if (valid)
+            l = lse - fmaf(1.f - p.eps, st->zy, (p.eps / static_cast<float>(p.V)) * st->sz);
+        else if (!ignored)
+            l = __int_as_float(0x7fc00000);  // bad label: NaN
+        if (p.loss) p.loss[r] = l;
+        if (p.argmax) p.argmax[r] = st->idx;
+    }
 }
 
 using ShardKernel = void (*)(ShardParams);
-ShardKernel stats_kernel(bool bf16, bool softcap) {
-    if (bf16) return softcap ? ce_shard_stats_kernel<true, true> : ce_shard_stats_kernel<true, false>;
-    return softcap ? ce_shard_stats_kernel<false, true> : ce_shard_stats_kernel<false, false>;
+template <int TH>
+ShardKernel stats_kernel_t(bool bf16, bool softcap) {
+    if (bf16) return softcap ? ce_shard_stats_kernel<true, true, TH> : ce_shard_stats_kernel<true, false, TH>;
+    return softcap ? ce_shard_stats_kernel<false, true, TH> : ce_shard_stats_kernel<false, false, TH>;
 }
-ShardKernel grad_kernel(bool bf16, bool softcap) {
-    if (bf16) return softcap ? ce_shard_grad_kernel<true, true> : ce_shard_grad_kernel<true, false>;
-    return softcap ? ce_shard_grad_kernel<false, true> : ce_shard_grad_kernel<false, false>;
+template <int TH>
+ShardKernel grad_kernel_t(bool bf16, bool softcap) {
+    if (bf16) return softcap ? ce_shard_grad_kernel<true, true, TH> : ce_shard_grad_kernel<true, false, TH>;
+    return softcap ? ce_shard_grad_kernel<false, true, TH> : ce_shard_grad_kernel<false, false, TH>;
+}
+ShardKernel stats_kernel(bool bf16, bool softcap, int threads) {
+    return threads == rows::kShortThreads ? stats_kernel_t<rows::kShortThreads>(bf16, softcap)
+                                          : stats_kernel_t<rows::kThreads>(bf16, softcap);
+}
+ShardKernel grad_kernel(bool bf16, bool softcap, int threads) {
+    return threads == rows::kShortThreads ? grad_kernel_t<rows::kShortThreads>(bf16, softcap)
+                                          : grad_kernel_t<rows::kThreads>(bf16, softcap);
+}
+// The row kernel's CTA size for the shard's rows (the same arithmetic order).
+int shard_threads(const void *logits, int32_t dtype, int64_t V_local, int64_t row_stride) {
+    const bool bf16 = dtype == VLMCE_BF16;
+    return rows::threads_for(
+        rows::row_granules(bf16, V_local, rows::rows_aligned(logits, row_stride, bf16 ? 2 : 4)));
 }
 
 constexpr int64_t kMaxVocab = int64_t(1) << 28;
@@ -277,8 +297,9 @@ extern "C" vlmce_status ce_shard_stats(const void *logits, int32_t dtype, const 
     p.stride_bytes = row_stride * (dtype == VLMCE_BF16 ? 2 : 4);
     p.softcap = softcap;
     p.stats = reinterpret_cast<RowPart *>(out_stats);
-    stats_kernel(dtype == VLMCE_BF16, softcap > 0.f)
-        <<<static_cast<unsigned>(N), rows::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    const int th = shard_threads(logits, dtype, V_local, row_stride);
+    stats_kernel(dtype == VLMCE_BF16, softcap > 0.f, th)
+        <<<static_cast<unsigned>(N), th, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaSuccess, "ce_shard_stats_kernel");
 }
 
@@ -350,8 +371,9 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
         p.loss = loss;
         p.argmax = amax;
         p.counts = counts;
-        grad_kernel(dtype == VLMCE_BF16, softcap > 0.f)
-            <<<static_cast<unsigned>(N), rows::kThreads, 0, cs>>>(p);
+        const int th = shard_threads(logits, dtype, V_local, row_stride);
+        grad_kernel(dtype == VLMCE_BF16, softcap > 0.f, th)
+            <<<static_cast<unsigned>(N), th, 0, cs>>>(p);
         if ((st = launch_status(cudaSuccess, "ce_shard_grad_kernel")) != VLMCE_OK) return st;
     }
     ce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index,

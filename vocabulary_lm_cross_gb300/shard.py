@@ -39,12 +39,21 @@ def argmax(stats: torch.Tensor) -> torch.Tensor:
     return stats.view(torch.int32)[:, 1]
 
 
+def _stats_out(out, N, dev):
+    if out is None:
+        return torch.empty((N, 8), dtype=torch.float32, device=dev)
+    if out.shape != (N, 8) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 [N, 8] tensor")
+    return out
+
+
 def shard_stats(logits: torch.Tensor, labels: torch.Tensor, vocab_start: int, V: int, *,
-                softcap: float = 0.0) -> torch.Tensor:
-    """Row statistics [N, 8] of the shard (columns vocab_start.. of the vocabulary V)."""
+                softcap: float = 0.0, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Row statistics [N, 8] of the shard (columns vocab_start.. of the vocabulary V),
+    written to ``out`` if given (e.g. this rank's slot of an all-gather buffer)."""
     _check(logits, labels)
     N, VL = logits.shape
-    out = torch.empty((N, 8), dtype=torch.float32, device=logits.device)
+    out = _stats_out(out, N, logits.device)
     st = capi.lib().ce_shard_stats(logits.data_ptr(), _DTYPES[logits.dtype], labels.data_ptr(), N,
                                    VL, logits.stride(0) if N > 1 else VL, vocab_start, V,
                                    float(softcap), out.data_ptr(), _stream(logits.device))
@@ -52,13 +61,14 @@ def shard_stats(logits: torch.Tensor, labels: torch.Tensor, vocab_start: int, V:
     return out
 
 
-def merge_stats(shards: torch.Tensor) -> torch.Tensor:
-    """Merge [k, N, 8] statistics in shard order into [N, 8]."""
+def merge_stats(shards: torch.Tensor, *, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Merge [k, N, 8] statistics in shard order into [N, 8] (``out`` if given)."""
     if shards.dim() != 3 or shards.shape[2] != 8 or shards.dtype != torch.float32:
         raise ValueError("shards must be float32 [k, N, 8]")
-    shards = shards.contiguous()
+    if not shards.is_contiguous():
+        raise ValueError("shards must be contiguous")
     k, N, _ = shards.shape
-    out = torch.empty((N, 8), dtype=torch.float32, device=shards.device)
+    out = _stats_out(out, N, shards.device)
     st = capi.lib().ce_merge_stats(shards.data_ptr(), k, N, out.data_ptr(), _stream(shards.device))
     capi.check(st, "ce_merge_stats")
     return out
