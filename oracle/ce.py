@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 DTYPES = {"f32": 0, "bf16": 1, "f64": 2}
-REDUCTIONS = {"mean": 1, "sum": 2}
+REDUCTIONS = {"none": 0, "mean": 1, "sum": 2}  # "none": per-token losses, gradient not averaged
 
 
 def build(force: bool = False) -> str:
@@ -133,17 +133,24 @@ def reduce(loss: np.ndarray, argmax: np.ndarray, labels: np.ndarray, V: int, ign
 
 def ce_fwd_bwd(x: np.ndarray, dtype: str, V: int, labels: np.ndarray, *, ignore_index: int = -100,
                label_smoothing: float = 0.0, softcap: float = 0.0, reduction: str = "mean",
-               grad_scale: float = 1.0, want_grad: bool = True, threads: int = 0) -> dict:
+               grad_scale: float = 1.0, grad_per_token: np.ndarray | None = None,
+               want_grad: bool = True, threads: int = 0) -> dict:
     """The whole forward + backward over all rows.
 
-    Returns a dict with loss [n] fp64, argmax [n] int64, grad [n, V] fp64 (or
-    None), reduced_loss, accuracy, n_valid, n_correct, n_bad and row_scale.
+    reduction "mean" / "sum" reduce the per-token losses; "none" keeps them
+    (reduced_loss is then their sum) and does not divide the gradient.
+    grad_per_token ([n] or None) multiplies each row's gradient: the upstream
+    gradient of a "none" reduction, row by row.  Returns a dict with loss [n]
+    fp64, argmax [n] int64, grad [n, V] fp64 (or None), reduced_loss, accuracy,
+    n_valid, n_correct, n_bad and row_scale (the scale common to all rows).
     """
     n_valid, n_bad = count(labels, V, ignore_index)
     s = scale(reduction, grad_scale, n_valid)
     loss, amax, grad = rows(x, dtype, V, labels, ignore_index=ignore_index,
                             label_smoothing=label_smoothing, softcap=softcap, row_scale=s,
                             want_grad=want_grad, threads=threads)
+    if grad is not None and grad_per_token is not None:
+        grad *= np.asarray(grad_per_token, np.float64)[:, None]
     red, acc, n_correct = reduce(loss, amax, labels, V, ignore_index, reduction)
     return dict(loss=loss, argmax=amax, grad=grad, reduced_loss=red, accuracy=acc,
                 n_valid=n_valid, n_correct=n_correct, n_bad=n_bad, row_scale=s)

@@ -307,3 +307,37 @@ def test_round_bf16_is_nearest_even_in_fp64():
     assert oc.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 0x3F82
     # a value a hair above the tie must not be double-rounded down
     assert oc.round_bf16(np.array([1.0 + 2.0 ** -8 + 2.0 ** -40]))[0] == 0x3F81
+
+
+# ---- reduction "none" with per-token upstream gradients (library special case:
+# torch's cross_entropy(reduction="none") and autograd with a gradient vector)
+@pytest.mark.parametrize("T,eps", [(0.0, 0.0), (0.0, 0.25), (7.0, 0.1)])
+def test_none_reduction_with_per_token_upstream_gradient_matches_torch(T, eps):
+    g = np.random.default_rng(41)
+    n, V = 9, 23
+    x = g.normal(0, 2, (n, V))
+    lab = g.integers(0, V, n)
+    lab[[2, 6]] = -100
+    up = g.normal(0, 1, n)
+    r = oc.ce_fwd_bwd(x, "f64", V, lab, label_smoothing=eps, softcap=T, reduction="none",
+                      grad_scale=0.5, grad_per_token=up)
+    xt = torch.tensor(x, requires_grad=True)
+    z = T * torch.tanh(xt / T) if T > 0 else xt
+    lt = torch.nn.functional.cross_entropy(z, torch.tensor(lab), ignore_index=-100,
+                                           label_smoothing=eps, reduction="none")
+    lt.backward(gradient=0.5 * torch.tensor(up))
+    np.testing.assert_allclose(r["loss"], lt.detach().numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r["grad"], xt.grad.numpy(), rtol=1e-10, atol=1e-15)
+    valid = lab != -100
+    assert abs(r["reduced_loss"] - r["loss"][valid].sum()) < 1e-12
+
+
+def test_uniform_per_token_gradient_equals_sum_reduction():
+    g = np.random.default_rng(42)
+    x = g.normal(0, 2, (7, 31))
+    lab = g.integers(0, 31, 7)
+    a = oc.ce_fwd_bwd(x, "f64", 31, lab, reduction="sum", grad_scale=0.3)
+    b = oc.ce_fwd_bwd(x, "f64", 31, lab, reduction="none", grad_scale=1.0,
+                      grad_per_token=np.full(7, 0.3))
+    np.testing.assert_allclose(b["grad"], a["grad"], rtol=1e-15, atol=0)
+    assert a["reduced_loss"] == b["reduced_loss"]
