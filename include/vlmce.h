@@ -57,7 +57,10 @@ typedef enum {
 } vlmce_status;
 
 typedef enum { VLMCE_F32 = 0, VLMCE_BF16 = 1 } vlmce_dtype;
-typedef enum { VLMCE_MEAN = 1, VLMCE_SUM = 2 } vlmce_reduction;
+/* VLMCE_NONE: per-token losses only; the gradient is not averaged (each row
+ * is scaled by grad_scale, and by grad_per_token[r] where given) and
+ * out_reduced[0] is the sum of the losses.  Not accepted by flce_fwd_bwd. */
+typedef enum { VLMCE_NONE = 0, VLMCE_MEAN = 1, VLMCE_SUM = 2 } vlmce_reduction;
 
 /* Bits of out_counts[3]: errors the kernels detected on the device. */
 #define VLMCE_DEVERR_TIMEOUT 1 /* an on-chip wait gave up; results are invalid */
@@ -94,8 +97,9 @@ size_t vlmce_ce_workspace_bytes(int64_t N, int64_t V, int32_t dtype);
  *              out_counts[2] (the reduced loss is then NaN).
  * N >= 0, 1 <= V <= vlmce_ce_max_vocab(dtype), row_stride >= V (elements).
  * label_smoothing in [0, 1]; softcap T >= 0 and finite (0 = off);
- * reduction VLMCE_MEAN (over rows with labels in [0, V); 0 when there are none)
- * or VLMCE_SUM; grad_scale finite: the upstream gradient of the reduced loss.
+ * reduction VLMCE_MEAN (over rows with labels in [0, V); 0 when there are none),
+ * VLMCE_SUM or VLMCE_NONE; grad_scale finite: the upstream gradient of the
+ * reduced loss.
  * out_loss     [N] fp32 per-token loss (0 for ignored rows), or NULL.
  * out_argmax   [N] int64, or NULL: per row the smallest j with x_j = max_k x_k
  *              (raw input values), written for ignored rows too.
@@ -117,6 +121,28 @@ vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int6
                         float softcap, int32_t reduction, float grad_scale, float *out_loss,
                         int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
                         void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
+
+/*
+ * ce_fwd_bwd_ex -- ce_fwd_bwd with a per-token upstream gradient and a
+ * forward-only mode ("Add opt-in Liger vocab-parallel cross entropy through
+ * ops/loss", Contribution process: arbitrary upstream gradients).
+ *   grad_per_token  device fp32 [N], 4-byte aligned, or NULL: row r's gradient
+ *                   is further multiplied by grad_per_token[r] (the upstream
+ *                   gradient of a VLMCE_NONE reduction; also allowed with MEAN
+ *                   and SUM).
+ *   compute_grad    0: forward only -- the logits are read once and left
+ *                   unchanged; losses, argmax, reduced values and counts are
+ *                   written as usual.  Otherwise as ce_fwd_bwd.
+ * All other arguments, results and errors are those of ce_fwd_bwd, which is
+ * ce_fwd_bwd_ex(..., grad_per_token = NULL, compute_grad = 1, ...).
+ */
+vlmce_status ce_fwd_bwd_ex(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                           int64_t V, int64_t row_stride, int64_t ignore_index,
+                           float label_smoothing, float softcap, int32_t reduction,
+                           float grad_scale, const float *grad_per_token, int32_t compute_grad,
+                           float *out_loss, int64_t *out_argmax, float *out_reduced,
+                           int64_t *out_counts, void *workspace, size_t workspace_bytes,
+                           vlmce_stream_t stream);
 
 /*
  * ce_fwd_bwd_host -- ce_fwd_bwd for data that lives in host memory.  logits

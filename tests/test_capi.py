@@ -89,7 +89,7 @@ def call(lib, **kw):
     (dict(softcap=math.nan), capi.ERR_INVALID_ARG),
     (dict(grad_scale=math.nan), capi.ERR_INVALID_ARG),
     (dict(grad_scale=math.inf), capi.ERR_INVALID_ARG),
-    (dict(reduction=0), capi.ERR_INVALID_ARG),
+    (dict(reduction=-1), capi.ERR_INVALID_ARG),
     (dict(reduction=3), capi.ERR_INVALID_ARG),
     (dict(V=(1 << 28) + 1, row_stride=(1 << 28) + 1), capi.ERR_TOO_LARGE),
     (dict(N=(1 << 31), row_stride=100), capi.ERR_TOO_LARGE),
@@ -105,6 +105,27 @@ def call(lib, **kw):
 ])
 def test_argument_errors_are_reported_before_any_launch(lib, kw, code):
     assert call(lib, **kw) == code
+
+
+def call_ex(lib, gpt, **kw):
+    a = dict(logits=P, dtype=capi.BF16, labels=P, N=4, V=100, row_stride=100, ignore_index=-100,
+             eps=0.0, softcap=0.0, reduction=capi.NONE, grad_scale=1.0, out_loss=P,
+             out_argmax=P, out_reduced=P, out_counts=P, ws=P, ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return lib.ce_fwd_bwd_ex(a["logits"], a["dtype"], a["labels"], a["N"], a["V"],
+                             a["row_stride"], a["ignore_index"], a["eps"], a["softcap"],
+                             a["reduction"], a["grad_scale"], gpt, 1, a["out_loss"],
+                             a["out_argmax"], a["out_reduced"], a["out_counts"], a["ws"],
+                             a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("gpt,kw,code", [
+    (P + 2, {}, capi.ERR_MISALIGNED),              # per-token gradients not 4-byte aligned
+    (P, dict(reduction=3), capi.ERR_INVALID_ARG),
+    (P, dict(eps=2.0), capi.ERR_INVALID_ARG),
+])
+def test_ex_argument_errors_are_reported_before_any_launch(lib, gpt, kw, code):
+    assert call_ex(lib, gpt, **kw) == code
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")

@@ -23,6 +23,7 @@ ERR_TOO_LARGE = 7
 
 F32 = 0
 BF16 = 1
+NONE = 0
 MEAN = 1
 SUM = 2
 DEVERR_TIMEOUT = 1
@@ -46,6 +47,8 @@ SIGNATURES = {
     "vlmce_ce_describe_plan": (_i32, [_i64, _i64, _i32, _f32, _i32, _vp]),
     "ce_fwd_bwd": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32, _vp, _vp,
                           _vp, _vp, _vp, _sz, _vp]),
+    "ce_fwd_bwd_ex": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32, _vp,
+                             _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "ce_fwd_bwd_host": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32, _vp,
                                _vp, _vp, _vp, _vp, _sz, _vp]),
     "vlmce_ce_host_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),

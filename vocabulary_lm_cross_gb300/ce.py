@@ -13,7 +13,7 @@ import torch
 from . import capi
 
 _DTYPES = {torch.float32: capi.F32, torch.bfloat16: capi.BF16}
-_REDUCTIONS = {"mean": capi.MEAN, "sum": capi.SUM}
+_REDUCTIONS = {"mean": capi.MEAN, "sum": capi.SUM, "none": capi.NONE}
 
 
 @dataclass
@@ -49,7 +49,8 @@ def max_vocab(dtype: torch.dtype) -> int:
 
 def ce_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, *, ignore_index: int = -100,
                label_smoothing: float = 0.0, softcap: float = 0.0, reduction: str = "mean",
-               grad_scale: float = 1.0, out: CEResult | None = None,
+               grad_scale: float = 1.0, grad_per_token: torch.Tensor | None = None,
+               compute_grad: bool = True, out: CEResult | None = None,
                workspace: torch.Tensor | None = None) -> CEResult:
     """Fused cross-entropy forward + backward; the gradient overwrites ``logits``.
 
@@ -59,6 +60,11 @@ def ce_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, *, ignore_index: int 
         gradient of ``grad_scale * reduced_loss`` and the input is gone; its
         autograd version counter is bumped so stale uses are caught.
     labels: int64 CUDA tensor [N].
+    reduction: "mean", "sum" or "none" (per-token losses; the gradient is not
+        averaged and ``reduced[0]`` is the sum of the losses).
+    grad_per_token: optional fp32 CUDA tensor [N] multiplying each row's
+        gradient (the upstream gradient of a "none" reduction).
+    compute_grad: False for a forward-only call (the logits are left unchanged).
     """
     if logits.dim() != 2 or labels.dim() != 1 or labels.shape[0] != logits.shape[0]:
         raise ValueError("logits must be [N, V] and labels [N]")
@@ -82,18 +88,26 @@ def ce_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, *, ignore_index: int 
     need = workspace_bytes(N, V, logits.dtype)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    gpt = None
+    if grad_per_token is not None:
+        if grad_per_token.shape != (N,) or grad_per_token.dtype != torch.float32 or \
+                not grad_per_token.is_contiguous() or grad_per_token.device != dev:
+            raise ValueError("grad_per_token must be a contiguous fp32 [N] tensor on the device")
+        gpt = grad_per_token.data_ptr()
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-    st = capi.lib().ce_fwd_bwd(
+    st = capi.lib().ce_fwd_bwd_ex(
         logits.data_ptr(), _DTYPES[logits.dtype], labels.data_ptr(), N, V, row_stride,
         ignore_index, float(label_smoothing), float(softcap), _REDUCTIONS[reduction],
-        float(grad_scale), out.loss.data_ptr(), out.argmax.data_ptr(), out.reduced.data_ptr(),
-        out.counts.data_ptr(), workspace.data_ptr(), workspace.numel(), stream)
+        float(grad_scale), gpt, int(bool(compute_grad)), out.loss.data_ptr(),
+        out.argmax.data_ptr(), out.reduced.data_ptr(), out.counts.data_ptr(),
+        workspace.data_ptr(), workspace.numel(), stream)
     capi.check(st, "ce_fwd_bwd")
-    try:
-        torch.autograd.graph.increment_version(logits)
-    except Exception:  # older/newer torch without the helper: nothing to bump
-        pass
+    if compute_grad:
+        try:
+            torch.autograd.graph.increment_version(logits)
+        except Exception:  # older/newer torch without the helper: nothing to bump
+            pass
     return out
 
 

@@ -233,9 +233,10 @@ namespace {
 // (plain loads and stores only), for logits in host memory.
 vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t N, int64_t V,
                     int64_t row_stride, int64_t ignore_index, float label_smoothing, float softcap,
-                    int32_t reduction, float grad_scale, float *out_loss, int64_t *out_argmax,
-                    float *out_reduced, int64_t *out_counts, void *workspace,
-                    size_t workspace_bytes_given, vlmce_stream_t stream, bool allow_split) {
+                    int32_t reduction, float grad_scale, const float *token_scale, bool want_grad,
+                    float *out_loss, int64_t *out_argmax, float *out_reduced,
+                    int64_t *out_counts, void *workspace, size_t workspace_bytes_given,
+                    vlmce_stream_t stream, bool allow_split) {
     // ---- host-side argument checks; nothing is enqueued on failure
     if (dtype != VLMCE_F32 && dtype != VLMCE_BF16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
     if (N < 0 || V < 1 || row_stride < V) return VLMCE_ERR_INVALID_ARG;
@@ -243,7 +244,8 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
     if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
     if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
     if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
-    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM && reduction != VLMCE_NONE)
+        return VLMCE_ERR_INVALID_ARG;
     if (V > kMaxVocab || N > INT_MAX) return VLMCE_ERR_TOO_LARGE;
     const int64_t elt = dtype == VLMCE_BF16 ? 2 : 4;
     if (N > 0 && row_stride > (INT64_MAX / elt) / N) return VLMCE_ERR_TOO_LARGE;
@@ -255,6 +257,7 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
     if (out_argmax && !aligned(out_argmax, 8)) return VLMCE_ERR_MISALIGNED;
     if (out_reduced && !aligned(out_reduced, 4)) return VLMCE_ERR_MISALIGNED;
     if (out_counts && !aligned(out_counts, 8)) return VLMCE_ERR_MISALIGNED;
+    if (token_scale && !aligned(token_scale, 4)) return VLMCE_ERR_MISALIGNED;
 
     DeviceInfo dev;
     vlmce_status st = current_device(&dev);
@@ -305,6 +308,8 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
             p.counts = w.counts;
             p.err = w.err;
             p.gran_per_cta = pl.gran_per_cta;
+            p.token_scale = token_scale;
+            p.want_grad = want_grad ? 1 : 0;
             const int64_t ncl = N < pl.max_clusters ? N : pl.max_clusters;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(static_cast<unsigned>(ncl * pl.k), 1, 1);
@@ -332,6 +337,8 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
             p.loss = loss;
             p.argmax = amax;
             p.counts = w.counts;
+            p.token_scale = token_scale;
+            p.want_grad = want_grad ? 1 : 0;
             const int th = rows::threads_for(G);
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(static_cast<unsigned>(N), 1, 1);
@@ -376,8 +383,21 @@ extern "C" vlmce_status ce_fwd_bwd(void *logits, int32_t dtype, const int64_t *l
                                    float *out_reduced, int64_t *out_counts, void *workspace,
                                    size_t workspace_bytes_given, vlmce_stream_t stream) {
     return run_ce(logits, dtype, labels, N, V, row_stride, ignore_index, label_smoothing, softcap,
-                  reduction, grad_scale, out_loss, out_argmax, out_reduced, out_counts, workspace,
-                  workspace_bytes_given, stream, true);
+                  reduction, grad_scale, nullptr, true, out_loss, out_argmax, out_reduced,
+                  out_counts, workspace, workspace_bytes_given, stream, true);
+}
+
+extern "C" vlmce_status ce_fwd_bwd_ex(void *logits, int32_t dtype, const int64_t *labels,
+                                      int64_t N, int64_t V, int64_t row_stride,
+                                      int64_t ignore_index, float label_smoothing, float softcap,
+                                      int32_t reduction, float grad_scale,
+                                      const float *grad_per_token, int32_t compute_grad,
+                                      float *out_loss, int64_t *out_argmax, float *out_reduced,
+                                      int64_t *out_counts, void *workspace,
+                                      size_t workspace_bytes_given, vlmce_stream_t stream) {
+    return run_ce(logits, dtype, labels, N, V, row_stride, ignore_index, label_smoothing, softcap,
+                  reduction, grad_scale, grad_per_token, compute_grad != 0, out_loss, out_argmax,
+                  out_reduced, out_counts, workspace, workspace_bytes_given, stream, true);
 }
 
 namespace vlmce {
@@ -478,7 +498,8 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
     if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
     if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
     if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
-    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM && reduction != VLMCE_NONE)
+        return VLMCE_ERR_INVALID_ARG;
     if (V > kMaxVocab || N > INT_MAX) return VLMCE_ERR_TOO_LARGE;
     const int64_t elt = dtype == VLMCE_BF16 ? 2 : 4;
     if (N > 0 && row_stride > (INT64_MAX / elt) / N) return VLMCE_ERR_TOO_LARGE;
@@ -557,6 +578,8 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
         p.loss = loss + r0;
         p.argmax = amax + r0;
         p.counts = w.counts;
+        p.token_scale = nullptr;
+        p.want_grad = 1;
         kern<<<static_cast<unsigned>(rows_i), th, 0, cs>>>(p);
         if ((st = launch_status(cudaSuccess, "ce_rows_kernel")) != VLMCE_OK) return st;
         if ((st = fail(cudaEventRecord(hp->computed[b], cs), "cudaEventRecord")) != VLMCE_OK) return st;
@@ -603,7 +626,7 @@ extern "C" vlmce_status ce_fwd_bwd_host(void *logits, int32_t dtype, const int64
         if (!device_alias(h[i], &d[i], &host[i])) return VLMCE_ERR_INVALID_ARG;
     if (!host[0])  // device logits: ce_fwd_bwd, with host labels / outputs read and written in place
         return run_ce(d[0], dtype, static_cast<const int64_t *>(d[1]), N, V, row_stride,
-                      ignore_index, label_smoothing, softcap, reduction, grad_scale,
+                      ignore_index, label_smoothing, softcap, reduction, grad_scale, nullptr, true,
                       static_cast<float *>(d[2]), static_cast<int64_t *>(d[3]),
                       static_cast<float *>(d[4]), static_cast<int64_t *>(d[5]), workspace,
                       workspace_bytes_given, stream, true);

@@ -50,7 +50,9 @@ struct Params {
     int reduction;
     float *loss;
     int64_t *argmax;
-    const int64_t *counts;  // [0] n_valid (written by the count kernel)
+    const int64_t *counts;      // [0] n_valid (written by the count kernel)
+    const float *token_scale;   // [N] per-row factor of the gradient, or null
+    int want_grad;              // 0: forward only, the logits are not written
 };
 
 using Kernel = void (*)(Params);
@@ -266,6 +268,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         }
     }
     __syncthreads();
+    if (!p.want_grad) return;  // forward only
 
     // ---- pass 2
     if (valid) {
@@ -275,6 +278,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         c.scale = p.grad_scale;
         if (p.reduction == VLMCE_MEAN)
             c.scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
+        if (p.token_scale) c.scale *= p.token_scale[r];
         c.c_smooth = c.scale * (p.eps / static_cast<float>(p.V));
         c.c_label = c.c_smooth + c.scale * (1.f - p.eps);
         c.nlseL = -*bcast * kLog2e;

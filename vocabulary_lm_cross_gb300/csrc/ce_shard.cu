@@ -332,7 +332,8 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
     if (st != VLMCE_OK) return st;
     if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
     if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
-    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM && reduction != VLMCE_NONE)
+        return VLMCE_ERR_INVALID_ARG;
     if (N > 0 && !global_stats) return VLMCE_ERR_INVALID_ARG;
     if (global_stats && !aligned(global_stats, 16)) return VLMCE_ERR_MISALIGNED;
     const size_t need = vlmce_ce_workspace_bytes(N, V, dtype);

@@ -78,6 +78,8 @@ struct SplitParams {
     const int64_t *counts;  // [0] n_valid (written by the count kernel)
     int *err;
     int gran_per_cta;       // granules of a row owned by one CTA (<= kSlots * kChunkGranules)
+    const float *token_scale;  // [N] per-row factor of the gradient, or null
+    int want_grad;             // 0: forward only, the logits are not written
 };
 
 using SplitKernel = void (*)(SplitParams);
@@ -346,13 +348,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
         // The label census of this call must be complete before it is read.
         ptx::griddep_wait();
         const int64_t n_valid = p.counts[0];
-        float scale = p.grad_scale;
+        float scale0 = p.grad_scale;
         if (p.reduction == VLMCE_MEAN)
-            scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
-        const float c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
-        const float c_label = c_smooth + scale * (1.f - p.eps);            // + scale (1 - eps)
-        const uint64_t scale2 = pk(scale, scale);
-        const uint64_t negc2 = pk(-c_smooth, -c_smooth);
+            scale0 = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
         const float T = p.softcap;
         const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
 
@@ -456,7 +454,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
             // ---- pass B: gradient from shared memory, stored over the logits
             unsigned char *grow = reinterpret_cast<unsigned char *>(g.gbase) + 16 * g.g_beg;
             const uint64_t nlseL2 = pk(-lse * kLog2e, -lse * kLog2e);
-            for (int c = 0; c < nch; ++c) {
+            const float scale = p.token_scale ? scale0 * p.token_scale[r] : scale0;
+            const float c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
+            const float c_label = c_smooth + scale * (1.f - p.eps);            // + scale (1 - eps)
+            const uint64_t scale2 = pk(scale, scale);
+            const uint64_t negc2 = pk(-c_smooth, -c_smooth);
+            for (int c = 0; c < nch && p.want_grad; ++c) {
                 const int slot = static_cast<int>((q + c) % kSlots);
                 const int gl = c * kChunkGranules + tid;
                 if (gl < g.n_my) {
