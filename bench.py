@@ -347,6 +347,38 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     kern_ms = statistics.fmean(kb[i].elapsed_time(ke[i]) for i in range(args.steps))
 
+    # forward only (compute_grad=False): one read of the logits per step
+    for i in range(n_buf):
+        bufs[i].copy_(x0)
+    torch.cuda.synchronize()
+    fw_steps = min(args.steps, n_buf) if fresh else min(args.steps, 20)
+    fe0 = torch.cuda.Event(enable_timing=True)
+    fe1 = torch.cuda.Event(enable_timing=True)
+    for i in range(min(3, n_buf)):
+        v.ce_fwd_bwd(bufs[i][:, :V], lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                     reduction=w.reduction, grad_scale=w.grad_scale, compute_grad=False, out=out,
+                     workspace=ws)
+    torch.cuda.synchronize()
+    fe0.record(stream)
+    for i in range(fw_steps):
+        v.ce_fwd_bwd(bufs[i % n_buf][:, :V], lab, label_smoothing=w.label_smoothing,
+                     softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
+                     compute_grad=False, out=out, workspace=ws)
+    fe1.record(stream)
+    torch.cuda.synchronize()
+    fw_ms = fe0.elapsed_time(fe1) / fw_steps
+    fw_bytes = w.N * V * x0.element_size()
+    peak_fw, peak_fw_src = load_peaks()
+    forward_only = {"metric": "CE forward only (no gradient, logits kept) GB/s",
+                    "value": world * fw_bytes / (fw_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": fw_ms, "steps": fw_steps, "bytes_per_step": fw_bytes,
+                    "roofline": {"bound": "hbm", "achieved": fw_bytes / (fw_ms * 1e-3) / 1e9,
+                                 "peak": peak_fw, "peak_source": f"{peak_fw_src} (copy GB/s)",
+                                 "unit": "GB/s",
+                                 "frac": fw_bytes / (fw_ms * 1e-3) / 1e9 / peak_fw,
+                                 "measured_over": "whole step (census, row kernel, finalize)"},
+                    "l2": "the ring of logits copies (each larger than L2), round robin"}
+
     # end to end through the public API with host buffers: ce_fwd_bwd_host on
     # page-locked host logits (streamed through the GPU in chunks of rows, the
     # gradient copied back in place), labels and outputs in host memory.  Each
@@ -453,6 +485,7 @@ def run_ours(args, w):
                 "device_status_ok": e2e_ok},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "forward_only": forward_only,
         "shard": shard,
         "flce": flce,
     }
