@@ -241,6 +241,28 @@ vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels
                               int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
                               void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
 
+/*
+ * Fused gate-up SwiGLU ("[Megatron] Add SwiGLU integration", Summary and
+ * Background).  x: device [T, x_stride] elements of `dtype` (VLMCE_BF16 or
+ * VLMCE_F32), the gate in columns [0, n) and the up projection in [n, 2n) of
+ * every row (x_stride >= 2n).  Arithmetic in fp32, results rounded to
+ * nearest even.  Argument errors are returned before anything is enqueued.
+ *
+ * swiglu_fwd: y [T, y_stride >= n] = silu(gate) * up, silu(a) = a / (1 + e^-a).
+ *             y must not overlap x.
+ * swiglu_bwd: dx [T, dx_stride >= 2n] = (d_gate | d_up) for dy [T, dy_stride
+ *             >= n]: d_up = dy silu(gate), d_gate = dy up silu'(gate).  dx may
+ *             be x itself with the same stride (in place); otherwise the
+ *             buffers must not overlap.
+ * 16-byte vector accesses when n, the strides and the bases allow it, else
+ * one element per thread.
+ */
+vlmce_status swiglu_fwd(const void *x, int32_t dtype, int64_t T, int64_t n, int64_t x_stride,
+                        void *y, int64_t y_stride, vlmce_stream_t stream);
+vlmce_status swiglu_bwd(const void *x, int64_t x_stride, const void *dy, int64_t dy_stride,
+                        void *dx, int64_t dx_stride, int32_t dtype, int64_t T, int64_t n,
+                        vlmce_stream_t stream);
+
 /* Bytes of device workspace flce_fwd_bwd needs (256-byte aligned): per-row
  * statistics of every 256-column logits tile, two bf16 [N, 8192] gradient
  * tiles and an fp32 [N, H] grad_hidden accumulator. */
