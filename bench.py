@@ -432,6 +432,8 @@ def run_ours(args, w):
 
     shard = run_shard(args, w, dev, world, barrier, sampler) if w.V % 8 == 0 else None
     torch.cuda.empty_cache()
+    swiglu = run_swiglu(args, dev, sampler) if not args.no_flce else None
+    torch.cuda.empty_cache()
 
     flce = None
     if not args.no_flce:
@@ -486,6 +488,7 @@ def run_ours(args, w):
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "forward_only": forward_only,
+        "swiglu": swiglu,
         "shard": shard,
         "flce": flce,
     }
@@ -590,6 +593,55 @@ def run_shard(args, w, dev, world, barrier, sampler, tp=8):
             "clocks": sampler.summary(t0, t1),
             "l2": f"ring of {nb} shard copies ({nb * bytes_step / 2 / 1e6:.0f} MB > 2 x L2); the "
                   "gradient pass re-reads the shard from L2"}
+
+
+def run_swiglu(args, dev, sampler, T=8192, ns=(32768, 4096)):
+    """The fused gate-up SwiGLU at the Megatron training shape of its page
+    (S = 2048 x B = 4 tokens, bf16): forward and out-of-place backward per
+    ffn width n, against the HBM roofline (bytes = what must move: x in and
+    y out for the forward; x and dy in, dx out for the backward)."""
+    import torch
+
+    from vocabulary_lm_cross_gb300.swiglu import swiglu_bwd, swiglu_fwd
+
+    peak, peak_src = load_peaks()
+    out = {}
+    for n in ns:
+        g = torch.Generator(device=dev)
+        g.manual_seed(n)
+        x = (torch.randn((T, 2 * n), generator=g, device=dev) * 2).to(torch.bfloat16)
+        dy = torch.randn((T, n), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((T, n), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((T, 2 * n), dtype=torch.bfloat16, device=dev)
+        flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.float32, device=dev)
+        res = {}
+        for name, fn, nbytes in (("forward", lambda: swiglu_fwd(x, out=y), 3 * T * n * 2),
+                                 ("backward", lambda: swiglu_bwd(x, dy, out=dx), 5 * T * n * 2)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            times = []
+            t0 = time.time()
+            for _ in range(min(args.steps, 20)):
+                flush.zero_()  # evict the previous step's lines from L2
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.fmean(times)
+            res[name] = {"ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                         "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "bytes": nbytes,
+                         "clocks": sampler.summary(t0, time.time())}
+        out[f"T{T}_n{n}"] = res
+        del x, dy, y, dx, flush
+        torch.cuda.empty_cache()
+    return {"metric": "fused gate-up SwiGLU GB/s (bf16, [tokens, 2n] layout)", "unit": "GB/s",
+            "peak": peak, "peak_source": f"{peak_src} (copy GB/s)", "bound": "hbm",
+            "l2": "a 258 MB buffer is written between timed launches (flushes L2)",
+            "gpu_launches_per_step": 1, "results": out}
 
 
 def flce_oracle_sample(w, budget_s=10.0):
@@ -836,7 +888,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ce-bf16-2048x131072-ls0.1-argmax")
     ap.add_argument("--no-flce", action="store_true",
-                    help="skip the fused linear cross-entropy leg of a cross-entropy run")
+                    help="skip the fused linear cross-entropy and SwiGLU legs of a "
+                         "cross-entropy run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
