@@ -56,7 +56,8 @@ typedef enum {
     VLMCE_ERR_TOO_LARGE = 7           /* a size beyond what the kernels support      */
 } vlmce_status;
 
-typedef enum { VLMCE_F32 = 0, VLMCE_BF16 = 1 } vlmce_dtype;
+/* VLMCE_F16: fp16, accepted by flce_fwd_bwd_ex and vlmce_gemm only. */
+typedef enum { VLMCE_F32 = 0, VLMCE_BF16 = 1, VLMCE_F16 = 2 } vlmce_dtype;
 /* VLMCE_NONE: per-token losses only; the gradient is not averaged (each row
  * is scaled by grad_scale, and by grad_per_token[r] where given) and
  * out_reduced[0] is the sum of the losses.  Not accepted by flce_fwd_bwd. */
@@ -296,6 +297,31 @@ vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, const void 
                           int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
                           void *grad_hidden, float *grad_weight, int32_t accumulate_grad_weight,
                           void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
+
+/*
+ * flce_fwd_bwd_ex -- flce_fwd_bwd for bf16 or fp16 hidden states and weight
+ * (dtype VLMCE_BF16 or VLMCE_F16; grad_hidden in the same dtype, grad_weight
+ * fp32), like the SM100 fused linear cross-entropy of "Add Liger Kernel
+ * support for Muse Glimmer" (FP16/BF16 input and weight, mean/sum).  The
+ * gradient tile between the products is kept without the row scale (times
+ * 2^14 in fp16, so that small probabilities do not underflow); the two
+ * gradient products apply the scale in their epilogues.  Other arguments,
+ * results and errors as flce_fwd_bwd, which is flce_fwd_bwd_ex(VLMCE_BF16).
+ */
+vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64_t hidden_stride,
+                             const void *weight, int64_t weight_stride, const int64_t *labels,
+                             int64_t N, int64_t H, int64_t V, int64_t ignore_index,
+                             float label_smoothing, float softcap, int32_t reduction,
+                             float grad_scale, float *out_loss, int64_t *out_argmax,
+                             float *out_reduced, int64_t *out_counts, void *grad_hidden,
+                             float *grad_weight, int32_t accumulate_grad_weight, void *workspace,
+                             size_t workspace_bytes, vlmce_stream_t stream);
+
+/* vlmce_gemm -- vlmce_gemm_bf16 with the operand type as an argument
+ * (VLMCE_BF16 or VLMCE_F16; A and B share it). */
+vlmce_status vlmce_gemm(const void *A, int32_t a_mn, const void *B, int32_t b_mn, float *C,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        int32_t accumulate, int32_t dtype, vlmce_stream_t stream);
 
 /*
  * vlmce_gemm_bf16 -- the library's tcgen05 GEMM on its own:

@@ -69,10 +69,33 @@ def test_gemm_engine_against_matmul(a_mn, b_mn, M, N, K):
     assert err <= 2e-5 * ref.abs().max().item(), err
 
 
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 1)])
+def test_gemm_engine_fp16_against_matmul(a_mn, b_mn):
+    M, N, K = 520, 264, 1032
+    g = torch.Generator(device=DEV)
+    g.manual_seed(17 + a_mn)
+    Al = torch.randn(M, K, generator=g, device=DEV).to(torch.float16)
+    Bl = torch.randn(N, K, generator=g, device=DEV).to(torch.float16)
+    A = Al.t().contiguous() if a_mn else Al
+    B = Bl.t().contiguous() if b_mn else Bl
+    ref = Al.double() @ Bl.double().t()
+    C = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    st = capi.lib().vlmce_gemm(A.data_ptr(), a_mn, B.data_ptr(), b_mn, C.data_ptr(), M, N, K,
+                               A.stride(0), B.stride(0), C.stride(0), 0, capi.F16,
+                               torch.cuda.current_stream().cuda_stream)
+    capi.check(st, "vlmce_gemm")
+    torch.cuda.synchronize()
+    assert (C.double() - ref).abs().max().item() <= 1e-5 * ref.abs().max().item()
+
+
 def near_tie_rows(h64, W64, labels=None):
     S = h64 @ W64.T
     top2 = np.sort(S, axis=1)[:, -2:]
     return np.abs(top2[:, 1] - top2[:, 0]) < 1e-3 * np.maximum(1.0, np.abs(top2[:, 1]))
+
+
+def widen(t):
+    return t.double().cpu().numpy() if t.dtype == torch.float16 else of.widen_bf16(bf16_bits_np(t))
 
 
 def run_small(w: FLCEWorkload, accumulate=False):
@@ -85,8 +108,8 @@ def run_small(w: FLCEWorkload, accumulate=False):
                        grad_weight=gw0.clone() if accumulate else None,
                        accumulate_grad_weight=accumulate)
     torch.cuda.synchronize()
-    h64 = of.widen_bf16(bf16_bits_np(h))
-    W64 = of.widen_bf16(bf16_bits_np(W))
+    h64 = widen(h)
+    W64 = widen(W)
     labh = lab.cpu().numpy()
     ref = of.flce_fwd_bwd(h64, W64, labh, label_smoothing=w.label_smoothing, softcap=w.softcap,
                           reduction=w.reduction, grad_scale=w.grad_scale)
@@ -109,10 +132,17 @@ def run_small(w: FLCEWorkload, accumulate=False):
     return res, ref
 
 
-def small(N, H, V, T=0.0, eps=0.0, red="mean", gs=1.0, seed=11, wsig=0.05):
+def small(N, H, V, T=0.0, eps=0.0, red="mean", gs=1.0, seed=11, wsig=0.05, dtype="bf16"):
     return FLCEWorkload(f"f{N}x{H}x{V}", N=N, H=H, V=V, hidden_sigma=1.0, weight_sigma=wsig,
                         multiplier=0.5, ignore_frac=0.05, label_smoothing=eps, softcap=T,
-                        reduction=red, grad_scale=gs, seed=seed)
+                        reduction=red, grad_scale=gs, seed=seed, dtype=dtype)
+
+
+@pytest.mark.parametrize("N,H,V,T,eps,red", [(256, 512, 8192, 30.0, 0.1, "mean"),
+                                             (600, 264, 17000, 0.0, 0.0, "sum"),
+                                             (130, 128, 300, 5.0, 0.2, "mean")])
+def test_flce_fp16(N, H, V, T, eps, red):
+    run_small(small(N, H, V, T=T, eps=eps, red=red, gs=0.5, seed=N + 1, dtype="f16"))
 
 
 @pytest.mark.parametrize("N,H,V", [(256, 512, 8192), (200, 264, 5000), (130, 128, 300)])

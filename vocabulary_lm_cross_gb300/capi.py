@@ -23,6 +23,7 @@ ERR_TOO_LARGE = 7
 
 F32 = 0
 BF16 = 1
+F16 = 2
 NONE = 0
 MEAN = 1
 SUM = 2
@@ -64,6 +65,10 @@ SIGNATURES = {
     "vlmce_flce_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "flce_fwd_bwd": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32,
                             _f32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "flce_fwd_bwd_ex": (_i32, [_vp, _i32, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _f32,
+                               _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "vlmce_gemm": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
+                          _i32, _vp]),
     "vlmce_gemm_bf16": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
                                _i32, _vp]),
     "vlmce_flce_profile_events": (None, [_vp, _vp]),

@@ -43,6 +43,9 @@ namespace {
 using ce::RowPart;
 
 constexpr int kChunk = 8192;  // vocabulary columns per gradient chunk
+// Factor of the fp16 gradient tile ((p - q)(1 - t^2) has |.| <= 1; x 2^14 stays
+// below the fp16 maximum and keeps small probabilities out of the subnormals).
+constexpr float kF16GradMul = 16384.f;
 constexpr int64_t kWsHeader = 256;
 
 // ----------------------------------------------------------------- kernels
@@ -92,9 +95,20 @@ __global__ void __launch_bounds__(1024) flce_count_kernel(const int64_t *__restr
 __global__ void __launch_bounds__(256) flce_merge_kernel(
     const RowPart *__restrict__ part, int64_t part_ld, int ntiles, const int64_t *__restrict__ labels,
     int64_t N, int64_t V, int64_t ignore_index, float eps, float grad_scale, int reduction,
-    const int64_t *counts, float *lse, float *row_scale, float *loss, int64_t *argmax) {
+    const int64_t *counts, float *lse, float *row_scale, float *loss, int64_t *argmax,
+    float inv_grad_mul, float *out_scale) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    if (row == 0 && lane == 0) {
+        // the scale every valid row shares, divided by the gradient tile's factor:
+        // the two gradient products multiply their accumulators by it
+        float s = grad_scale;
+        if (reduction == VLMCE_MEAN) {
+            const long long nv = counts[0];
+            s = nv > 0 ? grad_scale / static_cast<float>(nv) : 0.f;
+        }
+        *out_scale = s * inv_grad_mul;
+    }
     if (row >= N) return;
     RowPart a = ce::part_identity();
     for (int t = lane; t < ntiles; t += 32) {
@@ -186,7 +200,8 @@ struct Ws {
     RowPart *part;  // [ntiles][N]
     float *lse, *row_scale, *loss;
     int64_t *argmax;
-    __nv_bfloat16 *g[2];  // two [N, kChunk] gradient tiles
+    uint16_t *g[2];       // two [N, kChunk] gradient tiles (bf16 or fp16 bits)
+    float *out_scale;     // scale of the gradient products' accumulators
     float *gh;            // [N, H] grad_h accumulator
 };
 
@@ -206,6 +221,7 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
     Ws w;
     w.counts = reinterpret_cast<int64_t *>(p);
     w.err = reinterpret_cast<int *>(p + 64);
+    w.out_scale = reinterpret_cast<float *>(p + 128);
     p += kWsHeader;
     w.part = reinterpret_cast<RowPart *>(p);
     p += round_up(ntiles_of(V) * N * static_cast<int64_t>(sizeof(RowPart)), 256);
@@ -218,7 +234,7 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
     w.argmax = reinterpret_cast<int64_t *>(p);
     p += round_up(8 * N, 256);
     for (int i = 0; i < 2; ++i) {
-        w.g[i] = reinterpret_cast<__nv_bfloat16 *>(p);
+        w.g[i] = reinterpret_cast<uint16_t *>(p);
         p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     }
     w.gh = reinterpret_cast<float *>(p);
@@ -245,10 +261,12 @@ extern "C" size_t vlmce_flce_workspace_bytes(int64_t N, int64_t H, int64_t V) {
     return ws_bytes(N, H, V);
 }
 
-extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void *B, int32_t b_mn,
-                                        float *C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                                        int64_t ldb, int64_t ldc, int32_t accumulate,
-                                        vlmce_stream_t stream) {
+extern "C" vlmce_status vlmce_gemm(const void *A, int32_t a_mn, const void *B, int32_t b_mn,
+                                   float *C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                   int64_t ldb, int64_t ldc, int32_t accumulate, int32_t dtype,
+                                   vlmce_stream_t stream) {
+    if (dtype != VLMCE_BF16 && dtype != VLMCE_F16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
+    const bool f16 = dtype == VLMCE_F16;
     if (!A || !B || !C || M < 1 || N < 1 || K < 1) return VLMCE_ERR_INVALID_ARG;
     if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return VLMCE_ERR_TOO_LARGE;
     if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N) return VLMCE_ERR_INVALID_ARG;
@@ -258,13 +276,14 @@ extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void 
     vlmce_status st = current_device(&dev);
     if (st != VLMCE_OK) return st;
     gemm::Maps maps;
-    if (!gemm::make_operand_map(&maps.a[0], A, false, a_mn != 0, M, K, lda) ||
-        !gemm::make_operand_map(&maps.b[0], B, true, b_mn != 0, N, K, ldb)) {
+    if (!gemm::make_operand_map(&maps.a[0], A, false, a_mn != 0, M, K, lda, f16) ||
+        !gemm::make_operand_map(&maps.b[0], B, true, b_mn != 0, N, K, ldb, f16)) {
         record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
         return VLMCE_ERR_CUDA;
     }
     gemm::Params g = {};
     g.nprob = 1;
+    g.f16 = f16 ? 1 : 0;
     gemm::Problem &p = g.p[0];
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
@@ -279,7 +298,15 @@ extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void 
                          "vlmce_gemm_kernel");
 }
 
-extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, const void *weight,
+extern "C" vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void *B, int32_t b_mn,
+                                        float *C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                        int64_t ldb, int64_t ldc, int32_t accumulate,
+                                        vlmce_stream_t stream) {
+    return vlmce_gemm(A, a_mn, B, b_mn, C, M, N, K, lda, ldb, ldc, accumulate, VLMCE_BF16, stream);
+}
+
+extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64_t hidden_stride,
+                                     const void *weight,
                                      int64_t weight_stride, const int64_t *labels, int64_t N,
                                      int64_t H, int64_t V, int64_t ignore_index,
                                      float label_smoothing, float softcap, int32_t reduction,
@@ -289,6 +316,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                                      void *workspace, size_t workspace_bytes_given,
                                      vlmce_stream_t stream) {
     // ---- host-side argument checks; nothing is enqueued on failure
+    if (dtype != VLMCE_BF16 && dtype != VLMCE_F16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
+    const bool f16 = dtype == VLMCE_F16;
     if (N < 0 || H < 1 || V < 1) return VLMCE_ERR_INVALID_ARG;
     if (N > INT_MAX || H > INT_MAX || V > INT_MAX) return VLMCE_ERR_TOO_LARGE;
     if (hidden_stride < H || weight_stride < H) return VLMCE_ERR_INVALID_ARG;
@@ -332,6 +361,10 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
         base.lse = w.lse;
         base.row_scale = w.row_scale;
         base.err = w.err;
+        base.f16 = f16 ? 1 : 0;
+        // fp16 keeps the scale-free gradient tile (|.| <= 1) away from underflow
+        base.grad_mul = f16 ? kF16GradMul : 1.f;
+        base.out_scale = w.out_scale;
 
         cudaEvent_t eb = t_prof_begin, ee = t_prof_end;
         t_prof_begin = t_prof_end = nullptr;
@@ -345,8 +378,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
         // ---- pass 1: statistics of S = h' W^T over the whole vocabulary
         {
             gemm::Maps maps;
-            if (!gemm::make_operand_map(&maps.a[0], hidden, false, false, N, H, hidden_stride) ||
-                !gemm::make_operand_map(&maps.b[0], weight, true, false, V, H, weight_stride))
+            if (!gemm::make_operand_map(&maps.a[0], hidden, false, false, N, H, hidden_stride, f16) ||
+                !gemm::make_operand_map(&maps.b[0], weight, true, false, V, H, weight_stride, f16))
                 return map_fail();
             gemm::Params g = base;
             g.nprob = 1;
@@ -364,7 +397,8 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
 
         flce_merge_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, cs>>>(
             w.part, N, static_cast<int>(ntiles_of(V)), labels, N, V, ignore_index, label_smoothing,
-            grad_scale, reduction, w.counts, w.lse, w.row_scale, loss, amax);
+            grad_scale, reduction, w.counts, w.lse, w.row_scale, loss, amax,
+            1.f / (f16 ? kF16GradMul : 1.f), w.out_scale);
         st = launch_status(cudaSuccess, "flce_merge_kernel");
         if (st != VLMCE_OK) return st;
 
@@ -378,12 +412,11 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                 const int64_t cp = c - 1;
                 const int64_t v0 = cp * kChunk;
                 const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
-                const __nv_bfloat16 *wc =
-                    reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
-                const __nv_bfloat16 *gc = w.g[cp & 1];
+                const uint16_t *wc = static_cast<const uint16_t *>(weight) + v0 * weight_stride;
+                const uint16_t *gc = w.g[cp & 1];
                 // grad_h (+)= G_c W_c: A = G_c K-major [N, Vc], B = W_c N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, false, N, vc, kChunk) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, true, true, H, vc, weight_stride))
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, false, N, vc, kChunk, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, true, H, vc, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &ph = g.p[n++];
                 ph.M = static_cast<int>(N);
@@ -397,11 +430,11 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                 ph.b_mn = 1;
                 ph.C = w.gh;
                 ph.ldc = H;
-                ph.C16 = static_cast<__nv_bfloat16 *>(grad_hidden);
+                ph.C16 = static_cast<uint16_t *>(grad_hidden);
                 ph.ldc16 = hidden_stride;
                 // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, true, vc, N, kChunk) ||
-                    !gemm::make_operand_map(&maps.b[n], hidden, true, true, H, N, hidden_stride))
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, true, vc, N, kChunk, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], hidden, true, true, H, N, hidden_stride, f16))
                     return map_fail();
                 gemm::Problem &pw = g.p[n++];
                 pw.M = static_cast<int>(vc);
@@ -416,11 +449,10 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
             if (c < nchunks) {
                 const int64_t v0 = c * kChunk;
                 const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
-                const __nv_bfloat16 *wc =
-                    reinterpret_cast<const __nv_bfloat16 *>(weight) + v0 * weight_stride;
+                const uint16_t *wc = static_cast<const uint16_t *>(weight) + v0 * weight_stride;
                 // G_c = scale (softmax - q) (1 - t^2) from the recomputed S_c = h' W_c^T
-                if (!gemm::make_operand_map(&maps.a[n], hidden, false, false, N, H, hidden_stride) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, true, false, vc, H, weight_stride))
+                if (!gemm::make_operand_map(&maps.a[n], hidden, false, false, N, H, hidden_stride, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, false, vc, H, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &pg = g.p[n++];
                 pg.M = static_cast<int>(N);
@@ -442,4 +474,20 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
     flce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index, reduction,
                                              w.counts, w.err, out_reduced, out_counts);
     return launch_status(cudaSuccess, "flce_finalize_kernel");
+}
+
+extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, const void *weight,
+                                     int64_t weight_stride, const int64_t *labels, int64_t N,
+                                     int64_t H, int64_t V, int64_t ignore_index,
+                                     float label_smoothing, float softcap, int32_t reduction,
+                                     float grad_scale, float *out_loss, int64_t *out_argmax,
+                                     float *out_reduced, int64_t *out_counts, void *grad_hidden,
+                                     float *grad_weight, int32_t accumulate_grad_weight,
+                                     void *workspace, size_t workspace_bytes_given,
+                                     vlmce_stream_t stream) {
+    return flce_fwd_bwd_ex(hidden, VLMCE_BF16, hidden_stride, weight, weight_stride, labels, N, H,
+                           V, ignore_index, label_smoothing, softcap, reduction, grad_scale,
+                           out_loss, out_argmax, out_reduced, out_counts, grad_hidden,
+                           grad_weight, accumulate_grad_weight, workspace, workspace_bytes_given,
+                           stream);
 }

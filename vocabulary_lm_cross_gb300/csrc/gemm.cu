@@ -36,14 +36,15 @@ EncodeTiled encoder() {
 // A bf16 matrix of `outer` rows of `inner` elements (row stride `stride`
 // elements), read in boxes of box_inner x box_outer with 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, bool f16) {
     EncodeTiled enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {stride * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+    return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -93,9 +94,9 @@ int co_resident_clusters(int device, int csize, cudaError_t *err) {
 }  // namespace
 
 bool make_operand_map(CUtensorMap *m, const void *base, bool is_b, bool mn, int64_t rows,
-                      int64_t K, int64_t ld) {
-    if (mn) return make_map(m, base, rows, K, ld, 64, 64);
-    return make_map(m, base, K, rows, ld, 64, is_b ? 64 : kHalf);
+                      int64_t K, int64_t ld, bool f16) {
+    if (mn) return make_map(m, base, rows, K, ld, 64, 64, f16);
+    return make_map(m, base, K, rows, ld, 64, is_b ? 64 : kHalf, f16);
 }
 
 cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s) {

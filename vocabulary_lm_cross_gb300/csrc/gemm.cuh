@@ -46,6 +46,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ce_common.cuh"
 #include "gemm_types.h"
@@ -103,6 +104,31 @@ __device__ __forceinline__ void st_v4f(float *p, float a, float b, float c, floa
     *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
 }
 
+// Two fp32 values -> a bf16x2 or fp16x2 word, round to nearest even.
+__device__ __forceinline__ uint32_t pack16x2(float a, float b, bool f16) {
+    if (!f16) return ce::pack_bf16x2(a, b);
+    const __half2 v = __floats2half2_rn(a, b);  // a in the low half, as for bf16
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    return u;
+}
+__device__ __forceinline__ uint16_t to16(float a, bool f16) {
+    return f16 ? __half_as_ushort(__float2half_rn(a)) : __bfloat16_as_ushort(__float2bfloat16_rn(a));
+}
+__device__ __forceinline__ void store16x32(uint16_t *c16, const float (&o)[32], int nvalid, bool f16) {
+    if (nvalid == 32) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+            *reinterpret_cast<uint4 *>(c16 + j) =
+                make_uint4(pack16x2(o[j], o[j + 1], f16), pack16x2(o[j + 2], o[j + 3], f16),
+                           pack16x2(o[j + 4], o[j + 5], f16), pack16x2(o[j + 6], o[j + 7], f16));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < nvalid) c16[j] = to16(o[j], f16);
+    }
+}
+
 // Per-row state of the statistics epilogue (pass 1 of the fused linear CE).
 struct StatAcc {
     float mx;
@@ -110,15 +136,16 @@ struct StatAcc {
     float mz, s, sz, zy;
 };
 
-// fp32 / bf16 output modes on one 32-column chunk of one row.
+// fp32 / 16-bit output modes on one 32-column chunk of one row; the
+// accumulator is multiplied by `sc` first.
 template <int MODE>
 __device__ __forceinline__ void store_chunk(const Problem &P, const float (&v)[32], int row,
-                                            int cbase, int nvalid) {
+                                            int cbase, int nvalid, float sc, bool f16) {
+    float o[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = v[j] * sc;
     if constexpr (MODE == kStoreF32 || MODE == kAccF32 || MODE == kAccToBF16) {
         float *c = P.C + static_cast<int64_t>(row) * P.ldc + cbase;
-        float o[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = v[j];
         if constexpr (MODE != kStoreF32) {
             if (nvalid == 32) {
 #pragma unroll
@@ -136,18 +163,7 @@ __device__ __forceinline__ void store_chunk(const Problem &P, const float (&v)[3
             }
         }
         if constexpr (MODE == kAccToBF16) {
-            __nv_bfloat16 *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
-            if (nvalid == 32) {
-#pragma unroll
-                for (int j = 0; j < 32; j += 8)
-                    *reinterpret_cast<uint4 *>(c16 + j) = make_uint4(
-                        ce::pack_bf16x2(o[j], o[j + 1]), ce::pack_bf16x2(o[j + 2], o[j + 3]),
-                        ce::pack_bf16x2(o[j + 4], o[j + 5]), ce::pack_bf16x2(o[j + 6], o[j + 7]));
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j < nvalid) c16[j] = __float2bfloat16_rn(o[j]);
-            }
+            store16x32(P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase, o, nvalid, f16);
         } else {
             if (nvalid == 32) {
 #pragma unroll
@@ -159,17 +175,13 @@ __device__ __forceinline__ void store_chunk(const Problem &P, const float (&v)[3
             }
         }
     } else {  // kStoreBF16
-        __nv_bfloat16 *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
+        uint16_t *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
         if (nvalid == 32 && (P.ldc16 % 8) == 0) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8)
-                *reinterpret_cast<uint4 *>(c16 + j) = make_uint4(
-                    ce::pack_bf16x2(v[j], v[j + 1]), ce::pack_bf16x2(v[j + 2], v[j + 3]),
-                    ce::pack_bf16x2(v[j + 4], v[j + 5]), ce::pack_bf16x2(v[j + 6], v[j + 7]));
+            store16x32(c16, o, 32, f16);
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (j < nvalid) c16[j] = __float2bfloat16_rn(v[j]);
+                if (j < nvalid) c16[j] = to16(o[j], f16);
         }
     }
 }
@@ -237,13 +249,15 @@ __device__ __forceinline__ void stats_chunk(const Params &a, const Problem &P,
     }
 }
 
-// Gradient tile: G = rscale (softmax - q) (1 - t^2) of one 32-column chunk -> bf16.
+// Gradient tile of one 32-column chunk: (softmax - q) (1 - t^2) times m (the
+// launch's power-of-two grad_mul for a valid row, 0 otherwise) -> 16-bit.
+// The rows' common scale is applied by the products that consume the tile.
 __device__ __forceinline__ void grad_chunk(const Params &a, const Problem &P, const float (&v)[32],
-                                           int row, int cbase, int nvalid, int64_t y,
-                                           float rscale, float nlseL) {
+                                           int row, int cbase, int nvalid, int64_t y, float m,
+                                           float nlseL) {
     const bool cap = a.T > 0.f;
-    const float c_smooth = rscale * (a.eps / static_cast<float>(a.V));
-    const float c_label = c_smooth + rscale * (1.f - a.eps);
+    const float c_smooth = m * (a.eps / static_cast<float>(a.V));
+    const float c_label = c_smooth + m * (1.f - a.eps);
     const int64_t yl = y - P.col0 - cbase;
     float g[32];
 #pragma unroll
@@ -255,20 +269,9 @@ __device__ __forceinline__ void grad_chunk(const Params &a, const Problem &P, co
             dz = cz.dz;
         }
         const float pr = ptx::ex2(fmaf(z, ce::kLog2e, nlseL));
-        g[j] = fmaf(pr, rscale, (j == yl) ? -c_label : -c_smooth) * dz;
+        g[j] = fmaf(pr, m, (j == yl) ? -c_label : -c_smooth) * dz;
     }
-    __nv_bfloat16 *c16 = P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase;
-    if (nvalid == 32) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8)
-            *reinterpret_cast<uint4 *>(c16 + j) =
-                make_uint4(ce::pack_bf16x2(g[j], g[j + 1]), ce::pack_bf16x2(g[j + 2], g[j + 3]),
-                           ce::pack_bf16x2(g[j + 4], g[j + 5]), ce::pack_bf16x2(g[j + 6], g[j + 7]));
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < nvalid) c16[j] = __float2bfloat16_rn(g[j]);
-    }
+    store16x32(P.C16 + static_cast<int64_t>(row) * P.ldc16 + cbase, g, nvalid, a.f16 != 0);
 }
 
 // ------------------------------------------------------------ the kernel
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
                 const Tile tl = tile_of(a, t, npairs);
                 const Problem &P = a.p[tl.p];
-                const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, P.a_mn != 0, P.b_mn != 0);
+                const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, P.a_mn != 0, P.b_mn != 0, a.f16 != 0);
                 const int kblocks = (P.K + BK - 1) / BK;
                 const int b = it & 1;
                 wait_bar<true>(tempty(b), ((it >> 1) & 1) ^ 1, abort, a.err);
@@ -440,14 +443,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = tl.m0 + rl;
             const bool row_ok = row < P.M;
             int64_t y = -1;
-            float rscale = 0.f, nlseL = 0.f;
+            float m = 0.f, nlseL = 0.f;
             if ((P.mode == kStats || P.mode == kGrad) && row_ok) {
                 y = a.labels[row];
                 if (P.mode == kGrad) {
-                    rscale = a.row_scale[row];
+                    m = a.row_scale[row] != 0.f ? a.grad_mul : 0.f;
                     nlseL = -a.lse[row] * ce::kLog2e;
                 }
             }
+            const float sc = a.out_scale ? *a.out_scale : 1.f;
+            const bool f16 = a.f16 != 0;
             StatAcc st;
             st.mx = -INFINITY;
             st.idx = INT_MAX;
@@ -469,11 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nvalid <= 0 || !row_ok) continue;
                 switch (P.mode) {
                     case kStats: stats_chunk(a, P, v, cbase, nvalid, st, y); break;
-                    case kGrad: grad_chunk(a, P, v, row, cbase, nvalid, y, rscale, nlseL); break;
-                    case kStoreF32: store_chunk<kStoreF32>(P, v, row, cbase, nvalid); break;
-                    case kAccF32: store_chunk<kAccF32>(P, v, row, cbase, nvalid); break;
-                    case kStoreBF16: store_chunk<kStoreBF16>(P, v, row, cbase, nvalid); break;
-                    default: store_chunk<kAccToBF16>(P, v, row, cbase, nvalid); break;
+                    case kGrad: grad_chunk(a, P, v, row, cbase, nvalid, y, m, nlseL); break;
+                    case kStoreF32: store_chunk<kStoreF32>(P, v, row, cbase, nvalid, sc, f16); break;
+                    case kAccF32: store_chunk<kAccF32>(P, v, row, cbase, nvalid, sc, f16); break;
+                    case kStoreBF16: store_chunk<kStoreBF16>(P, v, row, cbase, nvalid, sc, f16); break;
+                    default: store_chunk<kAccToBF16>(P, v, row, cbase, nvalid, sc, f16); break;
                 }
             }
             if (P.mode == kStats && row_ok) {

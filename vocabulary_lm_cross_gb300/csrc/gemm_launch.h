@@ -13,11 +13,11 @@ namespace vlmce {
 namespace gemm {
 
 // Tensor map of operand A (rows = M) or B (is_b, rows = N) of C = A B^T,
-// bf16: K-major ([rows, ld], K contiguous) or MN-major ([K, ld], rows
-// contiguous).  Out-of-range elements read as zero.  False if the driver
-// refuses it.
+// bf16 (fp16 with f16): K-major ([rows, ld], K contiguous) or MN-major
+// ([K, ld], rows contiguous).  Out-of-range elements read as zero.  False if
+// the driver refuses it.
 bool make_operand_map(CUtensorMap *m, const void *base, bool is_b, bool mn, int64_t rows,
-                      int64_t K, int64_t ld);
+                      int64_t K, int64_t ld, bool f16 = false);
 
 // Fill p.mt / p.tile0 / a.tiles from the problems' shapes and launch them on
 // `s` as one persistent grid of clusters of one or two CTA pairs (a.nprob

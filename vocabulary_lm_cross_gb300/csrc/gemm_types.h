@@ -28,9 +28,9 @@ enum Mode : int {
     kStoreF32 = 0,   // C = acc (fp32)
     kAccF32 = 1,     // C += acc (fp32)
     kStats = 2,      // row statistics of the logits tile (fused linear CE, pass 1)
-    kGrad = 3,       // gradient tile G = scale (p - q) (1 - t^2) -> bf16 (pass 2)
-    kStoreBF16 = 4,  // C16 = bf16(acc)
-    kAccToBF16 = 5,  // C16 = bf16(C + acc)
+    kGrad = 3,       // gradient tile (p - q) (1 - t^2) grad_mul -> 16-bit (pass 2)
+    kStoreBF16 = 4,  // C16 = 16-bit(acc)
+    kAccToBF16 = 5,  // C16 = 16-bit(C + acc)
 };
 
 // One product of a launch.
@@ -42,7 +42,7 @@ struct Problem {
     int tile0;                 // number of the problem's first tile in the launch
     float *C;                  // fp32 [M, ldc]
     int64_t ldc;
-    __nv_bfloat16 *C16;        // bf16 [M, ldc16]
+    uint16_t *C16;             // bf16 or fp16 (Params::f16) [M, ldc16]
     int64_t ldc16;
     int col0;                  // kStats / kGrad: vocabulary column of n = 0
     ce::RowPart *part;         // kStats: part[n_tile * part_ld + row]
@@ -59,7 +59,10 @@ struct Params {
     int V;                     // vocabulary size
     float eps, T, k2;          // smoothing, softcap (0 = off), -2 log2e / T
     const float *lse;          // kGrad: [M]
-    const float *row_scale;    // kGrad: [M] scale of a valid row, 0 otherwise
+    const float *row_scale;    // kGrad: [M] nonzero for a valid row, 0 otherwise
+    float grad_mul;            // kGrad: power of two the stored tile is multiplied by
+    const float *out_scale;    // store modes: the accumulator is multiplied by *out_scale (null: 1)
+    int f16;                   // operands and 16-bit outputs are fp16 (else bf16)
     int *err;                  // device error word (may be null)
 };
 

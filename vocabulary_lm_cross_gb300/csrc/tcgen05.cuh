@@ -123,12 +123,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B, fp32 D,
-// M x N tile; a_mn / b_mn: operand stored M- (N-) major instead of K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor of tcgen05.mma.kind::f16: bf16 (or, with f16, fp16)
+// A and B, fp32 D, M x N tile; a_mn / b_mn: operand stored M- (N-) major
+// instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn,
+                                                      bool f16 = false) {
     return (1u << 4)                                    // D format: f32
-           | (1u << 7)                                  // A format: bf16
-           | (1u << 10)                                 // B format: bf16
+           | (static_cast<uint32_t>(!f16) << 7)         // A format: bf16 (1) or f16 (0)
+           | (static_cast<uint32_t>(!f16) << 10)        // B format: bf16 (1) or f16 (0)
            | (static_cast<uint32_t>(a_mn) << 15)        // A major
            | (static_cast<uint32_t>(b_mn) << 16)        // B major
            | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8

@@ -21,7 +21,7 @@ class FLCEResult:
     argmax: torch.Tensor       # int64 [N]
     reduced: torch.Tensor      # fp32 [2]: reduced loss, token accuracy
     counts: torch.Tensor       # int64 [4]: n_valid, n_correct, n_bad_labels, device error bits
-    grad_hidden: torch.Tensor  # bf16 [N, H]: gradient with respect to h' = m h
+    grad_hidden: torch.Tensor  # [N, H] in the input dtype: gradient with respect to h' = m h
     grad_weight: torch.Tensor  # fp32 [V, H]
 
 
@@ -41,8 +41,9 @@ def flce_fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tenso
     labels: int64 CUDA [N].  grad_weight (fp32 [V, H], contiguous) is
     allocated unless given; with accumulate_grad_weight it is added to.
     """
-    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
-        raise TypeError("flce_fwd_bwd takes bf16 hidden states and weight")
+    dtypes = {torch.bfloat16: capi.BF16, torch.float16: capi.F16}
+    if hidden.dtype not in dtypes or weight.dtype != hidden.dtype:
+        raise TypeError("flce_fwd_bwd takes bf16 or fp16 hidden states and weight of one dtype")
     if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
         raise ValueError("hidden must be [N, H] and weight [V, H]")
     if labels.dtype != torch.int64 or labels.shape != (hidden.shape[0],):
@@ -60,7 +61,7 @@ def flce_fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tenso
             grad_weight.dtype != torch.float32:
         raise ValueError("grad_weight must be a contiguous fp32 [V, H] tensor")
     hs = hidden.stride(0) if N > 1 else H
-    grad_hidden = torch.empty_strided((N, H), (hs, 1), dtype=torch.bfloat16, device=dev)
+    grad_hidden = torch.empty_strided((N, H), (hs, 1), dtype=hidden.dtype, device=dev)
     res = FLCEResult(loss=torch.empty(N, dtype=torch.float32, device=dev),
                      argmax=torch.empty(N, dtype=torch.int64, device=dev),
                      reduced=torch.empty(2, dtype=torch.float32, device=dev),
@@ -71,8 +72,9 @@ def flce_fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tenso
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-    st = capi.lib().flce_fwd_bwd(
-        hidden.data_ptr(), hs, weight.data_ptr(), weight.stride(0) if V > 1 else H,
+    st = capi.lib().flce_fwd_bwd_ex(
+        hidden.data_ptr(), dtypes[hidden.dtype], hs, weight.data_ptr(),
+        weight.stride(0) if V > 1 else H,
         labels.data_ptr(), N, H, V, ignore_index, float(label_smoothing), float(softcap),
         _REDUCTIONS[reduction], float(grad_scale), res.loss.data_ptr(), res.argmax.data_ptr(),
         res.reduced.data_ptr(), res.counts.data_ptr(), grad_hidden.data_ptr(),

@@ -84,14 +84,15 @@ class FLCEWorkload:
     reduction: str
     grad_scale: float
     seed: int
+    dtype: str = "bf16"        # "bf16" | "f16": hidden states, weight, grad_hidden
 
     @property
     def algorithmic_flops(self) -> int:
         """6 N V H: the logits GEMM and the two gradient GEMMs."""
         return 6 * self.N * self.V * self.H
 
-    def resized(self, N=None, H=None, V=None, seed=None) -> "FLCEWorkload":
-        kw = {k: v for k, v in dict(N=N, H=H, V=V, seed=seed).items() if v is not None}
+    def resized(self, N=None, H=None, V=None, seed=None, dtype=None) -> "FLCEWorkload":
+        kw = {k: v for k, v in dict(N=N, H=H, V=V, seed=seed, dtype=dtype).items() if v is not None}
         return replace(self, **kw)
 
 
@@ -192,24 +193,25 @@ def make_ce_inputs(w: CEWorkload, device="cpu"):
 
 
 def make_flce_inputs(w: FLCEWorkload, device="cpu"):
-    """(hidden, weight, labels): hidden bf16 [N, H] already multiplied by m
-    (exact for m = 0.5), weight bf16 [V, H], labels int64 [N] with exactly
-    round(ignore_frac N) ignored rows."""
+    """(hidden, weight, labels): hidden [N, H] in w.dtype (bf16 or fp16),
+    already multiplied by m (exact for m = 0.5), weight [V, H] in w.dtype,
+    labels int64 [N] with exactly round(ignore_frac N) ignored rows."""
     dev = torch.device(device)
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed)
     cg = _cpu_gen(w.seed + 7919)
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     h = torch.randn((w.N, w.H), generator=g, device=dev, dtype=torch.float32)
     h.mul_(w.hidden_sigma)
-    hb = h.to(torch.bfloat16)
+    hb = h.to(dt)
     del h
     hb.mul_(w.multiplier)
-    W = torch.empty((w.V, w.H), device=dev, dtype=torch.bfloat16)
+    W = torch.empty((w.V, w.H), device=dev, dtype=dt)
     chunk = max(1, (1 << 28) // max(1, w.H))
     for v0 in range(0, w.V, chunk):
         v1 = min(w.V, v0 + chunk)
         t = torch.randn((v1 - v0, w.H), generator=g, device=dev, dtype=torch.float32)
-        W[v0:v1] = (t * w.weight_sigma).to(torch.bfloat16)
+        W[v0:v1] = (t * w.weight_sigma).to(dt)
     labels = torch.randint(0, w.V, (w.N,), generator=g, device=dev, dtype=torch.int64)
     n_ign = int(round(w.ignore_frac * w.N))
     if n_ign:
