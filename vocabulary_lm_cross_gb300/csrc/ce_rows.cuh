@@ -12,6 +12,8 @@
 // L2.  The label census of the call is only needed by pass 2, so the kernel
 // waits for it (programmatic dependent launch) after pass 1.
 //
+// Pass 1 keeps two 16-byte loads in flight per thread, enough outstanding
+// bytes per SM to cover the DRAM latency.
 // The kernel is bound by instruction issue, so the inner loops run over whole
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
@@ -226,7 +228,16 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     a.nmL = INFINITY;
     a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
     if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, T, k2);
-    for (int gl = gs + tid; gl < ge; gl += THREADS)
+    // two granules in flight per thread (the loads of a warp would otherwise
+    // leave too few bytes outstanding to cover the DRAM latency); the folds
+    // keep the thread's column order
+    int gl = gs + tid;
+    for (; gl + THREADS < ge; gl += 2 * THREADS) {
+        const uint4 w0 = ld_v4(row + gl), w1 = ld_v4(row + gl + THREADS);
+        fold_full<BF16, SOFTCAP, SUMZ>(a, w0, gl * EPG - lead, p.V, T, k2);
+        fold_full<BF16, SOFTCAP, SUMZ>(a, w1, (gl + THREADS) * EPG - lead, p.V, T, k2);
+    }
+    for (; gl < ge; gl += THREADS)
         fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
     if (tid == tail_tid)
         fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, T, k2);

@@ -110,7 +110,14 @@ __global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
     a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
     if (g.head && tid == 0)
         rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, T, k2);
-    for (int gl = g.gs + tid; gl < g.ge; gl += THREADS)
+    int gl = g.gs + tid;
+    for (; gl + THREADS < g.ge; gl += 2 * THREADS) {  // two loads in flight, column order kept
+        const uint4 w0 = rows::ld_v4(g.row() + gl), w1 = rows::ld_v4(g.row() + gl + THREADS);
+        rows::fold_full<BF16, SOFTCAP, true>(a, w0, gl * EPG - g.lead, p.V_local, T, k2);
+        rows::fold_full<BF16, SOFTCAP, true>(a, w1, (gl + THREADS) * EPG - g.lead, p.V_local, T,
+                                             k2);
+    }
+    for (; gl < g.ge; gl += THREADS)
         rows::fold_full<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row() + gl), gl * EPG - g.lead,
                                              p.V_local, T, k2);
     if (tid == g.tail_tid)
