@@ -54,12 +54,15 @@ def test_per_token_upstream_gradients(monkeypatch, path, N, V, dtype, T, eps, re
 
 
 @pytest.mark.parametrize("path", ["rows", "split"])
-@pytest.mark.parametrize("dtype,T,eps,red", [("bf16", 0.0, 0.1, "mean"), ("f32", 30.0, 0.0, "sum"),
-                                             ("bf16", 5.0, 0.2, "none")])
+@pytest.mark.parametrize("dtype,T,eps,red,V,stride", [
+    ("bf16", 0.0, 0.1, "mean", 20011, 20016), ("f32", 30.0, 0.0, "sum", 20011, 20016),
+    ("bf16", 5.0, 0.2, "none", 20011, 20016),
+    ("bf16", 30.0, 0.1, "sum", 70001, 70008),  # wide softcap rows (row kernel)
+])
 def test_forward_only_leaves_the_logits_and_matches_the_full_call(monkeypatch, path, dtype, T, eps,
-                                                                  red):
+                                                                  red, V, stride):
     monkeypatch.setenv("VLMCE_CE_PATH", path)
-    w = wl(100, 20011, dtype, T, eps, red, seed=7, stride=20016)
+    w = wl(100, V, dtype, T, eps, red, seed=7, stride=stride)
     x0, lab = make_ce_inputs(w, device=DEV)
     iv = torch.int16 if dtype == "bf16" else torch.int32
     xf = x0.clone()

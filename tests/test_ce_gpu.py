@@ -102,6 +102,23 @@ def test_small_grid_strided_unaligned_rows(dtype, V, stride, T, eps, red, path, 
                   monkeypatch=monkeypatch)
 
 
+# Wide softcap rows on the row kernel (256-thread CTAs, more than 8192 16-byte
+# granules per row): rows on and off the 16-byte grid, ragged tails, ignored
+# rows, boosted labels and duplicate maxima far apart in the row.
+@pytest.mark.parametrize("dtype,V,stride", [("bf16", 65537, 65537), ("bf16", 65543, 65547),
+                                            ("bf16", 151936, 152064), ("f32", 32769, 32771),
+                                            ("f32", 40000, 40001)])
+@pytest.mark.parametrize("T,eps,red", [(30.0, 0.1, "sum"), (5.0, 0.0, "mean")])
+def test_wide_softcap_rows(dtype, V, stride, T, eps, red, monkeypatch):
+    w = small(13, V, dtype, stride=stride, eps=eps, T=T, reduction=red, gs=0.37, sigma=8.0,
+              boost=4.0, dup=0.3)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    monkeypatch.setenv("VLMCE_CE_PATH", "rows")  # few rows would otherwise take the V-split kernel
+    pl = v.describe_plan(w.N, V, dt, T, aligned_rows=(stride * dt.itemsize) % 16 == 0)
+    assert pl["kernel"] == "rows" and pl["threads"] == 256, pl
+    run_and_check(w)
+
+
 @pytest.mark.parametrize("k", ["1", "2", "3", "5", "8"])
 def test_every_cluster_shape_agrees(k, monkeypatch):
     w = small(23, 20000, "bf16", stride=20003, eps=0.1, T=30.0, boost=4.0, dup=0.2)
@@ -121,6 +138,7 @@ def test_plans_of_the_benchmarked_workloads():
         pl = v.describe_plan(w.N, w.V, dt, w.softcap)
         assert pl["ctas_per_row"] * pl["granules_per_cta"] * (8 if w.dtype == "bf16" else 4) >= w.V
         assert pl["kernel"] == "rows" and pl["resident"] >= 1, (name, pl)
+        assert pl["ctas_per_row"] == 1 and pl["threads"] in (256, 1024), (name, pl)
         print(name, pl)
 
 

@@ -37,6 +37,8 @@ def bits(t):
     (700, 65536, 65544, "bf16", 0.0, 0.1, "mean"),     # 3 chunks of 256 rows, last ragged
     (2100, 32768, 32768, "bf16", 30.0, 0.0, "sum"),    # 5 chunks through 3 slots
     (600, 20000, 20004, "f32", 0.0, 0.0, "mean"),      # 2 chunks, fp32
+    (60, 70001, 70007, "bf16", 30.0, 0.1, "sum"),      # wide softcap rows on 256-thread CTAs
+    (600, 40000, 40000, "f32", 30.0, 0.0, "mean"),     # the same, 3 chunks, fp32
 ])
 def test_host_results_equal_device_results(monkeypatch, N, V, stride, dtype, T, eps, red):
     monkeypatch.setenv("VLMCE_CE_PATH", "rows")  # the kernel the host path uses

@@ -167,6 +167,24 @@ bool use_split(int64_t N, int64_t G, const DeviceInfo &d) {
     return N < d.sm_count && G >= 4 * split::kChunkGranules && G <= cap;
 }
 
+// Launch the row kernel over N <= INT_MAX rows, one CTA per row, after the
+// previous launch on the stream when pdl is set (programmatic dependent
+// launch: the kernel waits for it before pass 2).
+vlmce_status launch_rows(rows::Kernel kern, const rows::Params &p, int64_t N, int threads, bool pdl,
+                         cudaStream_t cs) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(N), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = cs;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, p), "ce_rows_kernel");
+}
+
 thread_local cudaEvent_t t_prof_begin = nullptr;
 thread_local cudaEvent_t t_prof_end = nullptr;
 
@@ -208,9 +226,9 @@ extern "C" int32_t vlmce_ce_describe_plan(int64_t N, int64_t V, int32_t dtype, f
         out[5] = split::kSmemBytes;
     } else {
         out[0] = 0;
+        const int th = rows::threads_for(G, softcap > 0.f);
         out[1] = 1;
         out[2] = static_cast<int32_t>(G);
-        const int th = rows::threads_for(G);
         out[3] = rows::min_blocks(th, softcap > 0.f) * dev.sm_count;
         out[4] = th;
         out[5] = 0;
@@ -339,18 +357,9 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
             p.counts = w.counts;
             p.token_scale = token_scale;
             p.want_grad = want_grad ? 1 : 0;
-            const int th = rows::threads_for(G);
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(N), 1, 1);
-            cfg.blockDim = dim3(th, 1, 1);
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = cs;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            st = launch_status(cudaLaunchKernelEx(&cfg, bf16 ? rows::kernel_bf16(capped, th)
-                                                             : rows::kernel_f32(capped, th),
-                                                  p),
-                               "ce_rows_kernel");
+            const int th = rows::threads_for(G, capped);
+            st = launch_rows(bf16 ? rows::kernel_bf16(capped, th) : rows::kernel_f32(capped, th), p,
+                             N, th, true, cs);
         }
         if (st != VLMCE_OK) return st;
         if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
@@ -542,7 +551,7 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
 
     // the CTA size ce_fwd_bwd would pick for these rows (the same arithmetic order)
     const int th = rows::threads_for(
-        rows::row_granules(bf16, V, rows::rows_aligned(host_logits, row_stride, elt)));
+        rows::row_granules(bf16, V, rows::rows_aligned(host_logits, row_stride, elt)), softcap > 0.f);
     const rows::Kernel kern =
         bf16 ? rows::kernel_bf16(softcap > 0.f, th) : rows::kernel_f32(softcap > 0.f, th);
     const int64_t nchunks = N > 0 ? (N + R - 1) / R : 0;
@@ -580,8 +589,7 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
         p.counts = w.counts;
         p.token_scale = nullptr;
         p.want_grad = 1;
-        kern<<<static_cast<unsigned>(rows_i), th, 0, cs>>>(p);
-        if ((st = launch_status(cudaSuccess, "ce_rows_kernel")) != VLMCE_OK) return st;
+        if ((st = launch_rows(kern, p, rows_i, th, false, cs)) != VLMCE_OK) return st;
         if ((st = fail(cudaEventRecord(hp->computed[b], cs), "cudaEventRecord")) != VLMCE_OK) return st;
         // copy the gradient columns [0, V) of each row back
         if ((st = fail(cudaStreamWaitEvent(hp->out, hp->computed[b], 0), "cudaStreamWaitEvent")) !=

@@ -122,6 +122,45 @@ __device__ __forceinline__ Capped softcap_z(float x, float T, float neg2_log2e_o
     }
 }
 
+// The same softcap, two columns at a time, for the memory-bound row kernels,
+// which are bound by instruction issue and the MUFU unit when a softcap is
+// set.  a = exp(-2|x|/T) is the one MUFU op; r = 1/(1 + a) is formed in packed
+// fp32x2 arithmetic on the FMA pipe (one issue slot per two columns) by
+// Newton-type steps from the minimax line of 1/d on d = 1 + a in [1, 2]:
+//   r0 = 16/17 - (8/17) a                   |1 - d r0| <= 1/17
+//   r1 = r0 (1 + e + e^2),  e = 1 - d r0     |1 - d r1| = |e|^3 <= 2.1e-4
+//   r2 = r1 (1 + e),        e = 1 - d r1     |1 - d r2| = e^2  <= 4.2e-8
+// (plus the rounding of the last FMA): about one ulp, like the MUFU
+// reciprocal.  tanh(|x|/T) = (1 - a) r with 1 - a exact for a >= 1/2, and
+// 1 - tanh^2 = 4 a r^2.
+struct Cap2 {
+    uint64_t t;    // tanh(x/T) of the two columns, with the sign of x
+    uint64_t ar2;  // a r^2 of the two columns (dz/dx = 4 a r^2)
+};
+__device__ __forceinline__ Cap2 softcap2(float x0, float x1, float neg2_log2e_over_T) {
+    const uint64_t a = pk(ptx::ex2(fabsf(x0) * neg2_log2e_over_T),
+                          ptx::ex2(fabsf(x1) * neg2_log2e_over_T));
+    const uint64_t one = pk(1.f, 1.f), m_one = pk(-1.f, -1.f);
+    const uint64_t nd = fma2(a, m_one, m_one);  // -(1 + a)
+    uint64_t r = fma2(a, pk(-8.f / 17.f, -8.f / 17.f), pk(16.f / 17.f, 16.f / 17.f));
+    uint64_t e = fma2(nd, r, one);
+    r = fma2(r, fma2(e, e, e), r);
+    e = fma2(nd, r, one);
+    r = fma2(r, e, r);
+    float t0, t1;
+    upk(mul2(fma2(a, m_one, one), r), t0, t1);  // (1 - a) r
+    Cap2 c;
+    c.t = pk(copysignf(t0, x0), copysignf(t1, x1));
+    c.ar2 = mul2(mul2(a, r), r);
+    return c;
+}
+// tanh(x/T) of one column, by the same arithmetic as softcap2.
+__device__ __forceinline__ float softcap_t1(float x, float neg2_log2e_over_T) {
+    float t0, t1;
+    upk(softcap2(x, x, neg2_log2e_over_T).t, t0, t1);
+    return t0;
+}
+
 template <bool BF16>
 __device__ __forceinline__ void unpack(const uint4 w, float (&x)[Elem<BF16>::kPerGranule]) {
     if constexpr (BF16) {

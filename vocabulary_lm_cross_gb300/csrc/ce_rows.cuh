@@ -35,9 +35,9 @@ constexpr int kThreads = 1024;
 constexpr int kShortThreads = 256;
 constexpr int kShortGranules = 8192;
 // CTAs per SM the launch bounds ask for (the softcap variants need more
-// registers per thread).
+// registers per thread: 48 at five 256-thread CTAs per SM).
 constexpr int min_blocks(int threads, bool softcap) {
-    return threads == kThreads ? (softcap ? 1 : 2) : (softcap ? 4 : 8);
+    return threads == kThreads ? (softcap ? 1 : 2) : (softcap ? 5 : 8);
 }
 
 struct Params {
@@ -67,15 +67,48 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
     return v;
 }
 
-// Pass-1 state of one thread.
+// Pass-1 state of one thread.  The sums run over even and odd columns in
+// the two halves of packed fp32x2 registers.
 struct Acc {
-    float mv;      // max raw logit seen
-    int midx;      // its first column
-    float mz;      // z of mv: reference of s
-    float nmL;     // -mz log2e
-    float s0, s1;  // sums of exp(z - mz) (even, odd columns)
-    float z0, z1;  // sums of z
+    float mv;    // max raw logit seen
+    int midx;    // its first column
+    float mz;    // z of mv: reference of s
+    float nmL;   // -mz log2e
+    uint64_t s;  // sums of exp(z - mz) (even, odd columns)
+    uint64_t z;  // sums of z, or of tanh(x/T) when a softcap is set (even, odd columns)
 };
+
+__device__ __forceinline__ void acc_init(Acc &a) {
+    a.mv = -INFINITY;
+    a.midx = INT_MAX;
+    a.mz = -INFINITY;
+    a.nmL = INFINITY;
+    a.s = a.z = pk(0.f, 0.f);
+}
+
+// The thread's statistics as a RowPart (sum of z scaled back by T under a softcap).
+template <bool SOFTCAP>
+__device__ __forceinline__ RowPart acc_part(const Acc &a, float T) {
+    RowPart pt = part_identity();
+    float s0, s1, z0, z1;
+    upk(a.s, s0, s1);
+    upk(a.z, z0, z1);
+    pt.mx = a.mv;
+    pt.idx = a.midx;
+    pt.mz = a.mz;
+    pt.s = s0 + s1;
+    pt.sz = SOFTCAP ? T * (z0 + z1) : z0 + z1;
+    return pt;
+}
+
+// z of one column: the logit, or T tanh(x/T) under a softcap.
+template <bool SOFTCAP>
+__device__ __forceinline__ float z_of(float x, float T, float k2) {
+    if constexpr (SOFTCAP)
+        return T * softcap_t1(x, k2);
+    else
+        return x;
+}
 
 // New maximum gm in the granule starting at column jg: locate its first
 // column among the valid ones, rescale the running sums.
@@ -87,17 +120,21 @@ __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPe
 #pragma unroll
     for (int l = EPG - 1; l >= 0; --l)
         if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
-    const float nz = softcap_z<SOFTCAP>(gm, T, k2).z;
+    const float nz = z_of<SOFTCAP>(gm, T, k2);
     const float f = ptx::ex2((a.mz - nz) * kLog2e);
-    a.s0 = (a.s0 == 0.f) ? 0.f : a.s0 * f;
-    a.s1 = (a.s1 == 0.f) ? 0.f : a.s1 * f;
+    float s0, s1;
+    upk(a.s, s0, s1);
+    s0 = (s0 == 0.f) ? 0.f : s0 * f;
+    s1 = (s1 == 0.f) ? 0.f : s1 * f;
+    a.s = pk(s0, s1);
     a.mv = gm;
     a.midx = jg + li;
     a.mz = nz;
     a.nmL = -nz * kLog2e;
 }
 
-// Fold a whole granule (every column valid).
+// Fold a whole granule (every column valid), two columns per packed op.
+// Under a softcap the exponent is t (T log2e) - mz log2e with t = tanh(x/T).
 template <bool BF16, bool SOFTCAP, bool SUMZ>
 __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, float T, float k2) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
@@ -105,20 +142,21 @@ __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, 
     unpack<BF16>(w, x);
     const float gm = granule_max<BF16>(w);
     if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, T, k2);
+    const float L = SOFTCAP ? T * kLog2e : kLog2e;
+    const uint64_t L2 = pk(L, L), nmL2 = pk(a.nmL, a.nmL);
 #pragma unroll
     for (int l = 0; l < EPG; l += 2) {
-        const float za = softcap_z<SOFTCAP>(x[l], T, k2).z;
-        const float zb = softcap_z<SOFTCAP>(x[l + 1], T, k2).z;
-        a.s0 += ptx::ex2(fmaf(za, kLog2e, a.nmL));
-        a.s1 += ptx::ex2(fmaf(zb, kLog2e, a.nmL));
-        if constexpr (SUMZ) {
-            a.z0 += za;
-            a.z1 += zb;
-        }
+        uint64_t v;
+        if constexpr (SOFTCAP)
+            v = softcap2(x[l], x[l + 1], k2).t;
+        else
+            v = pk(x[l], x[l + 1]);
+        a.s = add2(a.s, ex2x2(fma2(v, L2, nmL2)));
+        if constexpr (SUMZ) a.z = add2(a.z, v);
     }
 }
 
-// Fold a granule of which only the columns in [0, V) count.
+// Fold a granule of which only the columns in [0, V) count (into the even sums).
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int V, float T,
                                              float k2) {
@@ -130,14 +168,20 @@ __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int 
     for (int l = 0; l < EPG; ++l)
         if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
     if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, T, k2);
+    const float L = SOFTCAP ? T * kLog2e : kLog2e;
+    float s0, s1, z0, z1;
+    upk(a.s, s0, s1);
+    upk(a.z, z0, z1);
 #pragma unroll
     for (int l = 0; l < EPG; ++l) {
         if (jg + l >= 0 && jg + l < V) {
-            const float z = softcap_z<SOFTCAP>(x[l], T, k2).z;
-            a.s0 += ptx::ex2(fmaf(z, kLog2e, a.nmL));
-            a.z0 += z;
+            const float v = SOFTCAP ? softcap_t1(x[l], k2) : x[l];
+            s0 += ptx::ex2(fmaf(v, L, a.nmL));
+            z0 += v;
         }
     }
+    a.s = pk(s0, s1);
+    a.z = pk(z0, z1);
 }
 
 struct GradCoef {
@@ -148,28 +192,46 @@ struct GradCoef {
     float T, k2;     // softcap and -2 log2e / T
 };
 
-// Gradients of the EPG elements of a granule, in fp32.
+// Gradients of the EPG elements of a granule, in fp32, two per packed op.
+// Under a softcap g = 4 scale (p - q) a r^2 (the factor 4 of dz/dx = 4 a r^2
+// is folded into the coefficients, exactly).
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, int label_lane,
                                             float (&g)[Elem<BF16>::kPerGranule]) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
+    const float L = SOFTCAP ? c.T * kLog2e : kLog2e;
+    const float f = SOFTCAP ? 4.f : 1.f;
+    const uint64_t L2 = pk(L, L), nlseL2 = pk(c.nlseL, c.nlseL);
+    const uint64_t scale2 = pk(f * c.scale, f * c.scale);
+    const uint64_t nc2 = pk(-f * c.c_smooth, -f * c.c_smooth);
 #pragma unroll
-    for (int l = 0; l < EPG; ++l) {
-        const Capped cz = softcap_z<SOFTCAP>(x[l], c.T, c.k2);
-        const float pr = ptx::ex2(fmaf(cz.z, kLog2e, c.nlseL));  // p_j
-        g[l] = fmaf(pr, c.scale, -c.c_smooth);                   // scale (p_j - eps/V)
-        if constexpr (SOFTCAP) g[l] *= cz.dz;
+    for (int l = 0; l < EPG; l += 2) {
+        uint64_t g2;
+        if constexpr (SOFTCAP) {
+            const Cap2 cz = softcap2(x[l], x[l + 1], c.k2);
+            g2 = mul2(fma2(ex2x2(fma2(cz.t, L2, nlseL2)), scale2, nc2), cz.ar2);
+        } else {
+            g2 = fma2(ex2x2(fma2(pk(x[l], x[l + 1]), L2, nlseL2)), scale2, nc2);
+        }
+        upk(g2, g[l], g[l + 1]);
     }
     if (label_lane >= 0) {  // the label column: q_y = 1 - eps + eps/V (rare)
 #pragma unroll
         for (int l = 0; l < EPG; ++l) {
             if (l == label_lane) {
-                const Capped cz = softcap_z<SOFTCAP>(x[l], c.T, c.k2);
-                const float pr = ptx::ex2(fmaf(cz.z, kLog2e, c.nlseL));
-                g[l] = fmaf(pr, c.scale, -c.c_label);
-                if constexpr (SOFTCAP) g[l] *= cz.dz;
+                if constexpr (SOFTCAP) {
+                    const Cap2 cz = softcap2(x[l], x[l], c.k2);
+                    float t, t_, ar2, ar2_;
+                    upk(cz.t, t, t_);
+                    upk(cz.ar2, ar2, ar2_);
+                    const float pr = ptx::ex2(fmaf(t, L, c.nlseL));
+                    g[l] = fmaf(pr, f * c.scale, -f * c.c_label) * ar2;
+                } else {
+                    const float pr = ptx::ex2(fmaf(x[l], L, c.nlseL));
+                    g[l] = fmaf(pr, c.scale, -c.c_label);
+                }
             }
         }
     }
@@ -222,11 +284,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
 
     // ---- pass 1
     Acc a;
-    a.mv = -INFINITY;
-    a.midx = INT_MAX;
-    a.mz = -INFINITY;
-    a.nmL = INFINITY;
-    a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
+    acc_init(a);
     if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, T, k2);
     // two granules in flight per thread (the loads of a warp would otherwise
     // leave too few bytes outstanding to cover the DRAM latency); the folds
@@ -242,12 +300,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     if (tid == tail_tid)
         fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, T, k2);
 
-    RowPart pt = part_identity();
-    pt.mx = a.mv;
-    pt.idx = a.midx;
-    pt.mz = a.mz;
-    pt.s = a.s0 + a.s1;
-    pt.sz = a.z0 + a.z1;
+    RowPart pt = acc_part<SOFTCAP>(a, T);
     warp_allreduce(pt);
     if (lane == 0) wpart[warp] = pt;
 
@@ -268,7 +321,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
                     xy = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
                 else
                     xy = *reinterpret_cast<const float *>(py);
-                const float zy = softcap_z<SOFTCAP>(xy, T, k2).z;
+                const float zy = z_of<SOFTCAP>(xy, T, k2);
                 l = lse - fmaf(1.f - p.eps, zy, (p.eps / static_cast<float>(p.V)) * q.sz);
             } else if (!ignored) {
                 l = __int_as_float(0x7fc00000);  // bad label: NaN
@@ -322,8 +375,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
 }
 
 // Long rows: two CTAs of 1024 threads per SM (32 registers per thread); short
-// rows: eight CTAs of 256.  The softcap's extra arithmetic needs more
-// registers, so its kernels run a quarter as many CTAs per SM.
+// rows: eight CTAs of 256.  Softcap rows: 256-thread CTAs, five per SM (48
+// registers).
 template <bool BF16, bool SOFTCAP, int THREADS>
 __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
     __shared__ RowPart wpart[THREADS / 32];
@@ -345,9 +398,13 @@ inline bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
     return (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ((row_stride * elt) % 16) == 0;
 }
 
-// CTA size of the row kernel for rows of G granules.
-inline int threads_for(int64_t G) { return G <= kShortGranules ? kShortThreads : kThreads; }
-
+// CTA size of the row kernel for rows of G granules (with or without a softcap).
+// Softcap rows always take 256-thread CTAs: five of them per SM keep more
+// warps resident than one CTA of 1024 at 64 registers, and their barriers
+// stall fewer warps at a time.
+inline int threads_for(int64_t G, bool softcap) {
+    return (softcap || G <= kShortGranules) ? kShortThreads : kThreads;
+}
 // The row kernel for the given softcap and CTA size, per element type
 // (ce_rows_bf16.cu, ce_rows_f32.cu).
 Kernel kernel_bf16(bool softcap, int threads);

@@ -92,8 +92,14 @@ __device__ __forceinline__ float load_x(uintptr_t a0, int64_t col) {
         return *reinterpret_cast<const float *>(py);
 }
 
+// CTAs per SM of the shard kernels: as the row kernel's, but four 256-thread
+// softcap CTAs (the shard bookkeeping needs more than 48 registers there).
+constexpr int min_blocks(int threads, bool softcap) {
+    return (softcap && threads == rows::kShortThreads) ? 4 : rows::min_blocks(threads, softcap);
+}
+
 template <bool BF16, bool SOFTCAP, int THREADS>
-__global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
+__global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     ce_shard_stats_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int kWarps = THREADS / 32;
@@ -103,11 +109,7 @@ __global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
     rows::Acc a;
-    a.mv = -INFINITY;
-    a.midx = INT_MAX;
-    a.mz = -INFINITY;
-    a.nmL = INFINITY;
-    a.s0 = a.s1 = a.z0 = a.z1 = 0.f;
+    rows::acc_init(a);
     if (g.head && tid == 0)
         rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, T, k2);
     int gl = g.gs + tid;
@@ -123,12 +125,7 @@ __global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
     if (tid == g.tail_tid)
         rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row() + (g.G - 1)),
                                           (g.G - 1) * EPG - g.lead, p.V_local, T, k2);
-    RowPart pt = part_identity();
-    pt.mx = a.mv;
-    pt.idx = a.midx;
-    pt.mz = a.mz;
-    pt.s = a.s0 + a.s1;
-    pt.sz = a.z0 + a.z1;
+    RowPart pt = rows::acc_part<SOFTCAP>(a, T);
     warp_allreduce(pt);
     if (lane == 0) wpart[warp] = pt;
     __syncthreads();
@@ -139,7 +136,7 @@ __global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
             const int64_t yl = p.labels[blockIdx.x] - p.vocab_start;
             q.zy = 0.f;
             if (yl >= 0 && yl < p.V_local)
-                q.zy = softcap_z<SOFTCAP>(load_x<BF16>(row_addr(p), yl), T, k2).z;
+                q.zy = rows::z_of<SOFTCAP>(load_x<BF16>(row_addr(p), yl), T, k2);
             q.idx = q.idx == INT_MAX ? INT_MAX : static_cast<int>(q.idx + p.vocab_start);
             q.pad0 = q.pad1 = 0.f;
             p.stats[blockIdx.x] = q;
@@ -162,7 +159,7 @@ __global__ void __launch_bounds__(256) ce_merge_stats_kernel(const RowPart *shar
 }
 
 template <bool BF16, bool SOFTCAP, int THREADS>
-__global__ void __launch_bounds__(THREADS, rows::min_blocks(THREADS, SOFTCAP))
+__global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     ce_shard_grad_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     const int tid = threadIdx.x;
@@ -248,10 +245,12 @@ ShardKernel grad_kernel(bool bf16, bool softcap, int threads) {
                                           : grad_kernel_t<rows::kThreads>(bf16, softcap);
 }
 // The row kernel's CTA size for the shard's rows (the same arithmetic order).
-int shard_threads(const void *logits, int32_t dtype, int64_t V_local, int64_t row_stride) {
+int shard_threads(const void *logits, int32_t dtype, int64_t V_local, int64_t row_stride,
+                  bool softcap) {
     const bool bf16 = dtype == VLMCE_BF16;
     return rows::threads_for(
-        rows::row_granules(bf16, V_local, rows::rows_aligned(logits, row_stride, bf16 ? 2 : 4)));
+        rows::row_granules(bf16, V_local, rows::rows_aligned(logits, row_stride, bf16 ? 2 : 4)),
+        softcap);
 }
 
 constexpr int64_t kMaxVocab = int64_t(1) << 28;
@@ -304,7 +303,7 @@ extern "C" vlmce_status ce_shard_stats(const void *logits, int32_t dtype, const 
     p.stride_bytes = row_stride * (dtype == VLMCE_BF16 ? 2 : 4);
     p.softcap = softcap;
     p.stats = reinterpret_cast<RowPart *>(out_stats);
-    const int th = shard_threads(logits, dtype, V_local, row_stride);
+    const int th = shard_threads(logits, dtype, V_local, row_stride, softcap > 0.f);
     stats_kernel(dtype == VLMCE_BF16, softcap > 0.f, th)
         <<<static_cast<unsigned>(N), th, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaSuccess, "ce_shard_stats_kernel");
@@ -379,7 +378,7 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
         p.loss = loss;
         p.argmax = amax;
         p.counts = counts;
-        const int th = shard_threads(logits, dtype, V_local, row_stride);
+        const int th = shard_threads(logits, dtype, V_local, row_stride, softcap > 0.f);
         grad_kernel(dtype == VLMCE_BF16, softcap > 0.f, th)
             <<<static_cast<unsigned>(N), th, 0, cs>>>(p);
         if ((st = launch_status(cudaSuccess, "ce_shard_grad_kernel")) != VLMCE_OK) return st;
