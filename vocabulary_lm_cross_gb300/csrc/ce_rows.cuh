@@ -12,8 +12,9 @@
 // L2.  The label census of the call is only needed by pass 2, so the kernel
 // waits for it (programmatic dependent launch) after pass 1.
 //
-// Pass 1 keeps two 16-byte loads in flight per thread, enough outstanding
-// bytes per SM to cover the DRAM latency.
+// Pass 1 keeps two 16-byte loads in flight per thread and prefetches the
+// pair two iterations ahead into L2, so that enough bytes are outstanding per
+// SM to cover the DRAM latency.
 // The kernel is bound by instruction issue, so the inner loops run over whole
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
@@ -281,6 +282,9 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const int tail_tid = tail ? (G - 1 - gs) % THREADS : -1;
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    // Pass 2 prefetches ahead where the rows in flight reach the size of L2:
+    // long rows, and softcap rows (five 256-thread CTAs per SM).
+    constexpr bool kPrefetch2 = SOFTCAP || THREADS == kThreads;
 
     // ---- pass 1
     Acc a;
@@ -292,6 +296,10 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     int gl = gs + tid;
     for (; gl + THREADS < ge; gl += 2 * THREADS) {
         const uint4 w0 = ld_v4(row + gl), w1 = ld_v4(row + gl + THREADS);
+        if (gl + 5 * THREADS < ge) {  // the pair two iterations ahead, into L2
+            ptx::prefetch_l2(row + gl + 4 * THREADS);
+            ptx::prefetch_l2(row + gl + 5 * THREADS);
+        }
         fold_full<BF16, SOFTCAP, SUMZ>(a, w0, gl * EPG - lead, p.V, T, k2);
         fold_full<BF16, SOFTCAP, SUMZ>(a, w1, (gl + THREADS) * EPG - lead, p.V, T, k2);
     }
@@ -356,6 +364,9 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
             store_partial<BF16>(gbase, -lead, p.V, g);
         }
         for (int gl = gs + tid; gl < ge; gl += THREADS) {
+            // the granule two iterations ahead, into L2 (where the row has
+            // partly left L2 since pass 1)
+            if (kPrefetch2 && gl + 2 * THREADS < ge) ptx::prefetch_l2(row + gl + 2 * THREADS);
             grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, gl == gy ? ly : -1, g);
             ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
         }

@@ -146,6 +146,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Prefetch the line holding p into L2 (no register result, nothing waits on it).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------- arithmetic
 // 2^x on the MUFU unit (relative error about 2^-22; subnormals flushed).
 __device__ __forceinline__ float ex2(float x) {
