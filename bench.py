@@ -444,6 +444,8 @@ def run_ours(args, w):
                 "ms_per_step": f["ms"], "steps": f["steps"], "roofline": f["roofline"],
                 "e2e": f["e2e"], "gpu_launches": f["gpu_launches"], "clocks": f["clocks"],
                 "config": f["config"], "device_status_ok": f["ok_status"]}
+        torch.cuda.empty_cache()
+        flce["row_chunked"] = run_flce_rows(fw, dev) if world == 1 else None
     sampler.stop()
 
     if rank != 0:
@@ -787,6 +789,51 @@ def run_flce(args, w, steps, dev, world, barrier, sampler):
                    "l2": "inputs larger than L2 (weight 2.69 GB streamed three times a step)"},
         "steps": steps,
     }
+
+
+def run_flce_rows(w, dev, steps=5, warmup=2, chunks=(1024, 4096)):
+    """The row-chunked schedule (flce_fwd_bwd_rows) on the same workload, timed
+    beside the vocabulary-chunked one: per block of rows the fp32 logits are
+    written once, so the executed tensor work is 6 N V H (no recompute)."""
+    import torch
+
+    import vocabulary_lm_cross_gb300 as v
+    from vocabulary_lm_cross_gb300.workloads import make_flce_inputs
+
+    h, W, lab = make_flce_inputs(w, device=dev)
+    gw = torch.empty((w.V, w.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_src = load_tensor_peak(sustained=True)
+    flops = w.algorithmic_flops
+    out = {}
+    for c in chunks:
+        ws = torch.empty(v.flce.workspace_bytes(w.N, w.H, w.V, c), dtype=torch.uint8, device=dev)
+
+        def step():
+            return v.flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                                  reduction=w.reduction, grad_scale=w.grad_scale, grad_weight=gw,
+                                  workspace=ws, chunk_rows=c)
+
+        for _ in range(warmup):
+            res = step()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            res = step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        tf = flops / (ms * 1e-3) / 1e12
+        out[f"chunk_rows_{c}"] = {
+            "ms": ms, "TFLOP/s": tf, "frac": tf / peak, "blocks": -(-w.N // c),
+            "workspace_bytes": ws.numel(), "device_status_ok": int(res.counts[3].item()) == 0}
+        del ws
+        torch.cuda.empty_cache()
+    return {"metric": "row-chunked FLCE (flce_fwd_bwd_rows) TFLOP/s of 6NVH, whole call",
+            "peak": peak, "peak_source": peak_src, "executed_flops": 6 * w.N * w.V * w.H,
+            "steps": steps, "results": out}
 
 
 def run_ours_flce(args, w):

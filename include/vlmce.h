@@ -317,6 +317,40 @@ vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64_t hidden_s
                              float *grad_weight, int32_t accumulate_grad_weight, void *workspace,
                              size_t workspace_bytes, vlmce_stream_t stream);
 
+/* Bytes of device workspace flce_fwd_bwd_rows needs (256-byte aligned): the
+ * per-token losses and argmax, the fp32 logits and the 16-bit gradient of one
+ * chunk of min(chunk_rows, N) rows, and the ce_fwd_bwd workspace of a chunk.
+ * 0 for arguments flce_fwd_bwd_rows rejects by size. */
+size_t vlmce_flce_rows_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows);
+
+/*
+ * flce_fwd_bwd_rows -- flce_fwd_bwd_ex on a row-chunked schedule instead of
+ * the vocabulary-chunked one: for each block of chunk_rows rows the logits
+ * S_k = h'_k W^T are written in fp32 to the workspace, ce_fwd_bwd_ex turns
+ * them into the block's losses, argmax and gradient in place, and two GEMMs
+ * give the block's grad_hidden and add its share to grad_weight.  The logits
+ * are formed once (tensor work 6 N V H instead of 8 N V H) at the cost of an
+ * [chunk_rows, V] fp32 logits block in device memory and a read-modify-write
+ * of the fp32 grad_weight for every block after the first.  Its precision is
+ * that of flce_fwd_bwd_ex (fp32 logits, 16-bit gradient between the products).
+ *
+ * chunk_rows   rows per block, >= 1 (VLMCE_ERR_INVALID_ARG otherwise); a value
+ *              >= N makes one block.
+ * workspace    >= vlmce_flce_rows_workspace_bytes(N, H, V, chunk_rows) bytes,
+ *              256-byte aligned.
+ * V must not exceed vlmce_ce_max_vocab(VLMCE_F32) (VLMCE_ERR_TOO_LARGE).
+ * Every other argument, result and error as flce_fwd_bwd_ex.  Deterministic.
+ */
+vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int64_t hidden_stride,
+                               const void *weight, int64_t weight_stride, const int64_t *labels,
+                               int64_t N, int64_t H, int64_t V, int64_t ignore_index,
+                               float label_smoothing, float softcap, int32_t reduction,
+                               float grad_scale, float *out_loss, int64_t *out_argmax,
+                               float *out_reduced, int64_t *out_counts, void *grad_hidden,
+                               float *grad_weight, int32_t accumulate_grad_weight,
+                               int64_t chunk_rows, void *workspace, size_t workspace_bytes,
+                               vlmce_stream_t stream);
+
 /* vlmce_gemm -- vlmce_gemm_bf16 with the operand type as an argument
  * (VLMCE_BF16 or VLMCE_F16; A and B share it). */
 vlmce_status vlmce_gemm(const void *A, int32_t a_mn, const void *B, int32_t b_mn, float *C,
@@ -337,7 +371,8 @@ vlmce_status vlmce_gemm_bf16(const void *A, int32_t a_mn, const void *B, int32_t
 
 /* Profiling hook of flce_fwd_bwd: like vlmce_profile_events, the next call on
  * this host thread records the two events around its tensor-core work (the
- * statistics GEMM, the row merge and every chunk's three GEMMs). */
+ * statistics GEMM, the row merge and every chunk's three GEMMs; for
+ * flce_fwd_bwd_rows every block's GEMMs, cross-entropy call and cast). */
 void vlmce_flce_profile_events(void *ev_begin, void *ev_end);
 
 /*

@@ -128,6 +128,44 @@ def test_ex_argument_errors_are_reported_before_any_launch(lib, gpt, kw, code):
     assert call_ex(lib, gpt, **kw) == code
 
 
+def call_flce_rows(lib, **kw):
+    a = dict(hidden=P, dtype=capi.BF16, hs=64, weight=P, ws_=64, labels=P, N=4, H=64, V=100,
+             ignore_index=-100, eps=0.0, softcap=0.0, reduction=capi.MEAN, grad_scale=1.0,
+             out_loss=P, out_argmax=P, out_reduced=P, out_counts=P, gh=P, gw=P, acc=0, chunk=2,
+             ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.flce_fwd_bwd_rows(a["hidden"], a["dtype"], a["hs"], a["weight"], a["ws_"],
+                                 a["labels"], a["N"], a["H"], a["V"], a["ignore_index"], a["eps"],
+                                 a["softcap"], a["reduction"], a["grad_scale"], a["out_loss"],
+                                 a["out_argmax"], a["out_reduced"], a["out_counts"], a["gh"],
+                                 a["gw"], a["acc"], a["chunk"], a["ws"], a["ws_bytes"],
+                                 a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk=0), capi.ERR_INVALID_ARG),
+    (dict(chunk=-3), capi.ERR_INVALID_ARG),
+    (dict(dtype=capi.F32), capi.ERR_UNSUPPORTED_DTYPE),
+    (dict(reduction=capi.NONE), capi.ERR_INVALID_ARG),
+    (dict(ws_bytes=1000), capi.ERR_WORKSPACE_TOO_SMALL),
+    (dict(ws=P + 16), capi.ERR_MISALIGNED),
+    (dict(H=60, hs=64, ws_=64), capi.ERR_MISALIGNED),
+    (dict(N=-1), capi.ERR_INVALID_ARG),
+])
+def test_flce_rows_argument_errors_are_reported_before_any_launch(lib, kw, code):
+    assert call_flce_rows(lib, **kw) == code
+
+
+def test_flce_rows_workspace_bytes(lib):
+    f = lib.vlmce_flce_rows_workspace_bytes
+    assert f(4096, 6656, 202048, 0) == 0
+    assert f(-1, 64, 100, 8) == 0
+    small, big = f(4096, 6656, 202048, 512), f(4096, 6656, 202048, 1024)
+    # the fp32 logits (4 B) and 16-bit gradient (2 B) of one block dominate
+    assert big - small >= 512 * 202048 * 6
+    assert f(4096, 6656, 202048, 1 << 20) == f(4096, 6656, 202048, 4096)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
 def test_valid_call_without_a_gpu_fails_cleanly(lib):
     st = call(lib)

@@ -98,7 +98,7 @@ def widen(t):
     return t.double().cpu().numpy() if t.dtype == torch.float16 else of.widen_bf16(bf16_bits_np(t))
 
 
-def run_small(w: FLCEWorkload, accumulate=False):
+def run_small(w: FLCEWorkload, accumulate=False, chunk_rows=None):
     h, W, lab = make_flce_inputs(w, device=DEV)
     gw0 = None
     if accumulate:
@@ -106,7 +106,7 @@ def run_small(w: FLCEWorkload, accumulate=False):
     res = flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
                        reduction=w.reduction, grad_scale=w.grad_scale,
                        grad_weight=gw0.clone() if accumulate else None,
-                       accumulate_grad_weight=accumulate)
+                       accumulate_grad_weight=accumulate, chunk_rows=chunk_rows)
     torch.cuda.synchronize()
     h64 = widen(h)
     W64 = widen(W)
@@ -164,6 +164,40 @@ def test_flce_two_pairs_per_cluster(N, H, V, T, eps):
     run_small(small(N, H, V, T=T, eps=eps, red="sum", gs=0.25, seed=N), accumulate=(N == 520))
 
 
+# The row-chunked schedule (flce_fwd_bwd_rows): one block, ragged blocks with
+# an accumulated weight gradient, vocabularies that are not multiples of 8
+# (padded logits / gradient rows), many small blocks (few rows per CE call),
+# fp16.
+@pytest.mark.parametrize("N,H,V,T,eps,red,chunk,dtype,acc", [
+    (256, 512, 8192, 30.0, 0.1, "mean", 256, "bf16", False),
+    (600, 264, 17000, 0.0, 0.0, "sum", 256, "bf16", True),
+    (200, 264, 5001, 5.0, 0.2, "mean", 64, "bf16", False),
+    (130, 128, 303, 30.0, 0.1, "sum", 7, "f16", False),
+    (1030, 200, 700, 0.0, 0.0, "mean", 1000, "f16", True),
+])
+def test_flce_row_chunked(N, H, V, T, eps, red, chunk, dtype, acc):
+    run_small(small(N, H, V, T=T, eps=eps, red=red, gs=0.5, seed=N + V, dtype=dtype),
+              accumulate=acc, chunk_rows=chunk)
+
+
+def test_flce_row_chunked_agrees_with_vocab_chunked():
+    # both schedules form fp32 logits and a 16-bit gradient between the products:
+    # losses agree to rounding, argmax exactly (the same fp32 products), the
+    # gradients to the 16-bit rounding of the gradient tile
+    w = small(520, 256, 12000, T=30.0, eps=0.1, red="mean", gs=0.5, seed=3)
+    h, W, lab = make_flce_inputs(w, device=DEV)
+    kw = dict(label_smoothing=w.label_smoothing, softcap=w.softcap, reduction=w.reduction,
+              grad_scale=w.grad_scale)
+    a = flce_fwd_bwd(h, W, lab, **kw)
+    b = flce_fwd_bwd(h, W, lab, chunk_rows=200, **kw)
+    torch.cuda.synchronize()
+    assert torch.allclose(a.loss, b.loss, rtol=0, atol=2e-5)
+    assert torch.equal(a.argmax, b.argmax)
+    assert torch.equal(a.counts, b.counts)
+    assert rel_l2(a.grad_hidden.float().cpu().numpy(), b.grad_hidden.float().cpu().numpy()) < 2e-3
+    assert rel_l2(a.grad_weight.cpu().numpy(), b.grad_weight.cpu().numpy()) < 2e-3
+
+
 def test_flce_deterministic():
     w = small(256, 512, 9000, T=30.0)
     outs = []
@@ -177,14 +211,15 @@ def test_flce_deterministic():
     assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
 
 
-def test_flce_full_size_workload_sampled():
+@pytest.mark.parametrize("chunk_rows", [None, 1024])
+def test_flce_full_size_workload_sampled(chunk_rows):
     w = FLCE_WORKLOADS["flce-bf16-4096x6656x202048-softcap30"]
     h, W, lab = make_flce_inputs(w, device=DEV)
     hb = bf16_bits_np(h)
     Wb = bf16_bits_np(W)
     labh = lab.cpu().numpy()
     res = flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
-                       reduction=w.reduction, grad_scale=w.grad_scale)
+                       reduction=w.reduction, grad_scale=w.grad_scale, chunk_rows=chunk_rows)
     torch.cuda.synchronize()
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([[0, w.N - 1], np.flatnonzero(labh == IGNORE_INDEX)[:2],
@@ -202,6 +237,7 @@ def test_flce_full_size_workload_sampled():
     gw = res.grad_weight.cpu().numpy()[cols]
     e_h = rel_l2(gh, ref["grad_hidden_rows"])
     e_w = rel_l2(gw, ref["grad_weight_cols"])
-    print("full-size FLCE: argmax mismatches", mism.size, "rel-L2 grad_hidden", e_h,
+    print("full-size FLCE (chunk_rows", chunk_rows, "): argmax mismatches", mism.size,
+          "rel-L2 grad_hidden", e_h,
           "grad_weight", e_w)
     assert e_h < 1e-2 and e_w < 1e-2

@@ -67,6 +67,10 @@ SIGNATURES = {
                             _f32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "flce_fwd_bwd_ex": (_i32, [_vp, _i32, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _f32,
                                _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "vlmce_flce_rows_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "flce_fwd_bwd_rows": (_i32, [_vp, _i32, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32,
+                                 _f32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp,
+                                 _sz, _vp]),
     "vlmce_gemm": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
                           _i32, _vp]),
     "vlmce_gemm_bf16": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64,

@@ -282,9 +282,9 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const int tail_tid = tail ? (G - 1 - gs) % THREADS : -1;
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
-    // Pass 2 prefetches ahead where the rows in flight reach the size of L2:
-    // long rows, and softcap rows (five 256-thread CTAs per SM).
-    constexpr bool kPrefetch2 = SOFTCAP || THREADS == kThreads;
+    // Pass 2 prefetches ahead where the rows in flight exceed L2: softcap
+    // rows (five 256-thread CTAs per SM, up to 760 rows in flight).
+    constexpr bool kPrefetch2 = SOFTCAP;
 
     // ---- pass 1
     Acc a;

@@ -24,11 +24,14 @@
 //   5. reduced loss and accuracy                               (1 CTA)
 // Executed tensor work 8 N V H (the logits twice); algorithmic 6 N V H.
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "ce_common.cuh"
 #include "gemm_launch.h"
@@ -193,6 +196,52 @@ __global__ void __launch_bounds__(1024) flce_finalize_kernel(
     }
 }
 
+// Row-chunked schedule: the scale every valid row's gradient shares, divided
+// by the factor of the 16-bit gradient (the products multiply their
+// accumulators by it); the same value flce_merge_kernel writes.
+__global__ void flce_rows_scale_kernel(const int64_t *counts, float grad_scale, int reduction,
+                                       float inv_grad_mul, float *out_scale) {
+    float s = grad_scale;
+    if (reduction == VLMCE_MEAN) {
+        const long long nv = counts[0];
+        s = nv > 0 ? grad_scale / static_cast<float>(nv) : 0.f;
+    }
+    *out_scale = s * inv_grad_mul;
+}
+
+// Row-chunked schedule: G[r, j] = 16-bit(S[r, j]) for j < V (bf16, or fp16
+// with F16; round to nearest even), four columns per thread, rows strided
+// over grid.y.  S rows are 16-byte aligned (lds % 4 == 0) and G rows 8-byte
+// aligned (ldg % 4 == 0).
+template <bool F16>
+__global__ void __launch_bounds__(256) flce_cast16_kernel(const float *__restrict__ S, int64_t lds,
+                                                          uint16_t *__restrict__ G, int64_t ldg,
+                                                          int64_t rows, int64_t V) {
+    const int64_t j = 4 * (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x);
+    if (j >= V) return;
+    auto pack = [](float a, float b) -> uint32_t {
+        uint32_t u;
+        if constexpr (F16) {
+            const __half2 h = __floats2half2_rn(a, b);
+            memcpy(&u, &h, 4);
+        } else {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            memcpy(&u, &h, 4);
+        }
+        return u;
+    };
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float *src = S + r * lds + j;
+        uint16_t *dst = G + r * ldg + j;
+        if (j + 4 <= V) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(pack(v.x, v.y), pack(v.z, v.w));
+        } else {
+            for (int64_t k = 0; j + k < V; ++k) dst[k] = static_cast<uint16_t>(pack(src[k], 0.f));
+        }
+    }
+}
+
 // ----------------------------------------------------------------- workspace
 struct Ws {
     int64_t *counts;
@@ -238,6 +287,92 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
         p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     }
     w.gh = reinterpret_cast<float *>(p);
+    return w;
+}
+
+// Sizes for which the workspace arithmetic stays in range.
+bool sizes_ok(int64_t N, int64_t H, int64_t V) {
+    return N >= 0 && H >= 1 && V >= 1 && N <= INT_MAX && H <= INT_MAX && V <= INT_MAX;
+}
+
+// Argument checks of both schedules; ws_needed: the schedule's workspace bytes.
+vlmce_status check_args(const void *hidden, int32_t dtype, int64_t hidden_stride, const void *weight,
+                        int64_t weight_stride, const int64_t *labels, int64_t N, int64_t H,
+                        int64_t V, float label_smoothing, float softcap, int32_t reduction,
+                        float grad_scale, const float *out_loss, const int64_t *out_argmax,
+                        const float *out_reduced, const int64_t *out_counts,
+                        const void *grad_hidden, const float *grad_weight, const void *workspace,
+                        size_t workspace_bytes_given, size_t ws_needed) {
+    if (dtype != VLMCE_BF16 && dtype != VLMCE_F16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
+    if (N < 0 || H < 1 || V < 1) return VLMCE_ERR_INVALID_ARG;
+    if (N > INT_MAX || H > INT_MAX || V > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+    if (hidden_stride < H || weight_stride < H) return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && (!hidden || !weight || !labels || !grad_hidden || !grad_weight))
+        return VLMCE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
+    if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
+    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes_given < ws_needed) return VLMCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return VLMCE_ERR_MISALIGNED;
+    if (N > 0 && (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(grad_hidden, 16) ||
+                  !aligned(grad_weight, 16) || !aligned(labels, 8)))
+        return VLMCE_ERR_MISALIGNED;
+    if (H % 8 || hidden_stride % 8 || weight_stride % 8) return VLMCE_ERR_MISALIGNED;
+    if ((out_loss && !aligned(out_loss, 4)) || (out_argmax && !aligned(out_argmax, 8)) ||
+        (out_reduced && !aligned(out_reduced, 4)) || (out_counts && !aligned(out_counts, 8)))
+        return VLMCE_ERR_MISALIGNED;
+    return VLMCE_OK;
+}
+
+// Row-chunked schedule workspace: counts / error word / product scale, the
+// per-token losses and argmax of all N rows, the fp32 logits of one chunk of
+// rows (row stride lds = V rounded up to 4), its 16-bit gradient (row stride
+// ldg = V rounded up to 8) and the workspace of the CE call on the chunk.
+struct RowsWs {
+    int64_t *counts;
+    int *err;
+    float *out_scale;
+    float *loss;
+    int64_t *argmax;
+    float *S;
+    uint16_t *G;
+    void *ce;
+    size_t ce_bytes;
+    int64_t nc, lds, ldg;
+};
+
+int64_t rows_chunk(int64_t N, int64_t chunk_rows) { return chunk_rows < N ? chunk_rows : N; }
+
+size_t rows_ws_bytes(int64_t N, int64_t V, int64_t chunk_rows) {
+    const int64_t nc = rows_chunk(N, chunk_rows);
+    const int64_t lds = round_up(V, 4), ldg = round_up(V, 8);
+    int64_t b = kWsHeader + round_up(4 * N, 256) + round_up(8 * N, 256);
+    b += round_up(4 * nc * lds, 256) + round_up(2 * nc * ldg, 256);
+    b += static_cast<int64_t>(vlmce_ce_workspace_bytes(nc, V, VLMCE_F32));
+    return static_cast<size_t>(b);
+}
+
+RowsWs rows_carve(void *ws, int64_t N, int64_t V, int64_t chunk_rows) {
+    unsigned char *p = static_cast<unsigned char *>(ws);
+    RowsWs w;
+    w.nc = rows_chunk(N, chunk_rows);
+    w.lds = round_up(V, 4);
+    w.ldg = round_up(V, 8);
+    w.counts = reinterpret_cast<int64_t *>(p);
+    w.err = reinterpret_cast<int *>(p + 64);
+    w.out_scale = reinterpret_cast<float *>(p + 128);
+    p += kWsHeader;
+    w.loss = reinterpret_cast<float *>(p);
+    p += round_up(4 * N, 256);
+    w.argmax = reinterpret_cast<int64_t *>(p);
+    p += round_up(8 * N, 256);
+    w.S = reinterpret_cast<float *>(p);
+    p += round_up(4 * w.nc * w.lds, 256);
+    w.G = reinterpret_cast<uint16_t *>(p);
+    p += round_up(2 * w.nc * w.ldg, 256);
+    w.ce = p;
+    w.ce_bytes = vlmce_ce_workspace_bytes(w.nc, V, VLMCE_F32);
     return w;
 }
 
@@ -316,29 +451,15 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
                                      void *workspace, size_t workspace_bytes_given,
                                      vlmce_stream_t stream) {
     // ---- host-side argument checks; nothing is enqueued on failure
-    if (dtype != VLMCE_BF16 && dtype != VLMCE_F16) return VLMCE_ERR_UNSUPPORTED_DTYPE;
+    vlmce_status st = check_args(hidden, dtype, hidden_stride, weight, weight_stride, labels, N, H, V,
+                                 label_smoothing, softcap, reduction, grad_scale, out_loss,
+                                 out_argmax, out_reduced, out_counts, grad_hidden, grad_weight,
+                                 workspace, workspace_bytes_given,
+                                 sizes_ok(N, H, V) ? ws_bytes(N, H, V) : 0);
+    if (st != VLMCE_OK) return st;
     const bool f16 = dtype == VLMCE_F16;
-    if (N < 0 || H < 1 || V < 1) return VLMCE_ERR_INVALID_ARG;
-    if (N > INT_MAX || H > INT_MAX || V > INT_MAX) return VLMCE_ERR_TOO_LARGE;
-    if (hidden_stride < H || weight_stride < H) return VLMCE_ERR_INVALID_ARG;
-    if (N > 0 && (!hidden || !weight || !labels || !grad_hidden || !grad_weight))
-        return VLMCE_ERR_INVALID_ARG;
-    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return VLMCE_ERR_INVALID_ARG;
-    if (!(softcap >= 0.f) || !std::isfinite(softcap)) return VLMCE_ERR_INVALID_ARG;
-    if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
-    if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM) return VLMCE_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes_given < ws_bytes(N, H, V)) return VLMCE_ERR_WORKSPACE_TOO_SMALL;
-    if (!aligned(workspace, 256)) return VLMCE_ERR_MISALIGNED;
-    if (N > 0 && (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(grad_hidden, 16) ||
-                  !aligned(grad_weight, 16) || !aligned(labels, 8)))
-        return VLMCE_ERR_MISALIGNED;
-    if (H % 8 || hidden_stride % 8 || weight_stride % 8) return VLMCE_ERR_MISALIGNED;
-    if ((out_loss && !aligned(out_loss, 4)) || (out_argmax && !aligned(out_argmax, 8)) ||
-        (out_reduced && !aligned(out_reduced, 4)) || (out_counts && !aligned(out_counts, 8)))
-        return VLMCE_ERR_MISALIGNED;
-
     DeviceInfo dev;
-    vlmce_status st = current_device(&dev);
+    st = current_device(&dev);
     if (st != VLMCE_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     Ws w = carve(workspace, N, H, V);
@@ -490,4 +611,159 @@ extern "C" vlmce_status flce_fwd_bwd(const void *hidden, int64_t hidden_stride, 
                            out_loss, out_argmax, out_reduced, out_counts, grad_hidden,
                            grad_weight, accumulate_grad_weight, workspace, workspace_bytes_given,
                            stream);
+}
+
+extern "C" size_t vlmce_flce_rows_workspace_bytes(int64_t N, int64_t H, int64_t V,
+                                                  int64_t chunk_rows) {
+    if (!sizes_ok(N, H, V) || chunk_rows < 1) return 0;
+    return rows_ws_bytes(N, V, chunk_rows);
+}
+
+// The row-chunked schedule (the comparison point of the vocabulary-chunked
+// one above): for each block of chunk_rows rows,
+//   S_k = h'_k W^T                  fp32 [nc, V] in the workspace   (GEMM)
+//   ce_fwd_bwd_ex on S_k: losses, argmax, and in place grad_mul (p - q)(1 - t^2)
+//                                   for the valid rows, 0 for the others
+//   G_k = 16-bit(S_k)                                              (cast)
+//   grad_h_k = G_k W, grad_W (+)= G_k^T h'_k, both times the shared scale
+//                                   (one grouped GEMM launch)
+// Executed tensor work 6 N V H (no recompute), at the price of the logits of a
+// chunk in HBM and of one read-modify-write of the fp32 grad_W per chunk after
+// the first.
+extern "C" vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int64_t hidden_stride,
+                                          const void *weight, int64_t weight_stride,
+                                          const int64_t *labels, int64_t N, int64_t H, int64_t V,
+                                          int64_t ignore_index, float label_smoothing,
+                                          float softcap, int32_t reduction, float grad_scale,
+                                          float *out_loss, int64_t *out_argmax,
+                                          float *out_reduced, int64_t *out_counts,
+                                          void *grad_hidden, float *grad_weight,
+                                          int32_t accumulate_grad_weight, int64_t chunk_rows,
+                                          void *workspace, size_t workspace_bytes_given,
+                                          vlmce_stream_t stream) {
+    // ---- host-side argument checks; nothing is enqueued on failure
+    if (chunk_rows < 1) return VLMCE_ERR_INVALID_ARG;
+    vlmce_status st = check_args(hidden, dtype, hidden_stride, weight, weight_stride, labels, N, H, V,
+                                 label_smoothing, softcap, reduction, grad_scale, out_loss,
+                                 out_argmax, out_reduced, out_counts, grad_hidden, grad_weight,
+                                 workspace, workspace_bytes_given,
+                                 sizes_ok(N, H, V) ? rows_ws_bytes(N, V, chunk_rows) : 0);
+    if (st != VLMCE_OK) return st;
+    if (V > vlmce_ce_max_vocab(VLMCE_F32)) return VLMCE_ERR_TOO_LARGE;
+    const bool f16 = dtype == VLMCE_F16;
+
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != VLMCE_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    RowsWs w = rows_carve(workspace, N, V, chunk_rows);
+    float *loss = out_loss ? out_loss : w.loss;
+    int64_t *amax = out_argmax ? out_argmax : w.argmax;
+    const float gmul = f16 ? kF16GradMul : 1.f;
+
+    flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
+    st = launch_status(cudaSuccess, "flce_count_kernel");
+    if (st != VLMCE_OK) return st;
+
+    if (N > 0) {
+        flce_rows_scale_kernel<<<1, 1, 0, cs>>>(w.counts, grad_scale, reduction, 1.f / gmul,
+                                                w.out_scale);
+        if ((st = launch_status(cudaSuccess, "flce_rows_scale_kernel")) != VLMCE_OK) return st;
+        cudaEvent_t eb = t_prof_begin, ee = t_prof_end;
+        t_prof_begin = t_prof_end = nullptr;
+        if (eb && (st = launch_status(cudaEventRecord(eb, cs), "cudaEventRecord")) != VLMCE_OK)
+            return st;
+        auto map_fail = [] {
+            record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+            return VLMCE_ERR_CUDA;
+        };
+        const int64_t gx = (round_up(V, 4) / 4 + 255) / 256;
+        if (gx > INT_MAX) return VLMCE_ERR_TOO_LARGE;
+        for (int64_t n0 = 0; n0 < N; n0 += w.nc) {
+            const int64_t rows = (N - n0) < w.nc ? (N - n0) : w.nc;
+            const uint16_t *hk = static_cast<const uint16_t *>(hidden) + n0 * hidden_stride;
+
+            // S_k = h'_k W^T, fp32
+            {
+                gemm::Maps maps;
+                if (!gemm::make_operand_map(&maps.a[0], hk, false, false, rows, H, hidden_stride, f16) ||
+                    !gemm::make_operand_map(&maps.b[0], weight, true, false, V, H, weight_stride, f16))
+                    return map_fail();
+                gemm::Params g = {};
+                g.nprob = 1;
+                g.f16 = f16 ? 1 : 0;
+                g.err = w.err;
+                gemm::Problem &p = g.p[0];
+                p.M = static_cast<int>(rows);
+                p.N = static_cast<int>(V);
+                p.K = static_cast<int>(H);
+                p.mode = gemm::kStoreF32;
+                p.C = w.S;
+                p.ldc = w.lds;
+                st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(logits)");
+                if (st != VLMCE_OK) return st;
+            }
+
+            // losses, argmax and grad_mul (p - q)(1 - t^2), in place
+            st = ce_fwd_bwd_ex(w.S, VLMCE_F32, labels + n0, rows, V, w.lds, ignore_index,
+                               label_smoothing, softcap, VLMCE_SUM, gmul, nullptr, 1, loss + n0,
+                               amax + n0, nullptr, nullptr, w.ce, w.ce_bytes, stream);
+            if (st != VLMCE_OK) return st;
+
+            // G_k = 16-bit(S_k)
+            {
+                const int64_t gy = rows < 65535 ? rows : 65535;
+                const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
+                if (f16)
+                    flce_cast16_kernel<true><<<grid, 256, 0, cs>>>(w.S, w.lds, w.G, w.ldg, rows, V);
+                else
+                    flce_cast16_kernel<false><<<grid, 256, 0, cs>>>(w.S, w.lds, w.G, w.ldg, rows, V);
+                if ((st = launch_status(cudaSuccess, "flce_cast16_kernel")) != VLMCE_OK) return st;
+            }
+
+            // grad_h_k = G_k W and grad_W (+)= G_k^T h'_k, scaled by *out_scale
+            {
+                gemm::Maps maps;
+                gemm::Params g = {};
+                g.f16 = f16 ? 1 : 0;
+                g.err = w.err;
+                g.out_scale = w.out_scale;
+                // grad_h_k: A = G_k K-major [rows, V], B = W N(=H)-major
+                if (!gemm::make_operand_map(&maps.a[0], w.G, false, false, rows, V, w.ldg, f16) ||
+                    !gemm::make_operand_map(&maps.b[0], weight, true, true, H, V, weight_stride, f16))
+                    return map_fail();
+                gemm::Problem &ph = g.p[0];
+                ph.M = static_cast<int>(rows);
+                ph.N = static_cast<int>(H);
+                ph.K = static_cast<int>(V);
+                ph.mode = gemm::kStoreBF16;
+                ph.a_mn = 0;
+                ph.b_mn = 1;
+                ph.C16 = static_cast<uint16_t *>(grad_hidden) + n0 * hidden_stride;
+                ph.ldc16 = hidden_stride;
+                // grad_W: A = G_k^T M(=V)-major, B = h'_k N(=H)-major
+                if (!gemm::make_operand_map(&maps.a[1], w.G, false, true, V, rows, w.ldg, f16) ||
+                    !gemm::make_operand_map(&maps.b[1], hk, true, true, H, rows, hidden_stride, f16))
+                    return map_fail();
+                gemm::Problem &pw = g.p[1];
+                pw.M = static_cast<int>(V);
+                pw.N = static_cast<int>(H);
+                pw.K = static_cast<int>(rows);
+                pw.mode = (n0 == 0 && !accumulate_grad_weight) ? gemm::kStoreF32 : gemm::kAccF32;
+                pw.a_mn = 1;
+                pw.b_mn = 1;
+                pw.C = grad_weight;
+                pw.ldc = H;
+                g.nprob = 2;
+                st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(products)");
+                if (st != VLMCE_OK) return st;
+            }
+        }
+        if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
+            return st;
+    }
+
+    flce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index, reduction,
+                                             w.counts, w.err, out_reduced, out_counts);
+    return launch_status(cudaSuccess, "flce_finalize_kernel");
 }

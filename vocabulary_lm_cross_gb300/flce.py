@@ -25,21 +25,28 @@ class FLCEResult:
     grad_weight: torch.Tensor  # fp32 [V, H]
 
 
-def workspace_bytes(N: int, H: int, V: int) -> int:
-    return int(capi.lib().vlmce_flce_workspace_bytes(N, H, V))
+def workspace_bytes(N: int, H: int, V: int, chunk_rows: int | None = None) -> int:
+    """Workspace bytes of the vocabulary-chunked schedule, or of the
+    row-chunked one when chunk_rows is given."""
+    if chunk_rows is None:
+        return int(capi.lib().vlmce_flce_workspace_bytes(N, H, V))
+    return int(capi.lib().vlmce_flce_rows_workspace_bytes(N, H, V, chunk_rows))
 
 
 def flce_fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tensor, *,
                  ignore_index: int = -100, label_smoothing: float = 0.0, softcap: float = 0.0,
                  reduction: str = "mean", grad_scale: float = 1.0,
                  grad_weight: torch.Tensor | None = None, accumulate_grad_weight: bool = False,
-                 workspace: torch.Tensor | None = None) -> FLCEResult:
+                 workspace: torch.Tensor | None = None,
+                 chunk_rows: int | None = None) -> FLCEResult:
     """Fused linear cross-entropy forward + backward.
 
     hidden: bf16 CUDA [N, H] (rows may be strided), the hidden states already
         multiplied by the logit multiplier; weight: bf16 CUDA [V, H];
     labels: int64 CUDA [N].  grad_weight (fp32 [V, H], contiguous) is
     allocated unless given; with accumulate_grad_weight it is added to.
+    chunk_rows: None for the vocabulary-chunked schedule (flce_fwd_bwd_ex),
+        else the rows per block of the row-chunked one (flce_fwd_bwd_rows).
     """
     dtypes = {torch.bfloat16: capi.BF16, torch.float16: capi.F16}
     if hidden.dtype not in dtypes or weight.dtype != hidden.dtype:
@@ -67,18 +74,24 @@ def flce_fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tenso
                      reduced=torch.empty(2, dtype=torch.float32, device=dev),
                      counts=torch.empty(4, dtype=torch.int64, device=dev),
                      grad_hidden=grad_hidden, grad_weight=grad_weight)
-    need = workspace_bytes(N, H, V)
+    if chunk_rows is not None and chunk_rows < 1:
+        raise ValueError("chunk_rows must be >= 1")
+    need = workspace_bytes(N, H, V, chunk_rows)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-    st = capi.lib().flce_fwd_bwd_ex(
-        hidden.data_ptr(), dtypes[hidden.dtype], hs, weight.data_ptr(),
-        weight.stride(0) if V > 1 else H,
-        labels.data_ptr(), N, H, V, ignore_index, float(label_smoothing), float(softcap),
-        _REDUCTIONS[reduction], float(grad_scale), res.loss.data_ptr(), res.argmax.data_ptr(),
-        res.reduced.data_ptr(), res.counts.data_ptr(), grad_hidden.data_ptr(),
-        grad_weight.data_ptr(), int(accumulate_grad_weight), workspace.data_ptr(),
-        workspace.numel(), stream)
-    capi.check(st, "flce_fwd_bwd")
+    args = (hidden.data_ptr(), dtypes[hidden.dtype], hs, weight.data_ptr(),
+            weight.stride(0) if V > 1 else H,
+            labels.data_ptr(), N, H, V, ignore_index, float(label_smoothing), float(softcap),
+            _REDUCTIONS[reduction], float(grad_scale), res.loss.data_ptr(), res.argmax.data_ptr(),
+            res.reduced.data_ptr(), res.counts.data_ptr(), grad_hidden.data_ptr(),
+            grad_weight.data_ptr(), int(accumulate_grad_weight))
+    if chunk_rows is None:
+        st = capi.lib().flce_fwd_bwd_ex(*args, workspace.data_ptr(), workspace.numel(), stream)
+        capi.check(st, "flce_fwd_bwd")
+    else:
+        st = capi.lib().flce_fwd_bwd_rows(*args, int(chunk_rows), workspace.data_ptr(),
+                                          workspace.numel(), stream)
+        capi.check(st, "flce_fwd_bwd_rows")
     return res
