@@ -198,6 +198,33 @@ def test_flce_row_chunked_agrees_with_vocab_chunked():
     assert rel_l2(a.grad_weight.cpu().numpy(), b.grad_weight.cpu().numpy()) < 2e-3
 
 
+def test_flce_agrees_with_torch_matmuls_around_the_ce_kernel():
+    # an independent composition: fp32 torch matmul logits -> ce_fwd_bwd (the
+    # row kernel on fp32 logits) -> torch matmuls for the two gradients
+    from vocabulary_lm_cross_gb300 import ce_fwd_bwd
+    w = small(300, 192, 7000, T=30.0, eps=0.1, red="mean", gs=0.5, seed=5)
+    h, W, lab = make_flce_inputs(w, device=DEV)
+    res = flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                       reduction=w.reduction, grad_scale=w.grad_scale)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        hf, Wf = h.float(), W.float()
+        S = hf @ Wf.T
+        ce = ce_fwd_bwd(S, lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
+                        reduction=w.reduction, grad_scale=w.grad_scale)
+        gh = S @ Wf     # S now holds d loss / d S
+        gw = S.T @ hf
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    torch.cuda.synchronize()
+    assert torch.allclose(res.loss, ce.loss, rtol=0, atol=2e-5)
+    assert abs(float(res.reduced[0]) - float(ce.reduced[0])) < 1e-5
+    assert int(res.counts[0]) == int(ce.counts[0]) and int(res.counts[2]) == int(ce.counts[2])
+    assert rel_l2(res.grad_hidden.float().cpu().numpy(), gh.cpu().numpy()) < 1e-2
+    assert rel_l2(res.grad_weight.cpu().numpy(), gw.cpu().numpy()) < 1e-2
+
+
 def test_flce_deterministic():
     w = small(256, 512, 9000, T=30.0)
     outs = []
