@@ -204,7 +204,8 @@ size_t vlmce_ce_host_workspace_bytes(int64_t N, int64_t V, int64_t row_stride, i
 typedef struct vlmce_row_stats {
     float x_max;     /* largest raw logit of the columns merged so far */
     int32_t argmax;  /* its smallest global column (INT32_MAX before any column) */
-    float m;         /* reference of s: z at x_max (z = T tanh(x/T), or x) */
+    float m;         /* reference of s, >= every z_j merged (z = T tanh(x/T), or
+                        x): z at x_max, or up to 8 above it */
     float s;         /* sum over the columns of exp(z_j - m) */
     float sum_z;     /* sum over the columns of z_j */
     float z_y;       /* z at the row's label column if merged so far, else 0 */

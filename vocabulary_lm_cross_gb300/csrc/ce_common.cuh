@@ -21,7 +21,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct __align__(16) RowPart {
     float mx;   // max of the raw logits x
     int idx;    // smallest column holding mx
-    float mz;   // reference maximum (z space) of s
+    float mz;   // reference of s (z space), >= every z folded
     float s;    // sum exp(z - mz)
     float sz;   // sum z
     float zy;   // z at the label column (only its owner adds it)

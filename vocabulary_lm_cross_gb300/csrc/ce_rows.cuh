@@ -13,8 +13,11 @@
 // waits for it (programmatic dependent launch) after pass 1.
 //
 // Pass 1 keeps two 16-byte loads in flight per thread and prefetches the
-// pair two iterations ahead into L2, so that enough bytes are outstanding per
-// SM to cover the DRAM latency.
+// next iteration's pair into L2, so that enough bytes are outstanding per SM
+// to cover the DRAM latency.  Its arithmetic is the rest of its cost: the
+// reference of the exponentials moves lazily (new_max), since with 16 or more
+// granules per thread some lane of a warp meets a new maximum in most
+// granules.
 // The kernel is bound by instruction issue, so the inner loops run over whole
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
@@ -73,8 +76,9 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
 struct Acc {
     float mv;    // max raw logit seen
     int midx;    // its first column
-    float mz;    // z of mv: reference of s
+    float mz;    // reference of s, at least the largest z seen
     float nmL;   // -mz log2e
+    float xthr;  // largest x whose z mz is known to cover
     uint64_t s;  // sums of exp(z - mz) (even, odd columns)
     uint64_t z;  // sums of z, or of tanh(x/T) when a softcap is set (even, odd columns)
 };
@@ -84,6 +88,7 @@ __device__ __forceinline__ void acc_init(Acc &a) {
     a.midx = INT_MAX;
     a.mz = -INFINITY;
     a.nmL = INFINITY;
+    a.xthr = -INFINITY;
     a.s = a.z = pk(0.f, 0.f);
 }
 
@@ -111,8 +116,15 @@ __device__ __forceinline__ float z_of(float x, float T, float k2) {
         return x;
 }
 
+// Margin (natural-log units) by which the sums' reference is set above a new
+// maximum, so that later maxima seldom move it: every term exp(z - mz) stays
+// <= 1, and one below e^-8 loses nothing (fp32 precision is relative).
+constexpr float kRefMargin = 8.f;
+
 // New maximum gm in the granule starting at column jg: locate its first
-// column among the valid ones, rescale the running sums.
+// column among the valid ones; only when gm passes xthr, move the reference
+// of the running sums to z(gm) + kRefMargin and rescale them.  (z grows no
+// faster than x, so mz covers every x <= gm + kRefMargin.)
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPerGranule],
                                         float gm, int jg, int V, float T, float k2) {
@@ -121,17 +133,20 @@ __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPe
 #pragma unroll
     for (int l = EPG - 1; l >= 0; --l)
         if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
-    const float nz = z_of<SOFTCAP>(gm, T, k2);
-    const float f = ptx::ex2((a.mz - nz) * kLog2e);
-    float s0, s1;
-    upk(a.s, s0, s1);
-    s0 = (s0 == 0.f) ? 0.f : s0 * f;
-    s1 = (s1 == 0.f) ? 0.f : s1 * f;
-    a.s = pk(s0, s1);
     a.mv = gm;
     a.midx = jg + li;
-    a.mz = nz;
-    a.nmL = -nz * kLog2e;
+    if (gm > a.xthr) {
+        const float nz = z_of<SOFTCAP>(gm, T, k2) + kRefMargin;
+        const float f = ptx::ex2((a.mz - nz) * kLog2e);
+        float s0, s1;
+        upk(a.s, s0, s1);
+        s0 = (s0 == 0.f) ? 0.f : s0 * f;
+        s1 = (s1 == 0.f) ? 0.f : s1 * f;
+        a.s = pk(s0, s1);
+        a.mz = nz;
+        a.nmL = -nz * kLog2e;
+        a.xthr = gm + kRefMargin;
+    }
 }
 
 // Fold a whole granule (every column valid), two columns per packed op.
@@ -296,9 +311,9 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     int gl = gs + tid;
     for (; gl + THREADS < ge; gl += 2 * THREADS) {
         const uint4 w0 = ld_v4(row + gl), w1 = ld_v4(row + gl + THREADS);
-        if (gl + 5 * THREADS < ge) {  // the pair two iterations ahead, into L2
-            ptx::prefetch_l2(row + gl + 4 * THREADS);
-            ptx::prefetch_l2(row + gl + 5 * THREADS);
+        if (gl + 3 * THREADS < ge) {  // the next iteration's pair, into L2
+            ptx::prefetch_l2(row + gl + 2 * THREADS);
+            ptx::prefetch_l2(row + gl + 3 * THREADS);
         }
         fold_full<BF16, SOFTCAP, SUMZ>(a, w0, gl * EPG - lead, p.V, T, k2);
         fold_full<BF16, SOFTCAP, SUMZ>(a, w1, (gl + THREADS) * EPG - lead, p.V, T, k2);
