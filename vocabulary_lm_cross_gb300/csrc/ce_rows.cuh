@@ -22,8 +22,9 @@
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
 // main loop, the last one after it, so every thread still meets its granules
-// in column order), the label column is patched in a rare branch, and the
-// sum of z is only formed when label smoothing needs it.
+// in column order), the label column's gradient is stored over the smoothed
+// value after pass 2's loop by the thread that owns it, and the sum of z is
+// only formed when label smoothing needs it.
 #pragma once
 
 #include "ce_common.cuh"
@@ -208,9 +209,27 @@ struct GradCoef {
     float T, k2;     // softcap and -2 log2e / T
 };
 
-// Gradients of the EPG elements of a granule, in fp32, two per packed op.
-// Under a softcap g = 4 scale (p - q) a r^2 (the factor 4 of dz/dx = 4 a r^2
-// is folded into the coefficients, exactly).
+// Gradient of the label column: q_y = 1 - eps + eps/V.
+template <bool SOFTCAP>
+__device__ __forceinline__ float label_grad(float x, const GradCoef &c) {
+    const float L = SOFTCAP ? c.T * kLog2e : kLog2e;
+    if constexpr (SOFTCAP) {
+        const Cap2 cz = softcap2(x, x, c.k2);
+        float t, t_, ar2, ar2_;
+        upk(cz.t, t, t_);
+        upk(cz.ar2, ar2, ar2_);
+        const float pr = ptx::ex2(fmaf(t, L, c.nlseL));
+        return fmaf(pr, 4.f * c.scale, -4.f * c.c_label) * ar2;
+    } else {
+        const float pr = ptx::ex2(fmaf(x, L, c.nlseL));
+        return fmaf(pr, c.scale, -c.c_label);
+    }
+}
+
+// Gradients of the EPG elements of a granule, in fp32, two per packed op;
+// label_lane >= 0: the label column's lane.  Under a softcap
+// g = 4 scale (p - q) a r^2 (the factor 4 of dz/dx = 4 a r^2 is folded into
+// the coefficients, exactly).
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, int label_lane,
                                             float (&g)[Elem<BF16>::kPerGranule]) {
@@ -233,23 +252,10 @@ __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, in
         }
         upk(g2, g[l], g[l + 1]);
     }
-    if (label_lane >= 0) {  // the label column: q_y = 1 - eps + eps/V (rare)
+    if (label_lane >= 0) {  // the label column (rare)
 #pragma unroll
-        for (int l = 0; l < EPG; ++l) {
-            if (l == label_lane) {
-                if constexpr (SOFTCAP) {
-                    const Cap2 cz = softcap2(x[l], x[l], c.k2);
-                    float t, t_, ar2, ar2_;
-                    upk(cz.t, t, t_);
-                    upk(cz.ar2, ar2, ar2_);
-                    const float pr = ptx::ex2(fmaf(t, L, c.nlseL));
-                    g[l] = fmaf(pr, f * c.scale, -f * c.c_label) * ar2;
-                } else {
-                    const float pr = ptx::ex2(fmaf(x[l], L, c.nlseL));
-                    g[l] = fmaf(pr, c.scale, -c.c_label);
-                }
-            }
-        }
+        for (int l = 0; l < EPG; ++l)
+            if (l == label_lane) g[l] = label_grad<SOFTCAP>(x[l], c);
     }
 }
 
@@ -373,6 +379,19 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         c.k2 = k2;
         const int gy = static_cast<int>((y + lead) / EPG);
         const int ly = static_cast<int>((y + lead) % EPG);
+        // The label column in a whole granule: the thread that owns the
+        // granule reads x_y now (the loop overwrites it), stores the granule
+        // like any other in the loop, then overwrites the one element with the
+        // label gradient, so the loop itself has no label test.
+        const int y_owner = (gy >= gs && gy < ge) ? (gy - gs) % THREADS : -1;
+        unsigned char *py = gbase + ELT * (static_cast<int64_t>(y) + lead);
+        float xy = 0.f;
+        if (tid == y_owner) {
+            if constexpr (BF16)
+                xy = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
+            else
+                xy = *reinterpret_cast<const float *>(py);
+        }
         float g[EPG];
         if (head && tid == 0) {
             grad_values<BF16, SOFTCAP>(ld_v4(row), c, gy == 0 ? ly : -1, g);
@@ -382,9 +401,10 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
             // the granule two iterations ahead, into L2 (where the row has
             // partly left L2 since pass 1)
             if (kPrefetch2 && gl + 2 * THREADS < ge) ptx::prefetch_l2(row + gl + 2 * THREADS);
-            grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, gl == gy ? ly : -1, g);
+            grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, -1, g);
             ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
         }
+        if (tid == y_owner) store_elem<BF16>(py, label_grad<SOFTCAP>(xy, c));
         if (tid == tail_tid) {
             grad_values<BF16, SOFTCAP>(ld_v4(row + (G - 1)), c, gy == G - 1 ? ly : -1, g);
             store_partial<BF16>(gbase + 16 * (G - 1), (G - 1) * EPG - lead, p.V, g);
