@@ -285,7 +285,8 @@ size_t vlmce_flce_workspace_bytes(int64_t N, int64_t H, int64_t V);
  * grad_hidden  out: bf16 [N, hidden_stride], d(grad_scale * loss) / d h'
  *              (the caller multiplies by m for d / d h).
  * grad_weight  fp32 [V, H] contiguous: overwritten with d(...)/dW, or added
- *              to when accumulate_grad_weight != 0.
+ *              to when accumulate_grad_weight != 0 (with N = 0 an overwritten
+ *              grad_weight is set to zero; it may then be NULL).
  * workspace    >= vlmce_flce_workspace_bytes(N, H, V) bytes, 256-byte aligned.
  * H, hidden_stride, weight_stride must be multiples of 8; every pointer
  * 16-byte aligned.  bf16 only (like the native Blackwell path on the pages).

@@ -180,6 +180,27 @@ def test_flce_row_chunked(N, H, V, T, eps, red, chunk, dtype, acc):
               accumulate=acc, chunk_rows=chunk)
 
 
+def test_flce_row_chunked_one_row_blocks():
+    run_small(small(5, 64, 1000, T=30.0, eps=0.1, red="sum", seed=9), chunk_rows=1)
+
+
+@pytest.mark.parametrize("chunk_rows", [None, 16])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_flce_no_rows(chunk_rows, accumulate):
+    # no rows: zero losses and counts; d loss / dW = 0, so an overwritten
+    # grad_weight is cleared and an accumulated one kept
+    h = torch.zeros(0, 64, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(100, 64, device=DEV).to(torch.bfloat16)
+    lab = torch.zeros(0, dtype=torch.int64, device=DEV)
+    gw = torch.full((100, 64), 7.0, device=DEV)
+    r = flce_fwd_bwd(h, W, lab, chunk_rows=chunk_rows, grad_weight=gw,
+                     accumulate_grad_weight=accumulate)
+    torch.cuda.synchronize()
+    assert r.loss.numel() == 0 and int(r.counts[0]) == 0 and int(r.counts[3]) == 0
+    assert float(r.reduced[0]) == 0.0
+    assert torch.equal(gw, torch.full_like(gw, 7.0) if accumulate else torch.zeros_like(gw))
+
+
 def test_flce_row_chunked_agrees_with_vocab_chunked():
     # both schedules form fp32 logits and a 16-bit gradient between the products:
     # losses agree to rounding, argmax exactly (the same fp32 products), the

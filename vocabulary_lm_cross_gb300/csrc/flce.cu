@@ -290,6 +290,16 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
     return w;
 }
 
+// With no rows, d loss / dW is zero: an overwritten grad_weight is cleared
+// (stream-ordered memset), an accumulated one is left as it is.
+vlmce_status clear_grad_weight_if_empty(int64_t N, int64_t H, int64_t V, float *grad_weight,
+                                        int32_t accumulate_grad_weight, cudaStream_t cs) {
+    if (N != 0 || !grad_weight || accumulate_grad_weight) return VLMCE_OK;
+    if (V > (INT64_MAX / 4) / H) return VLMCE_ERR_TOO_LARGE;
+    return launch_status(cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(4 * V * H), cs),
+                         "cudaMemsetAsync(grad_weight)");
+}
+
 // Sizes for which the workspace arithmetic stays in range.
 bool sizes_ok(int64_t N, int64_t H, int64_t V) {
     return N >= 0 && H >= 1 && V >= 1 && N <= INT_MAX && H <= INT_MAX && V <= INT_MAX;
@@ -468,6 +478,8 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
 
     flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
     st = launch_status(cudaSuccess, "flce_count_kernel");
+    if (st != VLMCE_OK) return st;
+    st = clear_grad_weight_if_empty(N, H, V, grad_weight, accumulate_grad_weight, cs);
     if (st != VLMCE_OK) return st;
 
     if (N > 0) {
@@ -663,6 +675,8 @@ extern "C" vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int
 
     flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
     st = launch_status(cudaSuccess, "flce_count_kernel");
+    if (st != VLMCE_OK) return st;
+    st = clear_grad_weight_if_empty(N, H, V, grad_weight, accumulate_grad_weight, cs);
     if (st != VLMCE_OK) return st;
 
     if (N > 0) {
