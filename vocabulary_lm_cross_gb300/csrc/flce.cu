@@ -14,11 +14,11 @@
 //   3. per row: merge the tile statistics in column order -> lse, loss,
 //      argmax, gradient scale                                  (1 warp / row)
 //   4. for chunk c = 0 .. C of Vc = 8192 vocabulary columns, one grouped
-//      GEMM launch each:
+//      GEMM launch each (tiles run in this order):
 //        grad_h  (+)= G_{c-1} W_{c-1}   (fp32 [N, H]; the last chunk writes bf16)
-//        grad_W_{c-1} (+)= G_{c-1}^T h' (fp32, rows of the chunk)
 //        G_c = scale (softmax - q) (1 - t^2), recomputed from S_c = h' W_c^T
 //              and stored in bf16 [N, Vc] (two buffers, alternating)
+//        grad_W_{c-1} (+)= G_{c-1}^T h' (fp32, rows of the chunk)
 //      so the two products of a chunk share a launch with the next chunk's
 //      gradient tile and every launch has one tail.
 //   5. reduced loss and accuracy                               (1 CTA)
@@ -535,26 +535,28 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
         st = launch_status(cudaSuccess, "flce_merge_kernel");
         if (st != VLMCE_OK) return st;
 
-        // ---- pass 2: launch c = the products of chunk c - 1 and the gradient tile of chunk c
+        // ---- pass 2: launch c = the products of chunk c - 1 and the gradient tile of chunk c,
+        // in the order grad_h, gradient tile, grad_W: the persistent grid runs the
+        // tiles in problem order, and grad_W's (the shortest, K = N) end the launch
         const int64_t nchunks = (V + kChunk - 1) / kChunk;
         for (int64_t c = 0; c <= nchunks; ++c) {
             gemm::Maps maps;
             gemm::Params g = base;
             int n = 0;
+            const int64_t cp = c - 1;  // the chunk whose products this launch computes
+            const int64_t pv0 = cp * kChunk;
+            const int64_t pvc = c >= 1 ? ((V - pv0) < kChunk ? (V - pv0) : kChunk) : 0;
+            const uint16_t *gc = c >= 1 ? w.g[cp & 1] : nullptr;
             if (c >= 1) {
-                const int64_t cp = c - 1;
-                const int64_t v0 = cp * kChunk;
-                const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
-                const uint16_t *wc = static_cast<const uint16_t *>(weight) + v0 * weight_stride;
-                const uint16_t *gc = w.g[cp & 1];
+                const uint16_t *wc = static_cast<const uint16_t *>(weight) + pv0 * weight_stride;
                 // grad_h (+)= G_c W_c: A = G_c K-major [N, Vc], B = W_c N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, false, N, vc, kChunk, f16) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, true, true, H, vc, weight_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, false, N, pvc, kChunk, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, true, H, pvc, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &ph = g.p[n++];
                 ph.M = static_cast<int>(N);
                 ph.N = static_cast<int>(H);
-                ph.K = static_cast<int>(vc);
+                ph.K = static_cast<int>(pvc);
                 ph.mode = nchunks == 1       ? gemm::kStoreBF16
                           : cp == 0           ? gemm::kStoreF32
                           : cp == nchunks - 1 ? gemm::kAccToBF16
@@ -565,19 +567,6 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
                 ph.ldc = H;
                 ph.C16 = static_cast<uint16_t *>(grad_hidden);
                 ph.ldc16 = hidden_stride;
-                // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, true, vc, N, kChunk, f16) ||
-                    !gemm::make_operand_map(&maps.b[n], hidden, true, true, H, N, hidden_stride, f16))
-                    return map_fail();
-                gemm::Problem &pw = g.p[n++];
-                pw.M = static_cast<int>(vc);
-                pw.N = static_cast<int>(H);
-                pw.K = static_cast<int>(N);
-                pw.mode = accumulate_grad_weight ? gemm::kAccF32 : gemm::kStoreF32;
-                pw.a_mn = 1;
-                pw.b_mn = 1;
-                pw.C = grad_weight + v0 * H;
-                pw.ldc = H;
             }
             if (c < nchunks) {
                 const int64_t v0 = c * kChunk;
@@ -595,6 +584,21 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
                 pg.col0 = static_cast<int>(v0);
                 pg.C16 = w.g[c & 1];
                 pg.ldc16 = kChunk;
+            }
+            if (c >= 1) {
+                // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, true, pvc, N, kChunk, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], hidden, true, true, H, N, hidden_stride, f16))
+                    return map_fail();
+                gemm::Problem &pw = g.p[n++];
+                pw.M = static_cast<int>(pvc);
+                pw.N = static_cast<int>(H);
+                pw.K = static_cast<int>(N);
+                pw.mode = accumulate_grad_weight ? gemm::kAccF32 : gemm::kStoreF32;
+                pw.a_mn = 1;
+                pw.b_mn = 1;
+                pw.C = grad_weight + pv0 * H;
+                pw.ldc = H;
             }
             g.nprob = n;
             st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(chunk)");
