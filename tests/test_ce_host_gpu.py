@@ -39,6 +39,7 @@ def bits(t):
     (600, 20000, 20004, "f32", 0.0, 0.0, "mean"),      # 2 chunks, fp32
     (60, 70001, 70007, "bf16", 30.0, 0.1, "sum"),      # wide softcap rows on 256-thread CTAs
     (600, 40000, 40000, "f32", 30.0, 0.0, "mean"),     # the same, 3 chunks, fp32
+    (2048, 131072, 131072, "bf16", 0.0, 0.1, "mean"),  # the headline shape, as bench.py's e2e
 ])
 def test_host_results_equal_device_results(monkeypatch, N, V, stride, dtype, T, eps, red):
     monkeypatch.setenv("VLMCE_CE_PATH", "rows")  # the kernel the host path uses

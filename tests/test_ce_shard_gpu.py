@@ -55,6 +55,10 @@ CASES = [
     (160, 4099, "f32", 30.0, 0.0, "sum", [2048]),
     (97, 32768, "bf16", 5.0, 0.2, "mean", [8192, 16384, 24576]),
     (64, 1000, "bf16", 0.0, 0.0, "mean", list(range(100, 1000, 100))),
+    # the benchmarked layouts: the headline row length in TP = 8 shards, and the
+    # softcap workload's row length in TP = 8 shards
+    (256, 131072, "bf16", 0.0, 0.1, "mean", [16384 * i for i in range(1, 8)]),
+    (64, 151936, "bf16", 30.0, 0.1, "sum", [18992 * i for i in range(1, 8)]),
 ]
 
 
