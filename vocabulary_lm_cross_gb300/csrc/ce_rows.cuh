@@ -361,11 +361,14 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         }
     }
     __syncthreads();
+    // The label census of this call, which pass 2 reads.  Every CTA waits (not
+    // only those that read it), so the grid completes after the census: the
+    // finalize kernel, launched dependent on this grid, reads its counts.
+    ptx::griddep_wait();
     if (!p.want_grad) return;  // forward only
 
     // ---- pass 2
     if (valid) {
-        ptx::griddep_wait();  // the label census of this call
         const int64_t n_valid = p.counts[0];
         GradCoef c;
         c.scale = p.grad_scale;

@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
 // in that order (out may be shards[0]).
 __global__ void __launch_bounds__(256) ce_merge_stats_kernel(const RowPart *shards, int k,
                                                             int64_t N, RowPart *out) {
+    ptx::griddep_wait();  // the gathered records (launched dependent on their producer)
     const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= N) return;
     RowPart a = shards[r];
@@ -172,6 +173,11 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     const int64_t y = p.labels[r];
     const bool ignored = y == p.ignore_index;
     const bool valid = !ignored && y >= 0 && y < p.V;
+    // The label census of this call (launched just before, this kernel
+    // dependent on it; the merged statistics were complete before the census
+    // started).  Every CTA waits, so that the grid completes after the census
+    // and the finalize kernel, dependent on this grid, may read its counts.
+    ptx::griddep_wait();
     if (valid) {
         const int64_t n_valid = p.counts[0];
         rows::GradCoef c;
@@ -253,6 +259,25 @@ int shard_threads(const void *logits, int32_t dtype, int64_t V_local, int64_t ro
         softcap);
 }
 
+// Launch a kernel dependent on the previous work on the stream (programmatic
+// dependent launch): it may start while its predecessor finishes and waits for
+// it with griddepcontrol.wait before using its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                             Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int64_t kMaxVocab = int64_t(1) << 28;
 
 // Checks shared by the shard entry points (nothing is enqueued on failure).
@@ -319,10 +344,12 @@ extern "C" vlmce_status ce_merge_stats(const vlmce_row_stats *shards, int32_t k,
     DeviceInfo dev;
     vlmce_status st = current_device(&dev);
     if (st != VLMCE_OK) return st;
-    ce_merge_stats_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0,
-                            reinterpret_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const RowPart *>(shards), k, N, reinterpret_cast<RowPart *>(out));
-    return launch_status(cudaSuccess, "ce_merge_stats_kernel");
+    return launch_status(
+        launch_dependent(ce_merge_stats_kernel, dim3(static_cast<unsigned>((N + 255) / 256)),
+                         dim3(256), reinterpret_cast<cudaStream_t>(stream),
+                         reinterpret_cast<const RowPart *>(shards), k, N,
+                         reinterpret_cast<RowPart *>(out)),
+        "ce_merge_stats_kernel");
 }
 
 extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels,
@@ -379,12 +406,16 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
         p.argmax = amax;
         p.counts = counts;
         const int th = shard_threads(logits, dtype, V_local, row_stride, softcap > 0.f);
-        grad_kernel(dtype == VLMCE_BF16, softcap > 0.f, th)
-            <<<static_cast<unsigned>(N), th, 0, cs>>>(p);
-        if ((st = launch_status(cudaSuccess, "ce_shard_grad_kernel")) != VLMCE_OK) return st;
+        st = launch_status(launch_dependent(grad_kernel(dtype == VLMCE_BF16, softcap > 0.f, th),
+                                            dim3(static_cast<unsigned>(N)), dim3(th), cs, p),
+                           "ce_shard_grad_kernel");
+        if (st != VLMCE_OK) return st;
     }
-    ce_finalize_kernel<<<1, 1024, 0, cs>>>(loss, amax, labels, N, V, ignore_index,
-                                           static_cast<int>(reduction), counts, err, out_reduced,
-                                           out_counts);
-    return launch_status(cudaSuccess, "ce_finalize_kernel");
+    return launch_status(
+        launch_dependent(ce_finalize_kernel, dim3(1), dim3(1024), cs,
+                         static_cast<const float *>(loss), static_cast<const int64_t *>(amax),
+                         labels, N, V, ignore_index, static_cast<int>(reduction),
+                         static_cast<const int64_t *>(counts), static_cast<const int *>(err),
+                         out_reduced, out_counts),
+        "ce_finalize_kernel");
 }
