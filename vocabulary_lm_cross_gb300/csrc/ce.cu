@@ -12,7 +12,7 @@
 //   1. ce_count_kernel    -- label census (n_valid for the mean, bad labels).
 //   2. the row work, by one of two kernels:
 //      ce_rows_kernel  (ce_rows.cuh)  -- one CTA per row, two passes, the second
-//                    served by L2; the default: every SM busy once N >= 304;
+//                    served mostly by L2; the default: every SM busy once N >= 304;
 //      ce_split_kernel (ce_split.cuh) -- a thread-block cluster per row,
 //                    the row split over its CTAs in shared memory and merged
 //                    through distributed shared memory; for few, wide rows,

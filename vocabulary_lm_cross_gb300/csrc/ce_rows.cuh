@@ -1,15 +1,17 @@
-// ce_rows.cuh -- the cross-entropy row kernel (default path): one CTA of 1024
-// threads per row, two CTAs per SM (64 warps: every SM is fully occupied).
+// ce_rows.cuh -- the cross-entropy row kernel (default path): one CTA per
+// row; 1024 threads (two CTAs, 64 warps per SM) for long rows, 256 threads
+// (eight CTAs per SM) for rows of at most kShortGranules granules and (five
+// per SM, for their registers) for softcap rows.
 //
 //   pass 1: stream the row from HBM in 16-byte granules: max and first argmax
 //           of the raw logits, online sum of exp(z - m) and sum of z;
-//   merge:  warp shuffles, then the 32 warp partials (fixed order);
-//   pass 2: read the row again -- it is still in the 129 MB L2, since at most
-//           2 x 152 rows (78 MB for 256 KB rows) are in flight -- and store the
-//           gradient scale (p - q) (1 - t^2), rounded to the storage dtype,
-//           with 16-byte evict-first stores over the logits.
-// HBM sees one read and one write of every byte; the second read is served by
-// L2.  The label census of the call is only needed by pass 2, so the kernel
+//   merge:  warp shuffles, then the warp partials (fixed order);
+//   pass 2: read the row again -- without a softcap it is still in the 129 MB
+//           L2, since at most 2 x 152 rows (78 MB for 256 KB rows) are in
+//           flight; softcap rows exceed L2 and are prefetched into it ahead --
+//           and store the gradient scale (p - q) (1 - t^2), rounded to the
+//           storage dtype, with 16-byte evict-first stores over the logits.
+// Without a softcap HBM sees about one read and one write of every byte.  The label census of the call is only needed by pass 2, so the kernel
 // waits for it (programmatic dependent launch) after pass 1.
 //
 // Pass 1 keeps two 16-byte loads in flight per thread and prefetches the
