@@ -23,13 +23,20 @@ __global__ void __launch_bounds__(1024) ce_count_kernel(const int64_t *__restric
                                                      int64_t *counts, int *err) {
     ptx::griddep_launch_dependents();
     long long nv = 0, nb = 0;
-    for (int64_t r = threadIdx.x; r < N; r += blockDim.x) {
-        const int64_t y = labels[r];
-        if (y == ignore_index) continue;
-        if (y >= 0 && y < V)
-            ++nv;
-        else
-            ++nb;
+    const int64_t st = blockDim.x;
+    // four labels in flight per thread (the loop is load-latency bound)
+    for (int64_t r0 = threadIdx.x; r0 < N; r0 += 4 * st) {
+        int64_t y[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) y[u] = r0 + u * st < N ? labels[r0 + u * st] : ignore_index;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (y[u] == ignore_index) continue;
+            if (y[u] >= 0 && y[u] < V)
+                ++nv;
+            else
+                ++nb;
+        }
     }
     __shared__ long long sv[32], sb[32];
 #pragma unroll
@@ -67,11 +74,25 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(
     ptx::griddep_wait();
     double acc = 0.0;
     long long nc = 0;
-    for (int64_t r = threadIdx.x; r < N; r += blockDim.x) {
-        const int64_t y = labels[r];
-        if (y == ignore_index) continue;
-        acc += static_cast<double>(loss[r]);
-        if (y >= 0 && y < V && argmax[r] == y) ++nc;
+    const int64_t st = blockDim.x;
+    // four rows' values in flight per thread (the loop is load-latency bound);
+    // each thread still adds its rows r, r + st, r + 2 st, ... in that order
+    for (int64_t r0 = threadIdx.x; r0 < N; r0 += 4 * st) {
+        int64_t y[4], am[4];
+        float l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t r = r0 + u * st;
+            y[u] = r < N ? labels[r] : ignore_index;
+            l[u] = r < N ? loss[r] : 0.f;
+            am[u] = r < N ? argmax[r] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (y[u] == ignore_index) continue;
+            acc += static_cast<double>(l[u]);
+            if (y[u] >= 0 && y[u] < V && am[u] == y[u]) ++nc;
+        }
     }
     __shared__ double sa[32];
     __shared__ long long sc[32];
