@@ -176,3 +176,14 @@ def test_binding_raises_loudly_on_bad_input():
     import vocabulary_lm_cross_gb300 as v
     with pytest.raises((ValueError, TypeError)):
         v.ce_fwd_bwd(torch.zeros(3, 4), torch.zeros(3, dtype=torch.int64))
+
+
+def test_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path):
+    # with no compiled library there is no CPU path: every call raises
+    import vocabulary_lm_cross_gb300 as v
+    monkeypatch.setattr(capi, "_lib", None)
+    monkeypatch.setattr(capi, "LIB", str(tmp_path / "libvlmce.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        capi.lib()
+    with pytest.raises(RuntimeError):
+        v.ce.workspace_bytes(4, 100, torch.bfloat16)
