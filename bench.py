@@ -5,17 +5,24 @@ One "step" is one ce_fwd_bwd call (label census, row kernel, finalize) over
 one batch of seeded synthetic logits already resident in HBM.  The default
 workload is bf16 logits [N=2048, V=131072] (sequence 2048 x batch 1, the
 128K vocabulary) with label smoothing 0.1, argmax and token accuracy.  The
-same run also times the fused linear cross-entropy (flce_fwd_bwd: hidden
-[4096, 6656] x weight [202048, 6656], softcap 30) and reports it in the
-line's "flce" object against the dense bf16 tensor roofline.
+same run times every other cross-entropy configuration the same way (the
+line's "configs" object: fp32 [256, 4096], bf16 [8192, 32000], bf16
+[8192, 151936] with a padded row stride and softcap 30, and 64 rows of
+151936 on both the V-split and the row kernel), the fused linear
+cross-entropy (flce_fwd_bwd: hidden [4096, 6656] x weight [202048, 6656],
+softcap 30) against the dense bf16 tensor roofline ("flce"), and companion
+legs (forward only, one vocabulary shard's rank step, SwiGLU).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-flce]
+                    [--no-configs]
     python bench.py --workload flce-bf16-4096x6656x202048-softcap30   # FLCE as the headline
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the rows of different batches never interact): weak scaling, no collective
-on the data path; the elapsed time is the max over ranks.
+on the data path; the elapsed time is the max over ranks.  A multi-GPU run
+times the headline (and its host-buffer e2e) only; the other configurations
+and legs run on one GPU.
 
 Prints ONE JSON line on rank 0.
 """
@@ -256,13 +263,193 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, w):
+# The other cross-entropy configurations timed beside the headline (one line
+# each in the "configs" object), and the few-wide-rows case on both kernels.
+CONFIG_WORKLOADS = ("ce-f32-256x4096", "ce-bf16-8192x32000",
+                    "ce-bf16-8192x151936-stride152064-softcap30-sum")
+WIDE_ROWS_WORKLOAD = "ce-bf16-64x151936-ls0.1-argmax"
+
+
+def time_ce(w, dev, steps, warmup, *, rank=0, world=1, barrier=lambda: None, sampler=None,
+            path=None, soak_s=0.0):
+    """Time ce_fwd_bwd on one workload with inputs resident in HBM.
+
+    Inputs larger than L2: a ring of copies, each timed step on a pristine one,
+    K steps back to back between two CUDA events.  Inputs that fit in L2: each
+    step on a pristine copy, a buffer twice the L2 size written before each
+    step (outside the events), one event pair per step.  Then a second pass
+    records the dominant kernel's duration per step (vlmce_profile_events).
+    ``path`` ("rows" | "split") forces the kernel through VLMCE_CE_PATH."""
     import torch
     import torch.distributed as dist
 
     import vocabulary_lm_cross_gb300 as v
     from vocabulary_lm_cross_gb300 import capi
     from vocabulary_lm_cross_gb300.workloads import make_ce_inputs
+
+    lib = capi.lib()
+    old_path = os.environ.get("VLMCE_CE_PATH")
+    if path:
+        os.environ["VLMCE_CE_PATH"] = path
+    try:
+        x0, lab = make_ce_inputs(w.resized(seed=w.seed + 1000 * rank), device=dev)
+        V = w.V
+        buf_bytes = x0.numel() * x0.element_size()
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 132e6)
+        big = buf_bytes > l2
+        n_buf = min(warmup + steps, max(2, int(64e9 // buf_bytes)))
+        bufs = [x0.clone() for _ in range(n_buf)]
+        fresh = n_buf >= warmup + steps
+        steps = min(steps, n_buf)  # every timed step on its own pristine copy
+        flush = None if big else torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+        out = v.CEResult(loss=torch.empty(w.N, dtype=torch.float32, device=dev),
+                         argmax=torch.empty(w.N, dtype=torch.int64, device=dev),
+                         reduced=torch.empty(2, dtype=torch.float32, device=dev),
+                         counts=torch.empty(4, dtype=torch.int64, device=dev))
+        ws_bytes = v.workspace_bytes(w.N, V, x0.dtype)
+        ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        plan = v.describe_plan(w.N, V, x0.dtype, w.softcap)
+
+        def step(i):
+            v.ce_fwd_bwd(bufs[i % n_buf][:, :V], lab, ignore_index=-100,
+                         label_smoothing=w.label_smoothing, softcap=w.softcap,
+                         reduction=w.reduction, grad_scale=w.grad_scale, out=out, workspace=ws)
+
+        def restore():
+            for b in bufs:
+                b.copy_(x0)
+            torch.cuda.synchronize()
+
+        def timed(i, kernel_events=None):
+            """One step; returns its event pair when the steps are timed one by one."""
+            if kernel_events is not None:
+                lib.vlmce_profile_events(ctypes_handle(kernel_events[0], stream),
+                                         ctypes_handle(kernel_events[1], stream))
+            if big:
+                step(i)
+                return None
+            flush.zero_()  # evict the previous step's lines from L2
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(i)
+            e1.record(stream)
+            return e0, e1
+
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize()
+        t_soak0 = time.time()
+        # soak: keep the GPU busy before the timed region so the clock samples
+        # describe the loaded state (untimed; the buffers then hold gradients)
+        j = 0
+        while time.time() < t_soak0 + soak_s:
+            for _ in range(10):
+                step(j)
+                j += 1
+            torch.cuda.synchronize()
+        restore()
+
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        ev0.record(stream)
+        pairs = [timed(warmup + i) for i in range(steps)]
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        ms = ev0.elapsed_time(ev1) / steps if big else \
+            statistics.fmean(e0.elapsed_time(e1) for e0, e1 in pairs)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        counts = out.counts.cpu().tolist()
+
+        # the dominant kernel's duration, events recorded by the library on the stream
+        restore()
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            timed(warmup + i, kev[i])
+        torch.cuda.synchronize()
+        kern_ms = statistics.fmean(b.elapsed_time(e) for b, e in kev)
+        del bufs, flush
+    finally:
+        if path:
+            if old_path is None:
+                os.environ.pop("VLMCE_CE_PATH", None)
+            else:
+                os.environ["VLMCE_CE_PATH"] = old_path
+    bytes_step = w.algorithmic_bytes
+    kernel = "ce_rows_kernel" if plan["kernel"] == "rows" else "ce_split_kernel"
+    peak, peak_src = load_peaks()
+    if big:
+        l2_note = (("inputs larger than L2: each timed step consumes its own fresh copy "
+                    f"of the {buf_bytes / 1e6:.0f} MB logits ({buf_bytes * n_buf / 1e9:.1f} GB)")
+                   if fresh else f"ring of {n_buf} buffers of {buf_bytes / 1e6:.0f} MB (> L2), "
+                   "restored before the timed steps, one pristine copy per timed step")
+    else:
+        l2_note = (f"{buf_bytes / 1e6:.1f} MB of logits fit in L2: a {2 * l2 / 1e6:.0f} MB buffer "
+                   "is written before every step (outside the events), each step on a pristine "
+                   "copy, one event pair per step")
+    return {"ms": ms, "kern_ms": kern_ms, "steps": steps, "bytes": bytes_step, "kernel": kernel,
+            "plan": plan,
+            "peak": peak, "peak_src": peak_src, "counts": counts, "ok": counts[3] == 0,
+            "workspace_bytes": ws_bytes, "l2": l2_note, "t0": t0, "t1": t1,
+            "t_soak0": t_soak0, "x0": x0, "lab": lab, "buf_bytes": buf_bytes,
+            "clocks": sampler.summary(t0, t1) if sampler else None}
+
+
+def config_entry(w, r):
+    """The per-configuration object of the bench line."""
+    gbs = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+    kgbs = r["bytes"] / (r["kern_ms"] * 1e-3) / 1e9
+    return {"N": w.N, "V": w.V, "row_stride": w.stride, "dtype": w.dtype,
+            "label_smoothing": w.label_smoothing, "softcap": w.softcap, "reduction": w.reduction,
+            "ms": r["ms"], "steps": r["steps"], "GB/s": gbs, "step_frac": gbs / r["peak"],
+            "roofline": {"bound": "hbm", "kernel": r["kernel"], "kernel_ms": r["kern_ms"],
+                         "achieved": kgbs, "peak": r["peak"],
+                         "peak_source": f"{r['peak_src']} (copy GB/s)", "unit": "GB/s",
+                         "frac": kgbs / r["peak"], "bytes_per_launch": r["bytes"],
+                         "traffic": recorded_traffic(r["kernel"], w.name)},
+            "workspace_bytes": r["workspace_bytes"], "plan": r["plan"],
+            "device_status_ok": r["ok"], "l2": r["l2"], "clocks": r["clocks"]}
+
+
+def run_configs(args, head_name, dev, sampler):
+    """Every other CE configuration, timed as the headline is (1 GPU)."""
+    import torch
+
+    from vocabulary_lm_cross_gb300.workloads import CE_WORKLOADS
+    steps = max(5, min(args.steps, 30))
+    out = {}
+    for name in CONFIG_WORKLOADS:
+        if name == head_name:
+            continue
+        w = CE_WORKLOADS[name]
+        out[name] = config_entry(w, time_ce(w, dev, steps, args.warmup, sampler=sampler))
+        torch.cuda.empty_cache()
+    w = CE_WORKLOADS[WIDE_ROWS_WORKLOAD]
+    out[w.name] = {path: config_entry(w, time_ce(w, dev, steps, args.warmup, sampler=sampler,
+                                                 path=path))
+                   for path in ("split", "rows")}
+    out[w.name]["note"] = ("fewer rows than SMs: the V-split kernel (a cluster per row, "
+                           "TMA-staged slices, DSMEM merge) is the default; the row kernel "
+                           "timed on the same inputs")
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import vocabulary_lm_cross_gb300 as v
 
     world = env_int("WORLD_SIZE", 1)
     rank = env_int("RANK", 0)
@@ -276,26 +463,6 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
-    lib = capi.lib()
-    x0, lab = make_ce_inputs(w.resized(seed=w.seed + 1000 * rank), device=dev)
-    V = w.V
-    buf_bytes = x0.numel() * x0.element_size()
-    n_buf = min(args.warmup + args.steps, max(2, int(64e9 // buf_bytes)))
-    bufs = [x0.clone() for _ in range(n_buf)]
-    fresh = n_buf >= args.warmup + args.steps
-    out = v.CEResult(loss=torch.empty(w.N, dtype=torch.float32, device=dev),
-                     argmax=torch.empty(w.N, dtype=torch.int64, device=dev),
-                     reduced=torch.empty(2, dtype=torch.float32, device=dev),
-                     counts=torch.empty(4, dtype=torch.int64, device=dev))
-    ws = torch.empty(v.workspace_bytes(w.N, V, x0.dtype), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i):
-        b = bufs[i % n_buf]
-        v.ce_fwd_bwd(b[:, :V], lab, ignore_index=-100, label_smoothing=w.label_smoothing,
-                     softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale, out=out,
-                     workspace=ws)
-
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -303,75 +470,42 @@ def run_ours(args, w):
         pass
     sampler = ClockSampler(uuid)
     sampler.start()
-    t_soak0 = time.time()
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    # soak: keep the GPU busy ~1 s before the timed region so the clock samples
-    # describe the loaded state (untimed; the buffers now hold gradients)
-    t_end = time.time() + 1.0
-    j = 0
-    while time.time() < t_end:
-        for _ in range(10):
-            step(j)
-            j += 1
-        torch.cuda.synchronize()
-    # restore pristine inputs for the timed steps
-    for i in range(n_buf):
-        bufs[i].copy_(x0)
-    torch.cuda.synchronize()
+    head = time_ce(w, dev, args.steps, args.warmup, rank=rank, world=world, barrier=barrier,
+                   sampler=sampler, soak_s=1.0)
+    x0, lab = head["x0"], head["lab"]
+    ms = head["ms"] * args.steps
+    kern_ms = head["kern_ms"]
+    ok_status = head["ok"]
+    V = w.V
+    stream = torch.cuda.current_stream(dev)
+    out = v.CEResult(loss=torch.empty(w.N, dtype=torch.float32, device=dev),
+                     argmax=torch.empty(w.N, dtype=torch.int64, device=dev),
+                     reduced=torch.empty(2, dtype=torch.float32, device=dev),
+                     counts=torch.empty(4, dtype=torch.int64, device=dev))
+    ws = torch.empty(v.workspace_bytes(w.N, V, x0.dtype), dtype=torch.uint8, device=dev)
 
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    t_timed0 = time.time()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    t_timed1 = time.time()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    counts = out.counts.cpu().tolist()
-    ok_status = counts[3] == 0
-
-    # per-kernel timing of the row kernel (events on the launching stream)
-    for i in range(n_buf):
-        bufs[i].copy_(x0)
-    torch.cuda.synchronize()
-    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        lib.vlmce_profile_events(ctypes_handle(kb[i], stream), ctypes_handle(ke[i], stream))
-        step(args.warmup + i)
-    torch.cuda.synchronize()
-    kern_ms = statistics.fmean(kb[i].elapsed_time(ke[i]) for i in range(args.steps))
-
-    # forward only (compute_grad=False): one read of the logits per step
-    for i in range(n_buf):
-        bufs[i].copy_(x0)
-    torch.cuda.synchronize()
-    fw_steps = min(args.steps, n_buf) if fresh else min(args.steps, 20)
+    # forward only (compute_grad=False): one read of the logits per step; the
+    # logits are not modified, so a ring of copies larger than L2 serves
+    fw_steps = min(args.steps, 20)
+    n_fw = max(2, min(fw_steps, int(2 * 129e6 // head["buf_bytes"]) + 2))
+    fbufs = [x0.clone() for _ in range(n_fw)]
     fe0 = torch.cuda.Event(enable_timing=True)
     fe1 = torch.cuda.Event(enable_timing=True)
-    for i in range(min(3, n_buf)):
-        v.ce_fwd_bwd(bufs[i][:, :V], lab, label_smoothing=w.label_smoothing, softcap=w.softcap,
-                     reduction=w.reduction, grad_scale=w.grad_scale, compute_grad=False, out=out,
-                     workspace=ws)
+
+    def fw_step(i):
+        v.ce_fwd_bwd(fbufs[i % n_fw][:, :V], lab, label_smoothing=w.label_smoothing,
+                     softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
+                     compute_grad=False, out=out, workspace=ws)
+
+    for i in range(3):
+        fw_step(i)
     torch.cuda.synchronize()
     fe0.record(stream)
     for i in range(fw_steps):
-        v.ce_fwd_bwd(bufs[i % n_buf][:, :V], lab, label_smoothing=w.label_smoothing,
-                     softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
-                     compute_grad=False, out=out, workspace=ws)
+        fw_step(i)
     fe1.record(stream)
     torch.cuda.synchronize()
+    del fbufs
     fw_ms = fe0.elapsed_time(fe1) / fw_steps
     fw_bytes = w.N * V * x0.element_size()
     peak_fw, peak_fw_src = load_peaks()
@@ -383,7 +517,7 @@ def run_ours(args, w):
                                  "unit": "GB/s",
                                  "frac": fw_bytes / (fw_ms * 1e-3) / 1e9 / peak_fw,
                                  "measured_over": "whole step (census, row kernel, finalize)"},
-                    "l2": "the ring of logits copies (each larger than L2), round robin"}
+                    "l2": f"ring of {n_fw} copies of the logits (together > 2 x L2), round robin"}
 
     # end to end through the public API with host buffers: ce_fwd_bwd_host on
     # page-locked host logits (streamed through the GPU in chunks of rows, the
@@ -432,17 +566,23 @@ def run_ours(args, w):
     h2d = w.N * row_bytes + lab_host.numel() * 8
     d2h = w.N * row_bytes + w.N * 4 + w.N * 8 + 8 + 32
     del x_host, x_pristine, ws_h
-    buf_gb = buf_bytes * n_buf / 1e9
-    del bufs
+    head.pop("x0")
+    head.pop("lab")
+    del x0, lab
     torch.cuda.empty_cache()
 
-    shard = run_shard(args, w, dev, world, barrier, sampler) if w.V % 8 == 0 else None
+    # the other configurations and the companion legs run on one GPU only: a
+    # multi-GPU run times the replicated headline alone
+    single = world == 1
+    configs = run_configs(args, w.name, dev, sampler) if single and not args.no_configs else None
+    shard = run_shard(args, w, dev, world, barrier, sampler) \
+        if single and w.V % 8 == 0 else None
     torch.cuda.empty_cache()
-    swiglu = run_swiglu(args, dev, sampler) if not args.no_flce else None
+    swiglu = run_swiglu(args, dev, sampler) if single and not args.no_flce else None
     torch.cuda.empty_cache()
 
     flce = None
-    if not args.no_flce:
+    if single and not args.no_flce:
         from vocabulary_lm_cross_gb300.workloads import FLCE_WORKLOADS
         fw = FLCE_WORKLOADS[FLCE_DEFAULT]
         f = run_flce(args, fw, min(args.steps, 10), dev, world, barrier, sampler)
@@ -451,7 +591,7 @@ def run_ours(args, w):
                 "e2e": f["e2e"], "gpu_launches": f["gpu_launches"], "clocks": f["clocks"],
                 "config": f["config"], "device_status_ok": f["ok_status"]}
         torch.cuda.empty_cache()
-        flce["row_chunked"] = run_flce_rows(fw, dev) if world == 1 else None
+        flce["row_chunked"] = run_flce_rows(fw, dev)
     sampler.stop()
 
     if rank != 0:
@@ -460,12 +600,12 @@ def run_ours(args, w):
         return
 
     bytes_step = w.algorithmic_bytes
-    plan = v.describe_plan(w.N, V, x0.dtype, w.softcap)
-    kernel_name = "ce_rows_kernel" if plan["kernel"] == "rows" else "ce_split_kernel"
+    plan = head["plan"]
+    kernel_name = head["kernel"]
     value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
     peak, peak_src = load_peaks()
     achieved = bytes_step / (kern_ms * 1e-3) / 1e9
-    clocks = sampler.summary(t_soak0, t_timed1)
+    clocks = sampler.summary(head["t_soak0"], head["t1"])
     cpu = cpu_baseline_sample(w) if world == 1 else None
     headline = w.name == "ce-bf16-2048x131072-ls0.1-argmax"
     line = {
@@ -476,12 +616,11 @@ def run_ours(args, w):
         "config": {"workload": w.name, "N": w.N, "V": V, "row_stride": w.stride,
                    "label_smoothing": w.label_smoothing, "softcap": w.softcap,
                    "reduction": w.reduction, "parallelism": f"replicas x{world}",
-                   "l2": ("inputs larger than L2: each timed step consumes its own fresh copy "
-                          f"of the {buf_bytes / 1e6:.0f} MB logits ({buf_gb:.1f} GB)") if fresh
-                         else f"ring of {n_buf} buffers of {buf_bytes / 1e6:.0f} MB (> L2)",
+                   "l2": head["l2"],
                    "vs_baseline_is": "value per GPU / 1510 GB/s = TE CE 0.711 ms on H100 "
                                      "(the pages' number, another machine: context)",
                    "device_status_ok": ok_status,
+                   "workspace_bytes": head["workspace_bytes"],
                    "plan": plan},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} (copy GB/s)", "unit": "GB/s",
@@ -495,6 +634,7 @@ def run_ours(args, w):
                 "device_status_ok": e2e_ok},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "configs": configs,
         "forward_only": forward_only,
         "swiglu": swiglu,
         "shard": shard,
@@ -943,6 +1083,8 @@ def main():
     ap.add_argument("--no-flce", action="store_true",
                     help="skip the fused linear cross-entropy and SwiGLU legs of a "
                          "cross-entropy run")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other cross-entropy configurations of a cross-entropy run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

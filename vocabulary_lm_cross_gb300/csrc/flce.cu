@@ -421,8 +421,8 @@ extern "C" vlmce_status vlmce_gemm(const void *A, int32_t a_mn, const void *B, i
     vlmce_status st = current_device(&dev);
     if (st != VLMCE_OK) return st;
     gemm::Maps maps;
-    if (!gemm::make_operand_map(&maps.a[0], A, false, a_mn != 0, M, K, lda, f16) ||
-        !gemm::make_operand_map(&maps.b[0], B, true, b_mn != 0, N, K, ldb, f16)) {
+    if (!gemm::make_operand_map(&maps.a[0], A, a_mn != 0, M, K, lda, f16) ||
+        !gemm::make_operand_map(&maps.b[0], B, b_mn != 0, N, K, ldb, f16)) {
         record_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
         return VLMCE_ERR_CUDA;
     }
@@ -511,8 +511,8 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
         // ---- pass 1: statistics of S = h' W^T over the whole vocabulary
         {
             gemm::Maps maps;
-            if (!gemm::make_operand_map(&maps.a[0], hidden, false, false, N, H, hidden_stride, f16) ||
-                !gemm::make_operand_map(&maps.b[0], weight, true, false, V, H, weight_stride, f16))
+            if (!gemm::make_operand_map(&maps.a[0], hidden, false, N, H, hidden_stride, f16) ||
+                !gemm::make_operand_map(&maps.b[0], weight, false, V, H, weight_stride, f16))
                 return map_fail();
             gemm::Params g = base;
             g.nprob = 1;
@@ -550,8 +550,8 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
             if (c >= 1) {
                 const uint16_t *wc = static_cast<const uint16_t *>(weight) + pv0 * weight_stride;
                 // grad_h (+)= G_c W_c: A = G_c K-major [N, Vc], B = W_c N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, false, N, pvc, kChunk, f16) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, true, true, H, pvc, weight_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, N, pvc, kChunk, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, true, H, pvc, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &ph = g.p[n++];
                 ph.M = static_cast<int>(N);
@@ -573,8 +573,8 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
                 const int64_t vc = (V - v0) < kChunk ? (V - v0) : kChunk;
                 const uint16_t *wc = static_cast<const uint16_t *>(weight) + v0 * weight_stride;
                 // G_c = scale (softmax - q) (1 - t^2) from the recomputed S_c = h' W_c^T
-                if (!gemm::make_operand_map(&maps.a[n], hidden, false, false, N, H, hidden_stride, f16) ||
-                    !gemm::make_operand_map(&maps.b[n], wc, true, false, vc, H, weight_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[n], hidden, false, N, H, hidden_stride, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], wc, false, vc, H, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &pg = g.p[n++];
                 pg.M = static_cast<int>(N);
@@ -587,8 +587,8 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
             }
             if (c >= 1) {
                 // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, true, pvc, N, kChunk, f16) ||
-                    !gemm::make_operand_map(&maps.b[n], hidden, true, true, H, N, hidden_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[n], gc, true, pvc, N, kChunk, f16) ||
+                    !gemm::make_operand_map(&maps.b[n], hidden, true, H, N, hidden_stride, f16))
                     return map_fail();
                 gemm::Problem &pw = g.p[n++];
                 pw.M = static_cast<int>(pvc);
@@ -704,8 +704,8 @@ extern "C" vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int
             // S_k = h'_k W^T, fp32
             {
                 gemm::Maps maps;
-                if (!gemm::make_operand_map(&maps.a[0], hk, false, false, rows, H, hidden_stride, f16) ||
-                    !gemm::make_operand_map(&maps.b[0], weight, true, false, V, H, weight_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[0], hk, false, rows, H, hidden_stride, f16) ||
+                    !gemm::make_operand_map(&maps.b[0], weight, false, V, H, weight_stride, f16))
                     return map_fail();
                 gemm::Params g = {};
                 g.nprob = 1;
@@ -747,8 +747,8 @@ extern "C" vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int
                 g.err = w.err;
                 g.out_scale = w.out_scale;
                 // grad_h_k: A = G_k K-major [rows, V], B = W N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[0], w.G, false, false, rows, V, w.ldg, f16) ||
-                    !gemm::make_operand_map(&maps.b[0], weight, true, true, H, V, weight_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[0], w.G, false, rows, V, w.ldg, f16) ||
+                    !gemm::make_operand_map(&maps.b[0], weight, true, H, V, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &ph = g.p[0];
                 ph.M = static_cast<int>(rows);
@@ -760,8 +760,8 @@ extern "C" vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int
                 ph.C16 = static_cast<uint16_t *>(grad_hidden) + n0 * hidden_stride;
                 ph.ldc16 = hidden_stride;
                 // grad_W: A = G_k^T M(=V)-major, B = h'_k N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[1], w.G, false, true, V, rows, w.ldg, f16) ||
-                    !gemm::make_operand_map(&maps.b[1], hk, true, true, H, rows, hidden_stride, f16))
+                if (!gemm::make_operand_map(&maps.a[1], w.G, true, V, rows, w.ldg, f16) ||
+                    !gemm::make_operand_map(&maps.b[1], hk, true, H, rows, hidden_stride, f16))
                     return map_fail();
                 gemm::Problem &pw = g.p[1];
                 pw.M = static_cast<int>(V);

@@ -52,10 +52,10 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
 constexpr int kMaxDevices = 64;
 
 // Clusters of `csize` CTAs that fit on the device at once (SMs of a GPC
-// that cannot complete a cluster stay idle); cached per device and size.
+// that cannot complete a cluster stay idle); cached per device.
 int co_resident_clusters(int device, int csize, cudaError_t *err) {
     static std::mutex mu;
-    static int cached[kMaxDevices][2] = {};
+    static int cached[kMaxDevices] = {};
     static bool attr_done = false;
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_done) {
@@ -67,9 +67,7 @@ int co_resident_clusters(int device, int csize, cudaError_t *err) {
         }
         attr_done = true;
     }
-    const int slot = csize == 4 ? 1 : 0;
-    if (device >= 0 && device < kMaxDevices && cached[device][slot] > 0)
-        return cached[device][slot];
+    if (device >= 0 && device < kMaxDevices && cached[device] > 0) return cached[device];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -87,28 +85,23 @@ int co_resident_clusters(int device, int csize, cudaError_t *err) {
         *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
         return 0;
     }
-    if (device >= 0 && device < kMaxDevices) cached[device][slot] = n;
+    if (device >= 0 && device < kMaxDevices) cached[device] = n;
     return n;
 }
 
 }  // namespace
 
-bool make_operand_map(CUtensorMap *m, const void *base, bool is_b, bool mn, int64_t rows,
-                      int64_t K, int64_t ld, bool f16) {
+bool make_operand_map(CUtensorMap *m, const void *base, bool mn, int64_t rows, int64_t K,
+                      int64_t ld, bool f16) {
     if (mn) return make_map(m, base, rows, K, ld, 64, 64, f16);
-    return make_map(m, base, K, rows, ld, 64, is_b ? 64 : kHalf, f16);
+    return make_map(m, base, K, rows, ld, 64, kHalf, f16);
 }
 
 cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s) {
-    // two pairs per cluster (sharing each B tile) unless a problem is at
-    // most one pair tile high
-    int npairs = 2;
-    for (int i = 0; i < a.nprob; ++i)
-        if (a.p[i].M <= BM) npairs = 1;
     int tiles = 0;
     for (int i = 0; i < a.nprob; ++i) {
         Problem &p = a.p[i];
-        p.mt = (p.M + BM * npairs - 1) / (BM * npairs);
+        p.mt = (p.M + BM - 1) / BM;
         p.tile0 = tiles;
         tiles += p.mt * ((p.N + BN - 1) / BN);
     }
@@ -118,7 +111,7 @@ cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     e = cudaSuccess;
-    const int csize = 2 * npairs;
+    constexpr int csize = 2;  // one CTA pair
     const int clusters_max = co_resident_clusters(device, csize, &e);
     if (clusters_max < 1) return e;
     const int clusters = tiles < clusters_max ? tiles : clusters_max;

@@ -18,7 +18,8 @@
 // Each CTA stages its own 128 rows of A and its own 128 rows of B (K = 64
 // per stage, 128-byte swizzle) in a 6-stage ring, so a CTA moves a third
 // less operand data per flop than a single-SM 128 x 256 tile would, and each
-// CTA's TMEM receives its 128 rows of the tile.  CTA = 6 warps:
+// CTA's TMEM receives its 128 rows of the tile.  Every operand copy is a
+// plain load into the issuing CTA's own shared memory.  CTA = 6 warps:
 //   warp 0      one lane issues the TMA loads of this CTA's halves; the
 //               copies of both CTAs count on the leader's "full" barrier;
 //   warp 1      allocates 512 TMEM columns per SM (two 128 x 256 fp32
@@ -88,15 +89,15 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int *er
 struct Tile {
     int p, m0, n0;
 };
-// Cluster tile t of the launch: problem, first row (BM x npairs rows), first column.
-__device__ __forceinline__ Tile tile_of(const Params &a, int t, int npairs) {
+// Pair tile t of the launch: problem, first row, first column.
+__device__ __forceinline__ Tile tile_of(const Params &a, int t) {
     int p = 0;
 #pragma unroll
     for (int i = 1; i < kMaxProblems; ++i)
         if (i < a.nprob && t >= a.p[i].tile0) p = i;
     const int lt = t - a.p[p].tile0;
     const int mt = a.p[p].mt;
-    return Tile{p, (lt % mt) * (BM * npairs), (lt / mt) * BN};
+    return Tile{p, (lt % mt) * BM, (lt / mt) * BN};
 }
 
 // ------------------------------------------------------------ epilogues
@@ -275,9 +276,8 @@ __device__ __forceinline__ void grad_chunk(const Params &a, const Problem &P, co
 }
 
 // ------------------------------------------------------------ the kernel
-// Launched with clusters of 2 or 4 CTAs (one or two pairs; the even CTA of
-// a pair is its leader) and a grid of co-resident clusters; needs
-// kSmemBytes of dynamic shared memory.
+// Launched with clusters of 2 CTAs (one pair; CTA 0 is its leader) and a
+// grid of co-resident clusters; needs kSmemBytes of dynamic shared memory.
 __global__ void __launch_bounds__(kThreads, 1)
     vlmce_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params a) {
     extern __shared__ unsigned char smem_raw[];
@@ -295,13 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t crank = ptx::cluster_ctarank();
-    const int npairs = static_cast<int>(ptx::cluster_nctarank()) >> 1;  // 1 or 2
-    const int pair = static_cast<int>(crank >> 1);
-    const uint32_t prank = crank & 1u;  // 0: the pair's leader
-    const uint32_t leader = crank & ~1u;
-    const uint16_t all_ctas = static_cast<uint16_t>((1u << (2 * npairs)) - 1u);
-    const uint16_t pair_ctas = static_cast<uint16_t>(3u << (2 * pair));
+    const uint32_t prank = ptx::cluster_ctarank();  // 0: the pair's leader
+    const uint16_t pair_ctas = 3u;
     const int cluster = static_cast<int>(ptx::cluster_id_x());
     const int nclusters = static_cast<int>(ptx::ncluster_x());
 
@@ -309,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             // leader: its producer's arrival + the bytes of both CTAs of the pair
             ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), npairs);  // one commit from every pair's leader
+            ptx::mbar_init(empty(s), 1);  // one commit from the leader's MMA issuer
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull(b), 1);
@@ -335,23 +330,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---- TMA producer (every CTA).  A: this CTA's 128 rows.  B: this
-        // CTA's 128-row half of the pair's B tile, made of two 64-row slices;
-        // with two pairs each CTA loads one slice and multicasts it to the
-        // CTA of the other pair that holds the same half.  Every copy counts
-        // on the full barrier of the receiving CTA's pair leader.
+        // ---- TMA producer (every CTA): this CTA's 128 rows of A and its
+        // 128-row half of the pair's B tile.  Every copy counts on the full
+        // barrier of the pair leader.
         if (lane == 0) {
-            const uint32_t full_leader = ptx::mapa(full(0), leader);
-            const uint16_t b_mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+            const uint32_t full_leader = ptx::mapa(full(0), 0);
             int s = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
             for (int t = cluster; t < a.tiles; t += nclusters) {
-                const Tile tl = tile_of(a, t, npairs);
+                const Tile tl = tile_of(a, t);
                 const Problem &P = a.p[tl.p];
                 const CUtensorMap *ma = &maps.a[tl.p];
                 const CUtensorMap *mb = &maps.b[tl.p];
-                const int ar = tl.m0 + BM * pair + kHalf * static_cast<int>(prank);
+                const int ar = tl.m0 + kHalf * static_cast<int>(prank);
                 const int br = tl.n0 + kHalf * static_cast<int>(prank);
                 const int kblocks = (P.K + BK - 1) / BK;
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -359,19 +351,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (prank == 0) ptx::mbar_arrive_expect_tx(full(s), 2 * kStageBytes);
                     const uint32_t sa = ring + s * kStageBytes, sb = sa + kOpBytes;
                     const uint32_t fb = full_leader + 8u * s;
+                    // K-major: one 64 x 128 box; MN-major: two 64 x 64 boxes
                     if (!P.a_mn) {
                         tc::tma_load_2d_pair(sa, ma, kb * BK, ar, fb);
                     } else {
                         tc::tma_load_2d_pair(sa, ma, ar, kb * BK, fb);
                         tc::tma_load_2d_pair(sa + 8192, ma, ar + 64, kb * BK, fb);
                     }
-                    for (int q = (npairs == 2 ? pair : 0); q < 2; q += npairs) {
-                        const int c0 = P.b_mn ? br + 64 * q : kb * BK;
-                        const int c1 = P.b_mn ? kb * BK : br + 64 * q;
-                        if (npairs == 2)
-                            tc::tma_load_2d_pair_multicast(sb + 8192 * q, mb, c0, c1, fb, b_mask);
-                        else
-                            tc::tma_load_2d_pair(sb + 8192 * q, mb, c0, c1, fb);
+                    if (!P.b_mn) {
+                        tc::tma_load_2d_pair(sb, mb, kb * BK, br, fb);
+                    } else {
+                        tc::tma_load_2d_pair(sb, mb, br, kb * BK, fb);
+                        tc::tma_load_2d_pair(sb + 8192, mb, br + 64, kb * BK, fb);
                     }
                     ++issued;
                     if (++s == kStages) {
@@ -397,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             int it = 0;
             for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
-                const Tile tl = tile_of(a, t, npairs);
+                const Tile tl = tile_of(a, t);
                 const Problem &P = a.p[tl.p];
                 const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, P.a_mn != 0, P.b_mn != 0, a.f16 != 0);
                 const int kblocks = (P.K + BK - 1) / BK;
@@ -417,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    : tc::smem_desc_sw128(sb + 32 * kk, 16, 1024);
                         tc::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    tc::mma_commit_pair(empty(s), all_ctas);  // the stage is free everywhere
+                    tc::mma_commit_pair(empty(s), pair_ctas);  // the stage is free in both CTAs
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1;
@@ -425,17 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::mma_commit_pair(tfull(b), pair_ctas);
             }
-            tc::mma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
+            tc::mma_commit_pair(drain, static_cast<uint16_t>(1u << prank));
             drain_bar(drain, 0, a.err);
         }
     } else {
         // ---- epilogue: warps 2-5 of every CTA, TMEM subpartition warp % 4
         const int q = warp & 3;
-        const int rl = BM * pair + static_cast<int>(prank) * kHalf + q * 32 + lane;
-        const uint32_t tempty_leader = ptx::mapa(tempty(0), leader);
+        const int rl = static_cast<int>(prank) * kHalf + q * 32 + lane;
+        const uint32_t tempty_leader = ptx::mapa(tempty(0), 0);
         int it = 0;
         for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
-            const Tile tl = tile_of(a, t, npairs);
+            const Tile tl = tile_of(a, t);
             const Problem &P = a.p[tl.p];
             const int b = it & 1;
             wait_bar(tfull(b), (it >> 1) & 1, abort, a.err);

@@ -12,15 +12,15 @@
 namespace vlmce {
 namespace gemm {
 
-// Tensor map of operand A (rows = M) or B (is_b, rows = N) of C = A B^T,
-// bf16 (fp16 with f16): K-major ([rows, ld], K contiguous) or MN-major
-// ([K, ld], rows contiguous).  Out-of-range elements read as zero.  False if
-// the driver refuses it.
-bool make_operand_map(CUtensorMap *m, const void *base, bool is_b, bool mn, int64_t rows,
-                      int64_t K, int64_t ld, bool f16 = false);
+// Tensor map of operand A (rows = M) or B (rows = N) of C = A B^T, bf16
+// (fp16 with f16): K-major ([rows, ld], K contiguous; boxes of 64 K x 128
+// rows) or MN-major ([K, ld], rows contiguous; boxes of 64 x 64).
+// Out-of-range elements read as zero.  False if the driver refuses it.
+bool make_operand_map(CUtensorMap *m, const void *base, bool mn, int64_t rows, int64_t K,
+                      int64_t ld, bool f16 = false);
 
 // Fill p.mt / p.tile0 / a.tiles from the problems' shapes and launch them on
-// `s` as one persistent grid of clusters of one or two CTA pairs (a.nprob
+// `s` as one persistent grid of clusters of one CTA pair (a.nprob
 // problems, maps.a/b[i] for problem i).  Returns the launch error.
 cudaError_t launch_group(const Maps &maps, Params &a, cudaStream_t s);
 

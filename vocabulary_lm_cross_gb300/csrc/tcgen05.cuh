@@ -1,8 +1,8 @@
 // tcgen05.cuh -- inline-PTX wrappers for the sm_100-family tensor cores,
 // in their CTA-pair form (.cta_group::2: one MMA spans the tensor cores of
 // two SMs of a cluster): tensor-memory (TMEM) allocation, tcgen05.mma with
-// bf16 operands and fp32 accumulators, commits multicast to mbarriers of
-// several CTAs, TMEM loads, tiled TMA loads (plain and multicast), and the
+// bf16 operands and fp32 accumulators, commits that arrive on the mbarriers
+// of both CTAs of the pair, TMEM loads, tiled TMA loads, and the
 // shared-memory / instruction descriptors the MMA consumes.  Every tcgen05
 // instruction of a kernel must use the same .cta_group.
 #pragma once
@@ -92,18 +92,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
         ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(tm), "r"(c0), "r"(c1), "r"(mbar_leader)
-        : "memory");
-}
-// Pair form, multicast: the box goes to shared-memory offset `dst` of every
-// CTA in `cta_mask`; the bytes each CTA receives are counted on the barrier
-// at the offset of `mbar_leader` in the leader CTA of that CTA's pair.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap *tm,
-                                                           int c0, int c1, uint32_t mbar_leader,
-                                                           uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(tm), "r"(c0), "r"(c1), "r"(mbar_leader), "h"(cta_mask)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {

@@ -30,15 +30,6 @@ def _check(logits, labels):
         raise ValueError("logits rows must be contiguous (stride(1) == 1)")
 
 
-def lse(stats: torch.Tensor) -> torch.Tensor:
-    """log-sum-exp of z per row from row statistics [N, 8]."""
-    return stats[:, 2] + torch.log(stats[:, 3])
-
-
-def argmax(stats: torch.Tensor) -> torch.Tensor:
-    return stats.view(torch.int32)[:, 1]
-
-
 def _stats_out(out, N, dev):
     if out is None:
         return torch.empty((N, 8), dtype=torch.float32, device=dev)
