@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
         c.nlseL = -lse * kLog2e;
         c.T = T;
         c.k2 = k2;
+        rows::set_flush<BF16, SOFTCAP>(c, lse);
         // the label's granule and lane when this shard holds it
         const int64_t yl = y - p.vocab_start;
         const bool mine = yl >= 0 && yl < p.V_local;
