@@ -395,7 +395,9 @@ void vlmce_flce_profile_events(void *ev_begin, void *ev_end);
  * calls that overlap on the GPU (different streams without ordering between
  * them) race on it and must not be issued; calls ordered on one stream are
  * safe.  The array keeps the last call's contents, none of which a call needs
- * to start at zero.
+ * to start at zero.  The looked-up address is kept for the life of the
+ * process: the entry point serves the primary context of each device (the
+ * one the CUDA runtime uses), and not calls made after cudaDeviceReset.
  */
 vlmce_status ce_fwd_bwd_noalloc(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
                                 int64_t V, int64_t row_stride, int64_t ignore_index,

@@ -56,11 +56,15 @@ def _z(S: np.ndarray, softcap: float) -> np.ndarray:
 def row_stats(h: np.ndarray, W_bits: np.ndarray, labels: np.ndarray, *, softcap: float = 0.0,
               block: int = 8192) -> dict:
     """Per row over the whole vocabulary, W (bf16 bits [V, H]) streamed in
-    blocks of `block` rows: lse of z, first argmax of S, z at the label, sum z."""
+    blocks of `block` rows: lse of z, first argmax of S, z at the label, sum z,
+    and the two largest logits S (``top``, ``second``: the largest two entries
+    of the row counted with multiplicity, so a duplicated maximum gives
+    second = top).  top - second is how close a row is to an argmax tie."""
     N = h.shape[0]
     V = W_bits.shape[0]
     lse = np.full(N, -np.inf)
     best = np.full(N, -np.inf)
+    second = np.full(N, -np.inf)
     amax = np.zeros(N, np.int64)
     zy = np.zeros(N)
     sumz = np.zeros(N)
@@ -72,20 +76,24 @@ def row_stats(h: np.ndarray, W_bits: np.ndarray, labels: np.ndarray, *, softcap:
         lse = np.logaddexp(lse, logsumexp(z, axis=1))
         bm = S.max(axis=1)
         bi = S.argmax(axis=1)  # first occurrence in the block
+        # the block's second largest (with multiplicity), merged with the running pair
+        b2 = np.partition(S, -2, axis=1)[:, -2] if S.shape[1] >= 2 else np.full(N, -np.inf)
+        second = np.maximum(np.minimum(best, bm), np.maximum(second, b2))
         upd = bm > best        # strictly greater: earlier blocks keep ties
         best = np.where(upd, bm, best)
         amax = np.where(upd, v0 + bi, amax)
         sumz += z.sum(axis=1)
         inb = (labels >= v0) & (labels < v1)
         zy[inb] = z[rows[inb], labels[inb] - v0]
-    return dict(lse=lse, argmax=amax, zy=zy, sumz=sumz)
+    return dict(lse=lse, argmax=amax, zy=zy, sumz=sumz, top=best, second=second)
 
 
 def sampled(h_bits: np.ndarray, W_bits: np.ndarray, labels: np.ndarray, rows, cols, *,
             ignore_index: int = -100, label_smoothing: float = 0.0, softcap: float = 0.0,
             reduction: str = "mean", grad_scale: float = 1.0, block: int = 8192) -> dict:
-    """Loss, argmax and reduced values of every row; grad_hidden of `rows`;
-    grad_weight of vocabulary rows `cols`.  h_bits [N, H], W_bits [V, H]: bf16 bits."""
+    """Loss, argmax, the two largest logits and reduced values of every row;
+    grad_hidden of `rows`; grad_weight of vocabulary rows `cols`.  h_bits
+    [N, H], W_bits [V, H]: bf16 bits."""
     h = widen_bf16(h_bits)
     V = W_bits.shape[0]
     labels = np.asarray(labels, np.int64)
@@ -102,7 +110,8 @@ def sampled(h_bits: np.ndarray, W_bits: np.ndarray, labels: np.ndarray, rows, co
     red, acc, n_correct = ce.reduce(loss, st["argmax"], labels, V, ignore_index, reduction)
     # hidden gradient of the sampled rows: their full logits through the CE oracle
     out = dict(loss=loss, argmax=st["argmax"], lse=st["lse"], reduced_loss=red, accuracy=acc,
-               n_valid=n_valid, n_correct=n_correct, n_bad=n_bad, row_scale=s)
+               n_valid=n_valid, n_correct=n_correct, n_bad=n_bad, row_scale=s, top=st["top"],
+               second=st["second"])
     if rows.size:
         hR = h[rows]
         SR = np.concatenate([hR @ widen_bf16(W_bits[v0:v0 + block]).T

@@ -16,6 +16,11 @@ Tolerances (stated once, used by every parity test):
   plus the MUFU exp2 error of about 2^-22; 3e-7 T: with the softcap,
   z = T tanh(x/T) is formed from 1 - exp(-2|x|/T), whose exp2 error of
   2^-22 turns into an absolute error of at most T 2^-22 in z).
+  The 4e-6 covers exponents e_j = (z_j - lse) log2 e and lse log2 e below 64
+  in magnitude.  Where the test supplies the inputs and lse, kappa is taken
+  per element as max(kappa(T), 1.35 (ln 2 (h(e_j) + h(lse log2 e)) + 2^-22)
+  + 3e-7 T), h(a) = half an fp32 ulp at a: the same two roundings for larger
+  exponents (rows with a wide spread, subnormal gradients).
   An element is "well conditioned" when that error term is at most half an
   ulp: kappa (|g_o| + |scale| q_j) <= ulp(g_o) / 2.  Every well-conditioned
   bf16 element must be within 1 ulp of RN(g_o) by ordered-integer distance
@@ -35,6 +40,34 @@ KAPPA_PER_T = 3e-7
 
 def kappa(softcap: float) -> float:
     return KAPPA0 + KAPPA_PER_T * softcap
+
+
+def half_ulp32(a: np.ndarray) -> np.ndarray:
+    """Half the fp32 spacing at |a| (normal range; 2^-150 below it)."""
+    a = np.abs(np.asarray(a, np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.exp2(np.maximum(e, -126) - 24)
+
+
+def kappa_elementwise(x64: np.ndarray, lse: np.ndarray, softcap: float) -> np.ndarray:
+    """Per-element kappa for rows x64 [n, V] (fp64 inputs) with fp64 lse [n]."""
+    z = softcap * np.tanh(x64 / softcap) if softcap > 0 else x64
+    lg = np.asarray(lse, np.float64)[:, None] * LOG2E
+    e = z * LOG2E - lg
+    k = 1.35 * (LN2 * (half_ulp32(e) + half_ulp32(lg)) + 2.0 ** -22) + KAPPA_PER_T * softcap
+    return np.maximum(kappa(softcap), k)
+
+
+def row_lse(x64: np.ndarray, softcap: float) -> np.ndarray:
+    """fp64 log-sum-exp of z per row (tolerance model only)."""
+    from scipy.special import logsumexp
+    z = softcap * np.tanh(x64 / softcap) if softcap > 0 else x64
+    return logsumexp(z, axis=1)
+
+
+LOG2E = 1.4426950408889634
+LN2 = 0.6931471805599453
 
 
 LOSS_ATOL = 1e-4
@@ -64,8 +97,14 @@ def ordered(bits: np.ndarray) -> np.ndarray:
 
 def check_grad(got: np.ndarray, ref: np.ndarray, labels: np.ndarray, V: int, eps: float,
                scale: float, dtype: str, softcap: float = 0.0, ignore_index: int = -100,
-               what: str = "grad") -> dict:
-    """got: [n, V] stored gradient (uint16 bf16 bits or float32); ref: fp64 [n, V]."""
+               what: str = "grad", x64: np.ndarray | None = None) -> dict:
+    """got: [n, V] stored gradient (uint16 bf16 bits or float32); ref: fp64 [n, V];
+    x64: the rows' fp64 inputs [n, V], if given, for the per-element kappa.
+
+    Returns statistics: the largest error / tolerance, and for bf16 the
+    fraction of well-conditioned elements, their largest ulp distance from
+    RN(oracle), and the count and largest ulp distance of the ill-conditioned
+    ones (where p_j ~ q_j and only the absolute bound applies)."""
     n = ref.shape[0]
     q = np.full((n, V), eps / V)
     rows = np.arange(n)
@@ -77,7 +116,8 @@ def check_grad(got: np.ndarray, ref: np.ndarray, labels: np.ndarray, V: int, eps
     else:
         g = got.astype(np.float64)
     u = ulp(ref, dtype)
-    cond = kappa(softcap) * (np.abs(ref) + abs(scale) * q)
+    k = kappa(softcap) if x64 is None else kappa_elementwise(x64, row_lse(x64, softcap), softcap)
+    cond = k * (np.abs(ref) + abs(scale) * q)
     tol = u + cond
     err = np.abs(g - ref)
     bad = ~(err <= tol)
@@ -93,6 +133,8 @@ def check_grad(got: np.ndarray, ref: np.ndarray, labels: np.ndarray, V: int, eps
         stats["well_conditioned_frac"] = float(np.mean(well))
         stats["max_ulp_well_conditioned"] = int(d[well].max()) if well.any() else 0
         stats["within_1ulp_frac"] = float(np.mean(d <= 1))
+        stats["ill_conditioned"] = int((~well).sum())
+        stats["max_ulp_ill_conditioned"] = int(d[~well].max()) if (~well).any() else 0
         if well.any() and d[well].max() > 1:
             i, j = np.argwhere(well & (d > 1))[0]
             raise AssertionError(

@@ -11,7 +11,7 @@ import torch
 
 import vocabulary_lm_cross_gb300 as v
 from oracle import ce as oc
-from tests.parity import bf16_bits_np, check_grad, check_loss, check_reduced
+from tests.parity import bf16_bits_np, bits_to_f64, check_grad, check_loss, check_reduced
 from vocabulary_lm_cross_gb300.workloads import (CE_WORKLOADS, IGNORE_INDEX, CEWorkload,
                                                  make_ce_inputs)
 
@@ -39,43 +39,57 @@ def got_rows(x: torch.Tensor, dtype: str) -> np.ndarray:
 def run_and_check(w: CEWorkload, *, full_grad: bool = True, sample_rows=None, env=None,
                   monkeypatch=None):
     x, lab = make_ce_inputs(w, device=DEV)
-    V = w.V
-    xin = host_rows(x, w.dtype)
-    labh = lab.cpu().numpy()
     for key, val in (env or {}).items():
         monkeypatch.setenv(key, val)
-    res = v.ce_fwd_bwd(x[:, :V], lab, ignore_index=IGNORE_INDEX, label_smoothing=w.label_smoothing,
-                       softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale)
+    return check_call(x, lab, w.V, w.dtype, eps=w.label_smoothing, T=w.softcap,
+                      red=w.reduction, gs=w.grad_scale, full_grad=full_grad,
+                      sample_rows=sample_rows)
+
+
+def check_call(x, lab, V, dtype, *, eps, T, red, gs, full_grad=True, sample_rows=None):
+    """ce_fwd_bwd on the device rows x[:, :V] (row stride x.stride(0)) against the oracle."""
+    xin = host_rows(x, dtype)
+    labh = lab.cpu().numpy()
+    N = x.shape[0]
+    res = v.ce_fwd_bwd(x[:, :V], lab, ignore_index=IGNORE_INDEX, label_smoothing=eps,
+                       softcap=T, reduction=red, grad_scale=gs)
     torch.cuda.synchronize()
-    out = got_rows(x, w.dtype)
+    out = got_rows(x, dtype)
     # loss / argmax / reductions over every row (oracle without the gradient)
-    ref = oc.ce_fwd_bwd(xin, w.dtype, V, labh, label_smoothing=w.label_smoothing,
-                        softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
-                        want_grad=False)
+    ref = oc.ce_fwd_bwd(xin, dtype, V, labh, label_smoothing=eps, softcap=T, reduction=red,
+                        grad_scale=gs, want_grad=False)
     check_loss(res.loss.cpu().numpy(), ref["loss"])
     assert np.array_equal(res.argmax.cpu().numpy(), ref["argmax"])
     counts = res.counts.cpu().numpy()
     assert counts[0] == ref["n_valid"] and counts[1] == ref["n_correct"]
     assert counts[2] == ref["n_bad"] and counts[3] == 0
-    red = res.reduced.cpu().numpy()
-    check_reduced(float(red[0]), ref["reduced_loss"], w.reduction)
-    assert red[1] == np.float32(ref["accuracy"])
+    red_out = res.reduced.cpu().numpy()
+    check_reduced(float(red_out[0]), ref["reduced_loss"], red)
+    assert red_out[1] == np.float32(ref["accuracy"])
     # gradient, element by element
-    rows = np.arange(w.N) if full_grad else np.asarray(sample_rows)
+    rows = np.arange(N) if full_grad else np.asarray(sample_rows)
     if rows.size:
-        _, _, g = oc.rows(xin[rows], w.dtype, V, labh[rows], ignore_index=IGNORE_INDEX,
-                          label_smoothing=w.label_smoothing, softcap=w.softcap,
-                          row_scale=ref["row_scale"])
-        stats = check_grad(out[rows][:, :V], g, labh[rows], V, w.label_smoothing,
-                           ref["row_scale"], w.dtype, softcap=w.softcap)
+        _, _, g = oc.rows(xin[rows], dtype, V, labh[rows], ignore_index=IGNORE_INDEX,
+                          label_smoothing=eps, softcap=T, row_scale=ref["row_scale"])
+        x64 = (bits_to_f64(xin[rows][:, :V]) if dtype == "bf16"
+               else xin[rows][:, :V].astype(np.float64))
+        stats = check_grad(out[rows][:, :V], g, labh[rows], V, eps, ref["row_scale"], dtype,
+                           softcap=T, x64=x64)
+        stats["oracle_grad"] = g
+        stats["rows"] = rows
     else:
         stats = {}
     # padding columns untouched
-    if w.stride > V:
+    if x.shape[1] > V:
         before = xin[:, V:]
         after = out[:, V:]
         assert np.array_equal(before.view(np.uint8), after.view(np.uint8)), "padding modified"
     return res, ref, stats
+
+
+def brief(stats):
+    """The scalar statistics of check_grad (well- and ill-conditioned elements)."""
+    return {k: v for k, v in stats.items() if k not in ("oracle_grad", "rows")}
 
 
 def small(N, V, dtype="bf16", stride=0, eps=0.0, T=0.0, reduction="mean", gs=1.0, seed=7,
@@ -133,12 +147,17 @@ def test_both_kernels_on_the_same_rows(path, monkeypatch):
 
 
 def test_plans_of_the_benchmarked_workloads():
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
     for name, w in CE_WORKLOADS.items():
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         pl = v.describe_plan(w.N, w.V, dt, w.softcap)
         assert pl["ctas_per_row"] * pl["granules_per_cta"] * (8 if w.dtype == "bf16" else 4) >= w.V
-        assert pl["kernel"] == "rows" and pl["resident"] >= 1, (name, pl)
-        assert pl["ctas_per_row"] == 1 and pl["threads"] in (256, 1024), (name, pl)
+        assert pl["resident"] >= 1, (name, pl)
+        if w.N < sms:  # fewer rows than SMs: a cluster of CTAs per row
+            assert pl["kernel"] == "split" and pl["ctas_per_row"] > 1, (name, pl)
+        else:
+            assert pl["kernel"] == "rows", (name, pl)
+            assert pl["ctas_per_row"] == 1 and pl["threads"] in (256, 1024), (name, pl)
         print(name, pl)
 
 
@@ -151,6 +170,31 @@ def test_widest_rows_of_each_kernel(monkeypatch):
     monkeypatch.setenv("VLMCE_CE_PATH", "rows")
     run_and_check(small(2, (1 << 21) + 3, "bf16", eps=0.1, ignore=0.0))
     run_and_check(small(2, (1 << 20) + 1, "f32", eps=0.0, ignore=0.0))
+
+
+# Rows whose logits spread over more than 87 (no softcap, or a softcap above
+# about 37): p_j = exp(z_j - lse) falls below 2^-126, where the MUFU exp2
+# flushes to zero, yet scale p_j is a representable fp32 / bf16 subnormal
+# gradient (sum reduction, grad_scale 1, eps 0: g_j = p_j).  Every element
+# must meet the same tolerance as elsewhere (1 ulp of the subnormal spacing).
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T,lo,hi", [(0.0, -140.0, 5.0), (0.0, -125.0, 0.0), (80.0, -420.0, 90.0)])
+@pytest.mark.parametrize("path", ["rows", "split"])
+def test_gradients_in_the_subnormal_range(dtype, T, lo, hi, path, monkeypatch):
+    N, V, stride = 41, 20011, 20016
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(hi - lo) + (T > 0))
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.full((N, stride), float("nan"), dtype=dt)
+    x[:, :V] = (lo + (hi - lo) * torch.rand((N, V), generator=g)).to(dt)
+    lab = torch.randint(0, V, (N,), generator=g)
+    lab[::9] = IGNORE_INDEX
+    monkeypatch.setenv("VLMCE_CE_PATH", path)
+    _, ref, stats = check_call(x.to(DEV), lab.to(DEV), V, dtype, eps=0.0, T=T, red="sum", gs=1.0)
+    go = stats["oracle_grad"]
+    sub = (np.abs(go) < 2.0 ** -126) & (np.abs(go) >= 2.0 ** -133)  # bf16-representable subnormals
+    assert sub.sum() > 1000, int(sub.sum())  # the case is exercised
+    print(dtype, T, path, "subnormal gradients", int(sub.sum()), brief(stats))
 
 
 def test_no_rows():
@@ -248,4 +292,4 @@ def test_full_size_workloads(name):
     torch.cuda.empty_cache()
     rows = _sample(w.N, labh, extra=dup_rows[:40])
     _, ref, stats = run_and_check(w, full_grad=False, sample_rows=rows)
-    print(name, stats)
+    print(name, brief(stats))

@@ -117,3 +117,35 @@ def test_grad_columns_equals_the_row_gradient_given_the_row_lse():
     gc = oc.grad_columns(x[:, cols], cols, V, lab, lse, np.full(n, 0.5), label_smoothing=0.3,
                          softcap=6.0)
     np.testing.assert_allclose(gc, r["grad"][:, cols], rtol=1e-11, atol=1e-16)
+
+
+@pytest.mark.parametrize("block", [1, 3, 7, 64])
+def test_row_stats_two_largest_logits_against_a_full_sort(block):
+    # brute force: the two largest entries of each fully formed row of S
+    # (with multiplicity), including maxima duplicated in one block, across
+    # blocks, and rows whose runner-up sits in an earlier block
+    g = rng(8)
+    N, H, V = 12, 16, 37
+    h = g.normal(0, 1, (N, H))
+    Wf = g.normal(0, 0.5, (V, H))
+    Wf[20] = Wf[5]          # exact duplicate column (any h): duplicated maximum possible
+    Wf[6] = Wf[5]           # in the same block as column 5 for blocks >= 7
+    h[0] = 0.0              # a row of all-equal logits
+    Wb = bf16_bits(Wf)
+    lab = g.integers(0, V, N)
+    st = of.row_stats(h, Wb, lab, block=block)
+    # one product per row and column, in Python loops (fp64 dot products; the
+    # blocked matmuls may round the last bit differently)
+    W64 = of.widen_bf16(Wb)
+    S = np.array([[float(np.dot(h[i], W64[j])) for j in range(V)] for i in range(N)])
+    srt = np.sort(S, axis=1)
+    np.testing.assert_allclose(st["top"], srt[:, -1], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(st["second"], srt[:, -2], rtol=1e-13, atol=1e-15)
+    # the argmax is a column holding the maximum (up to the last-bit rounding
+    # of duplicated columns)
+    at = S[np.arange(N), st["argmax"]]
+    np.testing.assert_allclose(at, srt[:, -1], rtol=1e-13, atol=1e-15)
+    # the duplicated columns make near-exact ties: second = top on those rows
+    dup = np.isclose(S[:, 5], srt[:, -1], rtol=1e-13, atol=1e-15)
+    assert dup.any()
+    np.testing.assert_allclose(st["second"][dup], st["top"][dup], rtol=1e-13, atol=1e-15)

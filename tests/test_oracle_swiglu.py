@@ -50,3 +50,56 @@ def test_closed_forms():
     r = -1.2784645427610738
     xr = np.array([[r, 1.0]])
     assert abs(osw.backward(xr, np.ones((1, 1)), 1)[0, 0]) < 1e-12
+
+
+def test_backward_terms_bound_the_gradient_and_equal_it_without_cancellation():
+    # |d_gate| <= t_gate with equality when both products share a sign (gate
+    # a >= 0), and d_up is a single product, so t_up = |d_up|
+    g = np.random.default_rng(6)
+    T, n = 9, 17
+    x = g.normal(0, 3, (T, 2 * n))
+    dy = g.normal(0, 1, (T, n))
+    d = osw.backward(x, dy, n)
+    t = osw.backward_terms(x, dy, n)
+    assert np.all(np.abs(d) <= t * (1 + 1e-14))
+    a = x[:, :n]
+    np.testing.assert_allclose(t[:, :n][a >= 0], np.abs(d[:, :n][a >= 0]), rtol=1e-14)
+    np.testing.assert_allclose(t[:, n:], np.abs(d[:, n:]), rtol=1e-14)
+
+
+def test_backward_terms_against_torch_pieces():
+    # the two products of d_gate from torch: dy b sigmoid(a), and dy b a sigmoid'(a)
+    # with sigmoid' from autograd; the product of d_up as dy silu(a)
+    g = np.random.default_rng(7)
+    T, n = 5, 11
+    x = g.normal(0, 4, (T, 2 * n))
+    dy = g.normal(0, 1, (T, n))
+    a = torch.tensor(x[:, :n], requires_grad=True)
+    b = torch.tensor(x[:, n:])
+    dyt = torch.tensor(dy)
+    s = torch.sigmoid(a)
+    s.backward(torch.ones_like(s))
+    ds = a.grad
+    t_gate = (dyt * b * s).abs() + (dyt * b * a.detach() * ds).abs()
+    t_up = (dyt * torch.nn.functional.silu(a.detach())).abs()
+    want = torch.cat([t_gate, t_up], dim=1).detach().numpy()
+    np.testing.assert_allclose(osw.backward_terms(x, dy, n), want, rtol=1e-13, atol=1e-300)
+
+
+def test_backward_terms_hand_worked():
+    # a = 0: sigmoid = 1/2 -> t_gate = |dy b| / 2, t_up = 0
+    # a = 2, b = 3, dy = -1: sigmoid(2) = 0.8807970779778823;
+    #   t_gate = 3 s + 3 * 2 * s (1 - s), t_up = 2 s
+    # at the zero r of silu' (1 + r (1 - s) = 0), t_gate = 2 |dy b s(r)| while d_gate = 0
+    s2 = 0.8807970779778823
+    r = -1.2784645427610738
+    sr = 1.0 / (1.0 + np.exp(-r))
+    x = np.array([[0.0, 2.0, r, 5.0, 3.0, 1.5]])
+    dy = np.array([[2.0, -1.0, 1.0]])
+    t = osw.backward_terms(x, dy, 3)[0]
+    np.testing.assert_allclose(t[0], 5.0, rtol=1e-15)
+    np.testing.assert_allclose(t[1], 3 * s2 + 6 * s2 * (1 - s2), rtol=1e-14)
+    np.testing.assert_allclose(t[2], 2 * 1.5 * sr, rtol=1e-12)
+    assert t[3] == 0.0
+    np.testing.assert_allclose(t[4], 2 * s2, rtol=1e-14)
+    np.testing.assert_allclose(t[5], abs(r) * sr, rtol=1e-14)

@@ -27,7 +27,9 @@ def _built():
     build.build()
 
 
-def _noalloc(x: torch.Tensor, lab: torch.Tensor, w: CEWorkload):
+def _noalloc(x: torch.Tensor, lab: torch.Tensor, w: CEWorkload, row_outputs: bool = True):
+    """One ce_fwd_bwd_noalloc call; without row outputs the per-row losses and
+    argmaxes live only in the library's fixed scratch."""
     N, V = w.N, w.V
     out = dict(loss=torch.empty(N, dtype=torch.float32, device=DEV),
                argmax=torch.empty(N, dtype=torch.int64, device=DEV),
@@ -36,9 +38,10 @@ def _noalloc(x: torch.Tensor, lab: torch.Tensor, w: CEWorkload):
     st = capi.lib().ce_fwd_bwd_noalloc(
         x.data_ptr(), capi.BF16 if w.dtype == "bf16" else capi.F32, lab.data_ptr(), N, V,
         x.stride(0), -100, w.label_smoothing, w.softcap,
-        capi.MEAN if w.reduction == "mean" else capi.SUM, w.grad_scale, out["loss"].data_ptr(),
-        out["argmax"].data_ptr(), out["reduced"].data_ptr(), out["counts"].data_ptr(),
-        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        capi.MEAN if w.reduction == "mean" else capi.SUM, w.grad_scale,
+        out["loss"].data_ptr() if row_outputs else None,
+        out["argmax"].data_ptr() if row_outputs else None, out["reduced"].data_ptr(),
+        out["counts"].data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     capi.check(st, "ce_fwd_bwd_noalloc")
     return out
 
@@ -73,6 +76,32 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
         check_grad(gb, ref_grad, lab.cpu().numpy(), w.V, w.label_smoothing, scale, w.dtype,
                    softcap=w.softcap)
         assert np.array_equal(ga.view(np.uint8), gb.view(np.uint8))
+
+
+def test_noalloc_at_its_row_limit_without_row_outputs_twice_in_a_row():
+    # N = 65536 rows with no per-row outputs: the losses and argmaxes the
+    # finalize step reduces live in the fixed scratch, all of it in use.  Two
+    # calls back to back on one stream with different inputs: the second
+    # call's results must not depend on what the first left in the scratch.
+    base = CEWorkload("noalloc-limit", N=65536, V=64, dtype="bf16", sigma=2.0, ignore_frac=0.05,
+                      label_smoothing=0.1, softcap=0.0, reduction="mean", grad_scale=1.0,
+                      seed=91, label_boost=2.0)
+    ws = [base, base.resized(seed=92)]
+    ins = [make_ce_inputs(w, device=DEV) for w in ws]
+    refs = []
+    for w, (x, lab) in zip(ws, ins):
+        xa = x.clone()
+        refs.append((v.ce_fwd_bwd(xa, lab, label_smoothing=w.label_smoothing,
+                                  reduction=w.reduction, grad_scale=w.grad_scale), xa))
+    xbs = [x.clone() for x, _ in ins]
+    gots = [_noalloc(xb, lab, w, row_outputs=False) for xb, (_, lab), w in zip(xbs, ins, ws)]
+    torch.cuda.synchronize()
+    for (ref, xa), got, xb in zip(refs, gots, xbs):
+        assert got["counts"].cpu().tolist() == ref.counts.cpu().tolist()
+        assert np.array_equal(got["reduced"].cpu().numpy(), ref.reduced.cpu().numpy())
+        assert np.array_equal(bf16_bits_np(xa), bf16_bits_np(xb))
+    # the two inputs differ, and so do their results
+    assert not np.array_equal(gots[0]["reduced"].cpu().numpy(), gots[1]["reduced"].cpu().numpy())
 
 
 def test_noalloc_rejects_more_rows_than_its_scratch_holds():

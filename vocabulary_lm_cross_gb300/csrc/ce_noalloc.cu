@@ -33,7 +33,9 @@ void *g_scratch[kMaxDevices] = {};
 
 // Device address of g_ce_scratch on the current device.  The first call on a
 // device looks it up (the host-side name is only a stand-in, not a device
-// address) and caches it.
+// address) and caches it for the life of the process, which assumes the
+// runtime's primary context: after cudaDeviceReset, or under another context,
+// the module is loaded again and the cached address would be stale.
 vlmce_status scratch_address(void **out) {
     int dev = -1;
     if (record_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess || dev < 0 ||
