@@ -16,11 +16,13 @@ Tolerances (stated once, used by every parity test):
   plus the MUFU exp2 error of about 2^-22; 3e-7 T: with the softcap,
   z = T tanh(x/T) is formed from 1 - exp(-2|x|/T), whose exp2 error of
   2^-22 turns into an absolute error of at most T 2^-22 in z).
-  The 4e-6 covers exponents e_j = (z_j - lse) log2 e and lse log2 e below 64
-  in magnitude.  Where the test supplies the inputs and lse, kappa is taken
-  per element as max(kappa(T), 1.35 (ln 2 (h(e_j) + h(lse log2 e)) + 2^-22)
-  + 3e-7 T), h(a) = half an fp32 ulp at a: the same two roundings for larger
-  exponents (rows with a wide spread, subnormal gradients).
+  The 4e-6 covers exponents e_j = (z_j - lse) log2 e down to about -40.
+  Where the test supplies the inputs, kappa is taken per element from the
+  roundings of the kernels' actual evaluation, which forms 2^(e_j + 24) (the
+  bias keeps subnormal gradients in the exp2 unit's range; the 2^-24 goes into
+  the scale): kappa_j = max(kappa(T), 1.35 (ln 2 (h(e_j + 24) + h(lse log2 e
+  - 24) + |e_j| d) + 2^-22) + 3e-7 T), h(a) = half an fp32 ulp at a, d = the
+  relative rounding error of log2 e in fp32 (rows with a wide spread).
   An element is "well conditioned" when that error term is at most half an
   ulp: kappa (|g_o| + |scale| q_j) <= ulp(g_o) / 2.  Every well-conditioned
   bf16 element must be within 1 ulp of RN(g_o) by ordered-integer distance
@@ -50,12 +52,18 @@ def half_ulp32(a: np.ndarray) -> np.ndarray:
     return np.exp2(np.maximum(e, -126) - 24)
 
 
+# the bias of the exponent in the kernels' evaluation of 2^e
+EXP_BIAS = 24.0
+
+
 def kappa_elementwise(x64: np.ndarray, lse: np.ndarray, softcap: float) -> np.ndarray:
     """Per-element kappa for rows x64 [n, V] (fp64 inputs) with fp64 lse [n]."""
     z = softcap * np.tanh(x64 / softcap) if softcap > 0 else x64
     lg = np.asarray(lse, np.float64)[:, None] * LOG2E
     e = z * LOG2E - lg
-    k = 1.35 * (LN2 * (half_ulp32(e) + half_ulp32(lg)) + 2.0 ** -22) + KAPPA_PER_T * softcap
+    d = abs(float(np.float32(LOG2E)) - LOG2E) / LOG2E
+    k = 1.35 * (LN2 * (half_ulp32(e + EXP_BIAS) + half_ulp32(lg - EXP_BIAS) + np.abs(e) * d)
+                + 2.0 ** -22) + KAPPA_PER_T * softcap
     return np.maximum(kappa(softcap), k)
 
 

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from oracle import ce as oc
-from tests.parity import bf16_bits_np, check_grad, check_loss, check_reduced
+from tests.parity import bf16_bits_np, bits_to_f64, check_grad, check_loss, check_reduced
 from vocabulary_lm_cross_gb300 import ce_fwd_bwd
 from vocabulary_lm_cross_gb300.workloads import CEWorkload, make_ce_inputs
 
@@ -50,7 +50,9 @@ def test_per_token_upstream_gradients(monkeypatch, path, N, V, dtype, T, eps, re
     assert np.array_equal(r.argmax.cpu().numpy(), ref["argmax"])
     check_reduced(float(r.reduced[0]), ref["reduced_loss"], "sum" if red == "none" else red)
     scale = ref["row_scale"] * up.double().numpy()[:, None]
-    check_grad(host(x, dtype)[:, :V], ref["grad"], labh, V, eps, scale, dtype, softcap=T)
+    x64 = bits_to_f64(xh[:, :V]) if dtype == "bf16" else xh[:, :V].astype(np.float64)
+    check_grad(host(x, dtype)[:, :V], ref["grad"], labh, V, eps, scale, dtype, softcap=T,
+               x64=x64)
 
 
 @pytest.mark.parametrize("path", ["rows", "split"])

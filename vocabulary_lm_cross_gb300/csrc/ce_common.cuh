@@ -201,58 +201,31 @@ __device__ __forceinline__ float granule_max(const uint4 w) {
 
 // ------------------------------------------- gradients in the subnormal range
 // ex2.approx.ftz returns 0 once its result would be subnormal (exponent e <
-// -126), while p_j = 2^e times the row scale can still be a representable
-// fp32 / bf16 subnormal gradient.  Granules that may hold such a column take
-// an exact path: 2^(e + 64) on the MUFU unit, with the 2^-64 moved into the
-// coefficient, so the one rounding of the fused multiply-add that applies the
-// scale lands on the subnormal result.  A column whose z is at least lse - 87
-// has e >= -125.5: no flush.
-constexpr float kEx2Flush = -126.f;
-constexpr float kEx2Shift = 64.f;
-constexpr float kEx2ShiftScale = 5.42101086242752217e-20f;  // 2^-64
-constexpr float kNoFlushBelowLse = 87.f;
+// -126), while scale p_j can still be a representable fp32 / bf16 subnormal
+// gradient.  The gradient kernels therefore form 2^(e + 24) -- the 24 folded
+// into the per-row constant -lse log2 e, at no extra instruction -- and move
+// the 2^-24 into the coefficient that multiplies it: results down to 2^-150
+// (below the smallest fp32 subnormal) are then rounded once, by the fused
+// multiply-add that applies the coefficient.  The cost is the rounding of the
+// biased exponent (magnitude up to 24 for the largest p_j: about 1e-6
+// relative), far below a bf16 ulp and within the fp32 parity bound.  Rows
+// whose scale is below 2^-100 keep the unbiased exponent (scale 2^-24 would
+// itself be subnormal there, and their gradients underflow anyway).
+constexpr float kGradExpBias = 24.f;
+constexpr float kGradExpBiasScale = 5.9604644775390625e-8f;  // 2^-24
+constexpr float kMinBiasedScale = 7.8886090522101181e-31f;   // 2^-100
 
-// Threshold word for granule_below: every column of a granule whose values are
-// all >= thr is safe.  bf16: thr rounded up to bf16, in both halves; fp32:
-// its bits.  +inf marks every granule, -inf none.
-template <bool BF16>
-__device__ __forceinline__ uint32_t flush_threshold(float thr) {
-    if constexpr (BF16) {
-        const __nv_bfloat16 b = __float2bfloat16_ru(thr);
-        const uint32_t h = __bfloat16_as_ushort(b);
-        return h | (h << 16);
-    } else {
-        return __float_as_uint(thr);
-    }
-}
-
-// Does any value of the (whole) granule lie below the threshold (or is NaN)?
-template <bool BF16>
-__device__ __forceinline__ bool granule_below(const uint4 w, uint32_t thr) {
-    if constexpr (BF16) {
-        const __nv_bfloat162 m =
-            __hmin2(__hmin2(as_bf162(w.x), as_bf162(w.y)), __hmin2(as_bf162(w.z), as_bf162(w.w)));
-        return !__hbge2(m, as_bf162(thr));
-    } else {
-        const float m = fminf(fminf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                              fminf(__uint_as_float(w.z), __uint_as_float(w.w)));
-        return !(m >= __uint_as_float(thr));
-    }
-}
-
-// 2^e for a pair of exponents, and the coefficient pair that scales it:
-// (2^e, s) where ex2 does not flush, (2^(e + 64), s_lo = s 2^-64) where it would.
-struct ExpPair {
-    uint64_t p, s;
+// The per-row exponent constant (-lse log2 e, plus the bias) and the
+// coefficient of 2^e (scale, times 2^-bias) of a row's gradient.
+struct ExpCoef {
+    float nlseL, scale;
 };
-__device__ __forceinline__ ExpPair ex2_exact2(uint64_t e2, float s, float s_lo) {
-    float e0, e1;
-    upk(e2, e0, e1);
-    const bool l0 = e0 < kEx2Flush, l1 = e1 < kEx2Flush;
-    ExpPair r;
-    r.p = pk(ptx::ex2(l0 ? e0 + kEx2Shift : e0), ptx::ex2(l1 ? e1 + kEx2Shift : e1));
-    r.s = pk(l0 ? s_lo : s, l1 ? s_lo : s);
-    return r;
+__device__ __forceinline__ ExpCoef grad_exp_coef(float lse, float scale) {
+    const bool bias = fabsf(scale) >= kMinBiasedScale;
+    ExpCoef c;
+    c.nlseL = fmaf(-lse, kLog2e, bias ? kGradExpBias : 0.f);
+    c.scale = bias ? scale * kGradExpBiasScale : scale;
+    return c;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

@@ -204,32 +204,23 @@ __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int 
 }
 
 struct GradCoef {
-    float nlseL;        // -lse log2e
-    float scale;        // grad_scale / n_valid (mean) or grad_scale (sum)
-    float scale_lo;     // scale 2^-64 (columns whose 2^e would be subnormal)
-    float c_smooth;     // scale eps / V
-    float c_label;      // scale (1 - eps + eps / V)
-    float T, k2;        // softcap and -2 log2e / T
-    uint32_t flush_thr; // no softcap: granules with a value below lse - 87 take the exact path
-    bool may_flush;     // softcap: z > -T, so only rows with lse + T > 87 can flush
+    float nlseL;     // -lse log2e (+ the exponent bias)
+    float scale;     // coefficient of 2^e: the row scale (times 2^-bias)
+    float c_smooth;  // scale eps / V (unbiased row scale)
+    float c_label;   // scale (1 - eps + eps / V)
+    float T, k2;     // softcap and -2 log2e / T
 };
 
-// The subnormal-range fields of the coefficients of a row with this lse.
-template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void set_flush(GradCoef &c, float lse) {
-    c.scale_lo = c.scale * kEx2ShiftScale;
-    if constexpr (SOFTCAP) {
-        c.may_flush = lse + c.T > kNoFlushBelowLse;
-        c.flush_thr = 0u;
-    } else {
-        c.may_flush = true;
-        c.flush_thr = flush_threshold<BF16>(lse - kNoFlushBelowLse);
-    }
+// GradCoef of a row with this lse and (unbiased) scale; T and k2 set apart.
+__device__ __forceinline__ void set_coef(GradCoef &c, float lse, float scale, float eps, int V) {
+    c.c_smooth = scale * (eps / static_cast<float>(V));
+    c.c_label = c.c_smooth + scale * (1.f - eps);
+    const ExpCoef ec = grad_exp_coef(lse, scale);
+    c.nlseL = ec.nlseL;
+    c.scale = ec.scale;
 }
 
-// Gradient of the label column: q_y = 1 - eps + eps/V.  It needs no exact
-// subnormal path: q_y >= 1/V, so a p_y below 2^-126 is far below one ulp of
-// scale q_y.
+// Gradient of the label column: q_y = 1 - eps + eps/V.
 template <bool SOFTCAP>
 __device__ __forceinline__ float label_grad(float x, const GradCoef &c) {
     const float L = SOFTCAP ? c.T * kLog2e : kLog2e;
@@ -261,35 +252,16 @@ __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, in
     const uint64_t L2 = pk(L, L), nlseL2 = pk(c.nlseL, c.nlseL);
     const uint64_t scale2 = pk(f * c.scale, f * c.scale);
     const uint64_t nc2 = pk(-f * c.c_smooth, -f * c.c_smooth);
-    // a granule that may hold a column whose 2^e the MUFU would flush (rare)
-    const bool exact = SOFTCAP ? c.may_flush : granule_below<BF16>(w, c.flush_thr);
-    if (!exact) {
 #pragma unroll
-        for (int l = 0; l < EPG; l += 2) {
-            uint64_t g2;
-            if constexpr (SOFTCAP) {
-                const Cap2 cz = softcap2(x[l], x[l + 1], c.k2);
-                g2 = mul2(fma2(ex2x2(fma2(cz.t, L2, nlseL2)), scale2, nc2), cz.ar2);
-            } else {
-                g2 = fma2(ex2x2(fma2(pk(x[l], x[l + 1]), L2, nlseL2)), scale2, nc2);
-            }
-            upk(g2, g[l], g[l + 1]);
+    for (int l = 0; l < EPG; l += 2) {
+        uint64_t g2;
+        if constexpr (SOFTCAP) {
+            const Cap2 cz = softcap2(x[l], x[l + 1], c.k2);
+            g2 = mul2(fma2(ex2x2(fma2(cz.t, L2, nlseL2)), scale2, nc2), cz.ar2);
+        } else {
+            g2 = fma2(ex2x2(fma2(pk(x[l], x[l + 1]), L2, nlseL2)), scale2, nc2);
         }
-    } else {
-#pragma unroll
-        for (int l = 0; l < EPG; l += 2) {
-            uint64_t g2;
-            if constexpr (SOFTCAP) {
-                const Cap2 cz = softcap2(x[l], x[l + 1], c.k2);
-                const ExpPair ep = ex2_exact2(fma2(cz.t, L2, nlseL2), f * c.scale, f * c.scale_lo);
-                g2 = mul2(fma2(ep.p, ep.s, nc2), cz.ar2);
-            } else {
-                const ExpPair ep =
-                    ex2_exact2(fma2(pk(x[l], x[l + 1]), L2, nlseL2), c.scale, c.scale_lo);
-                g2 = fma2(ep.p, ep.s, nc2);
-            }
-            upk(g2, g[l], g[l + 1]);
-        }
+        upk(g2, g[l], g[l + 1]);
     }
     if (label_lane >= 0) {  // the label column (rare)
 #pragma unroll
@@ -410,16 +382,13 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     if (valid) {
         const int64_t n_valid = p.counts[0];
         GradCoef c;
-        c.scale = p.grad_scale;
+        float scale = p.grad_scale;
         if (p.reduction == VLMCE_MEAN)
-            c.scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
-        if (p.token_scale) c.scale *= p.token_scale[r];
-        c.c_smooth = c.scale * (p.eps / static_cast<float>(p.V));
-        c.c_label = c.c_smooth + c.scale * (1.f - p.eps);
-        c.nlseL = -*bcast * kLog2e;
+            scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
+        if (p.token_scale) scale *= p.token_scale[r];
+        set_coef(c, *bcast, scale, p.eps, p.V);
         c.T = T;
         c.k2 = k2;
-        set_flush<BF16, SOFTCAP>(c, *bcast);
         const int gy = static_cast<int>((y + lead) / EPG);
         const int ly = static_cast<int>((y + lead) % EPG);
         // The label column in a whole granule: the thread that owns the

@@ -181,15 +181,12 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     if (valid) {
         const int64_t n_valid = p.counts[0];
         rows::GradCoef c;
-        c.scale = p.grad_scale;
+        float scale = p.grad_scale;
         if (p.reduction == VLMCE_MEAN)
-            c.scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
-        c.c_smooth = c.scale * (p.eps / static_cast<float>(p.V));
-        c.c_label = c.c_smooth + c.scale * (1.f - p.eps);
-        c.nlseL = -lse * kLog2e;
+            scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
+        rows::set_coef(c, lse, scale, p.eps, p.V);
         c.T = T;
         c.k2 = k2;
-        rows::set_flush<BF16, SOFTCAP>(c, lse);
         // the label's granule and lane when this shard holds it
         const int64_t yl = y - p.vocab_start;
         const bool mine = yl >= 0 && yl < p.V_local;

@@ -213,17 +213,18 @@ __device__ __forceinline__ void pass_a_granule(Acc &a, const uint4 w, int jg, in
     }
 }
 
-// Gradients of the columns of one granule (before the softcap's dz).  EXACT:
-// the granule may hold a column whose 2^e the MUFU would flush to zero; those
-// take 2^(e + 64) with the scale times 2^-64 (bit-identical elsewhere).
-template <bool BF16, bool SOFTCAP, bool EXACT>
-__device__ __forceinline__ void granule_grads(const float (&x)[Elem<BF16>::kPerGranule], float T,
-                                              float k2, uint64_t nlseL2, uint64_t scale2,
-                                              uint64_t negc2, int label_lane, float scale,
-                                              float scale_lo, float c_label,
-                                              float (&g)[Elem<BF16>::kPerGranule],
-                                              float (&dz)[Elem<BF16>::kPerGranule]) {
+// Gradient of one granule, stored over the logits.  nlseL2 / scale2: the
+// row's exponent constant and the coefficient of 2^e (grad_exp_coef); scale_p
+// multiplies 2^e at the label column, c_label its target term.
+template <bool BF16, bool SOFTCAP>
+__device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, unsigned char *dst,
+                                               float T, float k2, uint64_t nlseL2, uint64_t scale2,
+                                               uint64_t negc2, int label_lane, float scale_p,
+                                               float c_label) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
+    constexpr int ELT = Elem<BF16>::kBytes;
+    float x[EPG], g[EPG], dz[EPG];
+    unpack<BF16>(w, x);
     const uint64_t L2 = pk(kLog2e, kLog2e);
 #pragma unroll
     for (int l = 0; l < EPG; l += 2) {
@@ -231,48 +232,16 @@ __device__ __forceinline__ void granule_grads(const float (&x)[Elem<BF16>::kPerG
         const Capped cb = softcap_z<SOFTCAP>(x[l + 1], T, k2);
         dz[l] = ca.dz;
         dz[l + 1] = cb.dz;
-        const uint64_t e2 = fma2(pk(ca.z, cb.z), L2, nlseL2);
-        uint64_t p2, s2;  // p_j (maybe times 2^64) and its coefficient
-        if constexpr (EXACT) {
-            const ExpPair ep = ex2_exact2(e2, scale, scale_lo);
-            p2 = ep.p;
-            s2 = ep.s;
-        } else {
-            p2 = ex2x2(e2);
-            s2 = scale2;
-        }
-        const uint64_t g2 = fma2(p2, s2, negc2);  // scale (p_j - eps/V)
+        const uint64_t p2 = ex2x2(fma2(pk(ca.z, cb.z), L2, nlseL2));  // p_j (times 2^bias)
+        const uint64_t g2 = fma2(p2, scale2, negc2);                  // scale (p_j - eps/V)
         upk(g2, g[l], g[l + 1]);
         if (label_lane >= 0) {  // the label column: q_y = 1 - eps + eps/V
-            float pa, pb, sa, sb;
+            float pa, pb;
             upk(p2, pa, pb);
-            upk(s2, sa, sb);
-            if (label_lane == l) g[l] = fmaf(pa, sa, -c_label);
-            if (label_lane == l + 1) g[l + 1] = fmaf(pb, sb, -c_label);
+            if (label_lane == l) g[l] = fmaf(pa, scale_p, -c_label);
+            if (label_lane == l + 1) g[l + 1] = fmaf(pb, scale_p, -c_label);
         }
     }
-}
-
-// Gradient of one granule, stored over the logits.  flush_thr / may_flush:
-// which granules take the exact subnormal path (no softcap: a value below
-// lse - 87; softcap: every granule of a row with lse + T > 87).
-template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void pass_b_granule(const uint4 w, int jg, int V, unsigned char *dst,
-                                               float T, float k2, uint64_t nlseL2, uint64_t scale2,
-                                               uint64_t negc2, int label_lane, float scale,
-                                               float scale_lo, float c_label, uint32_t flush_thr,
-                                               bool may_flush) {
-    constexpr int EPG = Elem<BF16>::kPerGranule;
-    constexpr int ELT = Elem<BF16>::kBytes;
-    float x[EPG], g[EPG], dz[EPG];
-    unpack<BF16>(w, x);
-    const bool exact = SOFTCAP ? may_flush : granule_below<BF16>(w, flush_thr);
-    if (!exact)
-        granule_grads<BF16, SOFTCAP, false>(x, T, k2, nlseL2, scale2, negc2, label_lane, scale,
-                                            scale_lo, c_label, g, dz);
-    else
-        granule_grads<BF16, SOFTCAP, true>(x, T, k2, nlseL2, scale2, negc2, label_lane, scale,
-                                           scale_lo, c_label, g, dz);
     if constexpr (SOFTCAP) {
 #pragma unroll
         for (int l = 0; l < EPG; ++l) g[l] *= dz[l];
@@ -486,15 +455,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
 
             // ---- pass B: gradient from shared memory, stored over the logits
             unsigned char *grow = reinterpret_cast<unsigned char *>(g.gbase) + 16 * g.g_beg;
-            const uint64_t nlseL2 = pk(-lse * kLog2e, -lse * kLog2e);
             const float scale = p.token_scale ? scale0 * p.token_scale[r] : scale0;
             const float c_smooth = scale * (p.eps / static_cast<float>(p.V));  // scale eps / V
             const float c_label = c_smooth + scale * (1.f - p.eps);            // + scale (1 - eps)
-            const uint64_t scale2 = pk(scale, scale);
+            const ExpCoef ec = grad_exp_coef(lse, scale);
+            const uint64_t nlseL2 = pk(ec.nlseL, ec.nlseL);
+            const uint64_t scale2 = pk(ec.scale, ec.scale);
             const uint64_t negc2 = pk(-c_smooth, -c_smooth);
-            const float scale_lo = scale * kEx2ShiftScale;
-            const bool may_flush = SOFTCAP ? lse + T > kNoFlushBelowLse : true;
-            const uint32_t flush_thr = SOFTCAP ? 0u : flush_threshold<BF16>(lse - kNoFlushBelowLse);
             for (int c = 0; c < nch && p.want_grad; ++c) {
                 const int slot = static_cast<int>((q + c) % kSlots);
                 const int gl = c * kChunkGranules + tid;
@@ -504,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
                         const uint4 w =
                             *reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes + 16 * tid);
                         pass_b_granule<BF16, SOFTCAP>(w, jg, p.V, grow + 16 * gl, T, k2, nlseL2,
-                                                      scale2, negc2, gl == gy ? ly : -1, scale,
-                                                      scale_lo, c_label, flush_thr, may_flush);
+                                                      scale2, negc2, gl == gy ? ly : -1, ec.scale,
+                                                      c_label);
                     } else {
                         store_zero_granule<BF16>(jg, p.V, grow + 16 * gl);
                     }
