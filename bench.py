@@ -7,7 +7,7 @@ workload is bf16 logits [N=2048, V=131072] (sequence 2048 x batch 1, the
 128K vocabulary) with label smoothing 0.1, argmax and token accuracy.  The
 same run times every other cross-entropy configuration the same way (the
 line's "configs" object: fp32 [256, 4096], bf16 [8192, 32000], bf16
-[8192, 151936] with a padded row stride and softcap 30, and 64 rows of
+[8192, 151936] with a padded row stride and softcap 30, and 32 rows of
 151936 on both the V-split and the row kernel), the fused linear
 cross-entropy (flce_fwd_bwd: hidden [4096, 6656] x weight [202048, 6656],
 softcap 30) against the dense bf16 tensor roofline ("flce"), and companion
@@ -267,7 +267,7 @@ def run_reference(args, w):
 # each in the "configs" object), and the few-wide-rows case on both kernels.
 CONFIG_WORKLOADS = ("ce-f32-256x4096", "ce-bf16-8192x32000",
                     "ce-bf16-8192x151936-stride152064-softcap30-sum")
-WIDE_ROWS_WORKLOAD = "ce-bf16-64x151936-ls0.1-argmax"
+WIDE_ROWS_WORKLOAD = "ce-bf16-32x151936-ls0.1-argmax"
 
 
 def time_ce(w, dev, steps, warmup, *, rank=0, world=1, barrier=lambda: None, sampler=None,
@@ -438,7 +438,7 @@ def run_configs(args, head_name, dev, sampler):
     out[w.name] = {path: config_entry(w, time_ce(w, dev, steps, args.warmup, sampler=sampler,
                                                  path=path))
                    for path in ("split", "rows")}
-    out[w.name]["note"] = ("fewer rows than SMs: the V-split kernel (a cluster per row, "
+    out[w.name]["note"] = ("few wide rows: the V-split kernel (a cluster of CTAs per row, "
                            "TMA-staged slices, DSMEM merge) is the default; the row kernel "
                            "timed on the same inputs")
     torch.cuda.empty_cache()
@@ -647,8 +647,9 @@ def run_ours(args, w):
 
 def run_shard(args, w, dev, world, barrier, sampler, tp=8):
     """One rank's step of the vocabulary-sharded CE in a TP = `tp` layout of
-    the workload: statistics of its shard, merge of the `tp` gathered records,
-    loss and in-place gradient of its shard.  The other ranks' records are
+    the workload: statistics of its shard, then loss and in-place gradient of
+    its shard from the `tp` gathered records (merged inside the gradient
+    kernel: ce_shard_fwd_bwd_gathered).  The other ranks' records are
     formed beforehand (on a real group they arrive by an all-gather of
     N x 32 bytes each).  Each timed step works on a fresh copy of the shard."""
     import torch
@@ -675,17 +676,15 @@ def run_shard(args, w, dev, world, barrier, sampler, tp=8):
                    reduced=torch.empty(2, dtype=torch.float32, device=dev),
                    counts=torch.empty(4, dtype=torch.int64, device=dev))
     gathered = others.clone()
-    merged = torch.empty((w.N, 8), dtype=torch.float32, device=dev)
     ws = torch.empty(v_ws_bytes(w.N, V, mine0.dtype), dtype=torch.uint8, device=dev)
 
     def step(b):
         sh.shard_stats(b, lab, 0, V, softcap=w.softcap, out=gathered[0])
-        sh.merge_stats(gathered, out=merged)
-        sh.shard_fwd_bwd(b, lab, 0, V, merged, label_smoothing=w.label_smoothing,
+        sh.shard_fwd_bwd(b, lab, 0, V, gathered, label_smoothing=w.label_smoothing,
                          softcap=w.softcap, reduction=w.reduction, grad_scale=w.grad_scale,
                          out=out, workspace=ws)
 
-    # the rank step is five short launches: replay it as a CUDA graph, one per
+    # the rank step is four short launches: replay it as a CUDA graph, one per
     # buffer of the ring, so that host-side launch overhead is not timed
     for i in range(args.warmup):
         step(bufs[i % nb])
@@ -735,9 +734,10 @@ def run_shard(args, w, dev, world, barrier, sampler, tp=8):
             "roofline": {"bound": "hbm", "achieved": bytes_step / (ms * 1e-3) / 1e9,
                          "peak": peak, "peak_source": f"{peak_src} (copy GB/s)", "unit": "GB/s",
                          "frac": bytes_step / (ms * 1e-3) / 1e9 / peak,
-                         "measured_over": "the whole rank step (stats, merge, count, gradient, "
-                                          "finalize: 5 launches), replayed as a CUDA graph"},
-            "gpu_launches": 5 * steps, "device_status_ok": ok,
+                         "measured_over": "the whole rank step (stats, count, gradient with the "
+                                          "records' merge, finalize: 4 launches), replayed as "
+                                          "a CUDA graph"},
+            "gpu_launches": 4 * steps, "device_status_ok": ok,
             "clocks": sampler.summary(t0, t1),
             "l2": f"ring of {nb} shard copies ({nb * bytes_step / 2 / 1e6:.0f} MB > 2 x L2); the "
                   "gradient pass re-reads the shard from L2"}

@@ -198,7 +198,9 @@ size_t vlmce_ce_host_workspace_bytes(int64_t N, int64_t V, int64_t row_stride, i
  *                      on every rank that merges the same array);
  *   ce_shard_fwd_bwd -> per-token loss / argmax / reduced loss and accuracy
  *                      (the same on every rank) and the gradient of this
- *                      shard's columns, written in place.
+ *                      shard's columns, written in place;
+ *   or, in place of the last two, ce_shard_fwd_bwd_gathered on the gathered
+ *   array itself.
  * With one shard (vocab_start 0, V_local = V) this is ce_fwd_bwd.
  */
 typedef struct vlmce_row_stats {
@@ -242,6 +244,22 @@ vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels
                               const vlmce_row_stats *global_stats, float *out_loss,
                               int64_t *out_argmax, float *out_reduced, int64_t *out_counts,
                               void *workspace, size_t workspace_bytes, vlmce_stream_t stream);
+
+/* ce_merge_stats followed by ce_shard_fwd_bwd in one call, with no merged
+ * statistics buffer: gathered is the device [k][N] array of every shard's
+ * statistics in shard order (as an all-gather of the k ranks' ce_shard_stats
+ * outputs leaves it), k >= 1, 16-byte aligned.  Each row's k records are
+ * merged inside the gradient kernel with ce_merge_stats' operator and order,
+ * so every result is bit-identical to the two calls; one launch fewer on the
+ * rank's step.  Other arguments, results and errors as ce_shard_fwd_bwd. */
+vlmce_status ce_shard_fwd_bwd_gathered(void *logits, int32_t dtype, const int64_t *labels,
+                                       int64_t N, int64_t V_local, int64_t row_stride,
+                                       int64_t vocab_start, int64_t V, int64_t ignore_index,
+                                       float label_smoothing, float softcap, int32_t reduction,
+                                       float grad_scale, const vlmce_row_stats *gathered,
+                                       int32_t k, float *out_loss, int64_t *out_argmax,
+                                       float *out_reduced, int64_t *out_counts, void *workspace,
+                                       size_t workspace_bytes, vlmce_stream_t stream);
 
 /*
  * Fused gate-up SwiGLU ("[Megatron] Add SwiGLU integration", Summary and

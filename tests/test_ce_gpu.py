@@ -153,8 +153,9 @@ def test_plans_of_the_benchmarked_workloads():
         pl = v.describe_plan(w.N, w.V, dt, w.softcap)
         assert pl["ctas_per_row"] * pl["granules_per_cta"] * (8 if w.dtype == "bf16" else 4) >= w.V
         assert pl["resident"] >= 1, (name, pl)
-        if w.N < sms:  # fewer rows than SMs: a cluster of CTAs per row
-            assert pl["kernel"] == "split" and pl["ctas_per_row"] > 1, (name, pl)
+        if w.N <= 32 and w.V >= 131072:  # few wide rows: a cluster of >= 3 CTAs per row
+            assert pl["kernel"] == "split" and pl["ctas_per_row"] >= 3, (name, pl)
+            assert 3 * w.N * pl["ctas_per_row"] <= 5 * sms, (name, pl)
         else:
             assert pl["kernel"] == "rows", (name, pl)
             assert pl["ctas_per_row"] == 1 and pl["threads"] in (256, 1024), (name, pl)

@@ -174,3 +174,48 @@ def test_shard_argument_errors():
     assert lib.ce_shard_fwd_bwd(x.data_ptr(), capi.F32, lab.data_ptr(), 4, 16, 16, 0, 16, -100, 0.0,
                                 0.0, capi.MEAN, 1.0, out.data_ptr(), None, None, None, None,
                                 ws.data_ptr(), ws.numel(), s) == capi.ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.parametrize("N,V,dtype,T,eps,red,cuts", [CASES[0], CASES[1], CASES[4], CASES[5]])
+def test_gathered_call_is_merge_then_fwd_bwd_bit_for_bit(N, V, dtype, T, eps, red, cuts):
+    # ce_shard_fwd_bwd_gathered merges the [k, N] records inside the gradient
+    # kernel: every output equals ce_merge_stats + ce_shard_fwd_bwd, bit for bit
+    w = wl(N, V, dtype, T, eps, red, seed=N * 3 + V)
+    x, lab = make_ce_inputs(w, device=DEV)
+    edges, shards, stats, g, outs = run_protocol(x, lab, V, cuts, eps=eps, T=T, red=red, gs=0.5)
+    fresh = [x[:, a:b].contiguous() for a, b in zip(edges[:-1], edges[1:])]
+    for s_ref, s_new, a, o in zip(shards, fresh, edges[:-1], outs):
+        r = sh.shard_fwd_bwd(s_new, lab, a, V, stats, label_smoothing=eps, softcap=T,
+                             reduction=red, grad_scale=0.5)
+        torch.cuda.synchronize()
+        assert torch.equal(host_bits(s_new, dtype), host_bits(s_ref, dtype)), a
+        assert torch.equal(r.loss.view(torch.int32), o.loss.view(torch.int32))
+        assert torch.equal(r.argmax, o.argmax)
+        assert torch.equal(r.reduced.view(torch.int32), o.reduced.view(torch.int32))
+        assert torch.equal(r.counts, o.counts)
+
+
+def host_bits(t, dtype):
+    return t.view(torch.int16 if dtype == "bf16" else torch.int32).cpu()
+
+
+def test_gathered_argument_errors():
+    lib = capi.lib()
+    x = torch.zeros((4, 16), device=DEV)
+    lab = torch.zeros(4, dtype=torch.int64, device=DEV)
+    recs = torch.zeros((2, 4, 8), device=DEV)
+    ws = torch.empty(v_ws(4, 16), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    args = (x.data_ptr(), capi.F32, lab.data_ptr(), 4, 16, 16, 0, 16, -100, 0.0, 0.0, capi.MEAN,
+            1.0)
+    tail = (None, None, None, None, ws.data_ptr(), ws.numel(), s)
+    assert lib.ce_shard_fwd_bwd_gathered(*args, recs.data_ptr(), 0, *tail) == capi.ERR_INVALID_ARG
+    assert lib.ce_shard_fwd_bwd_gathered(*args, None, 2, *tail) == capi.ERR_INVALID_ARG
+    assert lib.ce_shard_fwd_bwd_gathered(*args, recs.data_ptr() + 4, 2, *tail) == \
+        capi.ERR_MISALIGNED
+    torch.cuda.synchronize()
+
+
+def v_ws(N, V):
+    from vocabulary_lm_cross_gb300.ce import workspace_bytes
+    return workspace_bytes(N, V, torch.float32)

@@ -57,6 +57,9 @@ SIGNATURES = {
     "ce_merge_stats": (_i32, [_vp, _i32, _i64, _vp, _vp]),
     "ce_shard_fwd_bwd": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _i32,
                                 _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "ce_shard_fwd_bwd_gathered": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
+                                         _f32, _i32, _f32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _sz,
+                                         _vp]),
     "swiglu_fwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp]),
     "swiglu_bwd": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i32, _i64, _i64, _vp]),
     "ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _f32,

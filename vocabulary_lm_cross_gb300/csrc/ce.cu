@@ -153,18 +153,23 @@ vlmce_status get_split_plan(const DeviceInfo &d, bool bf16, bool softcap, int64_
     return VLMCE_OK;
 }
 
-// Which kernel does the row work.  The row kernel keeps every SM busy once
-// N >= 2 x SMs; with fewer rows the V-split kernel spreads each row over a
-// cluster instead, when the row is wide enough to be worth splitting and fits
-// the clusters' shared memory.  Override: environment VLMCE_CE_PATH = "rows"
-// or "split".
+// Which kernel does the row work.  The V-split kernel spreads each row over a
+// cluster of k CTAs; it pays when the rows are wide (k >= 3) and so few that
+// all N k CTAs run at once with room to spare (N k <= 5/3 SMs): measured on
+// GB300 over 1..128 rows of 32000..262144 columns, the row kernel (one CTA
+// per row, the second pass served by L2) is as fast or faster beyond that.
+// Override: environment VLMCE_CE_PATH = "rows" or "split".
 bool use_split(int64_t N, int64_t G, const DeviceInfo &d) {
     const char *e = getenv("VLMCE_CE_PATH");
     const int64_t cap = static_cast<int64_t>(split::kMaxCluster) * split::kSlots *
                         split::kChunkGranules;
     if (e && strcmp(e, "split") == 0) return G <= cap;
     if (e && strcmp(e, "rows") == 0) return false;
-    return N < d.sm_count && G >= 4 * split::kChunkGranules && G <= cap;
+    if (G > cap) return false;
+    const int64_t pref = static_cast<int64_t>(split::kPreferredChunks) * split::kChunkGranules;
+    int64_t k = (G + pref - 1) / pref;
+    if (k > split::kMaxCluster) k = split::kMaxCluster;
+    return k >= 3 && 3 * N * k <= 5 * static_cast<int64_t>(d.sm_count);
 }
 
 // Launch the row kernel over N <= INT_MAX rows, one CTA per row, after the

@@ -315,8 +315,11 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
     // Pass 2 prefetches ahead where the rows in flight exceed L2: softcap
-    // rows (five 256-thread CTAs per SM, up to 760 rows in flight).
+    // rows (five 256-thread CTAs per SM, up to 760 rows in flight).  There it
+    // also walks the row backwards, so that it starts on the lines pass 1
+    // read last, the ones most likely still in L2.
     constexpr bool kPrefetch2 = SOFTCAP;
+    constexpr bool kReverse2 = SOFTCAP;
 
     // ---- pass 1
     Acc a;
@@ -395,7 +398,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         // granule reads x_y now (the loop overwrites it), stores the granule
         // like any other in the loop, then overwrites the one element with the
         // label gradient, so the loop itself has no label test.
-        const int y_owner = (gy >= gs && gy < ge) ? (gy - gs) % THREADS : -1;
+        const int y_owner =
+            (gy >= gs && gy < ge) ? (kReverse2 ? ge - 1 - gy : gy - gs) % THREADS : -1;
         unsigned char *py = gbase + ELT * (static_cast<int64_t>(y) + lead);
         float xy = 0.f;
         if (tid == y_owner) {
@@ -409,12 +413,20 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
             grad_values<BF16, SOFTCAP>(ld_v4(row), c, gy == 0 ? ly : -1, g);
             store_partial<BF16>(gbase, -lead, p.V, g);
         }
-        for (int gl = gs + tid; gl < ge; gl += THREADS) {
-            // the granule two iterations ahead, into L2 (where the row has
-            // partly left L2 since pass 1)
-            if (kPrefetch2 && gl + 2 * THREADS < ge) ptx::prefetch_l2(row + gl + 2 * THREADS);
-            grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, -1, g);
-            ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+        if constexpr (kReverse2) {
+            for (int gl = ge - 1 - tid; gl >= gs; gl -= THREADS) {
+                // the granule two iterations ahead, into L2 (where the row has
+                // partly left L2 since pass 1)
+                if (kPrefetch2 && gl - 2 * THREADS >= gs) ptx::prefetch_l2(row + gl - 2 * THREADS);
+                grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, -1, g);
+                ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+            }
+        } else {
+            for (int gl = gs + tid; gl < ge; gl += THREADS) {
+                if (kPrefetch2 && gl + 2 * THREADS < ge) ptx::prefetch_l2(row + gl + 2 * THREADS);
+                grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, -1, g);
+                ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+            }
         }
         if (tid == y_owner) store_elem<BF16>(py, label_grad<SOFTCAP>(xy, c));
         if (tid == tail_tid) {

@@ -46,7 +46,9 @@ struct ShardParams {
     int64_t ignore_index;
     float eps, softcap, grad_scale;
     int reduction;
-    RowPart *stats;         // stats kernel: out [N]; grad kernel: global stats in [N]
+    RowPart *stats;         // stats kernel: out [N]; grad kernel: k gathered records [k][N]
+    int k;                  // grad kernel: records per row, merged in order (1: already merged)
+    int64_t N;
     float *loss;
     int64_t *argmax;
     const int64_t *counts;
@@ -159,8 +161,14 @@ __global__ void __launch_bounds__(256) ce_merge_stats_kernel(const RowPart *shar
     out[r] = a;
 }
 
+// The gradient kernel keeps two granules in flight per thread; without a
+// softcap its 256-thread CTAs run five per SM (48 registers) to hold them.
+constexpr int grad_min_blocks(int threads, bool softcap) {
+    return (!softcap && threads == rows::kShortThreads) ? 5 : min_blocks(threads, softcap);
+}
+
 template <bool BF16, bool SOFTCAP, int THREADS>
-__global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
+__global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
     ce_shard_grad_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     const int tid = threadIdx.x;
@@ -168,8 +176,20 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
     const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
-    const RowPart *st = p.stats + r;
-    const float lse = st->mz + logf(st->s);
+    // the row's statistics over the whole vocabulary: its k gathered records
+    // merged in shard order (the operator and order of ce_merge_stats) by one
+    // thread, shared with the CTA
+    __shared__ RowPart srow;
+    if (tid == 0) {
+        RowPart st = p.stats[r];
+        for (int i = 1; i < p.k; ++i) {
+            const RowPart b = p.stats[static_cast<int64_t>(i) * p.N + r];
+            part_merge(st, b.mx, b.idx, b.mz, b.s, b.sz, b.zy);
+        }
+        srow = st;
+    }
+    __syncthreads();
+    const float lse = srow.mz + logf(srow.s);
     const int64_t y = p.labels[r];
     const bool ignored = y == p.ignore_index;
     const bool valid = !ignored && y >= 0 && y < p.V;
@@ -197,7 +217,17 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
             rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row()), c, gy == 0 ? ly : -1, gr);
             rows::store_partial<BF16>(g.gbase, -g.lead, p.V_local, gr);
         }
-        for (int gl = g.gs + tid; gl < g.ge; gl += THREADS) {
+        // two granules loaded before either is stored (the stores would
+        // otherwise keep each load waiting for the previous iteration)
+        int gl = g.gs + tid;
+        for (; gl + THREADS < g.ge; gl += 2 * THREADS) {
+            const uint4 w0 = rows::ld_v4(g.row() + gl), w1 = rows::ld_v4(g.row() + gl + THREADS);
+            rows::grad_values<BF16, SOFTCAP>(w0, c, gl == gy ? ly : -1, gr);
+            ptx::st_global_cs_v4(g.gbase + 16 * gl, rows::pack_granule<BF16>(gr));
+            rows::grad_values<BF16, SOFTCAP>(w1, c, gl + THREADS == gy ? ly : -1, gr);
+            ptx::st_global_cs_v4(g.gbase + 16 * (gl + THREADS), rows::pack_granule<BF16>(gr));
+        }
+        for (; gl < g.ge; gl += THREADS) {
             rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row() + gl), c, gl == gy ? ly : -1, gr);
             ptx::st_global_cs_v4(g.gbase + 16 * gl, rows::pack_granule<BF16>(gr));
         }
@@ -221,11 +251,11 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     if (tid == 0) {  // the row's loss and argmax (the same on every shard)
         float l = 0.f;
         if (valid)
-            l = lse - fmaf(1.f - p.eps, st->zy, (p.eps / static_cast<float>(p.V)) * st->sz);
+            l = lse - fmaf(1.f - p.eps, srow.zy, (p.eps / static_cast<float>(p.V)) * srow.sz);
         else if (!ignored)
             l = __int_as_float(0x7fc00000);  // bad label: NaN
         if (p.loss) p.loss[r] = l;
-        if (p.argmax) p.argmax[r] = st->idx;
+        if (p.argmax) p.argmax[r] = srow.idx;
     }
 }
 
@@ -350,14 +380,19 @@ extern "C" vlmce_status ce_merge_stats(const vlmce_row_stats *shards, int32_t k,
         "ce_merge_stats_kernel");
 }
 
-extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels,
-                                         int64_t N, int64_t V_local, int64_t row_stride,
-                                         int64_t vocab_start, int64_t V, int64_t ignore_index,
-                                         float label_smoothing, float softcap, int32_t reduction,
-                                         float grad_scale, const vlmce_row_stats *global_stats,
-                                         float *out_loss, int64_t *out_argmax, float *out_reduced,
-                                         int64_t *out_counts, void *workspace,
-                                         size_t workspace_bytes_given, vlmce_stream_t stream) {
+namespace vlmce {
+namespace ce {
+namespace shard {
+namespace {
+
+// ce_shard_fwd_bwd on k gathered records per row ([k][N]; k = 1: merged).
+vlmce_status shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, int64_t N,
+                           int64_t V_local, int64_t row_stride, int64_t vocab_start, int64_t V,
+                           int64_t ignore_index, float label_smoothing, float softcap,
+                           int32_t reduction, float grad_scale, const vlmce_row_stats *stats,
+                           int32_t k, float *out_loss, int64_t *out_argmax, float *out_reduced,
+                           int64_t *out_counts, void *workspace, size_t workspace_bytes_given,
+                           vlmce_stream_t stream) {
     vlmce_status st = check_shard(logits, dtype, labels, N, V_local, row_stride, vocab_start, V,
                                   softcap);
     if (st != VLMCE_OK) return st;
@@ -365,8 +400,9 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
     if (!std::isfinite(grad_scale)) return VLMCE_ERR_INVALID_ARG;
     if (reduction != VLMCE_MEAN && reduction != VLMCE_SUM && reduction != VLMCE_NONE)
         return VLMCE_ERR_INVALID_ARG;
-    if (N > 0 && !global_stats) return VLMCE_ERR_INVALID_ARG;
-    if (global_stats && !aligned(global_stats, 16)) return VLMCE_ERR_MISALIGNED;
+    if (k < 1) return VLMCE_ERR_INVALID_ARG;
+    if (N > 0 && !stats) return VLMCE_ERR_INVALID_ARG;
+    if (stats && !aligned(stats, 16)) return VLMCE_ERR_MISALIGNED;
     const size_t need = vlmce_ce_workspace_bytes(N, V, dtype);
     if (!workspace || workspace_bytes_given < need) return VLMCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 16)) return VLMCE_ERR_MISALIGNED;
@@ -399,7 +435,9 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
         p.softcap = softcap;
         p.grad_scale = grad_scale;
         p.reduction = reduction;
-        p.stats = reinterpret_cast<RowPart *>(const_cast<vlmce_row_stats *>(global_stats));
+        p.stats = reinterpret_cast<RowPart *>(const_cast<vlmce_row_stats *>(stats));
+        p.k = k;
+        p.N = N;
         p.loss = loss;
         p.argmax = amax;
         p.counts = counts;
@@ -416,4 +454,36 @@ extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int6
                          static_cast<const int64_t *>(counts), static_cast<const int *>(err),
                          out_reduced, out_counts),
         "ce_finalize_kernel");
+}
+
+}  // namespace
+}  // namespace shard
+}  // namespace ce
+}  // namespace vlmce
+
+extern "C" vlmce_status ce_shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels,
+                                         int64_t N, int64_t V_local, int64_t row_stride,
+                                         int64_t vocab_start, int64_t V, int64_t ignore_index,
+                                         float label_smoothing, float softcap, int32_t reduction,
+                                         float grad_scale, const vlmce_row_stats *global_stats,
+                                         float *out_loss, int64_t *out_argmax, float *out_reduced,
+                                         int64_t *out_counts, void *workspace,
+                                         size_t workspace_bytes_given, vlmce_stream_t stream) {
+    return shard_fwd_bwd(logits, dtype, labels, N, V_local, row_stride, vocab_start, V,
+                         ignore_index, label_smoothing, softcap, reduction, grad_scale,
+                         global_stats, 1, out_loss, out_argmax, out_reduced, out_counts, workspace,
+                         workspace_bytes_given, stream);
+}
+
+extern "C" vlmce_status ce_shard_fwd_bwd_gathered(
+    void *logits, int32_t dtype, const int64_t *labels, int64_t N, int64_t V_local,
+    int64_t row_stride, int64_t vocab_start, int64_t V, int64_t ignore_index,
+    float label_smoothing, float softcap, int32_t reduction, float grad_scale,
+    const vlmce_row_stats *gathered, int32_t k, float *out_loss, int64_t *out_argmax,
+    float *out_reduced, int64_t *out_counts, void *workspace, size_t workspace_bytes_given,
+    vlmce_stream_t stream) {
+    return shard_fwd_bwd(logits, dtype, labels, N, V_local, row_stride, vocab_start, V,
+                         ignore_index, label_smoothing, softcap, reduction, grad_scale, gathered, k,
+                         out_loss, out_argmax, out_reduced, out_counts, workspace,
+                         workspace_bytes_given, stream);
 }

@@ -66,17 +66,21 @@ def merge_stats(shards: torch.Tensor, *, out: torch.Tensor | None = None) -> tor
 
 
 def shard_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, vocab_start: int, V: int,
-                  global_stats: torch.Tensor, *, ignore_index: int = -100,
+                  stats: torch.Tensor, *, ignore_index: int = -100,
                   label_smoothing: float = 0.0, softcap: float = 0.0, reduction: str = "mean",
                   grad_scale: float = 1.0, out: CEResult | None = None,
                   workspace: torch.Tensor | None = None) -> CEResult:
-    """Loss and the shard's gradient (written over ``logits``) from the merged statistics."""
+    """Loss and the shard's gradient (written over ``logits``) from the whole
+    vocabulary's statistics: ``stats`` is either the merged [N, 8] records
+    (ce_shard_fwd_bwd) or the gathered [k, N, 8] records of every shard in
+    shard order, merged inside the gradient kernel (ce_shard_fwd_bwd_gathered)."""
     _check(logits, labels)
     N, VL = logits.shape
     dev = logits.device
-    if global_stats.shape != (N, 8) or global_stats.dtype != torch.float32 or \
-            not global_stats.is_contiguous():
-        raise ValueError("global_stats must be a contiguous float32 [N, 8] tensor")
+    gathered = stats.dim() == 3
+    ok_shape = (stats.shape[1:] == (N, 8)) if gathered else (stats.shape == (N, 8))
+    if not ok_shape or stats.dtype != torch.float32 or not stats.is_contiguous():
+        raise ValueError("stats must be a contiguous float32 [N, 8] or [k, N, 8] tensor")
     if out is None:
         out = CEResult(loss=torch.empty(N, dtype=torch.float32, device=dev),
                        argmax=torch.empty(N, dtype=torch.int64, device=dev),
@@ -85,12 +89,15 @@ def shard_fwd_bwd(logits: torch.Tensor, labels: torch.Tensor, vocab_start: int, 
     need = workspace_bytes(N, V, logits.dtype)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-    st = capi.lib().ce_shard_fwd_bwd(
-        logits.data_ptr(), _DTYPES[logits.dtype], labels.data_ptr(), N, VL,
-        logits.stride(0) if N > 1 else VL, vocab_start, V, ignore_index, float(label_smoothing),
-        float(softcap), _REDUCTIONS[reduction], float(grad_scale), global_stats.data_ptr(),
-        out.loss.data_ptr(), out.argmax.data_ptr(), out.reduced.data_ptr(), out.counts.data_ptr(),
-        workspace.data_ptr(), workspace.numel(), _stream(dev))
+    head = (logits.data_ptr(), _DTYPES[logits.dtype], labels.data_ptr(), N, VL,
+            logits.stride(0) if N > 1 else VL, vocab_start, V, ignore_index,
+            float(label_smoothing), float(softcap), _REDUCTIONS[reduction], float(grad_scale))
+    tail = (out.loss.data_ptr(), out.argmax.data_ptr(), out.reduced.data_ptr(),
+            out.counts.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev))
+    if gathered:
+        st = capi.lib().ce_shard_fwd_bwd_gathered(*head, stats.data_ptr(), stats.shape[0], *tail)
+    else:
+        st = capi.lib().ce_shard_fwd_bwd(*head, stats.data_ptr(), *tail)
     capi.check(st, "shard_fwd_bwd")
     try:
         torch.autograd.graph.increment_version(logits)

@@ -110,11 +110,11 @@ CE_WORKLOADS = {
         CEWorkload("ce-bf16-8192x151936-stride152064-softcap30-sum", N=8192, V=151936,
                    dtype="bf16", sigma=4.0, ignore_frac=0.05, label_smoothing=0.1, softcap=30.0,
                    reduction="sum", grad_scale=1.0 / 4096, seed=1004, row_stride=152064),
-        # few wide rows (fewer rows than SMs: the V-split kernel's case), e.g. an
-        # evaluation batch over the Qwen3 vocabulary
-        CEWorkload("ce-bf16-64x151936-ls0.1-argmax", N=64, V=151936, dtype="bf16", sigma=3.0,
+        # few wide rows (the V-split kernel's case: a cluster of CTAs per row),
+        # e.g. an evaluation batch of 32 tokens over the Qwen3 vocabulary
+        CEWorkload("ce-bf16-32x151936-ls0.1-argmax", N=32, V=151936, dtype="bf16", sigma=3.0,
                    ignore_frac=0.05, label_smoothing=0.1, softcap=0.0, reduction="mean",
-                   grad_scale=1.0, seed=1009, label_boost=4.0, dup_max_frac=0.05,
+                   grad_scale=1.0, seed=1009, label_boost=4.0, dup_max_frac=0.1,
                    want_argmax=True),
         # the headline recipe at a profiling size (268 MB, still larger than L2)
         CEWorkload("ce-bf16-1024x131072-ls0.1-argmax", N=1024, V=131072, dtype="bf16", sigma=3.0,
