@@ -445,6 +445,30 @@ def run_configs(args, head_name, dev, sampler):
     return out
 
 
+def bind_to_gpu_local_cpus(dev) -> str:
+    """Run this process on the CPUs local to the GPU (its NUMA node), so that
+    page-locked host buffers allocated afterwards sit next to the GPU's host
+    link; returns what was done (for the bench line).  The caller restores
+    the previous affinity (os.sched_setaffinity) when it is done."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bdf = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        path = f"/sys/bus/pci/devices/{bdf}/local_cpulist"
+        text = open(path).read().strip()
+        cpus = set()
+        for part in text.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0) or cpus
+        if not cpus or cpus == os.sched_getaffinity(0):
+            return f"unchanged ({path}: {text})"
+        os.sched_setaffinity(0, cpus)
+        return f"bound to the GPU's local CPUs {text}"
+    except Exception as e:  # no sysfs entry, or an older torch without PCI ids
+        return f"unchanged ({type(e).__name__})"
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -456,6 +480,8 @@ def run_ours(args, w):
     local = env_int("LOCAL_RANK", 0)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    cpus0 = os.sched_getaffinity(0)
+    affinity = bind_to_gpu_local_cpus(dev)
     if world > 1:
         dist.init_process_group("nccl")
 
@@ -566,6 +592,7 @@ def run_ours(args, w):
     h2d = w.N * row_bytes + lab_host.numel() * 8
     d2h = w.N * row_bytes + w.N * 4 + w.N * 8 + 8 + 32
     del x_host, x_pristine, ws_h
+    os.sched_setaffinity(0, cpus0)  # the CPU baseline below uses every host core
     head.pop("x0")
     head.pop("lab")
     del x0, lab
@@ -631,7 +658,7 @@ def run_ours(args, w):
         "e2e": {"value": bytes_step / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "ce_fwd_bwd_host on page-locked host logits, labels and outputs",
-                "device_status_ok": e2e_ok},
+                "host_memory": affinity, "device_status_ok": e2e_ok},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "configs": configs,

@@ -29,6 +29,8 @@
 // only formed when label smoothing needs it.
 #pragma once
 
+#include <type_traits>
+
 #include "ce_common.cuh"
 
 namespace vlmce {
@@ -110,11 +112,25 @@ __device__ __forceinline__ RowPart acc_part(const Acc &a, float T) {
     return pt;
 }
 
+// The softcap's constants of a thread: T, -2 log2e / T and the polynomial's.
+struct CapK {
+    float T, k2;
+    PolyCap pc;
+};
+template <bool SOFTCAP>
+__device__ __forceinline__ CapK cap_k(float T) {
+    CapK k;
+    k.T = T;
+    k.k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    k.pc = SOFTCAP ? poly_cap(T) : PolyCap{};
+    return k;
+}
+
 // z of one column: the logit, or T tanh(x/T) under a softcap.
 template <bool SOFTCAP>
-__device__ __forceinline__ float z_of(float x, float T, float k2) {
+__device__ __forceinline__ float z_of(float x, const CapK &k) {
     if constexpr (SOFTCAP)
-        return T * softcap_t1(x, k2);
+        return k.T * softcap_t_any(x, k.pc, k.k2);
     else
         return x;
 }
@@ -130,7 +146,7 @@ constexpr float kRefMargin = 8.f;
 // faster than x, so mz covers every x <= gm + kRefMargin.)
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPerGranule],
-                                        float gm, int jg, int V, float T, float k2) {
+                                        float gm, int jg, int V, const CapK &k) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     int li = EPG - 1;
 #pragma unroll
@@ -139,7 +155,7 @@ __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPe
     a.mv = gm;
     a.midx = jg + li;
     if (gm > a.xthr) {
-        const float nz = z_of<SOFTCAP>(gm, T, k2) + kRefMargin;
+        const float nz = z_of<SOFTCAP>(gm, k) + kRefMargin;
         const float f = ptx::ex2((a.mz - nz) * kLog2e);
         float s0, s1;
         upk(a.s, s0, s1);
@@ -153,21 +169,36 @@ __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPe
 }
 
 // Fold a whole granule (every column valid), two columns per packed op.
-// Under a softcap the exponent is t (T log2e) - mz log2e with t = tanh(x/T).
+// Under a softcap the exponent is t (T log2e) - mz log2e with t = tanh(x/T),
+// by the polynomial when the whole granule is within its range (else ok is
+// cleared and softcap2 is used).
 template <bool BF16, bool SOFTCAP, bool SUMZ>
-__device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, float T, float k2) {
+__device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, const CapK &k,
+                                          bool &ok) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
     const float gm = granule_max<BF16>(w);
-    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, T, k2);
-    const float L = SOFTCAP ? T * kLog2e : kLog2e;
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, k);
+    const float L = SOFTCAP ? k.T * kLog2e : kLog2e;
     const uint64_t L2 = pk(L, L), nmL2 = pk(a.nmL, a.nmL);
+    if constexpr (SOFTCAP) {
+        if (granule_in_poly_range<BF16>(w, k.pc)) {
+#pragma unroll
+            for (int l = 0; l < EPG; l += 2) {
+                const uint64_t v = tanh_poly2(pk(x[l], x[l + 1]), k.pc);
+                a.s = add2(a.s, ex2x2(fma2(v, L2, nmL2)));
+                if constexpr (SUMZ) a.z = add2(a.z, v);
+            }
+            return;
+        }
+        ok = false;
+    }
 #pragma unroll
     for (int l = 0; l < EPG; l += 2) {
         uint64_t v;
         if constexpr (SOFTCAP)
-            v = softcap2(x[l], x[l + 1], k2).t;
+            v = softcap2(x[l], x[l + 1], k.k2).t;
         else
             v = pk(x[l], x[l + 1]);
         a.s = add2(a.s, ex2x2(fma2(v, L2, nmL2)));
@@ -177,8 +208,7 @@ __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, 
 
 // Fold a granule of which only the columns in [0, V) count (into the even sums).
 template <bool BF16, bool SOFTCAP>
-__device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int V, float T,
-                                             float k2) {
+__device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int V, const CapK &k) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
@@ -186,15 +216,15 @@ __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int 
 #pragma unroll
     for (int l = 0; l < EPG; ++l)
         if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
-    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, T, k2);
-    const float L = SOFTCAP ? T * kLog2e : kLog2e;
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, k);
+    const float L = SOFTCAP ? k.T * kLog2e : kLog2e;
     float s0, s1, z0, z1;
     upk(a.s, s0, s1);
     upk(a.z, z0, z1);
 #pragma unroll
     for (int l = 0; l < EPG; ++l) {
         if (jg + l >= 0 && jg + l < V) {
-            const float v = SOFTCAP ? softcap_t1(x[l], k2) : x[l];
+            const float v = SOFTCAP ? softcap_t_any(x[l], k.pc, k.k2) : x[l];
             s0 += ptx::ex2(fmaf(v, L, a.nmL));
             z0 += v;
         }
@@ -208,10 +238,11 @@ struct GradCoef {
     float scale;     // coefficient of 2^e: the row scale (times 2^-bias)
     float c_smooth;  // scale eps / V (unbiased row scale)
     float c_label;   // scale (1 - eps + eps / V)
-    float T, k2;     // softcap and -2 log2e / T
+    CapK k;          // the softcap's constants
 };
 
-// GradCoef of a row with this lse and (unbiased) scale; T and k2 set apart.
+// GradCoef of a row with this lse and (unbiased) scale; the softcap's
+// constants set apart.
 __device__ __forceinline__ void set_coef(GradCoef &c, float lse, float scale, float eps, int V) {
     c.c_smooth = scale * (eps / static_cast<float>(V));
     c.c_label = c.c_smooth + scale * (1.f - eps);
@@ -220,48 +251,84 @@ __device__ __forceinline__ void set_coef(GradCoef &c, float lse, float scale, fl
     c.scale = ec.scale;
 }
 
-// Gradient of the label column: q_y = 1 - eps + eps/V.
+// Gradient of one column with target term q_coef = scale q_j (c_smooth, or
+// c_label at the label): under a softcap by the polynomial within its range
+// (g = scale (p - q) (1 - t^2)), else by softcap2 (g = 4 scale (p - q) a r^2,
+// the factor 4 of dz/dx = 4 a r^2 folded into the coefficients, exactly).
 template <bool SOFTCAP>
-__device__ __forceinline__ float label_grad(float x, const GradCoef &c) {
-    const float L = SOFTCAP ? c.T * kLog2e : kLog2e;
+__device__ __forceinline__ float column_grad(float x, float q_coef, const GradCoef &c) {
     if constexpr (SOFTCAP) {
-        const Cap2 cz = softcap2(x, x, c.k2);
+        const float L = c.k.T * kLog2e;
+        if (fabsf(x) <= c.k.pc.lim) {
+            float t, t_;
+            upk(tanh_poly2(pk(x, x), c.k.pc), t, t_);
+            const float pr = ptx::ex2(fmaf(t, L, c.nlseL));
+            return fmaf(pr, c.scale, -q_coef) * fmaf(-t, t, 1.f);
+        }
+        const Cap2 cz = softcap2(x, x, c.k.k2);
         float t, t_, ar2, ar2_;
         upk(cz.t, t, t_);
         upk(cz.ar2, ar2, ar2_);
         const float pr = ptx::ex2(fmaf(t, L, c.nlseL));
-        return fmaf(pr, 4.f * c.scale, -4.f * c.c_label) * ar2;
+        return fmaf(pr, 4.f * c.scale, -4.f * q_coef) * ar2;
     } else {
-        const float pr = ptx::ex2(fmaf(x, L, c.nlseL));
-        return fmaf(pr, c.scale, -c.c_label);
+        const float pr = ptx::ex2(fmaf(x, kLog2e, c.nlseL));
+        return fmaf(pr, c.scale, -q_coef);
     }
 }
+// Gradient of the label column: q_y = 1 - eps + eps/V.
+template <bool SOFTCAP>
+__device__ __forceinline__ float label_grad(float x, const GradCoef &c) {
+    return column_grad<SOFTCAP>(x, c.c_label, c);
+}
+
+// How pass 2 forms the softcap's tanh of a granule: the polynomial if the
+// whole granule is within its range, else softcap2 (kCapCheck: the decision
+// pass 1 took for the same granule); the polynomial without the test
+// (kCapPoly: pass 1 found every whole granule of the row in range); column by
+// column (kCapColumn: the partial granules at the ends of a row, which pass 1
+// also folds column by column).
+enum CapMode : int { kCapCheck = 0, kCapPoly = 1, kCapColumn = 2 };
 
 // Gradients of the EPG elements of a granule, in fp32, two per packed op;
-// label_lane >= 0: the label column's lane.  Under a softcap
-// g = 4 scale (p - q) a r^2 (the factor 4 of dz/dx = 4 a r^2 is folded into
-// the coefficients, exactly).
-template <bool BF16, bool SOFTCAP>
+// label_lane >= 0: the label column's lane.
+template <bool BF16, bool SOFTCAP, int MODE = kCapCheck>
 __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, int label_lane,
                                             float (&g)[Elem<BF16>::kPerGranule]) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
-    const float L = SOFTCAP ? c.T * kLog2e : kLog2e;
-    const float f = SOFTCAP ? 4.f : 1.f;
+    const float L = SOFTCAP ? c.k.T * kLog2e : kLog2e;
     const uint64_t L2 = pk(L, L), nlseL2 = pk(c.nlseL, c.nlseL);
-    const uint64_t scale2 = pk(f * c.scale, f * c.scale);
-    const uint64_t nc2 = pk(-f * c.c_smooth, -f * c.c_smooth);
+    if constexpr (SOFTCAP && MODE == kCapColumn) {
 #pragma unroll
-    for (int l = 0; l < EPG; l += 2) {
-        uint64_t g2;
-        if constexpr (SOFTCAP) {
-            const Cap2 cz = softcap2(x[l], x[l + 1], c.k2);
-            g2 = mul2(fma2(ex2x2(fma2(cz.t, L2, nlseL2)), scale2, nc2), cz.ar2);
-        } else {
-            g2 = fma2(ex2x2(fma2(pk(x[l], x[l + 1]), L2, nlseL2)), scale2, nc2);
+        for (int l = 0; l < EPG; ++l) g[l] = column_grad<SOFTCAP>(x[l], c.c_smooth, c);
+    } else if (SOFTCAP && (MODE == kCapPoly || granule_in_poly_range<BF16>(w, c.k.pc))) {
+        // g = (c_smooth - scale p) (t^2 - 1) = scale (p - q) (1 - t^2)
+        const uint64_t nscale2 = pk(-c.scale, -c.scale), c2 = pk(c.c_smooth, c.c_smooth);
+        const uint64_t m_one = pk(-1.f, -1.f);
+#pragma unroll
+        for (int l = 0; l < EPG; l += 2) {
+            const uint64_t t = tanh_poly2(pk(x[l], x[l + 1]), c.k.pc);
+            const uint64_t g2 =
+                mul2(fma2(ex2x2(fma2(t, L2, nlseL2)), nscale2, c2), fma2(t, t, m_one));
+            upk(g2, g[l], g[l + 1]);
         }
-        upk(g2, g[l], g[l + 1]);
+    } else {
+        const float f = SOFTCAP ? 4.f : 1.f;
+        const uint64_t scale2 = pk(f * c.scale, f * c.scale);
+        const uint64_t nc2 = pk(-f * c.c_smooth, -f * c.c_smooth);
+#pragma unroll
+        for (int l = 0; l < EPG; l += 2) {
+            uint64_t g2;
+            if constexpr (SOFTCAP) {
+                const Cap2 cz = softcap2(x[l], x[l + 1], c.k.k2);
+                g2 = mul2(fma2(ex2x2(fma2(cz.t, L2, nlseL2)), scale2, nc2), cz.ar2);
+            } else {
+                g2 = fma2(ex2x2(fma2(pk(x[l], x[l + 1]), L2, nlseL2)), scale2, nc2);
+            }
+            upk(g2, g[l], g[l + 1]);
+        }
     }
     if (label_lane >= 0) {  // the label column (rare)
 #pragma unroll
@@ -313,7 +380,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const bool tail = ge == G - 1 && G - 1 >= gs;  // granule G-1 partial, distinct from 0
     const int tail_tid = tail ? (G - 1 - gs) % THREADS : -1;
     const float T = p.softcap;
-    const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    const CapK k = cap_k<SOFTCAP>(T);
     // Pass 2 prefetches ahead where the rows in flight exceed L2: softcap
     // rows (five 256-thread CTAs per SM, up to 760 rows in flight).  There it
     // also walks the row backwards, so that it starts on the lines pass 1
@@ -324,7 +391,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     // ---- pass 1
     Acc a;
     acc_init(a);
-    if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, T, k2);
+    bool poly_ok = true;  // every whole granule of this thread took the polynomial softcap
+    if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, k);
     // two granules in flight per thread (the loads of a warp would otherwise
     // leave too few bytes outstanding to cover the DRAM latency); the folds
     // keep the thread's column order
@@ -335,13 +403,13 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
             ptx::prefetch_l2(row + gl + 2 * THREADS);
             ptx::prefetch_l2(row + gl + 3 * THREADS);
         }
-        fold_full<BF16, SOFTCAP, SUMZ>(a, w0, gl * EPG - lead, p.V, T, k2);
-        fold_full<BF16, SOFTCAP, SUMZ>(a, w1, (gl + THREADS) * EPG - lead, p.V, T, k2);
+        fold_full<BF16, SOFTCAP, SUMZ>(a, w0, gl * EPG - lead, p.V, k, poly_ok);
+        fold_full<BF16, SOFTCAP, SUMZ>(a, w1, (gl + THREADS) * EPG - lead, p.V, k, poly_ok);
     }
     for (; gl < ge; gl += THREADS)
-        fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, T, k2);
+        fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, k, poly_ok);
     if (tid == tail_tid)
-        fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, T, k2);
+        fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, k);
 
     RowPart pt = acc_part<SOFTCAP>(a, T);
     warp_allreduce(pt);
@@ -350,7 +418,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const int64_t y = p.labels[r];
     const bool ignored = (y == p.ignore_index);
     const bool valid = !ignored && y >= 0 && y < p.V;
-    __syncthreads();
+    // every whole granule of the row took the polynomial softcap in pass 1
+    const bool row_poly = __syncthreads_and(poly_ok) != 0;
     if (warp == 0) {
         RowPart q = lane < kWarps ? wpart[lane] : part_identity();
         warp_allreduce(q);
@@ -364,7 +433,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
                     xy = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
                 else
                     xy = *reinterpret_cast<const float *>(py);
-                const float zy = z_of<SOFTCAP>(xy, T, k2);
+                const float zy = z_of<SOFTCAP>(xy, k);
                 l = lse - fmaf(1.f - p.eps, zy, (p.eps / static_cast<float>(p.V)) * q.sz);
             } else if (!ignored) {
                 l = __int_as_float(0x7fc00000);  // bad label: NaN
@@ -390,8 +459,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
             scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
         if (p.token_scale) scale *= p.token_scale[r];
         set_coef(c, *bcast, scale, p.eps, p.V);
-        c.T = T;
-        c.k2 = k2;
+        c.k = k;
         const int gy = static_cast<int>((y + lead) / EPG);
         const int ly = static_cast<int>((y + lead) % EPG);
         // The label column in a whole granule: the thread that owns the
@@ -410,27 +478,39 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         }
         float g[EPG];
         if (head && tid == 0) {
-            grad_values<BF16, SOFTCAP>(ld_v4(row), c, gy == 0 ? ly : -1, g);
+            grad_values<BF16, SOFTCAP, kCapColumn>(ld_v4(row), c, gy == 0 ? ly : -1, g);
             store_partial<BF16>(gbase, -lead, p.V, g);
         }
-        if constexpr (kReverse2) {
-            for (int gl = ge - 1 - tid; gl >= gs; gl -= THREADS) {
-                // the granule two iterations ahead, into L2 (where the row has
-                // partly left L2 since pass 1)
-                if (kPrefetch2 && gl - 2 * THREADS >= gs) ptx::prefetch_l2(row + gl - 2 * THREADS);
-                grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, -1, g);
-                ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+        // the whole granules: without the range test when pass 1 found the
+        // whole row within the polynomial's range
+        auto whole = [&](auto mode) {
+            constexpr int M = decltype(mode)::value;
+            if constexpr (kReverse2) {
+                for (int gl = ge - 1 - tid; gl >= gs; gl -= THREADS) {
+                    // the granule two iterations ahead, into L2 (where the row has
+                    // partly left L2 since pass 1)
+                    if (kPrefetch2 && gl - 2 * THREADS >= gs)
+                        ptx::prefetch_l2(row + gl - 2 * THREADS);
+                    grad_values<BF16, SOFTCAP, M>(ld_v4(row + gl), c, -1, g);
+                    ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+                }
+            } else {
+                for (int gl = gs + tid; gl < ge; gl += THREADS) {
+                    if (kPrefetch2 && gl + 2 * THREADS < ge)
+                        ptx::prefetch_l2(row + gl + 2 * THREADS);
+                    grad_values<BF16, SOFTCAP, M>(ld_v4(row + gl), c, -1, g);
+                    ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+                }
             }
-        } else {
-            for (int gl = gs + tid; gl < ge; gl += THREADS) {
-                if (kPrefetch2 && gl + 2 * THREADS < ge) ptx::prefetch_l2(row + gl + 2 * THREADS);
-                grad_values<BF16, SOFTCAP>(ld_v4(row + gl), c, -1, g);
-                ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
-            }
-        }
+        };
+        if (!SOFTCAP || row_poly)
+            whole(std::integral_constant<int, kCapPoly>{});
+        else
+            whole(std::integral_constant<int, kCapCheck>{});
         if (tid == y_owner) store_elem<BF16>(py, label_grad<SOFTCAP>(xy, c));
         if (tid == tail_tid) {
-            grad_values<BF16, SOFTCAP>(ld_v4(row + (G - 1)), c, gy == G - 1 ? ly : -1, g);
+            grad_values<BF16, SOFTCAP, kCapColumn>(ld_v4(row + (G - 1)), c, gy == G - 1 ? ly : -1,
+                                                   g);
             store_partial<BF16>(gbase + 16 * (G - 1), (G - 1) * EPG - lead, p.V, g);
         }
     } else {

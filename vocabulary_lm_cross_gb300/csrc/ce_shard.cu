@@ -109,24 +109,25 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
-    const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    const rows::CapK k = rows::cap_k<SOFTCAP>(T);
+    bool poly_ok = true;
     rows::Acc a;
     rows::acc_init(a);
     if (g.head && tid == 0)
-        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, T, k2);
+        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, k);
     int gl = g.gs + tid;
     for (; gl + THREADS < g.ge; gl += 2 * THREADS) {  // two loads in flight, column order kept
         const uint4 w0 = rows::ld_v4(g.row() + gl), w1 = rows::ld_v4(g.row() + gl + THREADS);
-        rows::fold_full<BF16, SOFTCAP, true>(a, w0, gl * EPG - g.lead, p.V_local, T, k2);
-        rows::fold_full<BF16, SOFTCAP, true>(a, w1, (gl + THREADS) * EPG - g.lead, p.V_local, T,
-                                             k2);
+        rows::fold_full<BF16, SOFTCAP, true>(a, w0, gl * EPG - g.lead, p.V_local, k, poly_ok);
+        rows::fold_full<BF16, SOFTCAP, true>(a, w1, (gl + THREADS) * EPG - g.lead, p.V_local, k,
+                                             poly_ok);
     }
     for (; gl < g.ge; gl += THREADS)
         rows::fold_full<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row() + gl), gl * EPG - g.lead,
-                                             p.V_local, T, k2);
+                                             p.V_local, k, poly_ok);
     if (tid == g.tail_tid)
         rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row() + (g.G - 1)),
-                                          (g.G - 1) * EPG - g.lead, p.V_local, T, k2);
+                                          (g.G - 1) * EPG - g.lead, p.V_local, k);
     RowPart pt = rows::acc_part<SOFTCAP>(a, T);
     warp_allreduce(pt);
     if (lane == 0) wpart[warp] = pt;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
             const int64_t yl = p.labels[blockIdx.x] - p.vocab_start;
             q.zy = 0.f;
             if (yl >= 0 && yl < p.V_local)
-                q.zy = rows::z_of<SOFTCAP>(load_x<BF16>(row_addr(p), yl), T, k2);
+                q.zy = rows::z_of<SOFTCAP>(load_x<BF16>(row_addr(p), yl), k);
             q.idx = q.idx == INT_MAX ? INT_MAX : static_cast<int>(q.idx + p.vocab_start);
             q.pad0 = q.pad1 = 0.f;
             p.stats[blockIdx.x] = q;
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
     const int64_t r = blockIdx.x;
     const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
-    const float k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
+    const rows::CapK k = rows::cap_k<SOFTCAP>(T);
     // the row's statistics over the whole vocabulary: its k gathered records
     // merged in shard order (the operator and order of ce_merge_stats) by one
     // thread, shared with the CTA
@@ -205,8 +206,7 @@ __global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
         if (p.reduction == VLMCE_MEAN)
             scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
         rows::set_coef(c, lse, scale, p.eps, p.V);
-        c.T = T;
-        c.k2 = k2;
+        c.k = k;
         // the label's granule and lane when this shard holds it
         const int64_t yl = y - p.vocab_start;
         const bool mine = yl >= 0 && yl < p.V_local;
@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
         const int ly = mine ? static_cast<int>((yl + g.lead) % EPG) : -1;
         float gr[EPG];
         if (g.head && tid == 0) {
-            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row()), c, gy == 0 ? ly : -1, gr);
+            rows::grad_values<BF16, SOFTCAP, rows::kCapColumn>(rows::ld_v4(g.row()), c,
+                                                               gy == 0 ? ly : -1, gr);
             rows::store_partial<BF16>(g.gbase, -g.lead, p.V_local, gr);
         }
         // two granules loaded before either is stored (the stores would
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
             ptx::st_global_cs_v4(g.gbase + 16 * gl, rows::pack_granule<BF16>(gr));
         }
         if (tid == g.tail_tid) {
-            rows::grad_values<BF16, SOFTCAP>(rows::ld_v4(g.row() + (g.G - 1)), c,
+            rows::grad_values<BF16, SOFTCAP, rows::kCapColumn>(rows::ld_v4(g.row() + (g.G - 1)), c,
                                              gy == g.G - 1 ? ly : -1, gr);
             rows::store_partial<BF16>(g.gbase + 16 * (g.G - 1), (g.G - 1) * EPG - g.lead,
                                       p.V_local, gr);
