@@ -497,7 +497,7 @@ def run_ours(args, w):
     sampler = ClockSampler(uuid)
     sampler.start()
     head = time_ce(w, dev, args.steps, args.warmup, rank=rank, world=world, barrier=barrier,
-                   sampler=sampler, soak_s=1.0)
+                   sampler=sampler, soak_s=args.soak)
     x0, lab = head["x0"], head["lab"]
     ms = head["ms"] * args.steps
     kern_ms = head["kern_ms"]
@@ -939,18 +939,26 @@ def run_flce(args, w, steps, dev, world, barrier, sampler):
     d2h = gh_host.numel() * 2 + gw_host.numel() * 4 + w.N * 4 + 8
     nchunks = (w.V + 8191) // 8192
     flops = w.algorithmic_flops
-    peak, peak_src = load_tensor_peak(sustained=True)
-    peak_b, _ = load_tensor_peak(sustained=False)
-    achieved = flops / (kern_ms * 1e-3) / 1e12
+    # the dominant region is the whole call less the census, merge and
+    # finalize kernels (about 50 us of ~30 ms): achieved is taken over the
+    # whole call as timed above (a lower bound for the GEMM region), against
+    # the burst bf16 peak; the tensor region's own event time (a separate
+    # pass, perturbed by the events it records) is reported beside it
+    peak, peak_src = load_tensor_peak(sustained=False)
+    peak_s, _ = load_tensor_peak(sustained=True)
+    achieved = flops / (ms / steps * 1e-3) / 1e12
     return {
         "ms": ms / steps, "value": world * flops * steps / (ms * 1e-3) / 1e12,
         "roofline": {"bound": "tensor", "kernel": "vlmce_gemm_kernel",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst": achieved / peak_b,
-                     "kernel_ms": kern_ms, "flops_per_launch": flops,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "frac_of_sustained": achieved / peak_s,
+                     "measured_over": "the whole call (1 statistics GEMM, the row merge, "
+                                      f"{nchunks + 1} grouped chunk GEMM launches, census and "
+                                      "finalize), CUDA events around K calls",
+                     "tensor_region_ms": kern_ms, "flops_per_launch": flops,
                      "executed_flops": 8 * w.N * w.V * w.H,
-                     "measured_over": "the call's tensor-core region: 1 statistics GEMM, the "
-                                      f"row merge and {nchunks} x 3 chunk GEMMs",
+                     "executed_frac": 8 * w.N * w.V * w.H / (ms / steps * 1e-3) / 1e12 / peak,
                      "traffic": recorded_traffic("vlmce_gemm_kernel", w.name)},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -1112,6 +1120,10 @@ def main():
                          "cross-entropy run")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other cross-entropy configurations of a cross-entropy run")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed steps before the headline's timed steps (so the "
+                         "clock samples describe a loaded GPU); 0 for profiling commands, whose "
+                         "launch counts must not depend on time")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

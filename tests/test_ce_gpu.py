@@ -158,7 +158,7 @@ def test_plans_of_the_benchmarked_workloads():
             assert 3 * w.N * pl["ctas_per_row"] <= 5 * sms, (name, pl)
         else:
             assert pl["kernel"] == "rows", (name, pl)
-            assert pl["ctas_per_row"] == 1 and pl["threads"] in (256, 1024), (name, pl)
+            assert pl["ctas_per_row"] == 1 and pl["threads"] in (128, 256, 1024), (name, pl)
         print(name, pl)
 
 

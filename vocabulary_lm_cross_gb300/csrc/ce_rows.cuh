@@ -43,10 +43,16 @@ namespace rows {
 constexpr int kThreads = 1024;
 constexpr int kShortThreads = 256;
 constexpr int kShortGranules = 8192;
+// Rows of at most kTinyGranules granules (16384 bf16 columns, e.g. one
+// tensor-parallel shard of a 128K vocabulary): 128-thread CTAs, sixteen per
+// SM, so that 2432 rows run in a single wave.
+constexpr int kTinyThreads = 128;
+constexpr int kTinyGranules = 2048;
 // CTAs per SM the launch bounds ask for (the softcap variants need more
 // registers per thread: 48 at five 256-thread CTAs per SM).
 constexpr int min_blocks(int threads, bool softcap) {
-    return threads == kThreads ? (softcap ? 1 : 2) : (softcap ? 5 : 8);
+    return threads == kThreads ? (softcap ? 1 : 2)
+                               : threads == kTinyThreads ? 16 : (softcap ? 5 : 8);
 }
 
 struct Params {
@@ -553,6 +559,7 @@ inline bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
 // warps resident than one CTA of 1024 at 64 registers, and their barriers
 // stall fewer warps at a time.
 inline int threads_for(int64_t G, bool softcap) {
+    if (!softcap && G <= kTinyGranules) return kTinyThreads;
     return (softcap || G <= kShortGranules) ? kShortThreads : kThreads;
 }
 // The row kernel for the given softcap and CTA size, per element type

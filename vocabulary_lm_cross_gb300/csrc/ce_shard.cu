@@ -163,9 +163,12 @@ __global__ void __launch_bounds__(256) ce_merge_stats_kernel(const RowPart *shar
 }
 
 // The gradient kernel keeps two granules in flight per thread; without a
-// softcap its 256-thread CTAs run five per SM (48 registers) to hold them.
+// softcap its 256-thread CTAs run five per SM (48 registers) to hold them;
+// its 128-thread CTAs keep sixteen per SM (all 2432 rows of a wave at once).
 constexpr int grad_min_blocks(int threads, bool softcap) {
-    return (!softcap && threads == rows::kShortThreads) ? 5 : min_blocks(threads, softcap);
+    if (!softcap && threads == rows::kShortThreads) return 5;
+    if (!softcap && threads == rows::kTinyThreads) return 16;
+    return min_blocks(threads, softcap);
 }
 
 template <bool BF16, bool SOFTCAP, int THREADS>
@@ -272,10 +275,16 @@ ShardKernel grad_kernel_t(bool bf16, bool softcap) {
     return softcap ? ce_shard_grad_kernel<false, true, TH> : ce_shard_grad_kernel<false, false, TH>;
 }
 ShardKernel stats_kernel(bool bf16, bool softcap, int threads) {
+    if (threads == rows::kTinyThreads)  // no softcap
+        return bf16 ? ce_shard_stats_kernel<true, false, rows::kTinyThreads>
+                    : ce_shard_stats_kernel<false, false, rows::kTinyThreads>;
     return threads == rows::kShortThreads ? stats_kernel_t<rows::kShortThreads>(bf16, softcap)
                                           : stats_kernel_t<rows::kThreads>(bf16, softcap);
 }
 ShardKernel grad_kernel(bool bf16, bool softcap, int threads) {
+    if (threads == rows::kTinyThreads)  // no softcap
+        return bf16 ? ce_shard_grad_kernel<true, false, rows::kTinyThreads>
+                    : ce_shard_grad_kernel<false, false, rows::kTinyThreads>;
     return threads == rows::kShortThreads ? grad_kernel_t<rows::kShortThreads>(bf16, softcap)
                                           : grad_kernel_t<rows::kThreads>(bf16, softcap);
 }
