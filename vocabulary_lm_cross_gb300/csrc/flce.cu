@@ -46,9 +46,6 @@ namespace {
 using ce::RowPart;
 
 constexpr int kChunk = 8192;  // vocabulary columns per gradient chunk
-// Row stride (elements) of the two gradient tiles: kChunk plus 64, so that
-// the rows of a tile are not a power of two (16 KB) apart.
-constexpr int kLdG = kChunk + 64;
 // Factor of the fp16 gradient tile ((p - q)(1 - t^2) has |.| <= 1; x 2^14 stays
 // below the fp16 maximum and keeps small probabilities out of the subnormals).
 constexpr float kF16GradMul = 16384.f;
@@ -252,7 +249,7 @@ struct Ws {
     RowPart *part;  // [ntiles][N]
     float *lse, *row_scale, *loss;
     int64_t *argmax;
-    uint16_t *g[2];       // two [N, kChunk] gradient tiles (bf16 or fp16 bits), rows kLdG apart
+    uint16_t *g[2];       // two [N, kChunk] gradient tiles (bf16 or fp16 bits)
     float *out_scale;     // scale of the gradient products' accumulators
     float *gh;            // [N, H] grad_h accumulator
 };
@@ -263,7 +260,7 @@ size_t ws_bytes(int64_t N, int64_t H, int64_t V) {
     int64_t b = kWsHeader;
     b += round_up(ntiles_of(V) * N * static_cast<int64_t>(sizeof(RowPart)), 256);
     b += 3 * round_up(4 * N, 256) + round_up(8 * N, 256);
-    b += 2 * round_up(2 * N * static_cast<int64_t>(kLdG), 256);
+    b += 2 * round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     b += round_up(4 * N * H, 256);
     return static_cast<size_t>(b);
 }
@@ -287,7 +284,7 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
     p += round_up(8 * N, 256);
     for (int i = 0; i < 2; ++i) {
         w.g[i] = reinterpret_cast<uint16_t *>(p);
-        p += round_up(2 * N * static_cast<int64_t>(kLdG), 256);
+        p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     }
     w.gh = reinterpret_cast<float *>(p);
     return w;
@@ -553,7 +550,7 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
             if (c >= 1) {
                 const uint16_t *wc = static_cast<const uint16_t *>(weight) + pv0 * weight_stride;
                 // grad_h (+)= G_c W_c: A = G_c K-major [N, Vc], B = W_c N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, false, N, pvc, kLdG, f16) ||
+                if (!gemm::make_operand_map(&maps.a[n], gc, false, N, pvc, kChunk, f16) ||
                     !gemm::make_operand_map(&maps.b[n], wc, true, H, pvc, weight_stride, f16))
                     return map_fail();
                 gemm::Problem &ph = g.p[n++];
@@ -586,11 +583,11 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
                 pg.mode = gemm::kGrad;
                 pg.col0 = static_cast<int>(v0);
                 pg.C16 = w.g[c & 1];
-                pg.ldc16 = kLdG;
+                pg.ldc16 = kChunk;
             }
             if (c >= 1) {
                 // grad_W_c (+)= G_c^T h': A = G_c^T M(=Vc)-major, B = h' N(=H)-major
-                if (!gemm::make_operand_map(&maps.a[n], gc, true, pvc, N, kLdG, f16) ||
+                if (!gemm::make_operand_map(&maps.a[n], gc, true, pvc, N, kChunk, f16) ||
                     !gemm::make_operand_map(&maps.b[n], hidden, true, H, N, hidden_stride, f16))
                     return map_fail();
                 gemm::Problem &pw = g.p[n++];

@@ -346,17 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ar = tl.m0 + kHalf * static_cast<int>(prank);
                 const int br = tl.n0 + kHalf * static_cast<int>(prank);
                 const int kblocks = (P.K + BK - 1) / BK;
-                const bool pf_b = kPrefetchB > 0 && tl.m0 == 0;  // the column tile's first pair
-                if (pf_b) {
-                    for (int kb = 0; kb < kPrefetchB && kb < kblocks; ++kb) {
-                        if (!P.b_mn) {
-                            tc::tma_prefetch_2d(mb, kb * BK, br);
-                        } else {
-                            tc::tma_prefetch_2d(mb, br, kb * BK);
-                            tc::tma_prefetch_2d(mb, br + 64, kb * BK);
-                        }
-                    }
-                }
                 for (int kb = 0; kb < kblocks; ++kb) {
                     wait_bar(empty(s), ph ^ 1, abort, a.err);
                     if (prank == 0) ptx::mbar_arrive_expect_tx(full(s), 2 * kStageBytes);
@@ -374,15 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         tc::tma_load_2d_pair(sb, mb, br, kb * BK, fb);
                         tc::tma_load_2d_pair(sb + 8192, mb, br + 64, kb * BK, fb);
-                    }
-                    const int kp = kb + kPrefetchB;
-                    if (pf_b && kp < kblocks) {
-                        if (!P.b_mn) {
-                            tc::tma_prefetch_2d(mb, kp * BK, br);
-                        } else {
-                            tc::tma_prefetch_2d(mb, br, kp * BK);
-                            tc::tma_prefetch_2d(mb, br + 64, kp * BK);
-                        }
                     }
                     ++issued;
                     if (++s == kStages) {

@@ -23,10 +23,6 @@ constexpr int kBarriers = 2 * kStages + 5;  // full, empty, tmem full x2, tmem e
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kBarriers + 16;
 constexpr int kMaxProblems = 3;
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
-// The pairs on the first row tile of a column tile prefetch their B half this
-// many k-blocks ahead into L2; the pairs on the other row tiles, which read
-// the same B tile, then find it there.
-constexpr int kPrefetchB = 8;
 
 enum Mode : int {
     kStoreF32 = 0,   // C = acc (fp32)
