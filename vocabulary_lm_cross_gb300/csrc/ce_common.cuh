@@ -232,11 +232,6 @@ __device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
     return r;
 }
 
-// Max of the even and of the odd columns of a full bf16 granule, packed.
-__device__ __forceinline__ __nv_bfloat162 granule_max2(const uint4 w) {
-    return __hmax2(__hmax2(as_bf162(w.x), as_bf162(w.y)), __hmax2(as_bf162(w.z), as_bf162(w.w)));
-}
-
 // Max of a full granule (packed bf16x2 max for bf16).
 template <bool BF16>
 __device__ __forceinline__ float granule_max(const uint4 w) {

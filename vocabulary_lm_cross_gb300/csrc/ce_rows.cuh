@@ -85,9 +85,8 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
 // Pass-1 state of one thread.  The sums run over even and odd columns in
 // the two halves of packed fp32x2 registers.
 struct Acc {
-    float mv;      // max raw logit seen
-    uint32_t mv2;  // bf16 logits: mv in both halves of a bf16x2 word
-    int midx;      // its first column
+    float mv;    // max raw logit seen
+    int midx;    // its first column
     float mz;    // reference of s, at least the largest z seen
     float nmL;   // -mz log2e
     float xthr;  // largest x whose z mz is known to cover
@@ -97,7 +96,6 @@ struct Acc {
 
 __device__ __forceinline__ void acc_init(Acc &a) {
     a.mv = -INFINITY;
-    a.mv2 = 0xff80ff80u;  // -inf, -inf
     a.midx = INT_MAX;
     a.mz = -INFINITY;
     a.nmL = INFINITY;
@@ -161,10 +159,6 @@ __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPe
     for (int l = EPG - 1; l >= 0; --l)
         if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
     a.mv = gm;
-    if constexpr (BF16) {  // gm is one of the granule's bf16 values: exact
-        const uint32_t h = __float_as_uint(gm) >> 16;
-        a.mv2 = h | (h << 16);
-    }
     a.midx = jg + li;
     if (gm > a.xthr) {
         const float nz = z_of<SOFTCAP>(gm, k) + kRefMargin;
@@ -190,16 +184,8 @@ __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, 
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
-    if constexpr (BF16) {
-        // the granule's bf16x2 maximum against the running maximum, packed;
-        // the exact maximum is formed only when one half passes it (rare)
-        const __nv_bfloat162 c = granule_max2(w);
-        if (!__hble2(c, as_bf162(a.mv2)))
-            new_max<BF16, SOFTCAP>(a, x, fmaxf(__low2float(c), __high2float(c)), jg, V, k);
-    } else {
-        const float gm = granule_max<BF16>(w);
-        if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, k);
-    }
+    const float gm = granule_max<BF16>(w);
+    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, k);
     const float L = SOFTCAP ? k.T * kLog2e : kLog2e;
     const uint64_t L2 = pk(L, L), nmL2 = pk(a.nmL, a.nmL);
     if constexpr (SOFTCAP) {
