@@ -2,8 +2,9 @@
 // cross-entropy entry points (ce.cu, ce_shard.cu): one CTA each.
 //   ce_count_kernel    -- n_valid (labels in [0, V)) and bad labels (neither
 //                         ignore_index nor in range); clears the error word.
-//   ce_finalize_kernel -- fixed-order fp64 sum of the per-row losses (mean or
-//                         sum), token accuracy, the counts and error bits.
+//   ce_finalize_kernel -- fixed-order float-float sum of the per-row losses
+//                         (mean or sum), token accuracy, the counts and error
+//                         bits.
 // Internal linkage: each translation unit that launches them has its own copy.
 #pragma once
 
@@ -67,12 +68,31 @@ __global__ void __launch_bounds__(1024) ce_count_kernel(const int64_t *__restric
     }
 }
 
+// Float-float sum hi + lo: each addend goes through Knuth's TwoSum with hi
+// and its rounding error is gathered in lo, so fixed-order sums of the
+// per-row losses keep about 44 bits with fp32 arithmetic only (this GPU's
+// fp64 rate is a small fraction of its fp32 rate).
+struct FloatFloat {
+    float hi, lo;
+};
+__device__ __forceinline__ void ff_add(FloatFloat &a, float b) {
+    const float s = a.hi + b;
+    const float bb = s - a.hi;
+    const float e = (a.hi - (s - bb)) + (b - bb);
+    a.hi = s;
+    a.lo += e;
+}
+__device__ __forceinline__ void ff_add(FloatFloat &a, const FloatFloat &b) {
+    ff_add(a, b.hi);
+    a.lo += b.lo;
+}
+
 __global__ void __launch_bounds__(1024) ce_finalize_kernel(
     const float *__restrict__ loss, const int64_t *__restrict__ argmax,
     const int64_t *__restrict__ labels, int64_t N, int64_t V, int64_t ignore_index, int reduction,
     const int64_t *counts, const int *err, float *out_reduced, int64_t *out_counts) {
     ptx::griddep_wait();
-    double acc = 0.0;
+    FloatFloat acc = {0.f, 0.f};
     long long nc = 0;
     const int64_t st = blockDim.x;
     // four rows' values in flight per thread (the loop is load-latency bound);
@@ -90,15 +110,17 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             if (y[u] == ignore_index) continue;
-            acc += static_cast<double>(l[u]);
+            ff_add(acc, l[u]);
             if (y[u] >= 0 && y[u] < V && am[u] == y[u]) ++nc;
         }
     }
-    __shared__ double sa[32];
+    __shared__ FloatFloat sa[32];
     __shared__ long long sc[32];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const FloatFloat o = {__shfl_xor_sync(0xffffffffu, acc.hi, off),
+                              __shfl_xor_sync(0xffffffffu, acc.lo, off)};
+        ff_add(acc, o);
         nc += __shfl_xor_sync(0xffffffffu, nc, off);
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -109,17 +131,19 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(
     __syncthreads();
     if (warp == 0) {
         const int nw = blockDim.x >> 5;
-        acc = lane < nw ? sa[lane] : 0.0;
+        acc = lane < nw ? sa[lane] : FloatFloat{0.f, 0.f};
         nc = lane < nw ? sc[lane] : 0;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const FloatFloat o = {__shfl_xor_sync(0xffffffffu, acc.hi, off),
+                                  __shfl_xor_sync(0xffffffffu, acc.lo, off)};
+            ff_add(acc, o);
             nc += __shfl_xor_sync(0xffffffffu, nc, off);
         }
         if (lane == 0) {
             const long long nv = counts[0];
-            double red = acc;
-            if (reduction == VLMCE_MEAN) red = nv > 0 ? acc / static_cast<double>(nv) : 0.0;
+            double red = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
+            if (reduction == VLMCE_MEAN) red = nv > 0 ? red / static_cast<double>(nv) : 0.0;
             const double accuracy = nv > 0 ? static_cast<double>(nc) / static_cast<double>(nv) : 0.0;
             if (out_reduced) {
                 out_reduced[0] = static_cast<float>(red);

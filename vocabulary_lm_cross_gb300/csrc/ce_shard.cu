@@ -118,6 +118,10 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     int gl = g.gs + tid;
     for (; gl + THREADS < g.ge; gl += 2 * THREADS) {  // two loads in flight, column order kept
         const uint4 w0 = rows::ld_v4(g.row() + gl), w1 = rows::ld_v4(g.row() + gl + THREADS);
+        if (gl + 3 * THREADS < g.ge) {  // the next iteration's pair, into L2 (as the row kernel)
+            ptx::prefetch_l2(g.row() + gl + 2 * THREADS);
+            ptx::prefetch_l2(g.row() + gl + 3 * THREADS);
+        }
         rows::fold_full<BF16, SOFTCAP, true>(a, w0, gl * EPG - g.lead, p.V_local, k, poly_ok);
         rows::fold_full<BF16, SOFTCAP, true>(a, w1, (gl + THREADS) * EPG - g.lead, p.V_local, k,
                                              poly_ok);
