@@ -17,8 +17,8 @@
 //                    the row split over its CTAs in shared memory and merged
 //                    through distributed shared memory; for few, wide rows,
 //                    where one CTA per row would leave most SMs idle.
-//   3. ce_finalize_kernel -- fixed-order fp64 reduction of the per-row losses
-//      and correct-prediction count.
+//   3. ce_finalize_kernel -- fixed-order float-float reduction of the
+//      per-row losses and correct-prediction count.
 // Kernels 2 and 3 use programmatic dependent launch, so that their prologues
 // overlap the previous kernel's tail.  No floating-point atomics: results are
 // bit-reproducible.
