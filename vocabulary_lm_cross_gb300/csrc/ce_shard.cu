@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
     const rows::CapK k = rows::cap_k<SOFTCAP>(T);
+    // short rows: the whole row is requested into L2 at once (one bulk
+    // prefetch), so that the loads below wait for L2 rather than DRAM
+    if (THREADS == rows::kTinyThreads && tid == 0)
+        ptx::bulk_prefetch_l2(g.gbase, 16u * static_cast<uint32_t>(g.G));
     bool poly_ok = true;
     rows::Acc a;
     rows::acc_init(a);
