@@ -395,10 +395,6 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     constexpr bool kReverse2 = SOFTCAP;
 
     // ---- pass 1
-    // short rows: the whole row is requested into L2 at once (one bulk
-    // prefetch), so that the loads below wait for L2 rather than DRAM
-    if (THREADS == kTinyThreads && tid == 0)
-        ptx::bulk_prefetch_l2(gbase, 16u * static_cast<uint32_t>(G));
     Acc a;
     acc_init(a);
     bool poly_ok = true;  // every whole granule of this thread took the polynomial softcap

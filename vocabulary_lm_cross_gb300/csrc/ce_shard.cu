@@ -110,10 +110,6 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     const Geo g = geometry<BF16, THREADS>(p);
     const float T = p.softcap;
     const rows::CapK k = rows::cap_k<SOFTCAP>(T);
-    // short rows: the whole row is requested into L2 at once (one bulk
-    // prefetch), so that the loads below wait for L2 rather than DRAM
-    if (THREADS == rows::kTinyThreads && tid == 0)
-        ptx::bulk_prefetch_l2(g.gbase, 16u * static_cast<uint32_t>(g.G));
     bool poly_ok = true;
     rows::Acc a;
     rows::acc_init(a);
@@ -189,16 +185,36 @@ __global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
     const float T = p.softcap;
     const rows::CapK k = rows::cap_k<SOFTCAP>(T);
     // the row's statistics over the whole vocabulary: its k gathered records
-    // merged in shard order (the operator and order of ce_merge_stats) by one
-    // thread, shared with the CTA
+    // merged in shard order (the operator and order of ce_merge_stats) by the
+    // first warp -- lane i loads record i, so the k loads are in flight
+    // together -- and shared with the CTA
     __shared__ RowPart srow;
-    if (tid == 0) {
-        RowPart st = p.stats[r];
-        for (int i = 1; i < p.k; ++i) {
-            const RowPart b = p.stats[static_cast<int64_t>(i) * p.N + r];
-            part_merge(st, b.mx, b.idx, b.mz, b.s, b.sz, b.zy);
+    if (tid < 32) {
+        RowPart st = part_identity();
+        for (int base = 0; base < p.k; base += 32) {
+            RowPart mine = part_identity();
+            if (base + tid < p.k) mine = p.stats[static_cast<int64_t>(base + tid) * p.N + r];
+            const int n = p.k - base < 32 ? p.k - base : 32;
+            for (int i = 0; i < n; ++i) {
+                const float mx = __shfl_sync(0xffffffffu, mine.mx, i);
+                const int idx = __shfl_sync(0xffffffffu, mine.idx, i);
+                const float mz = __shfl_sync(0xffffffffu, mine.mz, i);
+                const float s = __shfl_sync(0xffffffffu, mine.s, i);
+                const float sz = __shfl_sync(0xffffffffu, mine.sz, i);
+                const float zy = __shfl_sync(0xffffffffu, mine.zy, i);
+                if (base + i == 0) {
+                    st.mx = mx;
+                    st.idx = idx;
+                    st.mz = mz;
+                    st.s = s;
+                    st.sz = sz;
+                    st.zy = zy;
+                } else {
+                    part_merge(st, mx, idx, mz, s, sz, zy);
+                }
+            }
         }
-        srow = st;
+        if (tid == 0) srow = st;
     }
     __syncthreads();
     const float lse = srow.mz + logf(srow.s);
