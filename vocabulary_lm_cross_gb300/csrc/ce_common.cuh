@@ -156,20 +156,19 @@ __device__ __forceinline__ Cap2 softcap2(float x0, float x1, float neg2_log2e_ov
     return c;
 }
 // ---------------------------------------------------- polynomial softcap
-// Where |x| <= 0.6 T (nearly every column at the softcaps the pages use),
-// tanh(x/T) = u P(u^2) with u = x/T and P the degree-5 least-squares fit of
-// tanh(u)/u on u in [0, 0.6] (relative error 2.6e-9 at 4000 Chebyshev nodes,
-// below fp32 rounding): eight packed fp32x2 FMA-pipe ops per column pair,
-// with the coefficients as constants, and no MUFU op, against about twelve
-// and two MUFU ops for softcap2 (measured fp32 error of t: below 1e-7).
-// There 1 - t^2 >= 0.64 is formed directly, with no cancellation.  Columns
-// beyond 0.6 T keep softcap2.
-constexpr float kPolyRange = 0.6f;
+// Where |x| <= 0.55 T (nearly every column at the softcaps the pages use),
+// tanh(x/T) = u P(u^2) with u = x/T and P the degree-4 least-squares fit of
+// tanh(u)/u on u in [0, 0.55] (relative error 3.3e-8 at 4000 Chebyshev nodes;
+// measured fp32 error of t below 8e-8): seven packed fp32x2 FMA-pipe ops per
+// column pair, with the coefficients as constants, and no MUFU op, against
+// about twelve and two MUFU ops for softcap2.  There 1 - t^2 >= 0.75 is formed
+// directly, with no cancellation.  Columns beyond 0.55 T keep softcap2.
+constexpr float kPolyRange = 0.55f;
 
 struct PolyCap {
     float rT;       // 1 / T
-    float lim;      // 0.6 T
-    uint32_t lim2;  // bf16x2: the largest bf16 at most 0.6 T, in both halves
+    float lim;      // 0.55 T
+    uint32_t lim2;  // bf16x2: the largest bf16 at most 0.55 T, in both halves
 };
 __device__ __forceinline__ PolyCap poly_cap(float T) {
     PolyCap pc;
@@ -179,16 +178,15 @@ __device__ __forceinline__ PolyCap poly_cap(float T) {
     pc.lim2 = h | (h << 16);
     return pc;
 }
-// tanh(x/T) of two columns (each |x| <= 0.6 T) by the polynomial.
+// tanh(x/T) of two columns (each |x| <= 0.55 T) by the polynomial.
 __device__ __forceinline__ uint64_t tanh_poly2(uint64_t x, const PolyCap &pc) {
     const uint64_t u = mul2(x, pk(pc.rT, pc.rT));
     const uint64_t s = mul2(u, u);
-    uint64_t a = fma2(pk(-0.005845389623524097f, -0.005845389623524097f), s,
-                      pk(0.020747493959974658f, 0.020747493959974658f));
-    a = fma2(a, s, pk(-0.05376675836931074f, -0.05376675836931074f));
-    a = fma2(a, s, pk(0.13331663695216267f, 0.13331663695216267f));
-    a = fma2(a, s, pk(-0.333332821049514f, -0.333332821049514f));
-    a = fma2(a, s, pk(0.9999999974262797f, 0.9999999974262797f));
+    uint64_t a = fma2(pk(0.016301813790173283f, 0.016301813790173283f), s,
+                      pk(-0.05258102516972439f, -0.05258102516972439f));
+    a = fma2(a, s, pk(0.13318718793849865f, 0.13318718793849865f));
+    a = fma2(a, s, pk(-0.33332785337019116f, -0.33332785337019116f));
+    a = fma2(a, s, pk(0.9999999667018895f, 0.9999999667018895f));
     return mul2(u, a);
 }
 
@@ -276,7 +274,7 @@ __device__ __forceinline__ ExpCoef grad_exp_coef(float lse, float scale) {
 }
 
 // Whether every value of a whole granule lies within the polynomial
-// softcap's range (|x| <= 0.6 T); NaN counts as outside.
+// softcap's range (|x| <= 0.55 T); NaN counts as outside.
 template <bool BF16>
 __device__ __forceinline__ bool granule_in_poly_range(const uint4 w, const PolyCap &pc) {
     if constexpr (BF16) {

@@ -1,7 +1,8 @@
 // ce_rows.cuh -- the cross-entropy row kernel (default path): one CTA per
 // row; 1024 threads (two CTAs, 64 warps per SM) for long rows, 256 threads
-// (eight CTAs per SM) for rows of at most kShortGranules granules and (five
-// per SM, for their registers) for softcap rows.
+// (eight CTAs per SM) for rows of at most kShortGranules granules and (six
+// per SM, for their registers) for softcap rows, 128 threads (sixteen per SM)
+// for rows of at most kTinyGranules granules.
 //
 //   pass 1: stream the row from HBM in 16-byte granules: max and first argmax
 //           of the raw logits, online sum of exp(z - m) and sum of z;
@@ -49,10 +50,11 @@ constexpr int kShortGranules = 8192;
 constexpr int kTinyThreads = 128;
 constexpr int kTinyGranules = 2048;
 // CTAs per SM the launch bounds ask for (the softcap variants need more
-// registers per thread: 48 at five 256-thread CTAs per SM).
+// registers per thread: 40 at six 256-thread CTAs per SM, a few of them spilled
+// on the rare paths).
 constexpr int min_blocks(int threads, bool softcap) {
     return threads == kThreads ? (softcap ? 1 : 2)
-                               : threads == kTinyThreads ? 16 : (softcap ? 5 : 8);
+                               : threads == kTinyThreads ? 16 : (softcap ? 6 : 8);
 }
 
 struct Params {
@@ -388,7 +390,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const float T = p.softcap;
     const CapK k = cap_k<SOFTCAP>(T);
     // Pass 2 prefetches ahead where the rows in flight exceed L2: softcap
-    // rows (five 256-thread CTAs per SM, up to 760 rows in flight).  There it
+    // rows (six 256-thread CTAs per SM, up to 912 rows in flight).  There it
     // also walks the row backwards, so that it starts on the lines pass 1
     // read last, the ones most likely still in L2.
     constexpr bool kPrefetch2 = SOFTCAP;
@@ -531,7 +533,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
 }
 
 // Long rows: two CTAs of 1024 threads per SM (32 registers per thread); short
-// rows: eight CTAs of 256.  Softcap rows: 256-thread CTAs, five per SM (48
+// rows: eight CTAs of 256.  Softcap rows: 256-thread CTAs, six per SM (40
 // registers).
 template <bool BF16, bool SOFTCAP, int THREADS>
 __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
@@ -555,7 +557,7 @@ inline bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
 }
 
 // CTA size of the row kernel for rows of G granules (with or without a softcap).
-// Softcap rows always take 256-thread CTAs: five of them per SM keep more
+// Softcap rows always take 256-thread CTAs: six of them per SM keep more
 // warps resident than one CTA of 1024 at 64 registers, and their barriers
 // stall fewer warps at a time.
 inline int threads_for(int64_t G, bool softcap) {
