@@ -207,6 +207,61 @@ def test_no_rows():
     assert res.counts.cpu().tolist() == [0, 0, 0, 0]
 
 
+def planted_maxima(N, V, stride, dtype, seed=11, top=40.0, pad=4096.0):
+    """Rows [N, stride] (device, dtype) whose maximum `top` is planted where the
+    kernels' argmax bookkeeping has its cases: the first column (inside the
+    partial first granule of an unaligned row), the last column (partial last
+    granule), two equal maxima in one granule, in adjacent granules (adjacent
+    threads), far apart (different warps), three of them, none planted, and
+    one in the last whole granule plus one in the partial last granule.  The
+    padding columns hold a larger value, so a kernel that lets a column
+    outside [0, V) of a partial granule into the maximum is caught.  Labels:
+    random, every fifth ignored, some on the first planted column."""
+    g = torch.Generator().manual_seed(seed)
+    xf = torch.randn(N, stride, generator=g, dtype=torch.float64) * 2.0
+    xf[:, V:] = pad
+    epg = 8 if dtype == "bf16" else 4
+    lab = torch.randint(0, V, (N,), generator=g)
+    for r in range(N):
+        lead = (r * stride) % epg  # elements of row r's first granule before column 0
+        a = 1000 - (1000 + lead) % epg  # a column that starts a granule
+        cols = {0: [0], 1: [V - 1], 2: [a + 1, a + 3], 3: [a + epg - 1, a + epg + 1],
+                4: [17, V - 20], 5: [0, V // 2, V - 1], 6: [], 7: [V - epg - 1, V - 1]}[r % 8]
+        for c in cols:
+            xf[r, c] = top
+        if r % 7 == 3 and cols:
+            lab[r] = cols[0]
+        if r % 5 == 0:
+            lab[r] = IGNORE_INDEX
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return xf.to(tdt).to(DEV), lab.to(DEV)
+
+
+# The argmax is the first column of the row's maximum wherever it sits: the
+# kernels record only the granule of a new maximum and resolve the column
+# once per row, by the thread that stores that granule in pass 2.
+@pytest.mark.parametrize("path", ["rows", "split"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [0.0, 30.0])
+@pytest.mark.parametrize("V,stride", [(5001, 5004), (70001, 70004)])
+def test_argmax_at_planted_maxima(path, dtype, T, V, stride, monkeypatch):
+    monkeypatch.setenv("VLMCE_CE_PATH", path)
+    x, lab = planted_maxima(48, V, stride, dtype)
+    x0 = x.clone()
+    # forward only: argmax and loss, the logits untouched
+    xin = host_rows(x, dtype)
+    ref = oc.ce_fwd_bwd(xin, dtype, V, lab.cpu().numpy(), label_smoothing=0.1, softcap=T,
+                        reduction="mean", want_grad=False)
+    rf = v.ce_fwd_bwd(x[:, :V], lab, label_smoothing=0.1, softcap=T, compute_grad=False)
+    torch.cuda.synchronize()
+    assert np.array_equal(rf.argmax.cpu().numpy(), ref["argmax"])
+    check_loss(rf.loss.cpu().numpy(), ref["loss"])
+    assert torch.equal(x, x0)
+    # with the gradient: every output against the oracle
+    res, ref2, _ = check_call(x, lab, V, dtype, eps=0.1, T=T, red="mean", gs=1.0)
+    assert torch.equal(res.argmax, rf.argmax)
+
+
 def test_all_rows_ignored_and_bad_labels():
     w = small(16, 3000, "bf16", ignore=1.0)
     res, ref, _ = run_and_check(w)

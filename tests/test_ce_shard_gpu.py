@@ -141,6 +141,28 @@ def test_one_shard_is_ce_fwd_bwd_bit_for_bit(monkeypatch, dtype, T, eps):
     assert torch.equal(ra.reduced.view(torch.int32), rb.reduced.view(torch.int32))
 
 
+# The shard statistics resolve the argmax column of each shard's maximum
+# after the merge of the warps; the record merge keeps the smallest column.
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [0.0, 30.0])
+def test_argmax_at_planted_maxima_across_shards(dtype, T):
+    from tests.test_ce_gpu import planted_maxima
+    V = 20001
+    x, lab = planted_maxima(64, V, V + 3, dtype)
+    cuts = [17, 1000, 1005, V // 2 + 1, V - 19]
+    edges, shards, stats, g, outs = run_protocol(x[:, :V], lab, V, cuts, eps=0.1, T=T,
+                                                 red="mean", gs=1.0)
+    xh = host_x(x[:, :V].contiguous(), dtype)
+    labh = lab.cpu().numpy()
+    ref = oc.ce_fwd_bwd(xh, dtype, V, labh, label_smoothing=0.1, softcap=T, reduction="mean",
+                        want_grad=False)
+    for i, (a, b) in enumerate(zip(edges[:-1], edges[1:])):
+        o = osh.shard_stats(widen(xh[:, a:b], dtype), a, labh, T)
+        assert np.array_equal(stats_argmax(stats[i]).cpu().numpy(), o["argmax"]), i
+    assert np.array_equal(stats_argmax(g).cpu().numpy(), ref["argmax"])
+    assert np.array_equal(outs[0].argmax.cpu().numpy(), ref["argmax"])
+
+
 def test_merge_in_place_and_of_identical_shards():
     N = 33
     x = torch.randn(N, 500, device=DEV).to(torch.bfloat16)

@@ -7,20 +7,27 @@
 //   pass 1: stream the row from HBM in 16-byte granules: max and first argmax
 //           of the raw logits, online sum of exp(z - m) and sum of z;
 //   merge:  warp shuffles, then the warp partials (fixed order);
-//   pass 2: read the row again -- without a softcap it is still in the 129 MB
-//           L2, since at most 2 x 152 rows (78 MB for 256 KB rows) are in
-//           flight; softcap rows exceed L2 and are prefetched into it ahead --
-//           and store the gradient scale (p - q) (1 - t^2), rounded to the
-//           storage dtype, with 16-byte evict-first stores over the logits.
+//   pass 2: read the row again, last granule first (the lines pass 1 read
+//           last are the likeliest still in L2) -- without a softcap it is
+//           mostly still in the 129 MB L2, since at most 2 x 152 rows (78 MB
+//           for 256 KB rows) are in flight; softcap rows exceed L2 and are
+//           prefetched into it ahead -- and store the gradient scale (p - q)
+//           (1 - t^2), rounded to the storage dtype, with 16-byte evict-first
+//           stores over the logits.
 // Without a softcap HBM sees about one read and one write of every byte.  The label census of the call is only needed by pass 2, so the kernel
 // waits for it (programmatic dependent launch) after pass 1.
 //
 // Pass 1 keeps two 16-byte loads in flight per thread and prefetches the
 // next iteration's pair into L2, so that enough bytes are outstanding per SM
-// to cover the DRAM latency.  Its arithmetic is the rest of its cost: the
-// reference of the exponentials moves lazily (new_max), since with 16 or more
-// granules per thread some lane of a warp meets a new maximum in most
-// granules.
+// to cover the DRAM latency.  Its arithmetic is the rest of its cost.  With
+// 16 to 80 granules per thread some lane of a warp meets a new maximum in
+// most granules, so the branch a new maximum takes (new_max) is kept short:
+// the reference of the exponentials moves lazily, and softcap rows, whose
+// pass 1 is bound by instruction issue, record only the granule of the
+// first maximum -- the column within it is found once per row, after the
+// merge (first_max_col).  Rows without a softcap locate the column in
+// new_max: measured on GB300, deferring it there saved 29 % of the
+// instructions but cost 4-6 % of the time (more of pass 2 missed L2).
 // The kernel is bound by instruction issue, so the inner loops run over whole
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
@@ -57,6 +64,13 @@ constexpr int min_blocks(int threads, bool softcap) {
                                : threads == kTinyThreads ? 16 : (softcap ? 6 : 8);
 }
 
+// What the merge hands every thread of the row: lse and the row's maximum
+// with the first column of its granule.
+struct RowBcast {
+    float lse, mx;
+    int idx;
+};
+
 struct Params {
     unsigned char *logits;
     const int64_t *labels;
@@ -88,7 +102,7 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
 // the two halves of packed fp32x2 registers.
 struct Acc {
     float mv;    // max raw logit seen
-    int midx;    // its first column
+    int midx;    // first column of mv; softcap rows: first column of its granule
     float mz;    // reference of s, at least the largest z seen
     float nmL;   // -mz log2e
     float xthr;  // largest x whose z mz is known to cover
@@ -113,7 +127,7 @@ __device__ __forceinline__ RowPart acc_part(const Acc &a, float T) {
     upk(a.s, s0, s1);
     upk(a.z, z0, z1);
     pt.mx = a.mv;
-    pt.idx = a.midx;
+    pt.idx = a.midx;  // softcap rows: a granule's first column, resolved by first_max_col
     pt.mz = a.mz;
     pt.s = s0 + s1;
     pt.sz = SOFTCAP ? T * (z0 + z1) : z0 + z1;
@@ -148,20 +162,25 @@ __device__ __forceinline__ float z_of(float x, const CapK &k) {
 // <= 1, and one below e^-8 loses nothing (fp32 precision is relative).
 constexpr float kRefMargin = 8.f;
 
-// New maximum gm in the granule starting at column jg: locate its first
-// column among the valid ones; only when gm passes xthr, move the reference
-// of the running sums to z(gm) + kRefMargin and rescale them.  (z grows no
-// faster than x, so mz covers every x <= gm + kRefMargin.)
+// New maximum gm in the granule starting at column jg: record its first
+// column (softcap rows: the granule's first column); only when gm passes
+// xthr, move the reference of the running sums to z(gm) + kRefMargin and
+// rescale them.  (z grows no faster than x, so mz covers every x <= gm +
+// kRefMargin.)
 template <bool BF16, bool SOFTCAP>
 __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPerGranule],
                                         float gm, int jg, int V, const CapK &k) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
-    int li = EPG - 1;
-#pragma unroll
-    for (int l = EPG - 1; l >= 0; --l)
-        if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
     a.mv = gm;
-    a.midx = jg + li;
+    if constexpr (SOFTCAP) {
+        a.midx = jg;
+    } else {
+        int li = EPG - 1;
+#pragma unroll
+        for (int l = EPG - 1; l >= 0; --l)
+            if (x[l] == gm && jg + l >= 0 && jg + l < V) li = l;
+        a.midx = jg + li;
+    }
     if (gm > a.xthr) {
         const float nz = z_of<SOFTCAP>(gm, k) + kRefMargin;
         const float f = ptx::ex2((a.mz - nz) * kLog2e);
@@ -174,6 +193,23 @@ __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPe
         a.nmL = -nz * kLog2e;
         a.xthr = gm + kRefMargin;
     }
+}
+
+// A softcap row's argmax from its merged statistics: the first column in
+// [0, V) of granule w (first column jg) that holds the maximum mv.  Threads visit
+// their granules in column order and keep the first granule that reaches
+// their maximum, and the merges keep the smallest granule among equal
+// maxima, so this is the smallest column holding the row's maximum.
+template <bool BF16>
+__device__ __forceinline__ int first_max_col(const uint4 w, float mv, int jg, int V) {
+    constexpr int EPG = Elem<BF16>::kPerGranule;
+    float x[EPG];
+    unpack<BF16>(w, x);
+    int li = EPG - 1;
+#pragma unroll
+    for (int l = EPG - 1; l >= 0; --l)
+        if (x[l] == mv && jg + l >= 0 && jg + l < V) li = l;
+    return jg + li;
 }
 
 // Fold a whole granule (every column valid), two columns per packed op.
@@ -368,7 +404,7 @@ __device__ __forceinline__ void store_partial(unsigned char *dst, int jg, int V,
 }
 
 template <bool BF16, bool SOFTCAP, bool SUMZ, int THREADS>
-__device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float *bcast) {
+__device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBcast *bc) {
     constexpr int kWarps = THREADS / 32;
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int ELT = Elem<BF16>::kBytes;
@@ -389,12 +425,11 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
     const int tail_tid = tail ? (G - 1 - gs) % THREADS : -1;
     const float T = p.softcap;
     const CapK k = cap_k<SOFTCAP>(T);
-    // Pass 2 prefetches ahead where the rows in flight exceed L2: softcap
-    // rows (six 256-thread CTAs per SM, up to 912 rows in flight).  There it
-    // also walks the row backwards, so that it starts on the lines pass 1
-    // read last, the ones most likely still in L2.
-    constexpr bool kPrefetch2 = SOFTCAP;
-    constexpr bool kReverse2 = SOFTCAP;
+    // Pass 2 walks the row backwards, so that it starts on the lines pass 1
+    // read last, the ones most likely still in L2.  Where the rows in flight
+    // exceed L2 -- softcap rows (six 256-thread CTAs per SM, up to 912 rows
+    // in flight) -- it keeps two granules in flight and prefetches ahead.
+    constexpr bool kAhead2 = SOFTCAP;
 
     // ---- pass 1
     Acc a;
@@ -447,11 +482,25 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
                 l = __int_as_float(0x7fc00000);  // bad label: NaN
             }
             p.loss[r] = l;
-            p.argmax[r] = q.idx;
-            *bcast = lse;
+            if (!SOFTCAP || q.idx == INT_MAX) p.argmax[r] = q.idx;  // INT_MAX: every logit -inf or NaN
+            bc->lse = lse;
+            bc->mx = q.mx;
+            bc->idx = q.idx;
         }
     }
     __syncthreads();
+    // A softcap row's argmax column: the granule of its first maximum is
+    // resolved by the thread that stores it in pass 2 (under every branch
+    // below), before it does so; so no other thread writes it, and no barrier
+    // waits for the load.
+    if (SOFTCAP && bc->idx != INT_MAX) {
+        const int gb = (bc->idx + lead) / EPG;
+        const bool rev = valid && p.want_grad;  // pass 2 proper walks backwards, the zeroing forwards
+        const int owner = (head && gb == 0)       ? 0
+                          : (tail && gb == G - 1) ? tail_tid
+                                                  : (rev ? ge - 1 - gb : gb - gs) % THREADS;
+        if (tid == owner) p.argmax[r] = first_max_col<BF16>(ld_v4(row + gb), bc->mx, bc->idx, p.V);
+    }
     // The label census of this call, which pass 2 reads.  Every CTA waits (not
     // only those that read it), so the grid completes after the census: the
     // finalize kernel, launched dependent on this grid, reads its counts.
@@ -466,7 +515,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         if (p.reduction == VLMCE_MEAN)
             scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
         if (p.token_scale) scale *= p.token_scale[r];
-        set_coef(c, *bcast, scale, p.eps, p.V);
+        set_coef(c, bc->lse, scale, p.eps, p.V);
         c.k = k;
         const int gy = static_cast<int>((y + lead) / EPG);
         const int ly = static_cast<int>((y + lead) % EPG);
@@ -475,7 +524,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         // like any other in the loop, then overwrites the one element with the
         // label gradient, so the loop itself has no label test.
         const int y_owner =
-            (gy >= gs && gy < ge) ? (kReverse2 ? ge - 1 - gy : gy - gs) % THREADS : -1;
+            (gy >= gs && gy < ge) ? (ge - 1 - gy) % THREADS : -1;
         unsigned char *py = gbase + ELT * (static_cast<int64_t>(y) + lead);
         float xy = 0.f;
         if (tid == y_owner) {
@@ -493,22 +542,25 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
         // whole row within the polynomial's range
         auto whole = [&](auto mode) {
             constexpr int M = decltype(mode)::value;
-            if constexpr (kReverse2) {
-                for (int gl = ge - 1 - tid; gl >= gs; gl -= THREADS) {
-                    // the granule two iterations ahead, into L2 (where the row has
-                    // partly left L2 since pass 1)
-                    if (kPrefetch2 && gl - 2 * THREADS >= gs)
+            int gl = ge - 1 - tid;
+            if constexpr (kAhead2) {
+                for (; gl - THREADS >= gs; gl -= 2 * THREADS) {
+                    // the pair two iterations ahead, into L2 (the row has partly
+                    // left L2 since pass 1)
+                    if (gl - 3 * THREADS >= gs) {
                         ptx::prefetch_l2(row + gl - 2 * THREADS);
-                    grad_values<BF16, SOFTCAP, M>(ld_v4(row + gl), c, -1, g);
+                        ptx::prefetch_l2(row + gl - 3 * THREADS);
+                    }
+                    const uint4 w0 = ld_v4(row + gl), w1 = ld_v4(row + gl - THREADS);
+                    grad_values<BF16, SOFTCAP, M>(w0, c, -1, g);
                     ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
+                    grad_values<BF16, SOFTCAP, M>(w1, c, -1, g);
+                    ptx::st_global_cs_v4(gbase + 16 * (gl - THREADS), pack_granule<BF16>(g));
                 }
-            } else {
-                for (int gl = gs + tid; gl < ge; gl += THREADS) {
-                    if (kPrefetch2 && gl + 2 * THREADS < ge)
-                        ptx::prefetch_l2(row + gl + 2 * THREADS);
-                    grad_values<BF16, SOFTCAP, M>(ld_v4(row + gl), c, -1, g);
-                    ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
-                }
+            }
+            for (; gl >= gs; gl -= THREADS) {
+                grad_values<BF16, SOFTCAP, M>(ld_v4(row + gl), c, -1, g);
+                ptx::st_global_cs_v4(gbase + 16 * gl, pack_granule<BF16>(g));
             }
         };
         if (!SOFTCAP || row_poly)
@@ -538,7 +590,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, float 
 template <bool BF16, bool SOFTCAP, int THREADS>
 __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
     __shared__ RowPart wpart[THREADS / 32];
-    __shared__ float bcast;
+    __shared__ RowBcast bcast;
     // sum z only matters with label smoothing; skip the adds without it
     if (p.eps > 0.f)
         row_work<BF16, SOFTCAP, true, THREADS>(p, wpart, &bcast);

@@ -140,10 +140,16 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
         RowPart q = lane < kWarps ? wpart[lane] : part_identity();
         warp_allreduce(q);
         if (lane == 0) {
+            // softcap rows: the granule of the shard's first maximum, whose
+            // column is resolved here; its load overlaps the label's
+            const uint4 wm = SOFTCAP && q.idx != INT_MAX
+                                 ? rows::ld_v4(g.row() + (q.idx + g.lead) / EPG)
+                                 : make_uint4(0u, 0u, 0u, 0u);
             const int64_t yl = p.labels[blockIdx.x] - p.vocab_start;
             q.zy = 0.f;
             if (yl >= 0 && yl < p.V_local)
                 q.zy = rows::z_of<SOFTCAP>(load_x<BF16>(row_addr(p), yl), k);
+            if (SOFTCAP && q.idx != INT_MAX) q.idx = rows::first_max_col<BF16>(wm, q.mx, q.idx, p.V_local);
             q.idx = q.idx == INT_MAX ? INT_MAX : static_cast<int>(q.idx + p.vocab_start);
             q.pad0 = q.pad1 = 0.f;
             p.stats[blockIdx.x] = q;
