@@ -363,8 +363,9 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
             p.token_scale = token_scale;
             p.want_grad = want_grad ? 1 : 0;
             const int th = rows::threads_for(G, capped);
-            st = launch_rows(bf16 ? rows::kernel_bf16(capped, th) : rows::kernel_f32(capped, th), p,
-                             N, th, true, cs);
+            st = launch_rows(bf16 ? rows::kernel_bf16(capped, th, !want_grad)
+                                  : rows::kernel_f32(capped, th, !want_grad),
+                             p, N, th, true, cs);
         }
         if (st != VLMCE_OK) return st;
         if (ee && (st = launch_status(cudaEventRecord(ee, cs), "cudaEventRecord")) != VLMCE_OK)
@@ -558,7 +559,7 @@ vlmce_status run_ce_staged(void *host_logits, int32_t dtype, const int64_t *labe
     const int th = rows::threads_for(
         rows::row_granules(bf16, V, rows::rows_aligned(host_logits, row_stride, elt)), softcap > 0.f);
     const rows::Kernel kern =
-        bf16 ? rows::kernel_bf16(softcap > 0.f, th) : rows::kernel_f32(softcap > 0.f, th);
+        bf16 ? rows::kernel_bf16(softcap > 0.f, th, false) : rows::kernel_f32(softcap > 0.f, th, false);
     const int64_t nchunks = N > 0 ? (N + R - 1) / R : 0;
     for (int64_t i = 0; i < nchunks; ++i) {
         const int b = static_cast<int>(i % kRing);

@@ -25,9 +25,10 @@
 // the reference of the exponentials moves lazily, and softcap rows, whose
 // pass 1 is bound by instruction issue, record only the granule of the
 // first maximum -- the column within it is found once per row, after the
-// merge (first_max_col).  Rows without a softcap locate the column in
-// new_max: measured on GB300, deferring it there saved 29 % of the
-// instructions but cost 4-6 % of the time (more of pass 2 missed L2).
+// merge (first_max_col); so do forward-only calls, which have no pass 2.
+// With a gradient, rows without a softcap locate the column in new_max:
+// measured on GB300, deferring it there saved 29 % of the instructions but
+// cost 4-6 % of the time (more of pass 2 missed L2).
 // The kernel is bound by instruction issue, so the inner loops run over whole
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
@@ -163,16 +164,16 @@ __device__ __forceinline__ float z_of(float x, const CapK &k) {
 constexpr float kRefMargin = 8.f;
 
 // New maximum gm in the granule starting at column jg: record its first
-// column (softcap rows: the granule's first column); only when gm passes
+// column (DEFER: the granule's first column); only when gm passes
 // xthr, move the reference of the running sums to z(gm) + kRefMargin and
 // rescale them.  (z grows no faster than x, so mz covers every x <= gm +
 // kRefMargin.)
-template <bool BF16, bool SOFTCAP>
+template <bool BF16, bool SOFTCAP, bool DEFER>
 __device__ __forceinline__ void new_max(Acc &a, const float (&x)[Elem<BF16>::kPerGranule],
                                         float gm, int jg, int V, const CapK &k) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     a.mv = gm;
-    if constexpr (SOFTCAP) {
+    if constexpr (DEFER) {
         a.midx = jg;
     } else {
         int li = EPG - 1;
@@ -216,14 +217,14 @@ __device__ __forceinline__ int first_max_col(const uint4 w, float mv, int jg, in
 // Under a softcap the exponent is t (T log2e) - mz log2e with t = tanh(x/T),
 // by the polynomial when the whole granule is within its range (else ok is
 // cleared and softcap2 is used).
-template <bool BF16, bool SOFTCAP, bool SUMZ>
+template <bool BF16, bool SOFTCAP, bool SUMZ, bool DEFER = SOFTCAP>
 __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, const CapK &k,
                                           bool &ok) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
     unpack<BF16>(w, x);
     const float gm = granule_max<BF16>(w);
-    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, k);
+    if (gm > a.mv) new_max<BF16, SOFTCAP, DEFER>(a, x, gm, jg, V, k);
     const float L = SOFTCAP ? k.T * kLog2e : kLog2e;
     const uint64_t L2 = pk(L, L), nmL2 = pk(a.nmL, a.nmL);
     if constexpr (SOFTCAP) {
@@ -251,7 +252,7 @@ __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, 
 }
 
 // Fold a granule of which only the columns in [0, V) count (into the even sums).
-template <bool BF16, bool SOFTCAP>
+template <bool BF16, bool SOFTCAP, bool DEFER = SOFTCAP>
 __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int V, const CapK &k) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     float x[EPG];
@@ -260,7 +261,7 @@ __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int 
 #pragma unroll
     for (int l = 0; l < EPG; ++l)
         if (jg + l >= 0 && jg + l < V) gm = fmaxf(gm, x[l]);
-    if (gm > a.mv) new_max<BF16, SOFTCAP>(a, x, gm, jg, V, k);
+    if (gm > a.mv) new_max<BF16, SOFTCAP, DEFER>(a, x, gm, jg, V, k);
     const float L = SOFTCAP ? k.T * kLog2e : kLog2e;
     float s0, s1, z0, z1;
     upk(a.s, s0, s1);
@@ -403,7 +404,7 @@ __device__ __forceinline__ void store_partial(unsigned char *dst, int jg, int V,
         if (jg + l >= 0 && jg + l < V) store_elem<BF16>(dst + ELT * l, g[l]);
 }
 
-template <bool BF16, bool SOFTCAP, bool SUMZ, int THREADS>
+template <bool BF16, bool SOFTCAP, bool SUMZ, int THREADS, bool DEFER>
 __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBcast *bc) {
     constexpr int kWarps = THREADS / 32;
     constexpr int EPG = Elem<BF16>::kPerGranule;
@@ -435,7 +436,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
     Acc a;
     acc_init(a);
     bool poly_ok = true;  // every whole granule of this thread took the polynomial softcap
-    if (head && tid == 0) fold_partial<BF16, SOFTCAP>(a, ld_v4(row), -lead, p.V, k);
+    if (head && tid == 0) fold_partial<BF16, SOFTCAP, DEFER>(a, ld_v4(row), -lead, p.V, k);
     // two granules in flight per thread (the loads of a warp would otherwise
     // leave too few bytes outstanding to cover the DRAM latency); the folds
     // keep the thread's column order
@@ -446,13 +447,13 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
             ptx::prefetch_l2(row + gl + 2 * THREADS);
             ptx::prefetch_l2(row + gl + 3 * THREADS);
         }
-        fold_full<BF16, SOFTCAP, SUMZ>(a, w0, gl * EPG - lead, p.V, k, poly_ok);
-        fold_full<BF16, SOFTCAP, SUMZ>(a, w1, (gl + THREADS) * EPG - lead, p.V, k, poly_ok);
+        fold_full<BF16, SOFTCAP, SUMZ, DEFER>(a, w0, gl * EPG - lead, p.V, k, poly_ok);
+        fold_full<BF16, SOFTCAP, SUMZ, DEFER>(a, w1, (gl + THREADS) * EPG - lead, p.V, k, poly_ok);
     }
     for (; gl < ge; gl += THREADS)
-        fold_full<BF16, SOFTCAP, SUMZ>(a, ld_v4(row + gl), gl * EPG - lead, p.V, k, poly_ok);
+        fold_full<BF16, SOFTCAP, SUMZ, DEFER>(a, ld_v4(row + gl), gl * EPG - lead, p.V, k, poly_ok);
     if (tid == tail_tid)
-        fold_partial<BF16, SOFTCAP>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, k);
+        fold_partial<BF16, SOFTCAP, DEFER>(a, ld_v4(row + (G - 1)), (G - 1) * EPG - lead, p.V, k);
 
     RowPart pt = acc_part<SOFTCAP>(a, T);
     warp_allreduce(pt);
@@ -482,18 +483,18 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
                 l = __int_as_float(0x7fc00000);  // bad label: NaN
             }
             p.loss[r] = l;
-            if (!SOFTCAP || q.idx == INT_MAX) p.argmax[r] = q.idx;  // INT_MAX: every logit -inf or NaN
+            if (!DEFER || q.idx == INT_MAX) p.argmax[r] = q.idx;  // INT_MAX: every logit -inf or NaN
             bc->lse = lse;
             bc->mx = q.mx;
             bc->idx = q.idx;
         }
     }
     __syncthreads();
-    // A softcap row's argmax column: the granule of its first maximum is
+    // DEFER: the argmax column; the granule of the row's first maximum is
     // resolved by the thread that stores it in pass 2 (under every branch
     // below), before it does so; so no other thread writes it, and no barrier
     // waits for the load.
-    if (SOFTCAP && bc->idx != INT_MAX) {
+    if (DEFER && bc->idx != INT_MAX) {
         const int gb = (bc->idx + lead) / EPG;
         const bool rev = valid && p.want_grad;  // pass 2 proper walks backwards, the zeroing forwards
         const int owner = (head && gb == 0)       ? 0
@@ -587,15 +588,15 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
 // Long rows: two CTAs of 1024 threads per SM (32 registers per thread); short
 // rows: eight CTAs of 256.  Softcap rows: 256-thread CTAs, six per SM (40
 // registers).
-template <bool BF16, bool SOFTCAP, int THREADS>
+template <bool BF16, bool SOFTCAP, int THREADS, bool DEFER = SOFTCAP>
 __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
     __shared__ RowPart wpart[THREADS / 32];
     __shared__ RowBcast bcast;
     // sum z only matters with label smoothing; skip the adds without it
     if (p.eps > 0.f)
-        row_work<BF16, SOFTCAP, true, THREADS>(p, wpart, &bcast);
+        row_work<BF16, SOFTCAP, true, THREADS, DEFER>(p, wpart, &bcast);
     else
-        row_work<BF16, SOFTCAP, false, THREADS>(p, wpart, &bcast);
+        row_work<BF16, SOFTCAP, false, THREADS, DEFER>(p, wpart, &bcast);
 }
 
 // Granules (16 B) of a row: exact when every row starts on a 16-byte boundary,
@@ -616,10 +617,11 @@ inline int threads_for(int64_t G, bool softcap) {
     if (!softcap && G <= kTinyGranules) return kTinyThreads;
     return (softcap || G <= kShortGranules) ? kShortThreads : kThreads;
 }
-// The row kernel for the given softcap and CTA size, per element type
+// The row kernel for the given softcap, CTA size and mode (forward only: the
+// argmax column deferred also without a softcap), per element type
 // (ce_rows_bf16.cu, ce_rows_f32.cu).
-Kernel kernel_bf16(bool softcap, int threads);
-Kernel kernel_f32(bool softcap, int threads);
+Kernel kernel_bf16(bool softcap, int threads, bool fwd_only);
+Kernel kernel_f32(bool softcap, int threads, bool fwd_only);
 
 }  // namespace rows
 }  // namespace ce

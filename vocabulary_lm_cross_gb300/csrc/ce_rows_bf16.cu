@@ -4,11 +4,19 @@
 namespace vlmce {
 namespace ce {
 namespace rows {
-Kernel kernel_bf16(bool softcap, int threads) {
-    if (threads == kTinyThreads) return ce_rows_kernel<true, false, kTinyThreads>;  // no softcap
-    if (threads == kShortThreads)
-        return softcap ? ce_rows_kernel<true, true, kShortThreads> : ce_rows_kernel<true, false, kShortThreads>;
-    return softcap ? ce_rows_kernel<true, true, kThreads> : ce_rows_kernel<true, false, kThreads>;
+Kernel kernel_bf16(bool softcap, int threads, bool fwd_only) {
+    if (softcap) {
+        if (threads == kShortThreads) return ce_rows_kernel<true, true, kShortThreads>;
+        return ce_rows_kernel<true, true, kThreads>;
+    }
+    if (fwd_only) {  // the argmax column deferred (no pass 2)
+        if (threads == kTinyThreads) return ce_rows_kernel<true, false, kTinyThreads, true>;
+        if (threads == kShortThreads) return ce_rows_kernel<true, false, kShortThreads, true>;
+        return ce_rows_kernel<true, false, kThreads, true>;
+    }
+    if (threads == kTinyThreads) return ce_rows_kernel<true, false, kTinyThreads>;
+    if (threads == kShortThreads) return ce_rows_kernel<true, false, kShortThreads>;
+    return ce_rows_kernel<true, false, kThreads>;
 }
 }  // namespace rows
 }  // namespace ce
