@@ -8,7 +8,8 @@
 //   1. ce_shard_stats   -- per row of the shard: largest raw logit and its
 //                          smallest global column, online sum of exp(z - m),
 //                          sum of z, z at the label when the shard holds it;
-//                          the row kernel's first pass, one CTA per row.
+//                          the row kernel's first pass, one CTA per row (the
+//                          argmax column resolved once, after the merge).
 //   2. (caller)         -- gather every shard's statistics.
 //   3. ce_merge_stats   -- merge k shards' statistics in shard order (the same
 //                          operator the kernels use between warps), so every
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     rows::Acc a;
     rows::acc_init(a);
     if (g.head && tid == 0)
-        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, k);
+        rows::fold_partial<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row()), -g.lead, p.V_local, k);
     int gl = g.gs + tid;
     for (; gl + THREADS < g.ge; gl += 2 * THREADS) {  // two loads in flight, column order kept
         const uint4 w0 = rows::ld_v4(g.row() + gl), w1 = rows::ld_v4(g.row() + gl + THREADS);
@@ -122,16 +123,16 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
             ptx::prefetch_l2(g.row() + gl + 2 * THREADS);
             ptx::prefetch_l2(g.row() + gl + 3 * THREADS);
         }
-        rows::fold_full<BF16, SOFTCAP, true>(a, w0, gl * EPG - g.lead, p.V_local, k, poly_ok);
-        rows::fold_full<BF16, SOFTCAP, true>(a, w1, (gl + THREADS) * EPG - g.lead, p.V_local, k,
-                                             poly_ok);
+        rows::fold_full<BF16, SOFTCAP, true, true>(a, w0, gl * EPG - g.lead, p.V_local, k, poly_ok);
+        rows::fold_full<BF16, SOFTCAP, true, true>(a, w1, (gl + THREADS) * EPG - g.lead, p.V_local,
+                                                   k, poly_ok);
     }
     for (; gl < g.ge; gl += THREADS)
-        rows::fold_full<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row() + gl), gl * EPG - g.lead,
-                                             p.V_local, k, poly_ok);
+        rows::fold_full<BF16, SOFTCAP, true, true>(a, rows::ld_v4(g.row() + gl), gl * EPG - g.lead,
+                                                   p.V_local, k, poly_ok);
     if (tid == g.tail_tid)
-        rows::fold_partial<BF16, SOFTCAP>(a, rows::ld_v4(g.row() + (g.G - 1)),
-                                          (g.G - 1) * EPG - g.lead, p.V_local, k);
+        rows::fold_partial<BF16, SOFTCAP, true>(a, rows::ld_v4(g.row() + (g.G - 1)),
+                                                (g.G - 1) * EPG - g.lead, p.V_local, k);
     RowPart pt = rows::acc_part<SOFTCAP>(a, T);
     warp_allreduce(pt);
     if (lane == 0) wpart[warp] = pt;
@@ -140,16 +141,17 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
         RowPart q = lane < kWarps ? wpart[lane] : part_identity();
         warp_allreduce(q);
         if (lane == 0) {
-            // softcap rows: the granule of the shard's first maximum, whose
-            // column is resolved here; its load overlaps the label's
-            const uint4 wm = SOFTCAP && q.idx != INT_MAX
+            // the granule of the shard's first maximum (pass 1 records only
+            // the granule), whose column is resolved here; its load overlaps
+            // the label's
+            const uint4 wm = q.idx != INT_MAX
                                  ? rows::ld_v4(g.row() + (q.idx + g.lead) / EPG)
                                  : make_uint4(0u, 0u, 0u, 0u);
             const int64_t yl = p.labels[blockIdx.x] - p.vocab_start;
             q.zy = 0.f;
             if (yl >= 0 && yl < p.V_local)
                 q.zy = rows::z_of<SOFTCAP>(load_x<BF16>(row_addr(p), yl), k);
-            if (SOFTCAP && q.idx != INT_MAX) q.idx = rows::first_max_col<BF16>(wm, q.mx, q.idx, p.V_local);
+            if (q.idx != INT_MAX) q.idx = rows::first_max_col<BF16>(wm, q.mx, q.idx, p.V_local);
             q.idx = q.idx == INT_MAX ? INT_MAX : static_cast<int>(q.idx + p.vocab_start);
             q.pad0 = q.pad1 = 0.f;
             p.stats[blockIdx.x] = q;
