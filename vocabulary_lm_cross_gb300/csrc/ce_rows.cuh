@@ -65,11 +65,13 @@ constexpr int min_blocks(int threads, bool softcap) {
                                : threads == kTinyThreads ? 16 : (softcap ? 6 : 8);
 }
 
-// What the merge hands every thread of the row: lse and the row's maximum
-// with the first column of its granule.
+// What the merge hands every thread of the row: lse, the row's maximum with
+// its first column (deferred: the first column of its granule), and the
+// row's gradient scale.
 struct RowBcast {
     float lse, mx;
     int idx;
+    float scale;
 };
 
 struct Params {
@@ -465,18 +467,21 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
     // every whole granule of the row took the polynomial softcap in pass 1
     const bool row_poly = __syncthreads_and(poly_ok) != 0;
     if (warp == 0) {
+        // the label's logit, loaded while the warp merges
+        float xy = 0.f;
+        if (lane == 0 && valid) {
+            const unsigned char *py = reinterpret_cast<const unsigned char *>(a0) + ELT * y;
+            if constexpr (BF16)
+                xy = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
+            else
+                xy = *reinterpret_cast<const float *>(py);
+        }
         RowPart q = lane < kWarps ? wpart[lane] : part_identity();
         warp_allreduce(q);
         if (lane == 0) {
             const float lse = q.mz + logf(q.s);
             float l = 0.f;
             if (valid) {
-                const unsigned char *py = reinterpret_cast<const unsigned char *>(a0) + ELT * y;
-                float xy;
-                if constexpr (BF16)
-                    xy = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(py)) << 16);
-                else
-                    xy = *reinterpret_cast<const float *>(py);
                 const float zy = z_of<SOFTCAP>(xy, k);
                 l = lse - fmaf(1.f - p.eps, zy, (p.eps / static_cast<float>(p.V)) * q.sz);
             } else if (!ignored) {
@@ -488,6 +493,17 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
             bc->mx = q.mx;
             bc->idx = q.idx;
         }
+    } else if (warp == 1 && lane == 0 && valid && p.want_grad) {
+        // meanwhile the row's gradient scale, from the label census of this
+        // call (waited for here; every thread waits again below)
+        ptx::griddep_wait();
+        float scale = p.grad_scale;
+        if (p.reduction == VLMCE_MEAN) {
+            const int64_t n_valid = p.counts[0];
+            scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
+        }
+        if (p.token_scale) scale *= p.token_scale[r];
+        bc->scale = scale;
     }
     __syncthreads();
     // DEFER: the argmax column; the granule of the row's first maximum is
@@ -510,13 +526,8 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
 
     // ---- pass 2
     if (valid) {
-        const int64_t n_valid = p.counts[0];
         GradCoef c;
-        float scale = p.grad_scale;
-        if (p.reduction == VLMCE_MEAN)
-            scale = n_valid > 0 ? p.grad_scale / static_cast<float>(n_valid) : 0.f;
-        if (p.token_scale) scale *= p.token_scale[r];
-        set_coef(c, bc->lse, scale, p.eps, p.V);
+        set_coef(c, bc->lse, bc->scale, p.eps, p.V);
         c.k = k;
         const int gy = static_cast<int>((y + lead) / EPG);
         const int ly = static_cast<int>((y + lead) % EPG);
