@@ -55,7 +55,10 @@ constexpr int64_t kWsHeader = 256;
 
 __global__ void __launch_bounds__(1024) flce_count_kernel(const int64_t *__restrict__ labels,
                                                           int64_t N, int64_t V, int64_t ignore_index,
-                                                          int64_t *counts, int *err) {
+                                                          int64_t *counts, int *err,
+                                                          unsigned int *tile_ctr, int n_ctr) {
+    // the GEMM launches' tile counters start from zero in every call
+    for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) tile_ctr[i] = 0u;
     long long nv = 0, nb = 0;
     for (int64_t r = threadIdx.x; r < N; r += blockDim.x) {
         const int64_t y = labels[r];
@@ -252,9 +255,12 @@ struct Ws {
     uint16_t *g[2];       // two [N, kChunk] gradient tiles (bf16 or fp16 bits)
     float *out_scale;     // scale of the gradient products' accumulators
     float *gh;            // [N, H] grad_h accumulator
+    unsigned int *tile_ctr;  // [nchunks + 2]: one tile counter per GEMM launch
 };
 
 int64_t ntiles_of(int64_t V) { return (V + gemm::BN - 1) / gemm::BN; }
+// GEMM launches of a vocabulary-chunked call: statistics + one per chunk + one.
+int64_t n_gemm_launches(int64_t V) { return (V + kChunk - 1) / kChunk + 2; }
 
 size_t ws_bytes(int64_t N, int64_t H, int64_t V) {
     int64_t b = kWsHeader;
@@ -262,6 +268,7 @@ size_t ws_bytes(int64_t N, int64_t H, int64_t V) {
     b += 3 * round_up(4 * N, 256) + round_up(8 * N, 256);
     b += 2 * round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     b += round_up(4 * N * H, 256);
+    b += round_up(4 * n_gemm_launches(V), 256);
     return static_cast<size_t>(b);
 }
 
@@ -287,6 +294,8 @@ Ws carve(void *ws, int64_t N, int64_t H, int64_t V) {
         p += round_up(2 * N * static_cast<int64_t>(kChunk), 256);
     }
     w.gh = reinterpret_cast<float *>(p);
+    p += round_up(4 * N * H, 256);
+    w.tile_ctr = reinterpret_cast<unsigned int *>(p);
     return w;
 }
 
@@ -476,7 +485,8 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
     float *loss = out_loss ? out_loss : w.loss;
     int64_t *amax = out_argmax ? out_argmax : w.argmax;
 
-    flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
+    flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err, w.tile_ctr,
+                                          static_cast<int>(n_gemm_launches(V)));
     st = launch_status(cudaSuccess, "flce_count_kernel");
     if (st != VLMCE_OK) return st;
     st = clear_grad_weight_if_empty(N, H, V, grad_weight, accumulate_grad_weight, cs);
@@ -524,6 +534,7 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
             p.col0 = 0;
             p.part = w.part;
             p.part_ld = N;
+            g.tile_ctr = w.tile_ctr;
             st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(stats)");
             if (st != VLMCE_OK) return st;
         }
@@ -601,6 +612,7 @@ extern "C" vlmce_status flce_fwd_bwd_ex(const void *hidden, int32_t dtype, int64
                 pw.ldc = H;
             }
             g.nprob = n;
+            g.tile_ctr = w.tile_ctr + 1 + c;
             st = launch_status(gemm::launch_group(maps, g, cs), "vlmce_gemm_kernel(chunk)");
             if (st != VLMCE_OK) return st;
         }
@@ -677,7 +689,7 @@ extern "C" vlmce_status flce_fwd_bwd_rows(const void *hidden, int32_t dtype, int
     int64_t *amax = out_argmax ? out_argmax : w.argmax;
     const float gmul = f16 ? kF16GradMul : 1.f;
 
-    flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
+    flce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err, nullptr, 0);
     st = launch_status(cudaSuccess, "flce_count_kernel");
     if (st != VLMCE_OK) return st;
     st = clear_grad_weight_if_empty(N, H, V, grad_weight, accumulate_grad_weight, cs);

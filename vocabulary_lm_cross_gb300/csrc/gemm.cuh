@@ -19,7 +19,7 @@
 // per stage, 128-byte swizzle) in a 6-stage ring, so a CTA moves a third
 // less operand data per flop than a single-SM 128 x 256 tile would, and each
 // CTA's TMEM receives its 128 rows of the tile.  Every operand copy is a
-// plain load into the issuing CTA's own shared memory.  CTA = 6 warps:
+// plain load into the issuing CTA's own shared memory.  CTA = 7 warps:
 //   warp 0      one lane issues the TMA loads of this CTA's halves; the
 //               copies of both CTAs count on the leader's "full" barrier;
 //   warp 1      allocates 512 TMEM columns per SM (two 128 x 256 fp32
@@ -28,7 +28,12 @@
 //   warps 2-5   epilogue: each reads its 32-lane TMEM subpartition (one
 //               accumulator row per thread) in 32-column chunks while the
 //               MMA fills the other accumulator; both CTAs' epilogue warps
-//               release an accumulator on the leader's "tmem empty" barrier.
+//               release an accumulator on the leader's "tmem empty" barrier;
+//   warp 6      in the leader, with a tile counter, one lane takes the tile
+//               numbers in order and publishes them to both CTAs (the tiles
+//               in flight then stay a window of consecutive numbers, so the
+//               row tiles that share a weight tile read it close in time).
+// Without a counter the clusters stride over the tiles statically.
 //
 // Operand tile layouts in shared memory (per CTA, bf16, 128-byte swizzle
 // atoms of 8 rows x 128 bytes):
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBarriers);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *tq = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kTileQ] tile numbers
     const uint32_t ring = ptx::smem_addr(smem);
     const uint32_t bar0 = ptx::smem_addr(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -293,6 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
     auto tempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
+    auto qfull = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
+    auto qempty = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + kTileQ + i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t prank = ptx::cluster_ctarank();  // 0: the pair's leader
@@ -311,6 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(tempty(b), 8);  // leader: 4 epilogue warps x 2 CTAs
         }
         ptx::mbar_init(drain, 1);
+        for (int i = 0; i < kTileQ; ++i) {
+            ptx::mbar_init(qfull(i), 1);                 // the leader producer's release-arrive
+            ptx::mbar_init(qempty(i), kTileQConsumers);  // used at the leader only
+        }
         *abort = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -329,6 +341,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
+    // The j-th tile this cluster runs (-1: none left).  Static order: tile
+    // cluster + j * #clusters.  Dynamic order (a.tile_ctr): the leader's
+    // scheduler warp takes tile numbers from the counter, up to kTileQ ahead
+    // of the slowest role, and publishes each to queue slot j % kTileQ of both
+    // CTAs; every role reads the slot and releases it on the leader.  A wait
+    // that gives up ends the sequence (the error bit is set).
+    const bool dyn = a.tile_ctr != nullptr;
+    auto static_tile = [&](int j) {
+        const int64_t t = cluster + static_cast<int64_t>(j) * nclusters;
+        return t < a.tiles ? static_cast<int>(t) : -1;
+    };
+    auto publish = [&](int j) {  // the leader's scheduler lane
+        const int slot = j % kTileQ;
+        int t = -1;
+        if (j < kTileQ || wait_bar<true>(qempty(slot), ((j / kTileQ) - 1) & 1, abort, a.err)) {
+            const unsigned int u = atomicAdd(a.tile_ctr, 1u);
+            t = u < static_cast<unsigned int>(a.tiles) ? static_cast<int>(u) : -1;
+        }
+        tq[slot] = t;
+        ptx::st_dsmem_u32(ptx::mapa(ptx::smem_addr(const_cast<int *>(tq) + slot), 1),
+                          static_cast<uint32_t>(t));
+        ptx::mbar_arrive(qfull(slot));
+        ptx::mbar_remote_arrive_release(ptx::mapa(qfull(slot), 1));
+        return t;
+    };
+    auto consume = [&](int j) {  // every other role; all lanes of a warp call it
+        const int slot = j % kTileQ;
+        int t = -1;
+        if (wait_bar<true>(qfull(slot), (j / kTileQ) & 1, abort, a.err)) t = tq[slot];
+        __syncwarp(__activemask());  // every lane has read the slot
+        if (lane == 0) {
+            if (prank == 0)
+                ptx::mbar_arrive(qempty(slot));
+            else
+                ptx::mbar_remote_arrive_release(ptx::mapa(qempty(slot), 0));
+        }
+        return t;
+    };
+
     if (warp == 0) {
         // ---- TMA producer (every CTA): this CTA's 128 rows of A and its
         // 128-row half of the pair's B tile.  Every copy counts on the full
@@ -338,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
-            for (int t = cluster; t < a.tiles; t += nclusters) {
+            for (int j = 0;; ++j) {
+                const int t = dyn ? consume(j) : static_tile(j);
+                if (t < 0) break;
                 const Tile tl = tile_of(a, t);
                 const Problem &P = a.p[tl.p];
                 const CUtensorMap *ma = &maps.a[tl.p];
@@ -386,8 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (prank == 0 && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            int it = 0;
-            for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
+            for (int it = 0;; ++it) {
+                const int t = dyn ? consume(it) : static_tile(it);
+                if (t < 0) break;
                 const Tile tl = tile_of(a, t);
                 const Problem &P = a.p[tl.p];
                 const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, P.a_mn != 0, P.b_mn != 0, a.f16 != 0);
@@ -419,13 +473,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit_pair(drain, static_cast<uint16_t>(1u << prank));
             drain_bar(drain, 0, a.err);
         }
+    } else if (warp == 6) {
+        // ---- tile scheduler (pair leader, dynamic order only)
+        if (dyn && prank == 0 && lane == 0) {
+            for (int j = 0;; ++j)
+                if (publish(j) < 0) break;
+        }
     } else {
         // ---- epilogue: warps 2-5 of every CTA, TMEM subpartition warp % 4
         const int q = warp & 3;
         const int rl = static_cast<int>(prank) * kHalf + q * 32 + lane;
         const uint32_t tempty_leader = ptx::mapa(tempty(0), 0);
-        int it = 0;
-        for (int t = cluster; t < a.tiles; t += nclusters, ++it) {
+        for (int it = 0;; ++it) {
+            const int t = dyn ? consume(it) : static_tile(it);
+            if (t < 0) break;
             const Tile tl = tile_of(a, t);
             const Problem &P = a.p[tl.p];
             const int b = it & 1;

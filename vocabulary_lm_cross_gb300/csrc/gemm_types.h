@@ -17,10 +17,16 @@ constexpr int kHalf = 128;                  // rows of A and of B held by one CT
 constexpr int kStages = 6;
 constexpr int kOpBytes = kHalf * BK * 2;    // 16 KB per operand per stage
 constexpr int kStageBytes = 2 * kOpBytes;   // 32 KB per CTA
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kTmemCols = 2 * BN;
-constexpr int kBarriers = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kBarriers + 16;
+// Dynamic tile order: a scheduler warp of the pair leader takes the next tile
+// number from a counter in global memory and publishes it to both CTAs'
+// roles through a queue of kTileQ slots.
+constexpr int kTileQ = 4;
+constexpr int kTileQConsumers = 11;  // leader: producer, MMA issuer, 4 epilogue warps; peer: producer, 4
+// full, empty, tmem full x2, tmem empty x2, drain, tile queue full / empty
+constexpr int kBarriers = 2 * kStages + 5 + 2 * kTileQ;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kBarriers + 16 + 4 * kTileQ;
 constexpr int kMaxProblems = 3;
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
 
@@ -64,6 +70,10 @@ struct Params {
     const float *out_scale;    // store modes: the accumulator is multiplied by *out_scale (null: 1)
     int f16;                   // operands and 16-bit outputs are fp16 (else bf16)
     int *err;                  // device error word (may be null)
+    // null: cluster c runs tiles c, c + #clusters, ...; else the tiles are
+    // taken in order from this counter (zero before the launch), so the
+    // tiles in flight stay a window of consecutive numbers
+    unsigned int *tile_ctr;
 };
 
 struct Maps {
