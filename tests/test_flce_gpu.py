@@ -262,6 +262,35 @@ def test_flce_deterministic():
     assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
 
 
+# The GEMM launches of a call take their tiles from counters in that call's
+# workspace: two calls in flight on two streams at once give the same bits as
+# one after the other.
+def test_flce_concurrent_calls_on_two_streams():
+    ws = [small(256, 512, 9000, T=30.0, seed=21), small(192, 512, 7000, eps=0.1, seed=22)]
+    inputs = [make_flce_inputs(w, device=DEV) for w in ws]
+
+    def call(w, h, W, lab):
+        return flce_fwd_bwd(h, W, lab, label_smoothing=w.label_smoothing, softcap=w.softcap)
+
+    ref = []
+    for w, (h, W, lab) in zip(ws, inputs):
+        ref.append(call(w, h, W, lab))
+        torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for st, w, (h, W, lab) in zip(streams, ws, inputs):
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            outs.append(call(w, h, W, lab))
+    torch.cuda.synchronize()
+    for a, b in zip(ref, outs):
+        assert torch.equal(a.grad_hidden.view(torch.int16), b.grad_hidden.view(torch.int16))
+        assert torch.equal(a.grad_weight.view(torch.int32), b.grad_weight.view(torch.int32))
+        assert torch.equal(a.loss.view(torch.int32), b.loss.view(torch.int32))
+        assert torch.equal(a.argmax, b.argmax)
+        assert torch.equal(a.counts, b.counts)
+
+
 @pytest.mark.parametrize("chunk_rows", [None, 1024])
 def test_flce_full_size_workload_sampled(chunk_rows):
     w = FLCE_WORKLOADS["flce-bf16-4096x6656x202048-softcap30"]
