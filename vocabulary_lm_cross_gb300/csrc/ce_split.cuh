@@ -414,18 +414,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
 
             // ---- publish this warp's partial to every CTA of the cluster, then
             // merge all k x 15 partials of the row (same order everywhere)
-            if (lane == 0) {
+            // (lane c serves CTA c: the k stores and release-arrives run in parallel)
+            if (static_cast<uint32_t>(lane) < k) {
                 const uint32_t dst = ptx::smem_addr(&ctl.xslot[pp][crank * kConsumerWarps + warp]);
                 const uint32_t bar = ptx::smem_addr(&ctl.stat[pp]);
                 const uint4 v0 = make_uint4(__float_as_uint(part.mx), static_cast<uint32_t>(part.idx),
                                             __float_as_uint(part.mz), __float_as_uint(part.s));
                 const uint4 v1 = make_uint4(__float_as_uint(part.sz), __float_as_uint(part.zy), 0u, 0u);
-                for (uint32_t c = 0; c < k; ++c) {
-                    const uint32_t ra = ptx::mapa(dst, c);
-                    ptx::st_dsmem_v4(ra, v0);
-                    ptx::st_dsmem_v4(ra + 16, v1);
-                }
-                for (uint32_t c = 0; c < k; ++c) ptx::mbar_remote_arrive_release(ptx::mapa(bar, c));
+                const uint32_t ra = ptx::mapa(dst, static_cast<uint32_t>(lane));
+                ptx::st_dsmem_v4(ra, v0);
+                ptx::st_dsmem_v4(ra + 16, v1);
+                ptx::mbar_remote_arrive_release(ptx::mapa(bar, static_cast<uint32_t>(lane)));
             }
             bounded_wait<true, false>(ptx::smem_addr(&ctl.stat[pp]),
                                       static_cast<uint32_t>((it >> 1) & 1), abort, p.err);
