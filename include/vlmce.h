@@ -408,8 +408,8 @@ void vlmce_flce_profile_events(void *ev_begin, void *ev_end);
  * the process exits.  N may not exceed vlmce_ce_noalloc_max_rows() (65536):
  * larger N returns VLMCE_ERR_TOO_LARGE before anything is enqueued.  No
  * device memory is allocated or freed.  The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress); make that first call
- * before any stream capture.  Every call on a device shares the one array:
+ * the array's device address (cudaGetSymbolAddress, a host-side query).
+ * Every call on a device shares the one array:
  * calls that overlap on the GPU (different streams without ordering between
  * them) race on it and must not be issued; calls ordered on one stream are
  * safe.  The array keeps the last call's contents, none of which a call needs
