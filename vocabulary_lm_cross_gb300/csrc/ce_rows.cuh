@@ -11,11 +11,13 @@
 //           last are the likeliest still in L2) -- without a softcap it is
 //           mostly still in the 129 MB L2, since at most 2 x 152 rows (78 MB
 //           for 256 KB rows) are in flight; softcap rows exceed L2 and are
-//           prefetched into it ahead -- and store the gradient scale (p - q)
-//           (1 - t^2), rounded to the storage dtype, with 16-byte evict-first
-//           stores over the logits.
-// Without a softcap HBM sees about one read and one write of every byte.  The label census of the call is only needed by pass 2, so the kernel
-// waits for it (programmatic dependent launch) after pass 1.
+//           prefetched into it ahead, two granules in flight per thread --
+//           and store the gradient scale (p - q) (1 - t^2), rounded to the
+//           storage dtype, with 16-byte evict-first stores over the logits.
+// Without a softcap HBM sees about one read and one write of every byte.
+// The label census of the call is only needed by pass 2, so the kernel waits
+// for it (programmatic dependent launch) after pass 1, in one warp while
+// another merges the warp partials.
 //
 // Pass 1 keeps two 16-byte loads in flight per thread and prefetches the
 // next iteration's pair into L2, so that enough bytes are outstanding per SM
@@ -29,7 +31,8 @@
 // With a gradient, rows without a softcap locate the column in new_max:
 // measured on GB300, deferring it there saved 29 % of the instructions but
 // cost 4-6 % of the time (more of pass 2 missed L2).
-// The kernel is bound by instruction issue, so the inner loops run over whole
+// Instruction issue bounds the kernel (softcap rows at full size: DRAM, with
+// the pass-2 re-reads), so the inner loops run over whole
 // granules only, with no per-element tests: the at most two partial granules
 // at the ends of a row are handled apart (the first one before a thread's
 // main loop, the last one after it, so every thread still meets its granules
