@@ -14,11 +14,12 @@
 //   pass A: one pass over the slice in shared memory: max and first argmax of
 //           the raw logits, online sum of exp(z - m) and sum of z (packed
 //           f32x2 arithmetic);
-//   merge:  warp shuffles; then every consumer warp writes its partial into
-//           every CTA of the cluster through distributed shared memory and
-//           release-arrives on each CTA's row barrier; after the acquire-wait
-//           every warp merges the k x 15 partials in the same fixed order, so
-//           every CTA holds the same lse;
+//   merge:  warp shuffles, then the 15 warp partials (fixed order) into the
+//           CTA's partial, which the first consumer warp writes into every CTA
+//           of the cluster through distributed shared memory (lane c to CTA
+//           c), release-arriving on each CTA's row barrier; after the
+//           acquire-wait every warp merges the k CTA partials in the same
+//           fixed order, so every CTA holds the same lse;
 //   pass B: gradient scale (p - q) (1 - t^2), rounded to the storage dtype,
 //           16-byte streaming stores over the logits.
 // Each byte of the row crosses HBM once in and once out.
@@ -54,10 +55,12 @@ constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per on-chip w
 struct Ctl {
     unsigned long long full[kSlots];   // slot landed (transaction bytes)
     unsigned long long empty[kSlots];  // slot released by the 15 consumer warps
-    unsigned long long stat[2];        // all partials of a row arrived (k x 15 arrivals)
-    // Row partials of every consumer warp of every CTA of the cluster, written
-    // by their owners through distributed shared memory; indexed by row parity.
-    RowPart xslot[2][kMaxCluster * kConsumerWarps];
+    unsigned long long stat[2];        // all partials of a row arrived (k arrivals)
+    // This CTA's consumer-warp partials, and the CTA partials of the cluster
+    // (written by their owners through distributed shared memory), indexed
+    // by row parity.
+    RowPart wslot[2][kConsumerWarps];
+    RowPart xslot[2][kMaxCluster];
     int abort;                         // an on-chip wait gave up
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
@@ -139,6 +142,12 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
         CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
     if (ok) return true;
     return bounded_wait_slow<CLUSTER, SKIP_IF_ABORT>(bar, parity, abort, err);
+}
+
+// Barrier 1 over the kConsumers consumer threads (the producer warp does not
+// take part).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
 // Per-thread pass-A accumulators.
@@ -332,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
             ptx::mbar_init(full0 + 8u * s, 1);
             ptx::mbar_init(empty0 + 8u * s, kConsumerWarps);
         }
-        ptx::mbar_init(ptx::smem_addr(&ctl.stat[0]), k * kConsumerWarps);
-        ptx::mbar_init(ptx::smem_addr(&ctl.stat[1]), k * kConsumerWarps);
+        ptx::mbar_init(ptx::smem_addr(&ctl.stat[0]), k);
+        ptx::mbar_init(ptx::smem_addr(&ctl.stat[1]), k);
         ctl.abort = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -412,33 +421,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) ce_split_kernel(const Sp
             part.zy = zy;
             warp_allreduce(part);
 
-            // ---- publish this warp's partial to every CTA of the cluster, then
-            // merge all k x 15 partials of the row (same order everywhere)
-            // (lane c serves CTA c: the k stores and release-arrives run in parallel)
-            if (static_cast<uint32_t>(lane) < k) {
-                const uint32_t dst = ptx::smem_addr(&ctl.xslot[pp][crank * kConsumerWarps + warp]);
-                const uint32_t bar = ptx::smem_addr(&ctl.stat[pp]);
-                const uint4 v0 = make_uint4(__float_as_uint(part.mx), static_cast<uint32_t>(part.idx),
-                                            __float_as_uint(part.mz), __float_as_uint(part.s));
-                const uint4 v1 = make_uint4(__float_as_uint(part.sz), __float_as_uint(part.zy), 0u, 0u);
-                const uint32_t ra = ptx::mapa(dst, static_cast<uint32_t>(lane));
-                ptx::st_dsmem_v4(ra, v0);
-                ptx::st_dsmem_v4(ra + 16, v1);
-                ptx::mbar_remote_arrive_release(ptx::mapa(bar, static_cast<uint32_t>(lane)));
+            // ---- the CTA's partial (the consumer warps meet on named barrier
+            // 1), published by the first consumer warp to every CTA of the
+            // cluster (lane c to CTA c, in parallel); then every warp merges
+            // the k CTA partials of the row (same order everywhere)
+            if (lane == 0) ctl.wslot[pp][warp] = part;
+            consumers_sync();
+            if (warp == 0) {
+                RowPart cp = part_identity();
+                if (lane < kConsumerWarps) cp = ctl.wslot[pp][lane];
+                warp_allreduce(cp);
+                if (static_cast<uint32_t>(lane) < k) {
+                    const uint32_t dst = ptx::smem_addr(&ctl.xslot[pp][crank]);
+                    const uint32_t bar = ptx::smem_addr(&ctl.stat[pp]);
+                    const uint4 v0 = make_uint4(__float_as_uint(cp.mx), static_cast<uint32_t>(cp.idx),
+                                                __float_as_uint(cp.mz), __float_as_uint(cp.s));
+                    const uint4 v1 = make_uint4(__float_as_uint(cp.sz), __float_as_uint(cp.zy), 0u, 0u);
+                    const uint32_t ra = ptx::mapa(dst, static_cast<uint32_t>(lane));
+                    ptx::st_dsmem_v4(ra, v0);
+                    ptx::st_dsmem_v4(ra + 16, v1);
+                    ptx::mbar_remote_arrive_release(ptx::mapa(bar, static_cast<uint32_t>(lane)));
+                }
             }
             bounded_wait<true, false>(ptx::smem_addr(&ctl.stat[pp]),
                                       static_cast<uint32_t>((it >> 1) & 1), abort, p.err);
             RowPart rp = part_identity();
-            {
-                const int n_parts = static_cast<int>(k) * kConsumerWarps;
-#pragma unroll
-                for (int e = lane; e < kMaxCluster * kConsumerWarps; e += 32) {
-                    if (e < n_parts) {
-                        const RowPart &o = ctl.xslot[pp][e];
-                        part_merge(rp, o.mx, o.idx, o.mz, o.s, o.sz, o.zy);
-                    }
-                }
-            }
+            if (static_cast<uint32_t>(lane) < k) rp = ctl.xslot[pp][lane];
             warp_allreduce(rp);
             const float lse = rp.mz + logf(rp.s);
 
