@@ -148,7 +148,8 @@ def test_flce_fp16(N, H, V, T, eps, red):
     run_small(small(N, H, V, T=T, eps=eps, red=red, gs=0.5, seed=N + 1, dtype="f16"))
 
 
-@pytest.mark.parametrize("N,H,V", [(256, 512, 8192), (200, 264, 5000), (130, 128, 300)])
+@pytest.mark.parametrize("N,H,V", [(256, 512, 8192), (200, 264, 5000), (130, 128, 300),
+                                   (1, 64, 1000), (3, 200, 513)])
 @pytest.mark.parametrize("T,eps,red", [(0.0, 0.0, "mean"), (30.0, 0.1, "sum")])
 def test_flce_small_single_chunk(N, H, V, T, eps, red):
     run_small(small(N, H, V, T=T, eps=eps, red=red, gs=0.5))
