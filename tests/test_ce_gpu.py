@@ -262,6 +262,49 @@ def test_argmax_at_planted_maxima(path, dtype, T, V, stride, monkeypatch):
     assert torch.equal(res.argmax, rf.argmax)
 
 
+def _golden_cases():
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "ce_closed_forms.jsonl")
+    with open(path) as f:
+        return [json.loads(line) for line in f if line.strip()]
+
+
+GOLDEN = _golden_cases()
+
+
+# The closed-form calls of tests/golden (inputs exact in bf16): losses within
+# 1e-4, argmax, counts and accuracy exact, gradients within one bf16 ulp of
+# the rounded closed form (fp32 logits: 2e-5 relative, the fp32 evaluation of
+# 1 - tanh^2 near saturation).
+@pytest.mark.parametrize("path", ["rows", "split"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("c", GOLDEN, ids=[c["case"] for c in GOLDEN])
+def test_closed_form_golden_calls(c, dtype, path, monkeypatch):
+    monkeypatch.setenv("VLMCE_CE_PATH", path)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.tensor(c["x"], dtype=torch.float64).to(tdt).to(DEV)
+    lab = torch.tensor(c["labels"], dtype=torch.int64, device=DEV)
+    res = v.ce_fwd_bwd(x, lab, label_smoothing=c["label_smoothing"], softcap=c["softcap"],
+                       reduction=c["reduction"], grad_scale=c["grad_scale"])
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(res.loss.cpu().numpy(), c["loss"], rtol=0, atol=1e-4)
+    assert res.argmax.cpu().tolist() == c["argmax"]
+    counts = res.counts.cpu().tolist()
+    assert counts[0] == c["n_valid"] and counts[1] == c["n_correct"] and counts[2:] == [0, 0]
+    red = res.reduced.cpu().numpy()
+    assert abs(float(red[0]) - c["reduced_loss"]) <= 1e-4 * max(1.0, abs(c["reduced_loss"]))
+    assert float(red[1]) == pytest.approx(c["accuracy"], abs=1e-7)
+    g = x.double().cpu().numpy()
+    e = np.asarray(c["grad"])
+    if dtype == "bf16":
+        e_r = torch.tensor(e).to(torch.bfloat16).double().numpy()  # round to nearest even
+        ulp = np.maximum(np.abs(e_r), 2.0 ** -126) * 2.0 ** -7
+        assert np.all(np.abs(g - e_r) <= ulp), (g, e_r)
+    else:
+        np.testing.assert_allclose(g, e, rtol=2e-5, atol=1e-7)
+
+
 def test_all_rows_ignored_and_bad_labels():
     w = small(16, 3000, "bf16", ignore=1.0)
     res, ref, _ = run_and_check(w)

@@ -263,6 +263,39 @@ def test_flce_deterministic():
     assert torch.equal(outs[0][2].view(torch.int32), outs[1][2].view(torch.int32))
 
 
+def _golden_flce():
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "flce_closed_forms.jsonl")
+    with open(path) as f:
+        return [json.loads(line) for line in f if line.strip()]
+
+
+GOLDEN = _golden_flce()
+
+
+# The closed-form fused linear CE calls of tests/golden (exact small inputs,
+# so the logits are exact in fp32): losses within 1e-4, argmax and counts
+# exact, both gradients within 1e-2 relative L2 (the gradient tile is rounded
+# to bf16 before the two products).
+@pytest.mark.parametrize("chunk_rows", [None, 2])
+@pytest.mark.parametrize("c", GOLDEN, ids=[c["case"] for c in GOLDEN])
+def test_flce_closed_form_golden_calls(c, chunk_rows):
+    h = torch.tensor(c["h"], dtype=torch.float64).to(torch.bfloat16).to(DEV)
+    W = torch.tensor(c["W"], dtype=torch.float64).to(torch.bfloat16).to(DEV)
+    lab = torch.tensor(c["labels"], dtype=torch.int64, device=DEV)
+    r = flce_fwd_bwd(h, W, lab, label_smoothing=c["label_smoothing"], softcap=c["softcap"],
+                     reduction=c["reduction"], grad_scale=c["grad_scale"], chunk_rows=chunk_rows)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(r.loss.cpu().numpy(), c["loss"], rtol=0, atol=1e-4)
+    assert r.argmax.cpu().tolist() == c["argmax"]
+    counts = r.counts.cpu().tolist()
+    assert counts[0] == c["n_valid"] and counts[1] == c["n_correct"] and counts[2:] == [0, 0]
+    assert abs(float(r.reduced[0]) - c["reduced_loss"]) <= 1e-4 * max(1.0, abs(c["reduced_loss"]))
+    assert rel_l2(r.grad_hidden.float().cpu().numpy(), np.asarray(c["grad_hidden"])) < 1e-2
+    assert rel_l2(r.grad_weight.cpu().numpy(), np.asarray(c["grad_weight"])) < 1e-2
+
+
 # The GEMM launches of a call take their tiles from counters in that call's
 # workspace: two calls in flight on two streams at once give the same bits as
 # one after the other.
