@@ -285,7 +285,9 @@ vlmce_status swiglu_bwd(const void *x, int64_t x_stride, const void *dy, int64_t
 
 /* Bytes of device workspace flce_fwd_bwd needs (256-byte aligned): per-row
  * statistics of every 256-column logits tile, two bf16 [N, 8192] gradient
- * tiles and an fp32 [N, H] grad_hidden accumulator. */
+ * tiles, an fp32 [N, H] grad_hidden accumulator and one 4-byte tile counter
+ * per GEMM launch of the call (the workspace of a call in flight belongs to
+ * that call: two calls at once need two workspaces). */
 size_t vlmce_flce_workspace_bytes(int64_t N, int64_t H, int64_t V);
 
 /*
