@@ -12,11 +12,11 @@
 namespace vlmce {
 namespace gemm {
 
-constexpr int BM = 256, BN = 256, BK = 64;  // pair tile
+constexpr int BM = 256, BN = 256, BK = 128;  // pair tile
 constexpr int kHalf = 128;                  // rows of A and of B held by one CTA
-constexpr int kStages = 6;
-constexpr int kOpBytes = kHalf * BK * 2;    // 16 KB per operand per stage
-constexpr int kStageBytes = 2 * kOpBytes;   // 32 KB per CTA
+constexpr int kStages = 3;
+constexpr int kOpBytes = kHalf * BK * 2;    // 32 KB per operand per stage
+constexpr int kStageBytes = 2 * kOpBytes;   // 64 KB per CTA
 constexpr int kThreads = 224;
 constexpr int kTmemCols = 2 * BN;
 // Dynamic tile order: a scheduler warp of the pair leader takes the next tile
