@@ -606,6 +606,9 @@ template <bool BF16, bool SOFTCAP, int THREADS, bool DEFER = SOFTCAP>
 __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
     __shared__ RowPart wpart[THREADS / 32];
     __shared__ RowBcast bcast;
+    // the finalize kernel (launched dependent on this grid, and waiting for it
+    // before it reads anything) may be scheduled once every CTA has started
+    ptx::griddep_launch_dependents();
     // sum z only matters with label smoothing; skip the adds without it
     if (p.eps > 0.f)
         row_work<BF16, SOFTCAP, true, THREADS, DEFER>(p, wpart, &bcast);

@@ -187,6 +187,9 @@ template <bool BF16, bool SOFTCAP, int THREADS>
 __global__ void __launch_bounds__(THREADS, grad_min_blocks(THREADS, SOFTCAP))
     ce_shard_grad_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
+    // the finalize kernel (dependent on this grid, waiting for it before it
+    // reads anything) may be scheduled once every CTA has started
+    ptx::griddep_launch_dependents();
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
     const Geo g = geometry<BF16, THREADS>(p);
