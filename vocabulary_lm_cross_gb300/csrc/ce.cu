@@ -19,9 +19,11 @@
 //                    where one CTA per row would leave most SMs idle.
 //   3. ce_finalize_kernel -- fixed-order float-float reduction of the
 //      per-row losses and correct-prediction count.
-// Kernels 2 and 3 use programmatic dependent launch, so that their prologues
-// overlap the previous kernel's tail.  No floating-point atomics: results are
-// bit-reproducible.
+// All three use programmatic dependent launch, so that each is resident
+// when its predecessor on the stream completes: the census waits for that
+// predecessor before it reads anything, the row work overlaps the census,
+// and the finalize waits for the row work.  No floating-point atomics:
+// results are bit-reproducible.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -301,13 +303,21 @@ vlmce_status run_ce(void *logits, int32_t dtype, const int64_t *labels, int64_t 
     float *loss = out_loss ? out_loss : w.loss;
     int64_t *amax = out_argmax ? out_argmax : w.argmax;
 
-    ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, w.counts, w.err);
-    st = launch_status(cudaSuccess, "ce_count_kernel");
-    if (st != VLMCE_OK) return st;
-
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cc = {};
+        cc.gridDim = dim3(1, 1, 1);
+        cc.blockDim = dim3(1024, 1, 1);
+        cc.stream = cs;
+        cc.attrs = attr;
+        cc.numAttrs = 1;
+        st = launch_status(cudaLaunchKernelEx(&cc, ce_count_kernel, labels, N, V, ignore_index,
+                                              w.counts, w.err),
+                           "ce_count_kernel");
+        if (st != VLMCE_OK) return st;
+    }
 
     if (N > 0) {
         cudaEvent_t eb = t_prof_begin, ee = t_prof_end;

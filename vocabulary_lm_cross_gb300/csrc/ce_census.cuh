@@ -22,6 +22,10 @@ namespace {
 __global__ void __launch_bounds__(1024) ce_count_kernel(const int64_t *__restrict__ labels, int64_t N,
                                                      int64_t V, int64_t ignore_index,
                                                      int64_t *counts, int *err) {
+    // Launched dependent on whatever precedes it on the stream: it waits for
+    // that work (whose results the row work may read), then lets the row
+    // work start while it counts.
+    ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     long long nv = 0, nb = 0;
     const int64_t st = blockDim.x;
@@ -91,6 +95,9 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(
     const float *__restrict__ loss, const int64_t *__restrict__ argmax,
     const int64_t *__restrict__ labels, int64_t N, int64_t V, int64_t ignore_index, int reduction,
     const int64_t *counts, const int *err, float *out_reduced, int64_t *out_counts) {
+    // the next call's census may be scheduled now (it waits for this kernel
+    // before it reads anything); this kernel waits for the row work
+    ptx::griddep_launch_dependents();
     ptx::griddep_wait();
     FloatFloat acc = {0.f, 0.f};
     long long nc = 0;

@@ -106,6 +106,10 @@ __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP))
     ce_shard_stats_kernel(const ShardParams p) {
     constexpr int EPG = Elem<BF16>::kPerGranule;
     constexpr int kWarps = THREADS / 32;
+    // a dependent launch that follows (the merge or a census, each waiting
+    // for this grid before it reads anything) may be scheduled once every CTA
+    // has started
+    ptx::griddep_launch_dependents();
     __shared__ RowPart wpart[kWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const Geo g = geometry<BF16, THREADS>(p);
@@ -465,8 +469,10 @@ vlmce_status shard_fwd_bwd(void *logits, int32_t dtype, const int64_t *labels, i
     int64_t *amax = out_argmax ? out_argmax
                                : reinterpret_cast<int64_t *>(wb + 256 + round_up(4 * N, 256));
 
-    ce_count_kernel<<<1, 1024, 0, cs>>>(labels, N, V, ignore_index, counts, err);
-    if ((st = launch_status(cudaSuccess, "ce_count_kernel")) != VLMCE_OK) return st;
+    if ((st = launch_status(launch_dependent(ce_count_kernel, dim3(1), dim3(1024), cs, labels, N,
+                                             V, ignore_index, counts, err),
+                            "ce_count_kernel")) != VLMCE_OK)
+        return st;
     if (N > 0) {
         ShardParams p = {};
         p.logits = static_cast<unsigned char *>(logits);
