@@ -900,34 +900,67 @@ def run_flce(args, w, steps, dev, world, barrier, sampler):
     torch.cuda.synchronize()
     kern_ms = statistics.fmean(kb[i].elapsed_time(ke[i]) for i in range(steps))
 
-    # end to end through the public API with host buffers
-    h_host = h.cpu().pin_memory()
-    W_host = W.cpu().pin_memory()
-    lab_host = lab.cpu().pin_memory()
-    gh_host = torch.empty((w.N, w.H), dtype=torch.bfloat16).pin_memory()
-    gw_host = torch.empty((w.V, w.H), dtype=torch.float32).pin_memory()
-    loss_host = torch.empty(w.N, dtype=torch.float32).pin_memory()
-    red_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    # end to end through the public API with host buffers: page-locked buffers
+    # on the GPU's NUMA node; every step copies its inputs in and its results
+    # (grad_hidden, grad_weight, loss, reduced) out.  Two sets of device
+    # buffers let step i's results go out (on one copy stream) and step i+1's
+    # inputs come in (on another) while a call computes, as a caller streaming
+    # host-resident weights would run it.
+    cpus0 = os.sched_getaffinity(0)
+    bind_to_gpu_local_cpus(dev)
+    try:
+        h_host = h.cpu().pin_memory()
+        W_host = W.cpu().pin_memory()
+        lab_host = lab.cpu().pin_memory()
+        gh_host = torch.empty((w.N, w.H), dtype=torch.bfloat16).pin_memory()
+        gw_host = torch.empty((w.V, w.H), dtype=torch.float32).pin_memory()
+        loss_host = torch.empty(w.N, dtype=torch.float32).pin_memory()
+        red_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    finally:
+        os.sched_setaffinity(0, cpus0)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    hb, Wb, lb = [h, torch.empty_like(h)], [W, torch.empty_like(W)], [lab, torch.empty_like(lab)]
+    gwb = [gw, torch.empty_like(gw)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    keep = [None, None]
 
-    def e2e_step():
-        h.copy_(h_host, non_blocking=True)
-        W.copy_(W_host, non_blocking=True)
-        lab.copy_(lab_host, non_blocking=True)
-        r = step()
-        gh_host.copy_(r.grad_hidden, non_blocking=True)
-        gw_host.copy_(gw, non_blocking=True)
-        loss_host.copy_(r.loss, non_blocking=True)
-        red_host.copy_(r.reduced, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        if i >= 2:  # set b's inputs were read by step i - 2
+            s_in.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_in):
+            hb[b].copy_(h_host, non_blocking=True)
+            Wb[b].copy_(W_host, non_blocking=True)
+            lb[b].copy_(lab_host, non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:  # set b's results of step i - 2 are out
+            stream.wait_event(ev_out[b])
+        r = v.flce_fwd_bwd(hb[b], Wb[b], lb[b], **dict(kw, grad_weight=gwb[b]))
+        ev_comp[b].record(stream)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            gh_host.copy_(r.grad_hidden, non_blocking=True)
+            gw_host.copy_(gwb[b], non_blocking=True)
+            loss_host.copy_(r.loss, non_blocking=True)
+            red_host.copy_(r.reduced, non_blocking=True)
+        ev_out[b].record(s_out)
+        keep[b] = r  # the result tensors stay allocated until copied out
 
-    e2e_step()
+    e2e_step(0)
     torch.cuda.synchronize()
-    e2e_steps = 3
+    e2e_steps = 6
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_event(ev_out[(e2e_steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
