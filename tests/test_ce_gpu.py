@@ -337,6 +337,43 @@ def test_deterministic_bit_identical():
     assert np.array_equal(outs[0][2].view(np.uint32), outs[1][2].view(np.uint32))
 
 
+def test_back_to_back_calls_keep_stream_order():
+    """Calls enqueued back to back on one stream (each launched dependent on
+    the work before it) give the bits of the same calls run one at a time:
+    a second call on the same buffer reads the first call's gradient, and
+    calls sharing one workspace each reduce their own losses and counts."""
+    w = small(300, 32000, "bf16", eps=0.1)
+    x, lab = make_ce_inputs(w, device=DEV)
+    lab2 = lab.flip(0).contiguous()
+    kw = dict(label_smoothing=0.1)
+
+    def outputs(buf, *rs):
+        return [bf16_bits_np(buf)] + [t.cpu().numpy().view(np.uint8).copy()
+                                      for r in rs for t in (r.loss, r.argmax, r.reduced, r.counts)]
+
+    a = x.clone()
+    ra = v.ce_fwd_bwd(a, lab, **kw)
+    torch.cuda.synchronize()
+    ra_out = outputs(a, ra)[1:]
+    fa = v.ce_fwd_bwd(a, lab2, compute_grad=False, **kw)
+    torch.cuda.synchronize()
+    rb = v.ce_fwd_bwd(a, lab2, **kw)
+    torch.cuda.synchronize()
+    ref = outputs(a, fa, rb)
+
+    b = x.clone()
+    ws = torch.empty(v.ce.workspace_bytes(300, 32000, b.dtype), dtype=torch.uint8, device=DEV)
+    r1 = v.ce_fwd_bwd(b, lab, workspace=ws, **kw)
+    f2 = v.ce_fwd_bwd(b, lab2, workspace=ws, compute_grad=False, **kw)
+    r2 = v.ce_fwd_bwd(b, lab2, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    got = outputs(b, f2, r2)
+    for g, e in zip(got, ref):
+        assert np.array_equal(g, e)
+    for g, e in zip(outputs(b, r1)[1:], ra_out):
+        assert np.array_equal(g, e)
+
+
 def test_guard_bytes_around_the_buffer_are_untouched():
     N, V = 17, 5001
     w = small(N, V, "bf16", eps=0.1)
