@@ -901,7 +901,7 @@ def run_flce(args, w, steps, dev, world, barrier, sampler):
     kern_ms = statistics.fmean(kb[i].elapsed_time(ke[i]) for i in range(steps))
 
     # end to end through the public API with host buffers: page-locked buffers
-    # on the GPU's NUMA node; every step copies its inputs in and its results
+    # (allocated on the GPU's local CPUs); every step copies its inputs in and its results
     # (grad_hidden, grad_weight, loss, reduced) out.  Two sets of device
     # buffers let step i's results go out (on one copy stream) and step i+1's
     # inputs come in (on another) while a call computes, as a caller streaming
