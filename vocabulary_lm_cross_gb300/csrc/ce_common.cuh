@@ -159,11 +159,18 @@ __device__ __forceinline__ Cap2 softcap2(float x0, float x1, float neg2_log2e_ov
 // Where |x| <= 0.55 T (nearly every column at the softcaps the pages use),
 // tanh(x/T) = u P(u^2) with u = x/T and P the degree-4 least-squares fit of
 // tanh(u)/u on u in [0, 0.55] (relative error 3.3e-8 at 4000 Chebyshev nodes;
-// measured fp32 error of t below 8e-8): seven packed fp32x2 FMA-pipe ops per
-// column pair, with the coefficients as constants, and no MUFU op, against
-// about twelve and two MUFU ops for softcap2.  There 1 - t^2 >= 0.75 is formed
+// measured fp32 error of t below 8e-8).  The row kernels evaluate it as
+// x Q(x^2), Q's i-th coefficient P's divided by T^(2i+1) (ce_rows.cuh): six
+// packed fp32x2 FMA-pipe ops per column pair and no MUFU op, against about
+// twelve and two MUFU ops for softcap2.  There 1 - t^2 >= 0.75 is formed
 // directly, with no cancellation.  Columns beyond 0.55 T keep softcap2.
 constexpr float kPolyRange = 0.55f;
+// P's coefficients, constant term first
+constexpr float kTanhP0 = 0.9999999667018895f;
+constexpr float kTanhP1 = -0.33332785337019116f;
+constexpr float kTanhP2 = 0.13318718793849865f;
+constexpr float kTanhP3 = -0.05258102516972439f;
+constexpr float kTanhP4 = 0.016301813790173283f;
 
 struct PolyCap {
     float rT;       // 1 / T
@@ -178,33 +185,12 @@ __device__ __forceinline__ PolyCap poly_cap(float T) {
     pc.lim2 = h | (h << 16);
     return pc;
 }
-// tanh(x/T) of two columns (each |x| <= 0.55 T) by the polynomial.
-__device__ __forceinline__ uint64_t tanh_poly2(uint64_t x, const PolyCap &pc) {
-    const uint64_t u = mul2(x, pk(pc.rT, pc.rT));
-    const uint64_t s = mul2(u, u);
-    uint64_t a = fma2(pk(0.016301813790173283f, 0.016301813790173283f), s,
-                      pk(-0.05258102516972439f, -0.05258102516972439f));
-    a = fma2(a, s, pk(0.13318718793849865f, 0.13318718793849865f));
-    a = fma2(a, s, pk(-0.33332785337019116f, -0.33332785337019116f));
-    a = fma2(a, s, pk(0.9999999667018895f, 0.9999999667018895f));
-    return mul2(u, a);
-}
 
 // tanh(x/T) of one column, by the same arithmetic as softcap2.
 __device__ __forceinline__ float softcap_t1(float x, float neg2_log2e_over_T) {
     float t0, t1;
     upk(softcap2(x, x, neg2_log2e_over_T).t, t0, t1);
     return t0;
-}
-// tanh(x/T) of one column: the polynomial within its range, else softcap2's arithmetic.
-__device__ __forceinline__ float softcap_t_any(float x, const PolyCap &pc,
-                                               float neg2_log2e_over_T) {
-    if (fabsf(x) <= pc.lim) {
-        float t0, t1;
-        upk(tanh_poly2(pk(x, x), pc), t0, t1);
-        return t0;
-    }
-    return softcap_t1(x, neg2_log2e_over_T);
 }
 
 template <bool BF16>

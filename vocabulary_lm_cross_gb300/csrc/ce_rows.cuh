@@ -144,6 +144,7 @@ __device__ __forceinline__ RowPart acc_part(const Acc &a, float T) {
 struct CapK {
     float T, k2;
     PolyCap pc;
+    float q[5];  // tanh(x/T) = x Q(x^2) within the polynomial's range: Q's coefficients
 };
 template <bool SOFTCAP>
 __device__ __forceinline__ CapK cap_k(float T) {
@@ -151,14 +152,41 @@ __device__ __forceinline__ CapK cap_k(float T) {
     k.T = T;
     k.k2 = SOFTCAP ? -2.f * kLog2e / T : 0.f;
     k.pc = SOFTCAP ? poly_cap(T) : PolyCap{};
+    // tanh(u)/u = P(u^2), u = x / T: Q's i-th coefficient is P's divided by T^(2i+1)
+    const float c[5] = {kTanhP0, kTanhP1, kTanhP2, kTanhP3, kTanhP4};
+    const float r = SOFTCAP ? k.pc.rT : 0.f, r2 = r * r;
+    float f = r;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        k.q[i] = c[i] * f;
+        f *= r2;
+    }
     return k;
+}
+// tanh(x/T) of two columns (each |x| <= 0.55 T) by the polynomial.
+__device__ __forceinline__ uint64_t tanh_q2(uint64_t x, const CapK &k) {
+    const uint64_t s = mul2(x, x);
+    uint64_t a = fma2(pk(k.q[4], k.q[4]), s, pk(k.q[3], k.q[3]));
+    a = fma2(a, s, pk(k.q[2], k.q[2]));
+    a = fma2(a, s, pk(k.q[1], k.q[1]));
+    a = fma2(a, s, pk(k.q[0], k.q[0]));
+    return mul2(x, a);
+}
+// tanh(x/T) of one column: the polynomial within its range, else softcap2's arithmetic.
+__device__ __forceinline__ float cap_t_any(float x, const CapK &k) {
+    if (fabsf(x) <= k.pc.lim) {
+        float t0, t1;
+        upk(tanh_q2(pk(x, x), k), t0, t1);
+        return t0;
+    }
+    return softcap_t1(x, k.k2);
 }
 
 // z of one column: the logit, or T tanh(x/T) under a softcap.
 template <bool SOFTCAP>
 __device__ __forceinline__ float z_of(float x, const CapK &k) {
     if constexpr (SOFTCAP)
-        return k.T * softcap_t_any(x, k.pc, k.k2);
+        return k.T * cap_t_any(x, k);
     else
         return x;
 }
@@ -236,7 +264,7 @@ __device__ __forceinline__ void fold_full(Acc &a, const uint4 w, int jg, int V, 
         if (granule_in_poly_range<BF16>(w, k.pc)) {
 #pragma unroll
             for (int l = 0; l < EPG; l += 2) {
-                const uint64_t v = tanh_poly2(pk(x[l], x[l + 1]), k.pc);
+                const uint64_t v = tanh_q2(pk(x[l], x[l + 1]), k);
                 a.s = add2(a.s, ex2x2(fma2(v, L2, nmL2)));
                 if constexpr (SUMZ) a.z = add2(a.z, v);
             }
@@ -274,7 +302,7 @@ __device__ __forceinline__ void fold_partial(Acc &a, const uint4 w, int jg, int 
 #pragma unroll
     for (int l = 0; l < EPG; ++l) {
         if (jg + l >= 0 && jg + l < V) {
-            const float v = SOFTCAP ? softcap_t_any(x[l], k.pc, k.k2) : x[l];
+            const float v = SOFTCAP ? cap_t_any(x[l], k) : x[l];
             s0 += ptx::ex2(fmaf(v, L, a.nmL));
             z0 += v;
         }
@@ -311,7 +339,7 @@ __device__ __forceinline__ float column_grad(float x, float q_coef, const GradCo
         const float L = c.k.T * kLog2e;
         if (fabsf(x) <= c.k.pc.lim) {
             float t, t_;
-            upk(tanh_poly2(pk(x, x), c.k.pc), t, t_);
+            upk(tanh_q2(pk(x, x), c.k), t, t_);
             const float pr = ptx::ex2(fmaf(t, L, c.nlseL));
             return fmaf(pr, c.scale, -q_coef) * fmaf(-t, t, 1.f);
         }
@@ -359,7 +387,7 @@ __device__ __forceinline__ void grad_values(const uint4 w, const GradCoef &c, in
         const uint64_t m_one = pk(-1.f, -1.f);
 #pragma unroll
         for (int l = 0; l < EPG; l += 2) {
-            const uint64_t t = tanh_poly2(pk(x[l], x[l + 1]), c.k.pc);
+            const uint64_t t = tanh_q2(pk(x[l], x[l + 1]), c.k);
             const uint64_t g2 =
                 mul2(fma2(ex2x2(fma2(t, L2, nlseL2)), nscale2, c2), fma2(t, t, m_one));
             upk(g2, g[l], g[l + 1]);
