@@ -1,6 +1,6 @@
 // ce_rows.cuh -- the cross-entropy row kernel (default path): one CTA per
 // row; 1024 threads (two CTAs, 64 warps per SM) for long rows, 256 threads
-// (eight CTAs per SM) for rows of at most kShortGranules granules and (six
+// (eight CTAs per SM) for rows of at most kShortGranules granules and (five
 // per SM, for their registers) for softcap rows, 128 threads (sixteen per SM)
 // for rows of at most kTinyGranules granules.
 //
@@ -61,11 +61,11 @@ constexpr int kShortGranules = 8192;
 constexpr int kTinyThreads = 128;
 constexpr int kTinyGranules = 2048;
 // CTAs per SM the launch bounds ask for (the softcap variants need more
-// registers per thread: 40 at six 256-thread CTAs per SM, a few of them spilled
-// on the rare paths).
+// registers per thread: 48 at five 256-thread CTAs per SM, which also keeps
+// fewer softcap rows in flight for L2 to hold until pass 2).
 constexpr int min_blocks(int threads, bool softcap) {
     return threads == kThreads ? (softcap ? 1 : 2)
-                               : threads == kTinyThreads ? 16 : (softcap ? 6 : 8);
+                               : threads == kTinyThreads ? 16 : (softcap ? 5 : 8);
 }
 
 // What the merge hands every thread of the row: lse, the row's maximum with
@@ -461,7 +461,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
     const CapK k = cap_k<SOFTCAP>(T);
     // Pass 2 walks the row backwards, so that it starts on the lines pass 1
     // read last, the ones most likely still in L2.  Where the rows in flight
-    // exceed L2 -- softcap rows (six 256-thread CTAs per SM, up to 912 rows
+    // exceed L2 -- softcap rows (five 256-thread CTAs per SM, up to 760 rows
     // in flight) -- it keeps two granules in flight and prefetches ahead.
     constexpr bool kAhead2 = SOFTCAP;
 
@@ -628,7 +628,7 @@ __device__ __forceinline__ void row_work(const Params &p, RowPart *wpart, RowBca
 }
 
 // Long rows: two CTAs of 1024 threads per SM (32 registers per thread); short
-// rows: eight CTAs of 256.  Softcap rows: 256-thread CTAs, six per SM (40
+// rows: eight CTAs of 256.  Softcap rows: 256-thread CTAs, five per SM (48
 // registers).
 template <bool BF16, bool SOFTCAP, int THREADS, bool DEFER = SOFTCAP>
 __global__ void __launch_bounds__(THREADS, min_blocks(THREADS, SOFTCAP)) ce_rows_kernel(const Params p) {
@@ -655,7 +655,7 @@ inline bool rows_aligned(const void *logits, int64_t row_stride, int64_t elt) {
 }
 
 // CTA size of the row kernel for rows of G granules (with or without a softcap).
-// Softcap rows always take 256-thread CTAs: six of them per SM keep more
+// Softcap rows always take 256-thread CTAs: five of them per SM keep more
 // warps resident than one CTA of 1024 at 64 registers, and their barriers
 // stall fewer warps at a time.
 inline int threads_for(int64_t G, bool softcap) {
