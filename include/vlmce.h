@@ -97,7 +97,10 @@ size_t vlmce_ce_workspace_bytes(int64_t N, int64_t V, int32_t dtype);
  *              loss is NaN, its gradient zero, and it is counted in
  *              out_counts[2] (the reduced loss is then NaN).
  * N >= 0, 1 <= V <= vlmce_ce_max_vocab(dtype), row_stride >= V (elements).
- * label_smoothing in [0, 1]; softcap T >= 0 and finite (0 = off);
+ * label_smoothing in [0, 1]; softcap T >= 0 and finite (0 = off).  The
+ * stated tolerances hold for 1e-4 <= T <= 1e4: the row kernels evaluate
+ * tanh(x/T) for |x| <= 0.55 T by a polynomial in x whose coefficients carry
+ * powers of 1/T up to the ninth, which leave the fp32 normal range outside it;
  * reduction VLMCE_MEAN (over rows with labels in [0, V); 0 when there are none),
  * VLMCE_SUM or VLMCE_NONE; grad_scale finite: the upstream gradient of the
  * reduced loss.
